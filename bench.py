@@ -1,0 +1,410 @@
+"""Decode-step throughput of the GB300 Q8_0 decode path.
+
+One step = one launch of the captured decode-step graph: every Q8_0 matvec
+(196 layer matvecs + lm_head), every layer's KV append + split-K attention,
+all glue, argmax; token and position stay in device memory.
+
+Workload (default): 7B-shaped model (hidden 3584, 28 layers, 28/4 heads,
+head_dim 128, FFN 18944, vocab 152064, Q8_0 weights = 7.51 GB + 0.58 GB
+embedding), f16 KV cache, context 2048 at the first timed step.  Inputs are
+seeded synthetic tensors drawn on the device; the weights streamed each
+step (7.5 GB) are 58x the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl q8d|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica (the decode step does not shard: replicas only) and
+`value` is the sum of the ranks' tokens over the max of their times.
+The reference arm (--impl reference) times the scalar C oracle on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "q8_matvec & gqa_decode_attn HBM GB/s (% of GB300 peak); decode-step tokens/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_index():
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    import torch
+    cur = torch.cuda.current_device()
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if cur < len(ids) and ids[cur].isdigit():
+            return int(ids[cur])
+    return cur
+
+
+# ---------------------------------------------------------------------------- sizes
+def matvec_bytes(n, p):
+    return 34 * p * (n // 32) + 4 * n + 4 * p
+
+
+def attn_bytes(L, Hk, D, H, esize, append=True):
+    return L * Hk * D * 2 * esize + 4 * 2 * H * D + (2 * Hk * D * esize if append else 0)
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for nm in ("q8d_rows.cu", "q8d_internal.cuh", "q8d_rows.cuh"):
+        with open(os.path.join(ROOT, "q8_block_quantized_matvec_gb300", "csrc", nm), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "q8_matvec_7b_decode_step.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    sha = traffic = None
+    for ln in txt.splitlines():
+        if ln.startswith("kernel_source_sha:"):
+            sha = ln.split(":", 1)[1].strip()
+        if ln.startswith(f"{kernel_key}_dram_bytes_per_launch:"):
+            traffic = float(ln.split(":", 1)[1].strip())
+    return traffic if sha == kernel_source_sha() else None
+
+
+# ---------------------------------------------------------------------------- oracle
+def oracle_sample(shape_name: str, context: int, seconds_hint: float = 20.0):
+    """Times the scalar oracle's decode step on a bounded sample of the
+    workload: the same shapes truncated to 2 layers (lm_head included), KV
+    at the same context; the full step's time is projected as
+    t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
+    Returns (tokens_per_s, threads, description)."""
+    import numpy as np
+
+    import synth
+    from oracle import oracle as orc
+    full = synth.MODELS[shape_name]
+    sample = synth.ModelShape(full.name + "-2layer", full.hidden, 2, full.n_heads, full.n_kv_heads,
+                              full.head_dim, full.ffn, full.vocab, full.qk_norm, full.qkv_bias,
+                              full.kv_dtype, full.rms_eps, full.rope_theta)
+    w = synth.step_weights(sample, seed=0)
+    cap = context
+    caches = [synth.kv_prefix(sample, 0, li, cap, context - 1) for li in range(2)]
+    host = orc.HostStep(w, cap, caches)
+    threads = orc.default_threads()
+    x = synth.normal_f32(0, "bench.x", full.hidden)
+    t0 = time.perf_counter()
+    orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
+    t_head = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    host.step(17, context - 1, threads)
+    t_step2 = time.perf_counter() - t0
+    per_layer = max(t_step2 - t_head, 1e-9) / 2
+    t_full = t_head + full.n_layers * per_layer
+    desc = (f"oracle decode step of the {full.name}-shaped model truncated to 2 of "
+            f"{full.n_layers} layers (+lm_head, KV context {context}); measured "
+            f"{t_step2:.2f} s, lm_head alone {t_head:.2f} s; projected full step {t_full:.2f} s")
+    return 1.0 / t_full, threads, desc
+
+
+# ---------------------------------------------------------------------------- main
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    tps, threads, desc = oracle_sample(args.model, args.context)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+        "steps": 1, "warmup": 0, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args)},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_name(args):
+    return (f"{args.model}-shaped decode step, Q8_0 weights, "
+            f"{'f16' if args.model != 'qwen2.5-0.5b' else 'f32'} KV cache, context {args.context}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="q8d", choices=["q8d", "reference"])
+    ap.add_argument("--model", default="qwen2.5-7b", choices=["qwen2.5-7b", "qwen3-0.6b", "qwen2.5-0.5b"])
+    ap.add_argument("--context", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-reps", type=int, default=3)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from __graft_entry__ import build
+    build()
+    import q8_block_quantized_matvec_gb300 as q8d
+    import synth
+    from q8_block_quantized_matvec_gb300.device import DeviceStep
+
+    shape = synth.MODELS[args.model]
+    ctx = args.context
+    cap = ctx + args.warmup + 2 * args.steps + 64
+    wts = synth.TorchStepWeights(shape, seed=rank)
+    kdt = torch.float16 if shape.kv_dtype == synth.KV_F16 else torch.float32
+    caches = []
+    for li in range(shape.n_layers):
+        kc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
+        vc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
+        kc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.kprefix", (ctx - 1, shape.kv_width), kdt)
+        vc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.vprefix", (ctx - 1, shape.kv_width), kdt)
+        caches.append((kc, vc))
+    stream = torch.cuda.Stream()
+    ds = DeviceStep(wts, cap, caches, stream=stream)
+    torch.cuda.synchronize()
+    kernels_per_step = ds.kernel_count()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-timed steps (inputs resident) ----
+    with torch.cuda.stream(stream):
+        ds.set_state(17, ctx - 1)
+        for _ in range(args.warmup):
+            ds.launch(stream)
+        ds.set_state(17, ctx - 1)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index()) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            ds.launch(stream)
+        e1.record(stream)
+        barrier()
+    t_dev = e0.elapsed_time(e1) / 1e3
+    assert ds.step.status(stream) == 0, "device error word set during the timed steps"
+    if dist:
+        tt = torch.tensor([t_dev], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_dev = float(tt.item())
+    value = world * args.steps / t_dev
+
+    # ---- end to end through the public API: H2D token+pos, graph, D2H token ----
+    h_in = torch.tensor([17, ctx - 1], dtype=torch.int32).pin_memory()
+    h_out = torch.empty(1, dtype=torch.int32).pin_memory()
+    barrier()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        h_in[1] = ctx - 1 + s
+        with torch.cuda.stream(stream):
+            ds.token.copy_(h_in[0:1], non_blocking=True)   # host -> device: token id
+            ds.pos.copy_(h_in[1:2], non_blocking=True)     # host -> device: position
+            ds.launch(stream)
+            h_out.copy_(ds.token, non_blocking=True)       # device -> host: next token id
+        stream.synchronize()
+        h_in[0] = int(h_out[0])
+    t_e2e = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": world * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 8,
+           "d2h_bytes_per_step": 4}
+
+    # ---- kernel legs: q8_matvec over the step's matrices, attention per layer ----
+    mats = []
+    for li, L in enumerate(ds.layers):
+        for nm in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            n = shape.hidden if nm not in ("wo", "wd") else (shape.q_width if nm == "wo" else shape.ffn)
+            p = {"wq": shape.q_width, "wk": shape.kv_width, "wv": shape.kv_width, "wo": shape.hidden,
+                 "wg": shape.ffn, "wu": shape.ffn, "wd": shape.hidden}[nm]
+            mats.append((L[nm], n, p))
+    mats.append((ds.lm_head, shape.hidden, shape.vocab))
+    xin = {n: synth.normal_torch(rank, f"bench.x{n}", n, torch.float32) for _, n, _ in mats}
+    yout = torch.empty(max(p for _, _, p in mats), device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in mats]
+    mv_times = []
+    for rep in range(args.kernel_reps + 1):
+        torch.cuda.synchronize()
+        for (w, n, p), (a, b) in zip(mats, ev):
+            a.record(stream)
+            q8d.q8d_matvec(xin[n], w, yout, n, p, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        if rep:
+            mv_times.append(sum(a.elapsed_time(b) for a, b in ev) / 1e3)
+    mv_time = statistics.median(mv_times)
+    mv_bytes = sum(matvec_bytes(n, p) for _, n, p in mats)
+    mv_launch_bytes = mv_bytes / len(mats)
+    mv_launch_s = mv_time / len(mats)
+    hbm, peak_kind = peaks()
+    mv_gbs = mv_bytes / mv_time / 1e9
+
+    esize = 2 if shape.kv_dtype == synth.KV_F16 else 4
+    H, Hk, D = shape.n_heads, shape.n_kv_heads, shape.head_dim
+    qv = synth.normal_torch(rank, "bench.q", H * D, torch.float32)
+    aout = torch.empty(H * D, device="cuda")
+    wsb = q8d.q8d_gqa_workspace_bytes(1, H, Hk, D, cap)
+    aws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+    aerr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    at_times = []
+    for rep in range(args.kernel_reps + 1):
+        tot = 0.0
+        for li in range(shape.n_layers):
+            flush.fill_(li & 0xFF)  # evict the previous layer's KV from L2
+            a, b = ev[0]
+            a.record(stream)
+            q8d.q8d_gqa_decode_attn(qv, None, None, caches[li][0], caches[li][1], shape.kv_dtype,
+                                    aout, 1, H, Hk, D, cap, 0, lens, 1 / math.sqrt(D), aws, wsb,
+                                    aerr, stream)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b) / 1e3
+        if rep:
+            at_times.append(tot)
+    at_time = statistics.median(at_times)
+    at_bytes_launch = attn_bytes(ctx, Hk, D, H, esize, append=False)
+    at_gbs = at_bytes_launch * shape.n_layers / at_time / 1e9
+
+    traffic = ncu_traffic("q8_rows_kernel")
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, threads, desc = oracle_sample(args.model, ctx)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_dev / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_name(args), "model_shape": shape.name,
+                       "context_first_step": ctx, "context_last_step": ctx + args.steps - 1,
+                       "weight_bytes_per_step": shape.weight_bytes(),
+                       "l2": "inputs larger than L2 (7.5 GB of weights streamed per step)"
+                       if shape.name == "qwen2.5-7b" else "weights streamed per step exceed L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "q8_rows_kernel (q8d_matvec)",
+                         "achieved": mv_launch_bytes / mv_launch_s / 1e9, "peak": hbm,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": mv_launch_bytes / mv_launch_s / 1e9 / hbm, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": mv_launch_bytes,
+                         "avg_launch_us": mv_launch_s * 1e6, "launches": len(mats)},
+            "kernels": {
+                "q8_matvec": {"GB_s": mv_gbs, "frac_of_peak": mv_gbs / hbm,
+                              "us_per_step_sum": mv_time * 1e6},
+                "gqa_decode_attn": {"GB_s": at_gbs, "frac_of_peak": at_gbs / hbm,
+                                    "us_per_layer": at_time / shape.n_layers * 1e6,
+                                    "context": ctx, "l2": "256 MB flush between layers"},
+            },
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    ds.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * q8d — Q8_0 single-token decode hot path for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer named d_* or documented as "device" is a device
+ * pointer owned by the caller (the library never frees it).  Every compute
+ * entry point is asynchronous on the CUDA stream passed as `stream`
+ * (a cudaStream_t cast to void*; NULL means the legacy default stream) and
+ * returns an int status:
+ *     0               success (work enqueued)
+ *     Q8D_EINVAL      null pointer or impossible size/shape
+ *     Q8D_EALIGN      a pointer or stride breaks the stated alignment
+ *     Q8D_EUNSUPPORTED a valid shape this build does not run
+ *                     (n % 32 != 0, head_dim not 64/128, H % Hk != 0, ...)
+ *     Q8D_ERANGE      an index/length outside its buffer (host-visible args)
+ *     Q8D_ECUDA       a CUDA call failed; q8d_last_cuda_error() has the code
+ *     Q8D_ETIMEOUT    a bounded host wait ran out
+ *     Q8D_ENOMEM      the library's own allocation failed (step create only)
+ * On any non-zero status nothing was launched.  There is no fallback path:
+ * an unsupported case is refused, never computed another way.
+ *
+ * Quantities that live in device memory (positions, lengths, token ids) are
+ * checked on the device: a bad value sets a bit in the caller's int error
+ * word (Q8D_DERR_*), the affected write is skipped and the affected outputs
+ * are set to NaN, so a silent no-write cannot pass for a result.
+ *
+ * Formats (from "IV.4: One command buffer per token", sections "Eight
+ * kernels" and "The decoder: kernels and helpers"):
+ *   Q8_0 block  34 bytes: little-endian IEEE binary16 scale (bytes 0-1) then
+ *               32 two's-complement int8 quants (bytes 2-33); value of quant
+ *               j is scale * q_j.
+ *   Q8_0 matrix [p][n], row-major, n % 32 == 0: row r is n/32 consecutive
+ *               blocks starting at byte r * (n/32) * 34 (no padding).
+ *               The base must be 16-byte aligned.
+ *   KV cache    per layer [cap][n_kv_heads * head_dim] of f32 or f16
+ *               (Q8D_KV_F32 / Q8D_KV_F16); KV head g occupies columns
+ *               [g*head_dim, (g+1)*head_dim) of every row ("minfer Metal
+ *               Backend Design" / "Metal Backend Optimizations", the
+ *               [nkv][nk*hd] layout shared with llama.cpp).
+ */
+#ifndef Q8D_H
+#define Q8D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8D_OK 0
+#define Q8D_EINVAL (-1)
+#define Q8D_EALIGN (-2)
+#define Q8D_EUNSUPPORTED (-3)
+#define Q8D_ERANGE (-4)
+#define Q8D_ECUDA (-5)
+#define Q8D_ETIMEOUT (-6)
+#define Q8D_ENOMEM (-7)
+
+#define Q8D_KV_F32 0
+#define Q8D_KV_F16 1
+
+/* Bits of the device-side error word. */
+#define Q8D_DERR_POS_RANGE 0x1   /* append position outside [0, cap)          */
+#define Q8D_DERR_LEN_RANGE 0x2   /* attended length outside [1, cap]          */
+#define Q8D_DERR_TOKEN_RANGE 0x4 /* token id outside [0, vocab)               */
+#define Q8D_DERR_WAIT 0x8        /* a bounded in-kernel wait gave up          */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int q8d_version(void);
+
+/* Static text for a status code. */
+const char* q8d_strerror(int status);
+
+/* The cudaError_t of the last Q8D_ECUDA returned on this thread (0 if none). */
+int q8d_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------
+ * q8d_matvec — Q8_0 dequantising matrix-vector product
+ * ("IV.4: One command buffer per token", "Eight kernels": q8_matvec).
+ *   out[r] = sum_{b < n/32} scale(r,b) * sum_{j < 32} q(r,b,j) * x[32b + j]
+ * x: device f32[n]; w_q8: device Q8_0 [p][n] (16-byte aligned);
+ * out: device f32[p], fully overwritten, must not overlap x or w.
+ * n % 32 == 0 (else Q8D_EUNSUPPORTED); n == 0 writes zeros; p == 0 is a
+ * no-op.  f32 accumulation; x is used as given (never quantised).
+ * ---------------------------------------------------------------------- */
+int q8d_matvec(const float* x, const void* w_q8, float* out, int n, int p, void* stream);
+
+/* ------------------------------------------------------------------------
+ * q8d_matmul_small_m — the same weight matrix applied to m activations
+ * ("Metal Backend Optimizations": the nt in [2, 8] batched-matvec gap and
+ * the quantised GEMM tier for nt >= 2).
+ *   Y[i][r] = sum_k X[i][k] * W[r][k],   i < m, r < p
+ * X: device f32, row i at X + i*ldx (ldx >= n); Y: device f32, row i at
+ * Y + i*ldy (ldy >= p), only the first p entries of each row are written.
+ * m <= 8: f32 CUDA-core path, weights read once for all m rows, f32 accuracy.
+ * m >= 9: tensor-core path (tcgen05.mma, bf16 operands from the dequantised
+ * weights and the rounded activations, f32 accumulation): relative accuracy
+ * ~2^-8 per product, i.e. within 1e-2 of sum|terms| per output.
+ * 1 <= m <= 256; n % 32 == 0.
+ * ---------------------------------------------------------------------- */
+int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m,
+                       int n, int p, void* stream);
+
+/* ------------------------------------------------------------------------
+ * q8d_kv_append — write one token's K and V rows into the caches
+ * ("IV.4: One command buffer per token", "Eight kernels": append_kv).
+ *   kcache[pos][i] = cvt(k[i]), vcache[pos][i] = cvt(v[i]), i < kv_width
+ * cvt is the identity for an f32 cache and round-to-nearest-even to binary16
+ * for an f16 cache.  pos is read from device memory (*d_pos) so a captured
+ * graph replays unchanged; pos outside [0, cap) sets Q8D_DERR_POS_RANGE in
+ * *d_err and writes nothing.  k, v: device f32[kv_width]; caches: device,
+ * [cap][kv_width]; d_err: device int (OR-ed into, never cleared).
+ * ---------------------------------------------------------------------- */
+int q8d_kv_append(const float* k, const float* v, void* kcache, void* vcache, int kv_dtype,
+                  int kv_width, int cap, const int* d_pos, int* d_err, void* stream);
+
+/* Bytes of scratch q8d_gqa_decode_attn needs for these sizes (split-K
+ * partials).  max_len is the largest length any call will see (<= cap). */
+size_t q8d_gqa_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len);
+
+/* ------------------------------------------------------------------------
+ * q8d_gqa_decode_attn — grouped-query attention of one query token per
+ * sequence over a resident KV cache, split over the context ("IV.4: One
+ * command buffer per token", "Eight kernels": attention_decode; "Metal
+ * Backend Optimizations" 3.3, split-attention partial + combine).
+ * For sequence s with length L = d_lens[s] (read on the device) and query
+ * head h, KV head g = h / (n_heads / n_kv_heads):
+ *   s_t = scale * q[s,h,:] . K[s][t][g*hd : (g+1)*hd],   t < L
+ *   out[s,h,:] = sum_t softmax(s)_t * V[s][t][g*hd : (g+1)*hd]
+ * If k_new/v_new are non-NULL, row L-1 of sequence s is first written with
+ * cvt(k_new[s]), cvt(v_new[s]) (as q8d_kv_append) and the rounded values
+ * are the ones attended to.
+ *   q, out:  device f32 [batch][n_heads*head_dim]
+ *   k_new, v_new: device f32 [batch][n_kv_heads*head_dim] or both NULL
+ *   kcache, vcache: device; sequence s's cache starts at element
+ *            s*cache_batch_stride, rows of n_kv_heads*head_dim elements,
+ *            16-byte aligned, cap rows
+ *   d_lens:  device int[batch]; 1 <= L <= cap, else Q8D_DERR_LEN_RANGE is
+ *            set in *d_err and that sequence's outputs are NaN
+ *   workspace: device scratch of at least
+ *            q8d_gqa_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, cap)
+ *            bytes (contents need no initialisation)
+ * head_dim in {64, 128}; n_heads % n_kv_heads == 0; n_heads/n_kv_heads <= 16.
+ * ---------------------------------------------------------------------- */
+int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, void* kcache,
+                        void* vcache, int kv_dtype, float* out, int batch, int n_heads,
+                        int n_kv_heads, int head_dim, int cap, long long cache_batch_stride,
+                        const int* d_lens, float scale, void* workspace, size_t ws_bytes,
+                        int* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Decode step graph ("IV.4: One command buffer per token", "One command
+ * buffer": the whole step encoded once and submitted as one unit).
+ * The step, per layer: RMSNorm -> q/k/v Q8_0 matvecs -> (q/k/v bias) ->
+ * (per-head q/k RMSNorm) -> RoPE(q, k) -> KV append -> attention -> o
+ * matvec -> residual add -> RMSNorm -> gate/up matvecs -> SiLU(gate)*up ->
+ * down matvec -> residual add; then final RMSNorm -> lm_head -> argmax.
+ * The token id and position are read from device memory at replay time,
+ * the argmax is written back as the next token and the position advanced,
+ * so consecutive launches decode consecutive tokens with no host work.
+ * All pointers in the descriptors are device pointers owned by the caller
+ * and must stay valid until q8d_step_destroy.
+ * ---------------------------------------------------------------------- */
+typedef struct q8d_layer_desc {
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd; /* Q8_0: [H*hd][hidden], [Hk*hd][hidden] x2,
+                                                   [hidden][H*hd], [ffn][hidden] x2,
+                                                   [hidden][ffn]                          */
+  const float *attn_norm, *ffn_norm;            /* f32 [hidden]                           */
+  const float *q_norm, *k_norm;                 /* f32 [head_dim] (qk_norm) or NULL       */
+  const float *bq, *bk, *bv;                    /* f32 biases (qkv_bias) or NULL          */
+  void *kcache, *vcache;                        /* [cap][Hk*hd] of kv_dtype               */
+} q8d_layer_desc;
+
+typedef struct q8d_step_desc {
+  int hidden, n_layers, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int qk_norm;  /* 1: Qwen3-style per-head RMSNorm of q and k after projection */
+  int qkv_bias; /* 1: Qwen2-style bias add on q, k, v                          */
+  int kv_dtype; /* Q8D_KV_F32 or Q8D_KV_F16                                    */
+  int cap;      /* rows of every KV cache                                      */
+  float rms_eps, rope_theta;
+  const void* embed;      /* Q8_0 [vocab][hidden]                 */
+  const float* out_norm;  /* f32 [hidden]                         */
+  const void* lm_head;    /* Q8_0 [vocab][hidden]                 */
+  const q8d_layer_desc* layers; /* host array of n_layers (copied at create) */
+  int* d_token;           /* device int: input token; receives the argmax     */
+  int* d_pos;             /* device int: position of the input token; +1 after */
+  int* d_err;             /* device int error word (OR-ed into)               */
+  float* d_logits;        /* device f32 [vocab] or NULL (library-owned then)  */
+} q8d_step_desc;
+
+typedef struct q8d_step q8d_step;
+
+/* Builds the step: allocates its activation workspace (the only allocation
+ * the library makes), prepares per-step tables with kernels on `stream`,
+ * captures the step into a CUDA graph and instantiates it.  Synchronises
+ * `stream`. */
+int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out);
+
+/* Enqueues one decode step (one graph launch) on `stream`. */
+int q8d_step_launch(q8d_step* step, void* stream);
+
+/* Copies the step's device error word into *err (synchronous; waits for
+ * work already enqueued on `stream`, polling with a time limit of
+ * timeout_ms milliseconds, <= 0 meaning 10 s).  Returns Q8D_ETIMEOUT if the
+ * limit ran out. */
+int q8d_step_status(q8d_step* step, void* stream, int timeout_ms, int* err);
+
+/* Number of kernel nodes one launch runs. */
+int q8d_step_kernel_count(const q8d_step* step);
+
+/* Device pointer of the step's logits buffer (f32 [vocab]). */
+float* q8d_step_logits(q8d_step* step);
+
+/* Releases the graph and the workspace (not the caller's buffers). */
+void q8d_step_destroy(q8d_step* step);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q8D_H */

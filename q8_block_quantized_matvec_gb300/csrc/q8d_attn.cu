@@ -1,0 +1,430 @@
+// KV append and grouped-query decode attention with split-K (sm_103a).
+//
+// Semantics ("IV.4: One command buffer per token", "Eight kernels":
+// append_kv and attention_decode): query head h attends with KV head
+// h / (H/Hk) over the first L cached rows; softmax(scale * q.K) weights V.
+//
+// Design for GB300 (the pages' kernel keeps one threadgroup per query head
+// and the whole score row in 16 KB of threadgroup memory, capped at 4096
+// positions; "Metal Backend Optimizations" 3.3 replaces it with a split
+// pass plus a combine):
+//  * One CTA per (sequence, KV head, context chunk).  It serves all G query
+//    heads of its KV head, so each K/V byte is read from HBM exactly once.
+//  * The chunk layout is derived on the device from the length in device
+//    memory (chunk = max(128, ceil(L / NC)) rows, NC fixed at launch), so a
+//    captured graph replays at any length; CTAs past the last chunk exit.
+//  * K/V rows (one KV head's head_dim slice: 128-256 bytes) stream into a
+//    two-stage shared-memory ring with 1-D cp.async.bulk copies completing
+//    on an mbarrier; K rows are padded by 16 bytes so the per-token score
+//    loop reads shared memory without bank conflicts.
+//  * Online softmax in the log2 domain (scores pre-scaled by log2 e), packed
+//    f32x2 FMAs for P.V, partials {m, l, O} per (query head, chunk) in the
+//    workspace; a second kernel merges them in chunk order (deterministic).
+//  * The append of row L-1 happens inside the CTA owning that row: it writes
+//    the rounded row to the cache, fences the async proxy and then streams
+//    it like any other row, so the attended values are exactly the cached.
+#include <algorithm>
+#include <cmath>
+
+#include "q8d_attn.cuh"
+#include "q8d_internal.cuh"
+
+namespace q8d {
+
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kMinChunk = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename KT>
+__device__ __forceinline__ KT to_cache(float v);
+template <>
+__device__ __forceinline__ __half to_cache<__half>(float v) {
+  return __float2half_rn(v);
+}
+template <>
+__device__ __forceinline__ float to_cache<float>(float v) {
+  return v;
+}
+
+// Converts 16 bytes of cache elements into floats.
+template <typename KT>
+struct Vec16;
+template <>
+struct Vec16<__half> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = u.x;
+    f[1] = u.y;
+    f[2] = u.z;
+    f[3] = u.w;
+  }
+};
+
+__device__ __forceinline__ int chunk_rows(int L, int nc) {
+  return max(kMinChunk, (L + nc - 1) / nc);
+}
+
+template <int D, typename KT, int GMAX>
+struct AttnCfg {
+  static constexpr int kRowBytes = D * (int)sizeof(KT);
+  static constexpr int kTS = 16384 / kRowBytes;            // tokens per sub-tile
+  static constexpr int kKStride = kRowBytes + 16;          // padded K row
+  static constexpr int kTPT = kAttnThreads / kTS;          // threads per token (scores)
+  static constexpr int kEPT = D / kTPT;                    // elements per thread (scores)
+  static constexpr int kPairs = D / 2;                     // output column pairs
+  static constexpr int kTG = kAttnThreads / kPairs;        // token groups (P.V)
+  static constexpr int kStageBytes = kTS * kKStride + kTS * kRowBytes;
+  // shared memory carve-up (bytes)
+  static constexpr int kOffStage = 0;
+  static constexpr int kOffQ = kOffStage + 2 * kStageBytes;
+  static constexpr int kOffS = kOffQ + GMAX * D * 4;              // scores [TPT][TS][GMAX]
+  static constexpr int kOffMisc = kOffS + kTPT * kTS * GMAX * 4;  // m, l, corr [3][GMAX]
+  static constexpr int kOffBar = kOffMisc + 3 * GMAX * 4;
+  static constexpr int kSmem = kOffBar + 2 * 8;
+  static_assert(kTS * kTPT == kAttnThreads, "token mapping");
+  static_assert(kPairs * kTG == kAttnThreads, "column mapping");
+  static_assert((kTG * GMAX * D * 4) <= 2 * kStageBytes, "reduction buffer fits the stages");
+};
+
+template <int D, typename KT, int GMAX>
+__global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParams P) {
+  using C = AttnCfg<D, KT, GMAX>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
+  float* sp = reinterpret_cast<float*>(smem + C::kOffS);
+  float* m_run = reinterpret_cast<float*>(smem + C::kOffMisc);
+  float* l_run = m_run + GMAX;
+  float* corr = l_run + GMAX;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = P.n_heads / P.n_kv_heads;
+  const int L = P.d_lens[b];
+  if (L < 1 || L > P.cap) {
+    if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
+    return;
+  }
+  const int tpc = chunk_rows(L, P.nc);
+  const int t_begin = c * tpc;
+  if (t_begin >= L) return;
+  const int t_end = min(L, t_begin + tpc);
+  const long long kvw = (long long)P.n_kv_heads * D;
+  KT* kbase = reinterpret_cast<KT*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
+  KT* vbase = reinterpret_cast<KT*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
+
+  // In-kernel append of row L-1 by the CTA that owns it.
+  if (P.k_new != nullptr && t_end == L) {
+    const float* kn = P.k_new + (long long)b * kvw + (long long)g * D;
+    const float* vn = P.v_new + (long long)b * kvw + (long long)g * D;
+    for (int j = tid; j < D; j += kAttnThreads) {
+      kbase[(long long)(L - 1) * kvw + j] = to_cache<KT>(kn[j]);
+      vbase[(long long)(L - 1) * kvw + j] = to_cache<KT>(vn[j]);
+    }
+    fence_proxy_async_global();
+  }
+
+  // Query rows of the group, pre-scaled into the log2 domain.
+  const float qscale = P.scale * kLog2e;
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    const int hh = e / D, j = e % D;
+    qs[hh * D + j] = P.q[((long long)b * P.n_heads + (long long)g * G + hh) * D + j] * qscale;
+  }
+  if (tid < GMAX) {
+    m_run[tid] = -INFINITY;
+    l_run[tid] = 0.f;
+  }
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const uint64_t pol = policy_evict_first();
+  const int n_sub = (t_end - t_begin + C::kTS - 1) / C::kTS;
+  auto issue = [&](int k) {  // warp 0 only
+    if (k >= n_sub) return;
+    const int r0 = t_begin + k * C::kTS;
+    const int nr = min(C::kTS, t_end - r0);
+    uint8_t* st = smem + C::kOffStage + (k & 1) * C::kStageBytes;
+    if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)(2 * nr * C::kRowBytes));
+    __syncwarp();
+    for (int r = lane; r < nr; r += 32) {
+      const long long row = (long long)(r0 + r) * kvw;
+      bulk_g2s(st + r * C::kKStride, kbase + row, C::kRowBytes, &bar[k & 1], pol);
+      bulk_g2s(st + C::kTS * C::kKStride + r * C::kRowBytes, vbase + row, C::kRowBytes,
+               &bar[k & 1], pol);
+    }
+  };
+  if (warp == 0) {
+    issue(0);
+    issue(1);
+  }
+
+  // P.V accumulators: column pair `pair`, tokens t % kTG == tg.
+  const int pair = tid % C::kPairs, tg = tid / C::kPairs;
+  uint64_t acc2[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) acc2[h] = pack2(0.f, 0.f);
+
+  // Score mapping: token st_tok of the sub-tile, element slice st_part.
+  // Slices are spread over warps (st_part uniform within a warp) so that the
+  // K reads of a quarter-warp hit distinct banks and the q reads broadcast.
+  const int st_tok = tid % C::kTS, st_part = tid / C::kTS;
+
+  for (int k = 0; k < n_sub; ++k) {
+    const int r0 = t_begin + k * C::kTS;
+    const int nr = min(C::kTS, t_end - r0);
+    const bool ok = mbar_wait(&bar[k & 1], (uint32_t)(k >> 1) & 1u);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+      return;
+    }
+    const uint8_t* st = smem + C::kOffStage + (k & 1) * C::kStageBytes;
+
+    // ---- partial scores s[part][t][h] = q_h . K_t over one slice (log2 domain) ----
+    {
+      float acc[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+      const uint8_t* krow = st + st_tok * C::kKStride + st_part * C::kEPT * (int)sizeof(KT);
+      const float* qp = qs + st_part * C::kEPT;
+#pragma unroll 2
+      for (int e = 0; e < C::kEPT; e += Vec16<KT>::N) {
+        float kf[Vec16<KT>::N];
+        Vec16<KT>::load(krow + e * sizeof(KT), kf);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          if (h < G) {
+#pragma unroll
+            for (int u = 0; u < Vec16<KT>::N; u += 4) {
+              const float4 qv = *reinterpret_cast<const float4*>(qp + h * D + e + u);
+              acc[h] = fmaf(qv.x, kf[u], acc[h]);
+              acc[h] = fmaf(qv.y, kf[u + 1], acc[h]);
+              acc[h] = fmaf(qv.z, kf[u + 2], acc[h]);
+              acc[h] = fmaf(qv.w, kf[u + 3], acc[h]);
+            }
+          }
+        }
+      }
+      float* spp = sp + (st_part * C::kTS + st_tok) * GMAX;
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+        if (h < G) spp[h] = acc[h];
+    }
+    __syncthreads();
+
+    // ---- online softmax update, one warp per head ----
+    for (int h = warp; h < G; h += kAttnThreads / 32) {
+      // total score of token t: the kTPT slice partials, added in slice order
+      float mx = -INFINITY;
+      for (int t = lane; t < nr; t += 32) {
+        float sc = sp[t * GMAX + h];
+#pragma unroll
+        for (int q = 1; q < C::kTPT; ++q) sc += sp[(q * C::kTS + t) * GMAX + h];
+        sp[t * GMAX + h] = sc;
+        mx = fmaxf(mx, sc);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_old = m_run[h];
+      const float m_new = fmaxf(m_old, mx);
+      float sum = 0.f;
+      for (int t = lane; t < C::kTS; t += 32) {
+        const float pt = (t < nr) ? exp2f(sp[t * GMAX + h] - m_new) : 0.f;
+        sp[t * GMAX + h] = pt;
+        sum += pt;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) {
+        const float cf = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+        corr[h] = cf;
+        l_run[h] = l_run[h] * cf + sum;
+        m_run[h] = m_new;
+      }
+    }
+    __syncthreads();
+
+    // ---- O_h = corr_h * O_h + sum_t p[t][h] * V_t ----
+    {
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+        if (h < G) acc2[h] = fma2(acc2[h], pack2(corr[h], corr[h]), pack2(0.f, 0.f));
+      const uint8_t* vt = st + C::kTS * C::kKStride;
+      for (int t = tg; t < nr; t += C::kTG) {
+        float v0, v1;
+        if constexpr (sizeof(KT) == 2) {
+          const float2 f = __half22float2(
+              *reinterpret_cast<const __half2*>(vt + t * C::kRowBytes + pair * 4));
+          v0 = f.x;
+          v1 = f.y;
+        } else {
+          const float2 f = *reinterpret_cast<const float2*>(vt + t * C::kRowBytes + pair * 8);
+          v0 = f.x;
+          v1 = f.y;
+        }
+        const uint64_t v2 = pack2(v0, v1);
+        const float* pr = sp + t * GMAX;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+          if (h < G) acc2[h] = fma2(v2, pack2(pr[h], pr[h]), acc2[h]);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) issue(k + 2);
+  }
+
+  // ---- reduce token groups, write the partial {m, l, O} ----
+  float* red = reinterpret_cast<float*>(smem + C::kOffStage);  // stages are idle now
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    if (h < G) {
+      float lo, hi;
+      unpack2(acc2[h], lo, hi);
+      red[(tg * GMAX + h) * D + 2 * pair] = lo;
+      red[(tg * GMAX + h) * D + 2 * pair + 1] = hi;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    const int h = e / D, j = e % D;
+    float s = 0.f;
+    for (int q = 0; q < C::kTG; ++q) s += red[(q * GMAX + h) * D + j];
+    const long long hq = (long long)b * P.n_heads + (long long)g * G + h;
+    P.ws_o[(hq * P.nc + c) * D + j] = s;
+    if (j == 0) {
+      P.ws_m[hq * P.nc + c] = m_run[h];
+      P.ws_l[hq * P.nc + c] = l_run[h];
+    }
+  }
+}
+
+template <int D>
+__global__ void gqa_combine_kernel(const AttnParams P) {
+  const int hq = blockIdx.x;  // b * H + h
+  const int b = hq / P.n_heads;
+  const int j = threadIdx.x;
+  const int L = P.d_lens[b];
+  float* o = P.out + (long long)hq * D;
+  if (L < 1 || L > P.cap) {
+    o[j] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int tpc = chunk_rows(L, P.nc);
+  const int nact = (L + tpc - 1) / tpc;
+  const float* M = P.ws_m + (long long)hq * P.nc;
+  const float* S = P.ws_l + (long long)hq * P.nc;
+  const float* O = P.ws_o + (long long)hq * P.nc * D;
+  float mx = -INFINITY;
+  for (int c = 0; c < nact; ++c) mx = fmaxf(mx, M[c]);
+  float s = 0.f, acc = 0.f;
+  for (int c = 0; c < nact; ++c) {
+    const float w = (M[c] == -INFINITY) ? 0.f : exp2f(M[c] - mx);
+    s = fmaf(S[c], w, s);
+    acc = fmaf(O[(long long)c * D + j], w, acc);
+  }
+  o[j] = acc / s;
+}
+
+template <typename KT>
+__global__ void kv_append_kernel(const float* k, const float* v, KT* kc, KT* vc, int kvw, int cap,
+                                 const int* d_pos, int* d_err) {
+  const int pos = *d_pos;
+  if (pos < 0 || pos >= cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && d_err) atomicOr(d_err, Q8D_DERR_POS_RANGE);
+    return;
+  }
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < kvw; i += gridDim.x * blockDim.x) {
+    kc[(long long)pos * kvw + i] = to_cache<KT>(k[i]);
+    vc[(long long)pos * kvw + i] = to_cache<KT>(v[i]);
+  }
+}
+
+template <int D, typename KT, int GMAX>
+int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
+  using C = AttnCfg<D, KT, GMAX>;
+  auto fn = gqa_split_kernel<D, KT, GMAX>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return record_cuda(e);
+    configured[dev] = true;
+  }
+  dim3 grid(P.nc, P.n_kv_heads, P.batch);
+  fn<<<grid, kAttnThreads, C::kSmem, stream>>>(P);
+  int rc = check_launch();
+  if (rc) return rc;
+  gqa_combine_kernel<D><<<P.batch * P.n_heads, D, 0, stream>>>(P);
+  return check_launch();
+}
+
+template <int D, typename KT>
+int launch_attn_g(const AttnParams& P, cudaStream_t stream) {
+  const int G = P.n_heads / P.n_kv_heads;
+  if (G <= 2) return launch_attn_t<D, KT, 2>(P, stream);
+  if (G <= 4) return launch_attn_t<D, KT, 4>(P, stream);
+  if (G <= 8) return launch_attn_t<D, KT, 8>(P, stream);
+  return launch_attn_t<D, KT, 16>(P, stream);
+}
+
+}  // namespace
+
+int attn_chunks(int batch, int n_kv_heads, int max_len) {
+  const int target = 4 * sm_count();
+  int nc = (target + batch * n_kv_heads - 1) / (batch * n_kv_heads);
+  const int cap_nc = (std::max(max_len, 1) + kMinChunk - 1) / kMinChunk;
+  return std::max(1, std::min(nc, cap_nc));
+}
+
+size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len) {
+  const size_t nc = (size_t)attn_chunks(batch, n_kv_heads, max_len);
+  return (size_t)batch * n_heads * nc * ((size_t)head_dim + 2) * sizeof(float);
+}
+
+int attn_launch(AttnParams P, cudaStream_t stream) {
+  const size_t nc = (size_t)P.nc;
+  float* ws = reinterpret_cast<float*>(P.workspace);
+  P.ws_o = ws;
+  P.ws_m = ws + (size_t)P.batch * P.n_heads * nc * P.head_dim;
+  P.ws_l = P.ws_m + (size_t)P.batch * P.n_heads * nc;
+  if (P.head_dim == 128)
+    return P.kv_dtype == Q8D_KV_F16 ? launch_attn_g<128, __half>(P, stream)
+                                    : launch_attn_g<128, float>(P, stream);
+  return P.kv_dtype == Q8D_KV_F16 ? launch_attn_g<64, __half>(P, stream)
+                                  : launch_attn_g<64, float>(P, stream);
+}
+
+int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,
+                     int cap, const int* d_pos, int* d_err, cudaStream_t stream) {
+  const int threads = 256, blocks = std::max(1, std::min(64, (kvw + threads - 1) / threads));
+  if (kv_dtype == Q8D_KV_F16)
+    kv_append_kernel<__half><<<blocks, threads, 0, stream>>>(
+        k, v, reinterpret_cast<__half*>(kc), reinterpret_cast<__half*>(vc), kvw, cap, d_pos, d_err);
+  else
+    kv_append_kernel<float><<<blocks, threads, 0, stream>>>(
+        k, v, reinterpret_cast<float*>(kc), reinterpret_cast<float*>(vc), kvw, cap, d_pos, d_err);
+  return check_launch();
+}
+
+}  // namespace q8d

@@ -1,0 +1,35 @@
+// Parameters of the KV-append and split-K decode-attention kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace q8d {
+
+struct AttnParams {
+  const float* q;       // [batch][H*D]
+  const float* k_new;   // [batch][Hk*D] or nullptr
+  const float* v_new;
+  void* kcache;         // sequence b at element b*batch_stride, rows of Hk*D
+  void* vcache;
+  int kv_dtype;
+  float* out;           // [batch][H*D]
+  int batch, n_heads, n_kv_heads, head_dim, cap;
+  long long batch_stride;
+  const int* d_lens;    // [batch]
+  float scale;
+  void* workspace;
+  int nc;               // context chunks per (sequence, KV head)
+  int* d_err;
+  // carved from the workspace by attn_launch
+  float* ws_o;
+  float* ws_m;
+  float* ws_l;
+};
+
+int attn_chunks(int batch, int n_kv_heads, int max_len);
+size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len);
+int attn_launch(AttnParams P, cudaStream_t stream);
+int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,
+                     int cap, const int* d_pos, int* d_err, cudaStream_t stream);
+
+}  // namespace q8d

@@ -1,0 +1,37 @@
+// Parameters of the CUDA-core Q8_0 row kernels (matvec, small-M, and the
+// multi-matrix launches the decode step uses).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q8d {
+
+// One Q8_0 matrix [p][n]; several matrices that read the same activations
+// (q|k|v, gate|up) are processed by one launch.
+struct RowSeg {
+  const uint8_t* w;  // block stream, 16-byte aligned
+  float* y;          // output row 0; row i of the output at y + i*ldy
+  int p;             // output rows
+  int tile_begin;    // filled by the planner
+};
+
+struct RowsParams {
+  RowSeg seg[3];
+  int nseg;
+  int n;               // input dim (multiple of 32)
+  const float* X;      // activations, row i at X + i*ldx, 16-byte aligned
+  int ldx;
+  int ldy;
+  int m;               // activation rows (1 = matvec)
+  int accumulate;      // 1: Y += result (residual add), 0: Y = result
+  int* d_err;          // device error word or nullptr
+  // filled by the planner
+  int bpr;
+  long long row_bytes;
+  int rows_per_tile, total_tiles, stage_bytes, nstages, segs_per_row;
+};
+
+// Plans tiles/stages and launches the kernel on `stream`.  Returns a status.
+int rows_plan_and_launch(RowsParams P, cudaStream_t stream);
+
+}  // namespace q8d

@@ -173,8 +173,9 @@ MODELS = {m.name: m for m in (QWEN3_0_6B, QWEN25_0_5B, QWEN25_7B)}
 
 
 def tiny_shape(n_layers: int = 2) -> ModelShape:
-    """A small step of the same structure for fast tests (several tiles,
-    ragged tails: hidden 96 is 3 blocks, head_dim 64, GQA group 3)."""
+    """A small step of the same structure for fast tests: hidden 192 (6
+    blocks), ffn 352 (11 blocks, so down-projection rows are only 2-byte
+    aligned), head_dim 64, GQA group 3, both QK-norm and q/k/v biases."""
     return ModelShape("tiny", 192, n_layers, 6, 2, 64, 352, 1000,
                       qk_norm=True, qkv_bias=True, kv_dtype=KV_F16)
 
@@ -190,15 +191,28 @@ class StepWeights:
 
 
 def step_weights(shape: ModelShape, seed: int = 0) -> StepWeights:
+    """Draws every tensor (matrices in parallel threads; each has its own
+    stream, so the values do not depend on the thread count)."""
+    import concurrent.futures as cf
+    import os
     s = shape
+    jobs = {}
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        for li in range(s.n_layers):
+            for nm, n, p in [("wq", s.hidden, s.q_width), ("wk", s.hidden, s.kv_width),
+                             ("wv", s.hidden, s.kv_width), ("wo", s.q_width, s.hidden),
+                             ("wg", s.hidden, s.ffn), ("wu", s.hidden, s.ffn),
+                             ("wd", s.ffn, s.hidden)]:
+                jobs[(li, nm)] = ex.submit(q8_matrix, seed, f"l{li}.{nm}", p, n)
+        fe = ex.submit(q8_matrix, seed, "embed", s.vocab, s.hidden)
+        fl = ex.submit(q8_matrix, seed, "lm_head", s.vocab, s.hidden)
+        mats = {k: f.result() for k, f in jobs.items()}
+        embed, lm_head = fe.result(), fl.result()
     layers = []
     for li in range(s.n_layers):
         L = {}
-        for nm, n, p in [("wq", s.hidden, s.q_width), ("wk", s.hidden, s.kv_width),
-                         ("wv", s.hidden, s.kv_width), ("wo", s.q_width, s.hidden),
-                         ("wg", s.hidden, s.ffn), ("wu", s.hidden, s.ffn),
-                         ("wd", s.ffn, s.hidden)]:
-            L[nm] = q8_matrix(seed, f"l{li}.{nm}", p, n)
+        for nm in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            L[nm] = mats[(li, nm)]
         L["attn_norm"] = gains(seed, f"l{li}.attn_norm", s.hidden)
         L["ffn_norm"] = gains(seed, f"l{li}.ffn_norm", s.hidden)
         if s.qk_norm:
@@ -209,10 +223,8 @@ def step_weights(shape: ModelShape, seed: int = 0) -> StepWeights:
             L["bk"] = biases(seed, f"l{li}.bk", s.kv_width)
             L["bv"] = biases(seed, f"l{li}.bv", s.kv_width)
         layers.append(L)
-    return StepWeights(s, layers,
-                       embed=q8_matrix(seed, "embed", s.vocab, s.hidden),
-                       out_norm=gains(seed, "out_norm", s.hidden),
-                       lm_head=q8_matrix(seed, "lm_head", s.vocab, s.hidden))
+    return StepWeights(s, layers, embed=embed, out_norm=gains(seed, "out_norm", s.hidden),
+                       lm_head=lm_head)
 
 
 def kv_prefix(shape: ModelShape, seed: int, layer: int, cap: int, rows: int):
@@ -226,3 +238,67 @@ def kv_prefix(shape: ModelShape, seed: int, layer: int, cap: int, rows: int):
         kc[:rows] = stream(seed, f"l{layer}.kprefix").standard_normal((rows, shape.kv_width)).astype(dt)
         vc[:rows] = stream(seed, f"l{layer}.vprefix").standard_normal((rows, shape.kv_width)).astype(dt)
     return kc, vc
+
+
+# ---------------------------------------------------------------------------
+# Device-side generation (same distributions, torch's generator) for
+# workloads too large to draw on the host in reasonable time.  Values differ
+# from the numpy streams above; they are used where no oracle comparison of
+# the exact values is made (throughput runs).
+# ---------------------------------------------------------------------------
+
+def _torch_gen(seed: int, name: str, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(((int(seed) & 0xFFFFFFFF) << 32) ^ zlib.crc32(name.encode()))
+    return g
+
+
+def q8_matrix_torch(seed: int, name: str, p: int, n: int, device="cuda", scale_lo: float = 1e-3,
+                    scale_hi: float = 2e-2):
+    import torch
+    g = _torch_gen(seed, name, device)
+    bpr = n // QBLOCK
+    out = torch.empty((p, bpr, QBLOCK_BYTES), dtype=torch.uint8, device=device)
+    q = torch.randint(-127, 128, (p, bpr, QBLOCK), dtype=torch.int8, device=device, generator=g)
+    out[:, :, 2:] = q.view(torch.uint8)
+    del q
+    s = torch.rand((p, bpr), dtype=torch.float32, device=device, generator=g)
+    s = (s * (scale_hi - scale_lo) + scale_lo).to(torch.float16)
+    out[:, :, 0:2] = s.view(torch.uint8).view(p, bpr, 2)
+    return out.view(p, bpr * QBLOCK_BYTES)
+
+
+def normal_torch(seed: int, name: str, shape, dtype, device="cuda"):
+    import torch
+    g = _torch_gen(seed, name, device)
+    return torch.randn(shape, dtype=torch.float32, device=device, generator=g).to(dtype)
+
+
+class TorchStepWeights:
+    """Same fields as StepWeights, holding device tensors drawn on the GPU."""
+
+    def __init__(self, shape: ModelShape, seed: int = 0, device="cuda"):
+        import torch
+        s = shape
+        self.shape = s
+        self.layers = []
+        for li in range(s.n_layers):
+            L = {}
+            for nm, n, p in [("wq", s.hidden, s.q_width), ("wk", s.hidden, s.kv_width),
+                             ("wv", s.hidden, s.kv_width), ("wo", s.q_width, s.hidden),
+                             ("wg", s.hidden, s.ffn), ("wu", s.hidden, s.ffn),
+                             ("wd", s.ffn, s.hidden)]:
+                L[nm] = q8_matrix_torch(seed, f"l{li}.{nm}", p, n, device)
+            for nm, n in [("attn_norm", s.hidden), ("ffn_norm", s.hidden)]:
+                L[nm] = 1.0 + 0.1 * normal_torch(seed, f"l{li}.{nm}", n, torch.float32, device)
+            if s.qk_norm:
+                for nm in ("q_norm", "k_norm"):
+                    L[nm] = 1.0 + 0.1 * normal_torch(seed, f"l{li}.{nm}", s.head_dim, torch.float32, device)
+            if s.qkv_bias:
+                for nm, n in [("bq", s.q_width), ("bk", s.kv_width), ("bv", s.kv_width)]:
+                    L[nm] = 0.1 * normal_torch(seed, f"l{li}.{nm}", n, torch.float32, device)
+            self.layers.append(L)
+        self.embed = q8_matrix_torch(seed, "embed", s.vocab, s.hidden, device)
+        self.out_norm = 1.0 + 0.1 * normal_torch(seed, "out_norm", s.hidden, torch.float32, device)
+        self.lm_head = q8_matrix_torch(seed, "lm_head", s.vocab, s.hidden, device)

@@ -18,3 +18,22 @@ def orc():
     from oracle import oracle as o
     o.build()
     return o
+
+
+@pytest.fixture(scope="session")
+def q8d():
+    """The CUDA library binding, built in-tree; GPU tests only."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from q8_block_quantized_matvec_gb300 import build
+    build.build()
+    import q8_block_quantized_matvec_gb300 as m
+    m.lib()
+    return m
+
+
+def dev(a):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()

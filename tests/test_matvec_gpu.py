@@ -1,0 +1,163 @@
+"""q8d_matvec and q8d_matmul_small_m (CUDA, through the C ABI) against the
+oracle.  Bar: |gpu - oracle| <= 1e-5 * sum|terms| per output (f32 path),
+1e-2 * sum|terms| for the bf16 tensor-core path (m >= 9); exact where the
+result is an exact integer or a single product."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+TOL_BF16 = 1e-2
+
+
+def gpu_matvec(q8d, w, x, n, p, canary=True):
+    wd, xd = dev(w), dev(x)
+    pad = 64
+    buf = torch.full((p + 2 * pad,), float("nan"), device="cuda")
+    out = buf[pad:pad + p]
+    q8d.q8d_matvec(xd, wd, out, n, p)
+    torch.cuda.synchronize()
+    if canary:
+        assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + p:]).all(), "wrote outside out"
+    return out.cpu().numpy()
+
+
+SHAPES = [(32, 1), (64, 3), (96, 50), (896, 33), (896, 137), (1024, 3072), (1024, 1),
+          (2048, 101), (3072, 77), (3584, 300), (4864, 200), (18944, 67), (160, 999)]
+
+
+@pytest.mark.parametrize("n,p", SHAPES)
+def test_matvec_parity(q8d, orc, n, p):
+    w = synth.q8_matrix(0, f"w{n}x{p}", p, n)
+    x = synth.normal_f32(0, f"x{n}", n)
+    ref, ab = orc.q8_matvec(w, x, n, p)
+    got = gpu_matvec(q8d, w, x, n, p)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= TOL * ab), (err / ab).max()
+
+
+def test_matvec_config0_deterministic(q8d, orc):
+    n, p = 1024, 3072
+    w = synth.q8_matrix(0, "config0.w", p, n)
+    x = synth.normal_f32(0, "config0.x", n)
+    a = gpu_matvec(q8d, w, x, n, p)
+    b = gpu_matvec(q8d, w, x, n, p)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    ref, ab = orc.q8_matvec(w, x, n, p)
+    assert np.all(np.abs(a - ref) <= TOL * ab)
+
+
+@pytest.mark.parametrize("n,p", [(32, 5), (3584, 64), (18944, 9), (896, 31)])
+def test_matvec_exact_integer_sums(q8d, n, p):
+    w = synth.q8_from_parts(5, "w", p, n, 0x3C00)
+    q = w.reshape(p, n // 32, 34)[:, :, 2:].view(np.int8).astype(np.int64).reshape(p, n)
+    got = gpu_matvec(q8d, w, np.ones(n, np.float32), n, p)
+    assert np.array_equal(got.astype(np.int64), q.sum(axis=1))
+
+
+def test_matvec_sum_of_x(q8d):
+    n, p = 3584, 5
+    w = synth.q8_const_matrix(p, n, 0x3C00, 1)
+    x = synth.normal_f32(1, "x", n)
+    got = gpu_matvec(q8d, w, x, n, p)
+    assert np.all(np.abs(got - np.sum(x, dtype=np.float64)) <= TOL * np.abs(x).sum())
+
+
+def test_matvec_one_hot(q8d):
+    n, p = 128, 7
+    w = synth.q8_matrix(9, "w", p, n)
+    blk = w.reshape(p, n // 32, 34)
+    sc = blk[:, :, 0:2].copy().view("<f2").astype(np.float32).reshape(p, n // 32)
+    q = blk[:, :, 2:].view(np.int8).astype(np.float32).reshape(p, n)
+    for j in range(n):
+        x = np.zeros(n, np.float32)
+        x[j] = 1.0
+        assert np.array_equal(gpu_matvec(q8d, w, x, n, p, canary=False), sc[:, j // 32] * q[:, j]), j
+
+
+def test_matvec_minus_128(q8d):
+    n, p = 64, 3
+    w = synth.q8_const_matrix(p, n, 0x3C00, -128)
+    assert np.array_equal(gpu_matvec(q8d, w, np.ones(n, np.float32), n, p), np.full(p, -8192.0, np.float32))
+
+
+def test_matvec_empty(q8d):
+    out = torch.full((5,), 3.0, device="cuda")
+    q8d.q8d_matvec(torch.zeros(4, device="cuda"), torch.zeros(16, dtype=torch.uint8, device="cuda"),
+                   out, 0, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(out, torch.zeros(5, device="cuda"))
+    q8d.q8d_matvec(None, None, out, 64, 0)  # p == 0: nothing
+
+
+def test_matvec_control_perturbed_byte(q8d):
+    """A changed weight byte must change exactly its row (guards a vacuous gate)."""
+    n, p = 256, 9
+    w = synth.q8_matrix(3, "w", p, n)
+    x = synth.normal_f32(3, "x", n)
+    a = gpu_matvec(q8d, w, x, n, p)
+    w2 = w.copy()
+    w2[4, 34 * 3 + 7] ^= 0x11
+    b = gpu_matvec(q8d, w2, x, n, p)
+    assert a[4] != b[4] and np.array_equal(np.delete(a, 4), np.delete(b, 4))
+
+
+SEVEN_B = [("q/o", 3584, 3584), ("k/v", 3584, 512), ("gate/up", 3584, 18944), ("down", 18944, 3584),
+           ("lm_head", 3584, 152064)]
+
+
+@pytest.mark.parametrize("name,n,p", SEVEN_B)
+def test_matvec_7b_shapes_sampled(q8d, orc, name, n, p):
+    """Full 7B-shaped matrices, the launch the bench times; 257 sampled rows
+    (first, last, seeded random) checked against the oracle row by row."""
+    w = synth.q8_matrix(0, f"7b.{name}", p, n)
+    x = synth.normal_f32(0, f"7b.x{n}", n)
+    got = gpu_matvec(q8d, w, x, n, p)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, p - 1], rng.integers(0, p, 255)])).astype(np.int64)
+    ref, ab = orc.q8_matvec_rows(w, x, n, rows)
+    assert np.all(np.abs(got[rows] - ref) <= TOL * ab)
+    assert np.isfinite(got).all()
+
+
+# ---------------------------------------------------------------------------- small M
+def gpu_small_m(q8d, w, X, n, p, ldx=None, ldy=None):
+    m = X.shape[0]
+    ldx = ldx or n
+    ldy = ldy or p
+    Xp = np.zeros((m, ldx), np.float32)
+    Xp[:, :n] = X
+    Y = torch.full((m, ldy), float("nan"), device="cuda")
+    q8d.q8d_matmul_small_m(dev(Xp), ldx, dev(w), Y, ldy, m, n, p)
+    torch.cuda.synchronize()
+    Yh = Y.cpu().numpy()
+    if ldy > p:
+        assert np.isnan(Yh[:, p:]).all()
+    return Yh[:, :p]
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("n,p", [(3584, 512), (96, 50), (18944, 40), (896, 33)])
+def test_small_m_f32_parity(q8d, orc, m, n, p):
+    w = synth.q8_matrix(2, f"sm.w{n}", p, n)
+    X = synth.normal_f32(2, f"sm.X{n}.{m}", (m, n))
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    got = gpu_small_m(q8d, w, X, n, p, ldx=n + 4 * (m % 2), ldy=p + 3)
+    assert np.all(np.abs(got - ref) <= TOL * ab)
+
+
+@pytest.mark.parametrize("m", [9, 16, 64])
+@pytest.mark.parametrize("n,p", [(3584, 512), (256, 384), (18944, 128)])
+def test_small_m_tensor_parity(q8d, orc, m, n, p):
+    w = synth.q8_matrix(4, f"tc.w{n}", p, n)
+    X = synth.normal_f32(4, f"tc.X{n}.{m}", (m, n))
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    got = gpu_small_m(q8d, w, X, n, p)
+    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+    # the norm-wise error is reported, and is far inside the bar
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) < 1e-2
