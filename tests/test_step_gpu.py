@@ -30,8 +30,12 @@ def caches_close(dstep, host, kv_dtype, pos):
             got = dev_c.cpu().numpy()
             assert np.array_equal(got[:pos], ref[:pos]), "rows before pos must be untouched"
             a, b = got[pos].astype(np.float64), ref[pos].astype(np.float64)
-            tol = np.abs(b) * (2.0 ** -10 if kv_dtype == synth.KV_F16 else 1e-5) + 1e-6
-            assert np.all(np.abs(a - b) <= tol)
+            # one f16 rounding of each side plus the f32 path's error, which is
+            # relative to the row's scale (the row comes out of a norm/matvec)
+            rms = np.sqrt(np.mean(b * b))
+            tol = np.abs(b) * (2.0 ** -10 if kv_dtype == synth.KV_F16 else 0.0) + 1e-5 * rms
+            bad = np.abs(a - b) > tol
+            assert not bad.any(), (li, np.flatnonzero(bad)[:5], a[bad][:5], b[bad][:5])
             assert np.array_equal(got[pos + 1:], ref[pos + 1:])
 
 
