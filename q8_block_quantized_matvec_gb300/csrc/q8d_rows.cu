@@ -33,8 +33,8 @@ namespace q8d {
 
 namespace {
 
-constexpr int kWarps = 8;        // warps per CTA
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                  // consumer warps per CTA
+constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 
 // Decodes the 32 quants of the block at byte offset `o` of the 4-byte
 // aligned shared buffer `s32` into 16 packed f32x2 pairs, and returns the
@@ -62,13 +62,56 @@ __device__ __forceinline__ float decode_block(const uint32_t* __restrict__ s32, 
   return f16_bits_to_f32(sbits);
 }
 
+// sum_j q_j x_j over one block with four independent f32x2 chains.
+__device__ __forceinline__ float block_dot(const uint64_t (&q2)[16], const uint64_t (&x2)[16]) {
+  uint64_t c0 = pack2(0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
+#pragma unroll
+  for (int j = 0; j < 16; j += 4) {
+    c0 = fma2(q2[j], x2[j], c0);
+    c1 = fma2(q2[j + 1], x2[j + 1], c1);
+    c2 = fma2(q2[j + 2], x2[j + 2], c2);
+    c3 = fma2(q2[j + 3], x2[j + 3], c3);
+  }
+  const uint64_t s = add2(add2(c0, c1), add2(c2, c3));
+  float lo, hi;
+  unpack2(s, lo, hi);
+  return lo + hi;
+}
+
+// Streams one block straight from shared memory into the dot product with
+// x (no decoded copy is kept): returns scale * sum_j q_j x_j.
+__device__ __forceinline__ float block_dot_smem(const uint32_t* __restrict__ s32, uint32_t o,
+                                                const uint64_t (&x2)[16]) {
+  const uint32_t wi = o >> 2;
+  const bool odd = (o & 2u) != 0;
+  uint32_t a[9];
+#pragma unroll
+  for (int k = 0; k < 9; ++k) a[k] = s32[wi + k];
+  const float sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
+  const uint32_t sh = odd ? 32u : 16u;
+  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
+  uint64_t c[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t w = __funnelshift_rc(a[k], a[k + 1], sh) ^ 0x80808080u;
+    const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
+    const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
+    c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
+    c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
+  }
+  const uint64_t t = add2(add2(c[0], c[1]), add2(c[2], c[3]));
+  float lo, hi;
+  unpack2(t, lo, hi);
+  return sc * (lo + hi);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Loads the activation pairs of `m_here` vectors for block columns
+// Loads the activation pairs of vectors v0..v0+MV-1 for block columns
 // seg*32K + k*32 + lane into registers (zeros past the row end / m).
 template <int K, int MV>
 __device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int lane,
@@ -91,133 +134,177 @@ __device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int
   }
 }
 
+// One tile of the CTA's contiguous row range: rows [r0, r0 + rows) of
+// segment `seg`, which are rows [vrow0, vrow0 + rows) of the CTA.
+struct Tile {
+  int seg, rows, vrow0;
+  long long r0;
+};
+
+__device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long long v0,
+                                        long long v1) {
+  Tile t;
+  int sg = 0;
+  while (sg + 1 < P.nseg && cur >= P.vbegin[sg + 1]) ++sg;
+  t.seg = sg;
+  t.r0 = cur - P.vbegin[sg];
+  const long long seg_end = P.vbegin[sg] + P.seg[sg].p;
+  t.rows = (int)min((long long)P.rows_per_tile, min(seg_end, v1) - cur);
+  t.vrow0 = (int)(cur - v0);
+  return t;
+}
+
+// Warp-specialised kernel: warp kWarps is the producer (bulk copies into a
+// ring of stages, recycled through per-stage "empty" barriers), warps
+// 0..kWarps-1 consume.  Each CTA owns a contiguous range of output rows;
+// per-(row, segment) partials wait in shared memory and are reduced in a
+// fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int K, int MV>
-__global__ void __launch_bounds__(kThreads) q8_rows_kernel(const RowsParams P) {
+__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 224)
+    q8_rows_kernel(const RowsParams P) {
+  // Two rows are decoded together (independent instruction streams) when
+  // the activations leave registers for it.
+  constexpr bool kPair = (K * MV <= 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = P.segs_per_row;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
-  float* part = reinterpret_cast<float*>(full + P.nstages);  // [2][R][NS][MV]
-  const int part_stride = P.rows_per_tile * NS * MV;
+  uint64_t* empty = full + P.nstages;
+  float* part = reinterpret_cast<float*>(empty + P.nstages);  // [rows_cta][NS][m]
+
+  const long long v0 = (long long)blockIdx.x * P.rows_per_cta;
+  const long long v1 = min(P.total_rows, v0 + P.rows_per_cta);
+  const int rows_cta = (int)max(0LL, v1 - v0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < P.nstages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < P.nstages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
     fence_barrier_init();
   }
   __syncthreads();
 
-  const uint64_t pol = policy_evict_first();
-
-  // Producer (thread 0): fill stage i % nstages with this CTA's i-th tile.
-  auto issue = [&](int i) {
-    const int t = blockIdx.x + i * gridDim.x;
-    if (t >= P.total_tiles) return;
-    int sg = 0;
-    while (sg + 1 < P.nseg && t >= P.seg[sg + 1].tile_begin) ++sg;
-    const RowSeg& S = P.seg[sg];
-    const long long r0 = (long long)(t - S.tile_begin) * P.rows_per_tile;
-    const long long r1 = min((long long)S.p, r0 + P.rows_per_tile);
-    const long long start = r0 * P.row_bytes, end = r1 * P.row_bytes;
-    const long long total = (long long)S.p * P.row_bytes;
-    const long long a0 = start & ~15LL;
-    long long a1 = (end + 15) & ~15LL;
-    const long long cap16 = total & ~15LL;
-    uint8_t* dst = smem + (size_t)P.stage_bytes * (i % P.nstages);
-    if (a1 > cap16) {
-      // Last tile of a matrix whose byte size is not a multiple of 16: the
-      // final few bytes are copied by hand (generic proxy), before the
-      // arrive that publishes the stage.
-      a1 = cap16 > a0 ? cap16 : a0;
-      for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(S.w + o);
+  bool ok = true;
+  if (warp == kWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      long long cur = v0;
+      for (int i = 0; cur < v1; ++i) {
+        const Tile t = tile_at(P, cur, v0, v1);
+        const int s = i % P.nstages;
+        if (i >= P.nstages && !mbar_wait(&empty[s], (uint32_t)((i / P.nstages) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        const RowSeg& S = P.seg[t.seg];
+        const long long start = t.r0 * P.row_bytes, end = (t.r0 + t.rows) * P.row_bytes;
+        const long long total = (long long)S.p * P.row_bytes;
+        const long long a0 = start & ~15LL;
+        long long a1 = (end + 15) & ~15LL;
+        const long long cap16 = total & ~15LL;
+        uint8_t* dst = smem + (size_t)P.stage_bytes * s;
+        if (a1 > cap16) {
+          // Last tile of a matrix whose byte size is not a multiple of 16:
+          // the final bytes are copied by hand before the arrive publishes them.
+          a1 = cap16 > a0 ? cap16 : a0;
+          for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(S.w + o);
+        }
+        const uint32_t bytes = (uint32_t)(a1 - a0);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        if (bytes) bulk_g2s(dst, S.w + a0, bytes, &full[s], pol);
+        cur += t.rows;
+      }
     }
-    const uint32_t bytes = (uint32_t)(a1 - a0);
-    uint64_t* bar = &full[i % P.nstages];
-    mbar_arrive_expect_tx(bar, bytes);
-    if (bytes) bulk_g2s(dst, S.w + a0, bytes, bar, pol);
-  };
+  } else {
+    // ---------------- consumers ----------------
+    const bool x_static = (NS <= kWarps) && (P.m <= MV);
+    const int RG = NS <= kWarps ? kWarps / NS : 1;
+    const int my_seg0 = NS <= kWarps ? warp % NS : warp;
+    const int seg_step = NS <= kWarps ? NS : kWarps;
+    const int my_rg = NS <= kWarps ? warp / NS : 0;
+    const bool active = (NS <= kWarps) ? (warp < NS * RG) : true;
 
-  if (threadIdx.x == 0)
-    for (int i = 0; i < P.nstages; ++i) issue(i);
+    uint64_t xr[MV][K][16];
+    if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, xr);
 
-  // Ownership of (segment, rows) inside a tile.
-  const bool x_static = (NS <= kWarps) && (P.m <= MV);
-  const int RG = NS <= kWarps ? kWarps / NS : 1;
-  const int my_seg0 = NS <= kWarps ? warp % NS : warp;
-  const int seg_step = NS <= kWarps ? NS : kWarps;   // only used when NS > kWarps
-  const int my_rg = NS <= kWarps ? warp / NS : 0;
-  const bool active_warp = (NS <= kWarps) ? (warp < NS * RG) : true;
-
-  uint64_t xr[MV][K][16];
-  if (x_static && active_warp) load_x<K, MV>(P, 0, my_seg0, lane, xr);
-
-  for (int i = 0;; ++i) {
-    const int t = blockIdx.x + i * gridDim.x;
-    if (t >= P.total_tiles) break;
-    int sg = 0;
-    while (sg + 1 < P.nseg && t >= P.seg[sg + 1].tile_begin) ++sg;
-    const RowSeg& S = P.seg[sg];
-    const long long r0 = (long long)(t - S.tile_begin) * P.rows_per_tile;
-    const int rows = (int)min((long long)P.rows_per_tile, (long long)S.p - r0);
-    const int stage = i % P.nstages;
-    const uint32_t parity = (uint32_t)(i / P.nstages) & 1u;
-    const bool ok = mbar_wait(&full[stage], parity);
-    if (!__syncthreads_and(ok)) {
-      if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
-      return;
-    }
-    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * stage);
-    const uint32_t delta = (uint32_t)((r0 * P.row_bytes) & 15LL);
-
-    for (int v0 = 0; v0 < P.m; v0 += MV) {
-      float* pb = part + (size_t)(i & 1) * part_stride;
-      if (active_warp) {
-        for (int seg = my_seg0; seg < NS; seg += (NS <= kWarps ? NS : seg_step)) {
-          if (!x_static) load_x<K, MV>(P, v0, seg, lane, xr);
-          for (int rl = my_rg; rl < rows; rl += RG) {
-            float acc[MV];
+    long long cur = v0;
+    for (int i = 0; cur < v1; ++i) {
+      const Tile t = tile_at(P, cur, v0, v1);
+      const int s = i % P.nstages;
+      if (!mbar_wait(&full[s], (uint32_t)(i / P.nstages) & 1u)) {
+        ok = false;
+        break;
+      }
+      if (active) {
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * s);
+        const uint32_t delta = (uint32_t)((t.r0 * P.row_bytes) & 15LL);
+        const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
+        for (int v0m = 0; v0m < P.m; v0m += MV) {
+          for (int seg = my_seg0; seg < NS; seg += seg_step) {
+            if (!x_static) load_x<K, MV>(P, v0m, seg, lane, xr);
+            for (int rl = first; rl < t.rows; rl += (kPair ? 2 : 1) * RG) {
+              const int rl2 = rl + RG;
+              const bool two = kPair && rl2 < t.rows;
+              float acc[2][MV];
 #pragma unroll
-            for (int m = 0; m < MV; ++m) acc[m] = 0.f;
+              for (int m = 0; m < MV; ++m) acc[0][m] = acc[1][m] = 0.f;
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-              const int b = seg * 32 * K + k * 32 + lane;
-              if (b < P.bpr) {
-                uint64_t q2[16];
-                const uint32_t o = delta + (uint32_t)(rl * P.bpr + b) * kQBlockBytes;
-                const float sc = decode_block(s32, o, q2);
+              for (int k = 0; k < K; ++k) {
+                const int b = seg * 32 * K + k * 32 + lane;
+                if (b < P.bpr) {
+                  const uint32_t oa = delta + (uint32_t)(rl * P.bpr + b) * kQBlockBytes;
+                  const uint32_t ob = delta + (uint32_t)(rl2 * P.bpr + b) * kQBlockBytes;
+                  if (MV == 1) {
+                    acc[0][0] += block_dot_smem(s32, oa, xr[0][k]);
+                    if (two) acc[1][0] += block_dot_smem(s32, ob, xr[0][k]);
+                  } else {
+                    uint64_t qa[16];
+                    const float sa = decode_block(s32, oa, qa);
 #pragma unroll
-                for (int m = 0; m < MV; ++m) {
-                  uint64_t s2 = pack2(0.f, 0.f);
+                    for (int m = 0; m < MV; ++m) acc[0][m] = fmaf(sa, block_dot(qa, xr[m][k]), acc[0][m]);
+                    if (two) {
+                      const float sb = decode_block(s32, ob, qa);
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) s2 = fma2(q2[j], xr[m][k][j], s2);
-                  float lo, hi;
-                  unpack2(s2, lo, hi);
-                  acc[m] = fmaf(sc, lo + hi, acc[m]);
+                      for (int m = 0; m < MV; ++m) acc[1][m] = fmaf(sb, block_dot(qa, xr[m][k]), acc[1][m]);
+                    }
+                  }
+                }
+              }
+#pragma unroll
+              for (int m = 0; m < MV; ++m) {
+                const float va = warp_sum(acc[0][m]);
+                const float vb = two ? warp_sum(acc[1][m]) : 0.f;
+                if (lane == 0 && v0m + m < P.m) {
+                  part[((size_t)(t.vrow0 + rl) * NS + seg) * P.m + v0m + m] = va;
+                  if (two) part[((size_t)(t.vrow0 + rl2) * NS + seg) * P.m + v0m + m] = vb;
                 }
               }
             }
-#pragma unroll
-            for (int m = 0; m < MV; ++m) {
-              const float v = warp_sum(acc[m]);
-              if (lane == 0) pb[((size_t)rl * NS + seg) * MV + m] = v;
-            }
           }
-          if (NS <= kWarps) break;
         }
       }
-      __syncthreads();
-      // Reduce the NS segment partials of each (row, vector) in order.
-      const int mv_here = min(MV, P.m - v0);
-      for (int e = threadIdx.x; e < rows * mv_here; e += kThreads) {
-        const int rl = e / mv_here, m = e % mv_here;
-        float s = 0.f;
-        for (int seg = 0; seg < NS; ++seg) s += pb[((size_t)rl * NS + seg) * MV + m];
-        float* y = S.y + (size_t)(v0 + m) * P.ldy + (r0 + rl);
-        *y = P.accumulate ? (*y + s) : s;
-      }
-      if (v0 + MV < P.m) __syncthreads();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      cur += t.rows;
     }
-    // Stage `stage` is free once every warp passed the barrier above.
-    if (threadIdx.x == 0) issue(i + P.nstages);
+  }
+
+  // ---- reduce the segment partials of each (row, vector) in order ----
+  if (!__syncthreads_and(ok)) {
+    if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+    return;
+  }
+  for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
+    const int rc = e / P.m, m = e % P.m;
+    float sum = 0.f;
+    for (int seg = 0; seg < NS; ++seg) sum += part[((size_t)rc * NS + seg) * P.m + m];
+    const long long vr = v0 + rc;
+    int sg = 0;
+    while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
+    float* y = P.seg[sg].y + (size_t)m * P.ldy + (vr - P.vbegin[sg]);
+    *y = P.accumulate ? (*y + sum) : sum;
   }
 }
 
@@ -228,21 +315,16 @@ __global__ void fill_zero_kernel(float* y, int ldy, int m, int p) {
 }
 
 template <int K, int MV>
-int launch_rows(const RowsParams& P, int smem_bytes, cudaStream_t stream) {
+int launch_rows(const RowsParams& P, int smem_bytes, int grid, cudaStream_t stream) {
   auto fn = q8_rows_kernel<K, MV>;
   static int configured_bytes[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && configured_bytes[dev] < smem_bytes) {
+  if (dev >= 0 && dev < 64 && configured_bytes[dev] < smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return record_cuda(e);
     configured_bytes[dev] = 200 * 1024;
   }
-  int occ = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, smem_bytes);
-  if (e != cudaSuccess) return record_cuda(e);
-  occ = std::max(occ, 1);
-  const int grid = std::min(P.total_tiles, sm_count() * occ);
   fn<<<grid, kThreads, smem_bytes, stream>>>(P);
   return check_launch();
 }
@@ -252,7 +334,10 @@ int launch_rows(const RowsParams& P, int smem_bytes, cudaStream_t stream) {
 int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   if (P.m <= 0) return Q8D_OK;
   long long p_total = 0;
-  for (int s = 0; s < P.nseg; ++s) p_total += P.seg[s].p;
+  for (int s = 0; s < P.nseg; ++s) {
+    P.vbegin[s] = p_total;
+    p_total += P.seg[s].p;
+  }
   if (p_total == 0) return Q8D_OK;
   if (P.n == 0) {
     if (P.accumulate) return Q8D_OK;
@@ -267,44 +352,40 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   }
   P.bpr = P.n / kQBlock;
   P.row_bytes = (long long)P.bpr * kQBlockBytes;
+  P.total_rows = p_total;
 
-  // Blocks per lane K (1..4): fewest segments per row up to 8 warps with
-  // little idle; x for MV vectors stays in registers (32*K*MV floats <= 128).
+  // Blocks per lane K (1..3): the fewest segments per row that still fit
+  // kWarps warps; with several activation vectors K = 1 (registers).
   int K = 1;
-  for (K = 1; K < 4; ++K) {
-    const int ns = (P.bpr + 32 * K - 1) / (32 * K);
-    if (ns <= kWarps) break;
-  }
-  if (P.m > 1) K = 1;  // activations of several vectors compete for registers
+  for (K = 1; K < 3; ++K)
+    if ((P.bpr + 32 * K - 1) / (32 * K) <= kWarps) break;
+  if (P.m > 1) K = 1;
   const int NS = (P.bpr + 32 * K - 1) / (32 * K);
   const int MV = (K > 1 || P.m == 1) ? 1 : (P.m == 2 ? 2 : 4);
   P.segs_per_row = NS;
 
-  // Tile rows: ~16 KB stages, but enough tiles to give every SM work.
+  // Stage size ~12 KB (whole rows), 4-6 stages; CTAs own contiguous row
+  // ranges, two or three per SM.
   const int sms = sm_count();
-  long long R = std::max<long long>(1, 16384 / P.row_bytes);
-  R = std::min<long long>(R, std::max<long long>(1, p_total / (2LL * sms)));
-  R = std::min<long long>(R, 64);
-  P.rows_per_tile = (int)R;
-  int tiles = 0;
-  for (int s = 0; s < P.nseg; ++s) {
-    P.seg[s].tile_begin = tiles;
-    tiles += (int)((P.seg[s].p + R - 1) / R);
-  }
-  P.total_tiles = tiles;
+  long long R = std::max<long long>(1, 12288 / P.row_bytes);
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
-  P.nstages = P.stage_bytes <= 12 * 1024 ? 6 : (P.stage_bytes <= 24 * 1024 ? 4 : 3);
-  const int part_floats = (int)R * NS * MV;
-  const int smem = P.stage_bytes * P.nstages + 8 * P.nstages + 4 * 2 * part_floats;
+  P.nstages = P.stage_bytes <= 8 * 1024 ? 6 : (P.stage_bytes <= 16 * 1024 ? 5 : 3);
+  long long grid = std::min<long long>(p_total, 2LL * sms);
+  long long rows_cta = (p_total + grid - 1) / grid;
+  grid = (p_total + rows_cta - 1) / rows_cta;
+  P.rows_per_cta = rows_cta;
+  R = std::min<long long>(R, rows_cta);
+  P.rows_per_tile = (int)R;
+  const long long part_bytes = 4LL * rows_cta * NS * P.m;
+  const long long smem = (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + part_bytes;
   if (smem > 200 * 1024) return Q8D_EUNSUPPORTED;
 
   switch (K * 10 + MV) {
-    case 11: return launch_rows<1, 1>(P, smem, stream);
-    case 12: return launch_rows<1, 2>(P, smem, stream);
-    case 14: return launch_rows<1, 4>(P, smem, stream);
-    case 21: return launch_rows<2, 1>(P, smem, stream);
-    case 31: return launch_rows<3, 1>(P, smem, stream);
-    case 41: return launch_rows<4, 1>(P, smem, stream);
+    case 11: return launch_rows<1, 1>(P, (int)smem, (int)grid, stream);
+    case 12: return launch_rows<1, 2>(P, (int)smem, (int)grid, stream);
+    case 14: return launch_rows<1, 4>(P, (int)smem, (int)grid, stream);
+    case 21: return launch_rows<2, 1>(P, (int)smem, (int)grid, stream);
+    case 31: return launch_rows<3, 1>(P, (int)smem, (int)grid, stream);
     default: return Q8D_EUNSUPPORTED;
   }
 }

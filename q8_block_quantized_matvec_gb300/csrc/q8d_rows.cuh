@@ -12,7 +12,7 @@ struct RowSeg {
   const uint8_t* w;  // block stream, 16-byte aligned
   float* y;          // output row 0; row i of the output at y + i*ldy
   int p;             // output rows
-  int tile_begin;    // filled by the planner
+  int reserved;
 };
 
 struct RowsParams {
@@ -28,7 +28,10 @@ struct RowsParams {
   // filled by the planner
   int bpr;
   long long row_bytes;
-  int rows_per_tile, total_tiles, stage_bytes, nstages, segs_per_row;
+  long long vbegin[3];     // first virtual row of each matrix (concatenated rows)
+  long long total_rows;    // sum of p
+  long long rows_per_cta;  // contiguous virtual rows owned by one CTA
+  int rows_per_tile, stage_bytes, nstages, segs_per_row;
 };
 
 // Plans tiles/stages and launches the kernel on `stream`.  Returns a status.
