@@ -34,7 +34,6 @@ namespace q8d {
 namespace {
 
 constexpr int kAttnThreads = 128;
-constexpr int kMinChunk = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename KT>
@@ -76,10 +75,6 @@ struct Vec16<float> {
     f[3] = u.w;
   }
 };
-
-__device__ __forceinline__ int chunk_rows(int L, int nc) {
-  return max(kMinChunk, (L + nc - 1) / nc);
-}
 
 template <int D, typename KT, int GMAX>
 struct AttnCfg {
@@ -375,8 +370,7 @@ int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
   fn<<<grid, kAttnThreads, C::kSmem, stream>>>(P);
   int rc = check_launch();
   if (rc) return rc;
-  gqa_combine_kernel<D><<<P.batch * P.n_heads, D, 0, stream>>>(P);
-  return check_launch();
+  return attn_combine_launch(P, stream);
 }
 
 template <int D, typename KT>
@@ -389,6 +383,14 @@ int launch_attn_g(const AttnParams& P, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int attn_combine_launch(const AttnParams& P, cudaStream_t stream) {
+  if (P.head_dim == 128)
+    gqa_combine_kernel<128><<<P.batch * P.n_heads, 128, 0, stream>>>(P);
+  else
+    gqa_combine_kernel<64><<<P.batch * P.n_heads, 64, 0, stream>>>(P);
+  return check_launch();
+}
 
 int attn_chunks(int batch, int n_kv_heads, int max_len) {
   const int target = 4 * sm_count();
@@ -408,11 +410,9 @@ int attn_launch(AttnParams P, cudaStream_t stream) {
   P.ws_o = ws;
   P.ws_m = ws + (size_t)P.batch * P.n_heads * nc * P.head_dim;
   P.ws_l = P.ws_m + (size_t)P.batch * P.n_heads * nc;
-  if (P.head_dim == 128)
-    return P.kv_dtype == Q8D_KV_F16 ? launch_attn_g<128, __half>(P, stream)
-                                    : launch_attn_g<128, float>(P, stream);
-  return P.kv_dtype == Q8D_KV_F16 ? launch_attn_g<64, __half>(P, stream)
-                                  : launch_attn_g<64, float>(P, stream);
+  if (P.kv_dtype == Q8D_KV_F16) return attn_mma_launch(P, stream);
+  if (P.head_dim == 128) return launch_attn_g<128, float>(P, stream);
+  return launch_attn_g<64, float>(P, stream);
 }
 
 int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,

@@ -26,7 +26,17 @@ struct AttnParams {
   float* ws_l;
 };
 
+// Context rows per chunk for attended length L with nc chunk slots: at least
+// kMinChunk rows so the partials stay small next to the K/V they summarise.
+constexpr int kMinChunk = 128;
+__host__ __device__ __forceinline__ int chunk_rows(int L, int nc) {
+  const int c = (L + nc - 1) / nc;
+  return c > kMinChunk ? c : kMinChunk;
+}
+
 int attn_chunks(int batch, int n_kv_heads, int max_len);
+int attn_combine_launch(const AttnParams& P, cudaStream_t stream);
+int attn_mma_launch(const AttnParams& P, cudaStream_t stream);  // f16 cache, tensor cores
 size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len);
 int attn_launch(AttnParams P, cudaStream_t stream);
 int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,

@@ -1,0 +1,338 @@
+// Split-K decode attention over an f16 KV cache on the tensor cores.
+//
+// Same contract as the CUDA-core kernel in q8d_attn.cu ("IV.4: One command
+// buffer per token", attention_decode; "Metal Backend Optimizations" 3.3,
+// split partial + combine), organised for GB300:
+//  * The G <= 16 query heads of one KV head are the 16 rows of an
+//    m16n8k16 MMA; tokens are the N dimension of Q.K^T and the K dimension of
+//    P.V.  With G of 2..8 a tcgen05 tile (M >= 64) would be mostly padding
+//    and would move the scores out to TMEM between the two products, so the
+//    warp-level MMA keeps scores, softmax and P in registers (the
+//    accumulator layout of Q.K^T is the A-operand layout of P.V).
+//  * f32 accuracy from f16 tensor cores: K and V are f16 already (exact);
+//    q is scaled per head by a power of two into f16 range and split into
+//    f16 hi + lo parts (q = hi + lo to ~2^-22), and so are the
+//    probabilities (scaled by 2^12 first); every product is exact in the f32
+//    accumulator, so the result matches f32 CUDA-core arithmetic.
+//  * Each warp runs its own online softmax over 16 tokens of every 64-token
+//    sub-tile; the four warps' {m, l, O} are merged once at the end of the
+//    chunk and written as the chunk's partial for the combine kernel.
+//  * K/V rows stream through a two-stage ring of bulk copies; rows are padded
+//    by 16 bytes so fragment loads and ldmatrix.trans hit distinct banks.
+#include <cuda_fp16.h>
+
+#include "q8d_attn.cuh"
+#include "q8d_internal.cuh"
+
+namespace q8d {
+namespace {
+
+constexpr int kWarpsA = 4;
+constexpr int kThreadsA = kWarpsA * 32;
+constexpr int kTS = 64;                // tokens per sub-tile (16 per warp)
+constexpr float kLog2eA = 1.4426950408889634f;
+constexpr float kPScale = 4096.f;      // probabilities scaled by 2^12 before the f16 split
+
+template <int D>
+struct MCfg {
+  static constexpr int kRow = D * 2;                // f16 row bytes
+  static constexpr int kStride = kRow + 16;         // padded shared-memory row
+  static constexpr int kStage = 2 * kTS * kStride;  // K rows, then V rows
+  static constexpr int kOffQ = 2 * kStage;          // f32 q [16][D], power-of-two scaled
+  static constexpr int kOffF = kOffQ + 16 * D * 4;  // per-head score factor [16]
+  static constexpr int kOffBar = kOffF + 16 * 4;
+  static constexpr int kSmem = kOffBar + 16;
+  static_assert(kWarpsA * 16 * (D + 2) * 4 <= 2 * kStage, "merge buffer fits the stages");
+};
+
+// v = hi + lo with hi = f16(v), lo = f16(v - hi), for a pair of floats.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) {
+  using C = MCfg<D>;
+  constexpr int KS = D / 16;  // k-steps over head_dim (Q.K^T)
+  constexpr int NT = D / 8;   // n-tiles over head_dim (P.V)
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
+  float* fh = reinterpret_cast<float*>(smem + C::kOffF);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, cq = lane & 3;
+  const int G = P.n_heads / P.n_kv_heads;
+  const int L = P.d_lens[b];
+  if (L < 1 || L > P.cap) {
+    if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
+    return;
+  }
+  const int tpc = chunk_rows(L, P.nc);
+  const int t_begin = c * tpc;
+  if (t_begin >= L) return;
+  const int t_end = min(L, t_begin + tpc);
+  const long long kvw = (long long)P.n_kv_heads * D;
+  __half* kbase = reinterpret_cast<__half*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
+  __half* vbase = reinterpret_cast<__half*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
+
+  // In-kernel append of row L-1 by the CTA that owns it; the bulk copies
+  // below read it back, so attended values are exactly the cached ones.
+  if (P.k_new != nullptr && t_end == L) {
+    const float* kn = P.k_new + (long long)b * kvw + (long long)g * D;
+    const float* vn = P.v_new + (long long)b * kvw + (long long)g * D;
+    for (int j = tid; j < D; j += kThreadsA) {
+      kbase[(long long)(L - 1) * kvw + j] = __float2half_rn(kn[j]);
+      vbase[(long long)(L - 1) * kvw + j] = __float2half_rn(vn[j]);
+    }
+    fence_proxy_async_global();
+  }
+
+  // Query rows scaled per head by 2^sh so that max|q| < 2^11; the score
+  // factor 2^-sh * scale * log2(e) undoes it in the log2 domain.
+  for (int hh = warp; hh < 16; hh += kWarpsA) {
+    const float* qrow = P.q + ((long long)b * P.n_heads + (long long)g * G + hh) * D;
+    float mx = 0.f;
+    if (hh < G)
+      for (int j = lane; j < D; j += 32) mx = fmaxf(mx, fabsf(qrow[j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    const int sh = (mx > 0.f) ? 11 - e : 0;
+    for (int j = lane; j < D; j += 32) qs[hh * D + j] = (hh < G) ? ldexpf(qrow[j], sh) : 0.f;
+    if (lane == 0) fh[hh] = (hh < G) ? ldexpf(P.scale * kLog2eA, -sh) : 0.f;
+  }
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const uint64_t pol = policy_evict_first();
+  const int n_sub = (t_end - t_begin + kTS - 1) / kTS;
+  auto issue = [&](int k) {  // warp 0
+    if (k >= n_sub) return;
+    const int r0 = t_begin + k * kTS;
+    const int nr = min(kTS, t_end - r0);
+    uint8_t* st = smem + (k & 1) * C::kStage;
+    if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)(2 * nr * C::kRow));
+    __syncwarp();
+    for (int r = lane; r < nr; r += 32) {
+      const long long row = (long long)(r0 + r) * kvw;
+      bulk_g2s(st + r * C::kStride, kbase + row, C::kRow, &bar[k & 1], pol);
+      bulk_g2s(st + (kTS + r) * C::kStride, vbase + row, C::kRow, &bar[k & 1], pol);
+    }
+  };
+  if (warp == 0) {
+    issue(0);
+    issue(1);
+  }
+
+  // A fragments of q (rows gq and gq + 8, K = head_dim), hi and lo parts.
+  uint32_t qh[KS][4], ql[KS][4];
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    const int d0 = 16 * kk + 2 * cq;
+    split2(qs[gq * D + d0], qs[gq * D + d0 + 1], qh[kk][0], ql[kk][0]);
+    split2(qs[(gq + 8) * D + d0], qs[(gq + 8) * D + d0 + 1], qh[kk][1], ql[kk][1]);
+    split2(qs[gq * D + d0 + 8], qs[gq * D + d0 + 9], qh[kk][2], ql[kk][2]);
+    split2(qs[(gq + 8) * D + d0 + 8], qs[(gq + 8) * D + d0 + 9], qh[kk][3], ql[kk][3]);
+  }
+  const float f0 = fh[gq], f1 = fh[gq + 8];
+
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool ok = true;
+
+  for (int k = 0; k < n_sub; ++k) {
+    const int nr = min(kTS, t_end - (t_begin + k * kTS));
+    ok = mbar_wait(&bar[k & 1], (uint32_t)(k >> 1) & 1u);
+    if (!__syncthreads_and(ok)) break;
+    const uint8_t* st = smem + (k & 1) * C::kStage;
+    const int base_t = warp * 16;
+
+    // ---- S = Q.K^T for this warp's 16 tokens (two n-tiles of 8) ----
+    float s[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+      const int tok = min(base_t + 8 * j + gq, nr - 1);
+      const uint8_t* krow = st + tok * C::kStride + 4 * cq;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 32 * kk);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 32 * kk + 16);
+        mma16816(s[j], qh[kk], b0, b1);
+        mma16816(s[j], ql[kk], b0, b1);
+      }
+    }
+    // ---- log2-domain scores, mask, online softmax per row ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = base_t + 8 * j + 2 * cq + (e & 1);
+        const float v = s[j][e] * (e < 2 ? f0 : f1);
+        s[j][e] = tok < nr ? v : -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+    }
+#pragma unroll
+    for (int o_ = 1; o_ < 4; o_ <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float c0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+    const float c1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float mrow = e < 2 ? mn0 : mn1;
+        const float pv = (s[j][e] == -INFINITY) ? 0.f : exp2f(s[j][e] - mrow);
+        s[j][e] = pv;
+        if (e < 2) rs0 += pv; else rs1 += pv;
+      }
+    }
+#pragma unroll
+    for (int o_ = 1; o_ < 4; o_ <<= 1) {
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, o_);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, o_);
+    }
+    l0 = l0 * c0 + rs0;
+    l1 = l1 * c1 + rs1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= c0;
+      o[n][1] *= c0;
+      o[n][2] *= c1;
+      o[n][3] *= c1;
+    }
+    // ---- P (16 heads x 16 tokens) as the A operand, hi/lo ----
+    uint32_t ph[4], pl[4];
+    split2(s[0][0] * kPScale, s[0][1] * kPScale, ph[0], pl[0]);
+    split2(s[0][2] * kPScale, s[0][3] * kPScale, ph[1], pl[1]);
+    split2(s[1][0] * kPScale, s[1][1] * kPScale, ph[2], pl[2]);
+    split2(s[1][2] * kPScale, s[1][3] * kPScale, ph[3], pl[3]);
+    // ---- O += P.V ----
+    {
+      const int mi = lane >> 3, r = lane & 7;
+      const int tok = min(base_t + (mi & 1) * 8 + r, nr - 1);
+      const uint32_t vrow = smem_u32(st + (kTS + tok) * C::kStride + (mi >> 1) * 16);
+#pragma unroll
+      for (int dn = 0; dn < D / 16; ++dn) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vrow + dn * 32, v0, v1, v2, v3);
+        mma16816(o[2 * dn], ph, v0, v1);
+        mma16816(o[2 * dn], pl, v0, v1);
+        mma16816(o[2 * dn + 1], ph, v2, v3);
+        mma16816(o[2 * dn + 1], pl, v2, v3);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) issue(k + 2);
+  }
+
+  // ---- merge the four warps' {m, l, O}; write the chunk's partial ----
+  __syncthreads();
+  float* mm = reinterpret_cast<float*>(smem);  // stages are idle now
+  float* ll = mm + kWarpsA * 16;
+  float* oo = ll + kWarpsA * 16;
+  if (cq == 0) {
+    mm[warp * 16 + gq] = m0;
+    mm[warp * 16 + gq + 8] = m1;
+    ll[warp * 16 + gq] = l0;
+    ll[warp * 16 + gq + 8] = l1;
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int col = 8 * n + 2 * cq;
+    oo[(warp * 16 + gq) * D + col] = o[n][0];
+    oo[(warp * 16 + gq) * D + col + 1] = o[n][1];
+    oo[(warp * 16 + gq + 8) * D + col] = o[n][2];
+    oo[(warp * 16 + gq + 8) * D + col + 1] = o[n][3];
+  }
+  __syncthreads();
+  if (!ok) {
+    if (tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+  }
+  for (int e = tid; e < G * D; e += kThreadsA) {
+    const int h = e / D, j = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarpsA; ++w) M = fmaxf(M, mm[w * 16 + h]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsA; ++w) {
+      const float mw = mm[w * 16 + h];
+      if (mw == -INFINITY) continue;
+      const float wgt = exp2f(mw - M);
+      acc = fmaf(oo[(w * 16 + h) * D + j], wgt, acc);
+      lsum = fmaf(ll[w * 16 + h], wgt, lsum);
+    }
+    const long long hq = (long long)b * P.n_heads + (long long)g * G + h;
+    P.ws_o[(hq * P.nc + c) * D + j] = ok ? acc * (1.f / kPScale) : __int_as_float(0x7fc00000);
+    if (j == 0) {
+      P.ws_m[hq * P.nc + c] = M;
+      P.ws_l[hq * P.nc + c] = lsum;
+    }
+  }
+}
+
+template <int D>
+int launch_mma(const AttnParams& P, cudaStream_t stream) {
+  using C = MCfg<D>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gqa_mma_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return record_cuda(e);
+    configured[dev] = true;
+  }
+  dim3 grid(P.nc, P.n_kv_heads, P.batch);
+  gqa_mma_kernel<D><<<grid, kThreadsA, C::kSmem, stream>>>(P);
+  const int rc = check_launch();
+  if (rc) return rc;
+  return attn_combine_launch(P, stream);
+}
+
+}  // namespace
+
+int attn_mma_launch(const AttnParams& P, cudaStream_t stream) {
+  return P.head_dim == 128 ? launch_mma<128>(P, stream) : launch_mma<64>(P, stream);
+}
+
+}  // namespace q8d

@@ -160,7 +160,7 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int K, int MV>
-__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 224)
+__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 200)
     q8_rows_kernel(const RowsParams P) {
   // Two rows are decoded together (independent instruction streams) when
   // the activations leave registers for it.
