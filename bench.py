@@ -424,20 +424,21 @@ def main():
     aerr = torch.zeros(1, dtype=torch.int32, device="cuda")
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     at_times = []
-    for rep in range(args.kernel_reps + 1):
-        tot = 0.0
-        for li in range(shape.n_layers):
-            flush.fill_(li & 0xFF)  # evict the previous layer's KV from L2
-            a, b = ev[0]
-            a.record(stream)
-            q8d.q8d_gqa_decode_attn(qv, None, None, caches[li][0], caches[li][1], shape.kv_dtype,
-                                    aout, 1, H, Hk, D, cap, 0, lens, 1 / math.sqrt(D), aws, wsb,
-                                    aerr, stream)
-            b.record(stream)
-            b.synchronize()
-            tot += a.elapsed_time(b) / 1e3
-        if rep:
-            at_times.append(tot)
+    with torch.cuda.stream(stream):
+        for rep in range(args.kernel_reps + 1):
+            tot = 0.0
+            for li in range(shape.n_layers):
+                flush.fill_(li & 0xFF)  # evict the previous layer's KV from L2 (same stream)
+                a, b = ev[0]
+                a.record(stream)
+                q8d.q8d_gqa_decode_attn(qv, None, None, caches[li][0], caches[li][1], shape.kv_dtype,
+                                        aout, 1, H, Hk, D, cap, 0, lens, 1 / math.sqrt(D), aws, wsb,
+                                        aerr, stream)
+                b.record(stream)
+                b.synchronize()
+                tot += a.elapsed_time(b) / 1e3
+            if rep:
+                at_times.append(tot)
     at_time = statistics.median(at_times)
     at_bytes_launch = attn_bytes(ctx, Hk, D, H, esize, append=False)
     at_gbs = at_bytes_launch * shape.n_layers / at_time / 1e9

@@ -160,11 +160,8 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int K, int MV>
-__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 200)
+__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 168)
     q8_rows_kernel(const RowsParams P) {
-  // Two rows are decoded together (independent instruction streams) when
-  // the activations leave registers for it.
-  constexpr bool kPair = (K * MV <= 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = P.segs_per_row;
@@ -229,6 +226,53 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 20
     uint64_t xr[MV][K][16];
     if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, xr);
 
+    if (MV == 1 && x_static) {
+      // Matvec fast path: branch-free inner loop.  Lanes past the row end
+      // read a valid block with zero activations; an odd last row is
+      // computed twice and stored once; two rows are reduced together.
+      const uint32_t rowb = (uint32_t)P.row_bytes;
+      uint32_t boff[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int b = my_seg0 * 32 * K + k * 32 + lane;
+        boff[k] = (uint32_t)(b < P.bpr ? b : P.bpr - 1) * kQBlockBytes;
+      }
+      long long cur = v0;
+      for (int i = 0; cur < v1; ++i) {
+        const Tile t = tile_at(P, cur, v0, v1);
+        const int s = i % P.nstages;
+        if (!mbar_wait(&full[s], (uint32_t)(i / P.nstages) & 1u)) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * s);
+          const uint32_t delta = (uint32_t)((t.r0 * P.row_bytes) & 15LL);
+          const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
+          float* prow = part + (size_t)t.vrow0 * NS + my_seg0;
+          for (int rl = first; rl < t.rows; rl += 2 * RG) {
+            const int rl2 = min(rl + RG, t.rows - 1);
+            float a = 0.f, c = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+              a += block_dot_smem(s32, delta + (uint32_t)rl * rowb + boff[k], xr[0][k]);
+              c += block_dot_smem(s32, delta + (uint32_t)rl2 * rowb + boff[k], xr[0][k]);
+            }
+            // lanes 0-15 reduce row rl, lanes 16-31 row rl2
+            float v = (lane & 16) ? c : a;
+            const float w = (lane & 16) ? a : c;
+            v += __shfl_xor_sync(0xffffffffu, w, 16);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) prow[(size_t)rl * NS] = v;
+            if (lane == 16 && rl + RG < t.rows) prow[(size_t)rl2 * NS] = v;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        cur += t.rows;
+      }
+    } else {
     long long cur = v0;
     for (int i = 0; cur < v1; ++i) {
       const Tile t = tile_at(P, cur, v0, v1);
@@ -244,42 +288,25 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 20
         for (int v0m = 0; v0m < P.m; v0m += MV) {
           for (int seg = my_seg0; seg < NS; seg += seg_step) {
             if (!x_static) load_x<K, MV>(P, v0m, seg, lane, xr);
-            for (int rl = first; rl < t.rows; rl += (kPair ? 2 : 1) * RG) {
-              const int rl2 = rl + RG;
-              const bool two = kPair && rl2 < t.rows;
-              float acc[2][MV];
+            for (int rl = first; rl < t.rows; rl += RG) {
+              float acc[MV];
 #pragma unroll
-              for (int m = 0; m < MV; ++m) acc[0][m] = acc[1][m] = 0.f;
+              for (int m = 0; m < MV; ++m) acc[m] = 0.f;
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 const int b = seg * 32 * K + k * 32 + lane;
-                if (b < P.bpr) {
-                  const uint32_t oa = delta + (uint32_t)(rl * P.bpr + b) * kQBlockBytes;
-                  const uint32_t ob = delta + (uint32_t)(rl2 * P.bpr + b) * kQBlockBytes;
-                  if (MV == 1) {
-                    acc[0][0] += block_dot_smem(s32, oa, xr[0][k]);
-                    if (two) acc[1][0] += block_dot_smem(s32, ob, xr[0][k]);
-                  } else {
-                    uint64_t qa[16];
-                    const float sa = decode_block(s32, oa, qa);
+                const uint32_t o =
+                    delta + (uint32_t)(rl * P.bpr + (b < P.bpr ? b : P.bpr - 1)) * kQBlockBytes;
+                uint64_t q[16];
+                const float sc = decode_block(s32, o, q);
 #pragma unroll
-                    for (int m = 0; m < MV; ++m) acc[0][m] = fmaf(sa, block_dot(qa, xr[m][k]), acc[0][m]);
-                    if (two) {
-                      const float sb = decode_block(s32, ob, qa);
-#pragma unroll
-                      for (int m = 0; m < MV; ++m) acc[1][m] = fmaf(sb, block_dot(qa, xr[m][k]), acc[1][m]);
-                    }
-                  }
-                }
+                for (int m = 0; m < MV; ++m) acc[m] = fmaf(sc, block_dot(q, xr[m][k]), acc[m]);
               }
 #pragma unroll
               for (int m = 0; m < MV; ++m) {
-                const float va = warp_sum(acc[0][m]);
-                const float vb = two ? warp_sum(acc[1][m]) : 0.f;
-                if (lane == 0 && v0m + m < P.m) {
-                  part[((size_t)(t.vrow0 + rl) * NS + seg) * P.m + v0m + m] = va;
-                  if (two) part[((size_t)(t.vrow0 + rl2) * NS + seg) * P.m + v0m + m] = vb;
-                }
+                const float v = warp_sum(acc[m]);
+                if (lane == 0 && v0m + m < P.m)
+                  part[((size_t)(t.vrow0 + rl) * NS + seg) * P.m + v0m + m] = v;
               }
             }
           }
@@ -288,6 +315,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 20
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       cur += t.rows;
+    }
     }
   }
 
@@ -361,15 +389,17 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
     if ((P.bpr + 32 * K - 1) / (32 * K) <= kWarps) break;
   if (P.m > 1) K = 1;
   const int NS = (P.bpr + 32 * K - 1) / (32 * K);
-  const int MV = (K > 1 || P.m == 1) ? 1 : (P.m == 2 ? 2 : 4);
+  const int MV = (K > 1 || P.m == 1) ? 1 : 2;
   P.segs_per_row = NS;
 
   // Stage size ~12 KB (whole rows), 4-6 stages; CTAs own contiguous row
   // ranges, two or three per SM.
   const int sms = sm_count();
-  long long R = std::max<long long>(1, 12288 / P.row_bytes);
+  const int RG = NS <= kWarps ? kWarps / NS : 1;
+  long long R = std::max<long long>(1, 24576 / P.row_bytes);
+  if (R >= 2 * RG) R -= R % (2 * RG);  // whole row pairs for every row group
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
-  P.nstages = P.stage_bytes <= 8 * 1024 ? 6 : (P.stage_bytes <= 16 * 1024 ? 5 : 3);
+  P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 32 * 1024 ? 3 : 2);
   long long grid = std::min<long long>(p_total, 2LL * sms);
   long long rows_cta = (p_total + grid - 1) / grid;
   grid = (p_total + rows_cta - 1) / rows_cta;
@@ -383,7 +413,6 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   switch (K * 10 + MV) {
     case 11: return launch_rows<1, 1>(P, (int)smem, (int)grid, stream);
     case 12: return launch_rows<1, 2>(P, (int)smem, (int)grid, stream);
-    case 14: return launch_rows<1, 4>(P, (int)smem, (int)grid, stream);
     case 21: return launch_rows<2, 1>(P, (int)smem, (int)grid, stream);
     case 31: return launch_rows<3, 1>(P, (int)smem, (int)grid, stream);
     default: return Q8D_EUNSUPPORTED;
