@@ -250,22 +250,35 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 16
           const uint32_t delta = (uint32_t)((t.r0 * P.row_bytes) & 15LL);
           const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
           float* prow = part + (size_t)t.vrow0 * NS + my_seg0;
-          for (int rl = first; rl < t.rows; rl += 2 * RG) {
-            const int rl2 = min(rl + RG, t.rows - 1);
-            float a = 0.f, c = 0.f;
+          int rl = first;
+          // four rows at a time: independent decode streams, one transposed
+          // shuffle tree (lane 8j ends with the sum of row j)
+          for (; rl + 3 * RG < t.rows; rl += 4 * RG) {
+            float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              a += block_dot_smem(s32, delta + (uint32_t)rl * rowb + boff[k], xr[0][k]);
-              c += block_dot_smem(s32, delta + (uint32_t)rl2 * rowb + boff[k], xr[0][k]);
+              const uint32_t o = delta + (uint32_t)rl * rowb + boff[k];
+              const uint32_t st = (uint32_t)RG * rowb;
+              v0 += block_dot_smem(s32, o, xr[0][k]);
+              v1 += block_dot_smem(s32, o + st, xr[0][k]);
+              v2 += block_dot_smem(s32, o + 2 * st, xr[0][k]);
+              v3 += block_dot_smem(s32, o + 3 * st, xr[0][k]);
             }
-            // lanes 0-15 reduce row rl, lanes 16-31 row rl2
-            float v = (lane & 16) ? c : a;
-            const float w = (lane & 16) ? a : c;
-            v += __shfl_xor_sync(0xffffffffu, w, 16);
+            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+            const float u0 = (b4 ? v2 : v0) + __shfl_xor_sync(0xffffffffu, b4 ? v0 : v2, 16);
+            const float u1 = (b4 ? v3 : v1) + __shfl_xor_sync(0xffffffffu, b4 ? v1 : v3, 16);
+            float w = (b3 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, b3 ? u0 : u1, 8);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) prow[(size_t)rl * NS] = v;
-            if (lane == 16 && rl + RG < t.rows) prow[(size_t)rl2 * NS] = v;
+            for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if ((lane & 7) == 0) prow[(size_t)(rl + (lane >> 3) * RG) * NS] = w;
+          }
+          for (; rl < t.rows; rl += RG) {
+            float a = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+              a += block_dot_smem(s32, delta + (uint32_t)rl * rowb + boff[k], xr[0][k]);
+            a = warp_sum(a);
+            if (lane == 0) prow[(size_t)rl * NS] = a;
           }
         }
         __syncwarp();
@@ -396,10 +409,11 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   // ranges, two or three per SM.
   const int sms = sm_count();
   const int RG = NS <= kWarps ? kWarps / NS : 1;
-  long long R = std::max<long long>(1, 24576 / P.row_bytes);
-  if (R >= 2 * RG) R -= R % (2 * RG);  // whole row pairs for every row group
+  long long R = std::max<long long>(1, 36864 / P.row_bytes);
+  if (R >= 4 * RG) R -= R % (4 * RG);       // whole row quads for every row group
+  else if (R >= 2 * RG) R -= R % (2 * RG);
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
-  P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 32 * 1024 ? 3 : 2);
+  P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 36 * 1024 ? 3 : 2);
   long long grid = std::min<long long>(p_total, 2LL * sms);
   long long rows_cta = (p_total + grid - 1) / grid;
   grid = (p_total + rows_cta - 1) / rows_cta;
