@@ -51,20 +51,6 @@ __device__ __forceinline__ float to_cache<float>(float v) {
 template <typename KT>
 struct Vec16;
 template <>
-struct Vec16<__half> {
-  static constexpr int N = 8;
-  __device__ __forceinline__ static void load(const void* p, float (&f)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 t = __half22float2(h[i]);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
-  }
-};
-template <>
 struct Vec16<float> {
   static constexpr int N = 4;
   __device__ __forceinline__ static void load(const void* p, float (&f)[4]) {
@@ -313,11 +299,18 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   }
 }
 
+// Merges the chunk partials of one (sequence, query head):
+//   M = max_c m_c,  w_c = 2^(m_c - M),  out = sum_c w_c O_c / sum_c w_c l_c
+// The chunk weights are computed once into shared memory (all chunks'
+// loads in flight together), the sums run in a fixed order: deterministic.
 template <int D>
-__global__ void gqa_combine_kernel(const AttnParams P) {
+__global__ void __launch_bounds__(D) gqa_combine_kernel(const AttnParams P) {
+  extern __shared__ float wsm[];  // [nc] chunk weights
+  __shared__ float red[D / 32];
+  __shared__ float s_tot;
   const int hq = blockIdx.x;  // b * H + h
   const int b = hq / P.n_heads;
-  const int j = threadIdx.x;
+  const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
   const int L = P.d_lens[b];
   float* o = P.out + (long long)hq * D;
   if (L < 1 || L > P.cap) {
@@ -330,14 +323,41 @@ __global__ void gqa_combine_kernel(const AttnParams P) {
   const float* S = P.ws_l + (long long)hq * P.nc;
   const float* O = P.ws_o + (long long)hq * P.nc * D;
   float mx = -INFINITY;
-  for (int c = 0; c < nact; ++c) mx = fmaxf(mx, M[c]);
-  float s = 0.f, acc = 0.f;
-  for (int c = 0; c < nact; ++c) {
-    const float w = (M[c] == -INFINITY) ? 0.f : exp2f(M[c] - mx);
-    s = fmaf(S[c], w, s);
-    acc = fmaf(O[(long long)c * D + j], w, acc);
+  for (int c = j; c < nact; c += D) mx = fmaxf(mx, M[c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) mx = fmaxf(mx, red[w]);
+  float sl = 0.f;
+  for (int c = j; c < nact; c += D) {
+    const float mc = M[c];
+    const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - mx);
+    wsm[c] = w;
+    sl = fmaf(S[c], w, sl);
   }
-  o[j] = acc / s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, off);
+  __syncthreads();  // red[] reads above are done
+  if (lane == 0) red[warp] = sl;
+  __syncthreads();
+  if (j == 0) {
+    float t = 0.f;
+    for (int w = 0; w < D / 32; ++w) t += red[w];
+    s_tot = t;
+  }
+  __syncthreads();
+  float acc0 = 0.f, acc1 = 0.f;
+  int c = 0;
+#pragma unroll 4
+  for (; c + 1 < nact; c += 2) {
+    acc0 = fmaf(O[(long long)c * D + j], wsm[c], acc0);
+    acc1 = fmaf(O[(long long)(c + 1) * D + j], wsm[c + 1], acc1);
+  }
+  if (c < nact) acc0 = fmaf(O[(long long)c * D + j], wsm[c], acc0);
+  o[j] = (acc0 + acc1) / s_tot;
 }
 
 template <typename KT>
@@ -386,9 +406,9 @@ int launch_attn_g(const AttnParams& P, cudaStream_t stream) {
 
 int attn_combine_launch(const AttnParams& P, cudaStream_t stream) {
   if (P.head_dim == 128)
-    gqa_combine_kernel<128><<<P.batch * P.n_heads, 128, 0, stream>>>(P);
+    gqa_combine_kernel<128><<<P.batch * P.n_heads, 128, P.nc * sizeof(float), stream>>>(P);
   else
-    gqa_combine_kernel<64><<<P.batch * P.n_heads, 64, 0, stream>>>(P);
+    gqa_combine_kernel<64><<<P.batch * P.n_heads, 64, P.nc * sizeof(float), stream>>>(P);
   return check_launch();
 }
 

@@ -177,20 +177,30 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     const int base_t = warp * 16;
 
     // ---- S = Q.K^T for this warp's 16 tokens (two n-tiles of 8) ----
-    float s[2][4];
+    // hi and lo products accumulate in separate chains (4 independent MMA
+    // chains per warp) and are added at the end
+    float s[2][4], sl[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-      const int tok = min(base_t + 8 * j + gq, nr - 1);
-      const uint8_t* krow = st + tok * C::kStride + 4 * cq;
+      sl[j][0] = sl[j][1] = sl[j][2] = sl[j][3] = 0.f;
+    }
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 32 * kk);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 32 * kk + 16);
+    for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = min(base_t + 8 * j + gq, nr - 1);
+        const uint8_t* krow = st + tok * C::kStride + 4 * cq + 32 * kk;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16);
         mma16816(s[j], qh[kk], b0, b1);
-        mma16816(s[j], ql[kk], b0, b1);
+        mma16816(sl[j], ql[kk], b0, b1);
       }
     }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] += sl[j][e];
     // ---- log2-domain scores, mask, online softmax per row ----
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll

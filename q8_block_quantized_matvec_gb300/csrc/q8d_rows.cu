@@ -33,8 +33,8 @@ namespace q8d {
 
 namespace {
 
-constexpr int kWarps = 8;                  // consumer warps per CTA
-constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
+constexpr int kWarps = 8;              // warps per CTA, all consume
+constexpr int kThreads = kWarps * 32;  // lane 0 of warp 0 also produces
 
 // Decodes the 32 quants of the block at byte offset `o` of the 4-byte
 // aligned shared buffer `s32` into 16 packed f32x2 pairs, and returns the
@@ -154,13 +154,13 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
   return t;
 }
 
-// Warp-specialised kernel: warp kWarps is the producer (bulk copies into a
-// ring of stages, recycled through per-stage "empty" barriers), warps
-// 0..kWarps-1 consume.  Each CTA owns a contiguous range of output rows;
+// Streaming kernel: lane 0 of warp 0 fills a ring of stages with bulk
+// copies (recycled through per-stage "empty" barriers that every warp
+// arrives on); all warps consume.  Each CTA owns a contiguous range of output rows;
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int K, int MV>
-__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 168)
+__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 168)
     q8_rows_kernel(const RowsParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,38 +183,43 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 16
   __syncthreads();
 
   bool ok = true;
-  if (warp == kWarps) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      long long cur = v0;
-      for (int i = 0; cur < v1; ++i) {
-        const Tile t = tile_at(P, cur, v0, v1);
-        const int s = i % P.nstages;
-        if (i >= P.nstages && !mbar_wait(&empty[s], (uint32_t)((i / P.nstages) - 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        const RowSeg& S = P.seg[t.seg];
-        const long long start = t.r0 * P.row_bytes, end = (t.r0 + t.rows) * P.row_bytes;
-        const long long total = (long long)S.p * P.row_bytes;
-        const long long a0 = start & ~15LL;
-        long long a1 = (end + 15) & ~15LL;
-        const long long cap16 = total & ~15LL;
-        uint8_t* dst = smem + (size_t)P.stage_bytes * s;
-        if (a1 > cap16) {
-          // Last tile of a matrix whose byte size is not a multiple of 16:
-          // the final bytes are copied by hand before the arrive publishes them.
-          a1 = cap16 > a0 ? cap16 : a0;
-          for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(S.w + o);
-        }
-        const uint32_t bytes = (uint32_t)(a1 - a0);
-        mbar_arrive_expect_tx(&full[s], bytes);
-        if (bytes) bulk_g2s(dst, S.w + a0, bytes, &full[s], pol);
-        cur += t.rows;
+  // Producer state (lane 0 of warp 0): next tile index and its first row.
+  // A stage is refilled as soon as every warp has released it, so up to
+  // nstages tiles are in flight while the warps compute.
+  long long pcur = v0;
+  int pi = 0;
+  const uint64_t pol = policy_evict_first();
+  auto produce = [&](int upto) {
+    while (pi < upto && pcur < v1) {
+      const Tile t = tile_at(P, pcur, v0, v1);
+      const int s = pi % P.nstages;
+      if (pi >= P.nstages && !mbar_wait(&empty[s], (uint32_t)((pi / P.nstages) - 1) & 1u)) {
+        ok = false;
+        return;
       }
+      const RowSeg& S = P.seg[t.seg];
+      const long long start = t.r0 * P.row_bytes, end = (t.r0 + t.rows) * P.row_bytes;
+      const long long total = (long long)S.p * P.row_bytes;
+      const long long a0 = start & ~15LL;
+      long long a1 = (end + 15) & ~15LL;
+      const long long cap16 = total & ~15LL;
+      uint8_t* dst = smem + (size_t)P.stage_bytes * s;
+      if (a1 > cap16) {
+        // Last tile of a matrix whose byte size is not a multiple of 16:
+        // the final bytes are copied by hand before the arrive publishes them.
+        a1 = cap16 > a0 ? cap16 : a0;
+        for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(S.w + o);
+      }
+      const uint32_t bytes = (uint32_t)(a1 - a0);
+      mbar_arrive_expect_tx(&full[s], bytes);
+      if (bytes) bulk_g2s(dst, S.w + a0, bytes, &full[s], pol);
+      pcur += t.rows;
+      ++pi;
     }
-  } else {
+  };
+  const bool producer = (warp == 0 && lane == 0);
+  if (producer) produce(P.nstages);
+  {
     // ---------------- consumers ----------------
     const bool x_static = (NS <= kWarps) && (P.m <= MV);
     const int RG = NS <= kWarps ? kWarps / NS : 1;
@@ -283,6 +288,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 16
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (producer) produce(i + 1 + P.nstages);
         cur += t.rows;
       }
     } else {
@@ -327,6 +333,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 112 : 16
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (producer) produce(i + 1 + P.nstages);
       cur += t.rows;
     }
     }
@@ -356,17 +363,39 @@ __global__ void fill_zero_kernel(float* y, int ldy, int m, int p) {
 }
 
 template <int K, int MV>
-int launch_rows(const RowsParams& P, int smem_bytes, int grid, cudaStream_t stream) {
+int launch_rows(RowsParams P, long long R, cudaStream_t stream) {
   auto fn = q8_rows_kernel<K, MV>;
-  static int configured_bytes[64] = {0};
+  static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && configured_bytes[dev] < smem_bytes) {
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return record_cuda(e);
-    configured_bytes[dev] = 200 * 1024;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return record_cuda(e);
+    configured[dev] = 1;
   }
-  fn<<<grid, kThreads, smem_bytes, stream>>>(P);
+  // One wave of resident CTAs, each owning a contiguous row range.
+  const int sms = sm_count();
+  const long long p_total = P.total_rows;
+  auto smem_for = [&](long long rows_cta) {
+    return (long long)P.stage_bytes * P.nstages + 16LL * P.nstages +
+           4LL * rows_cta * P.segs_per_row * P.m;
+  };
+  long long smem = smem_for((p_total + sms - 1) / sms);
+  if (smem > 200 * 1024) return Q8D_EUNSUPPORTED;
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, (size_t)smem);
+  if (e != cudaSuccess) return record_cuda(e);
+  occ = std::max(occ, 1);
+  long long grid = std::min<long long>(p_total, (long long)sms * occ);
+  long long rows_cta = (p_total + grid - 1) / grid;
+  grid = (p_total + rows_cta - 1) / rows_cta;
+  P.rows_per_cta = rows_cta;
+  P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
+  smem = smem_for(rows_cta);
+  fn<<<(int)grid, kThreads, (size_t)smem, stream>>>(P);
   return check_launch();
 }
 
@@ -405,30 +434,19 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   const int MV = (K > 1 || P.m == 1) ? 1 : 2;
   P.segs_per_row = NS;
 
-  // Stage size ~12 KB (whole rows), 4-6 stages; CTAs own contiguous row
-  // ranges, two or three per SM.
-  const int sms = sm_count();
+  // Stages of ~36 KB (whole row quads per row group), 2-5 of them; the
+  // launcher sizes a single wave of resident CTAs.
   const int RG = NS <= kWarps ? kWarps / NS : 1;
   long long R = std::max<long long>(1, 36864 / P.row_bytes);
   if (R >= 4 * RG) R -= R % (4 * RG);       // whole row quads for every row group
   else if (R >= 2 * RG) R -= R % (2 * RG);
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 36 * 1024 ? 3 : 2);
-  long long grid = std::min<long long>(p_total, 2LL * sms);
-  long long rows_cta = (p_total + grid - 1) / grid;
-  grid = (p_total + rows_cta - 1) / rows_cta;
-  P.rows_per_cta = rows_cta;
-  R = std::min<long long>(R, rows_cta);
-  P.rows_per_tile = (int)R;
-  const long long part_bytes = 4LL * rows_cta * NS * P.m;
-  const long long smem = (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + part_bytes;
-  if (smem > 200 * 1024) return Q8D_EUNSUPPORTED;
-
   switch (K * 10 + MV) {
-    case 11: return launch_rows<1, 1>(P, (int)smem, (int)grid, stream);
-    case 12: return launch_rows<1, 2>(P, (int)smem, (int)grid, stream);
-    case 21: return launch_rows<2, 1>(P, (int)smem, (int)grid, stream);
-    case 31: return launch_rows<3, 1>(P, (int)smem, (int)grid, stream);
+    case 11: return launch_rows<1, 1>(P, R, stream);
+    case 12: return launch_rows<1, 2>(P, R, stream);
+    case 21: return launch_rows<2, 1>(P, R, stream);
+    case 31: return launch_rows<3, 1>(P, R, stream);
     default: return Q8D_EUNSUPPORTED;
   }
 }
