@@ -149,6 +149,34 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
                         int* d_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * q8d_gqa_decode_attn_noalloc — q8d_gqa_decode_attn without a caller
+ * workspace.  The pages have no counterpart to this entry point.
+ * It exists for callers that cannot allocate device memory: code whose
+ * device memory is owned by a host framework's allocator or pool that
+ * forbids side allocations, and latency-sensitive loops that cannot afford
+ * cudaMalloc's implicit device-wide synchronisation.  The split-K scratch
+ * lives instead in one fixed array inside libq8d, of
+ * q8d_noalloc_scratch_bytes() bytes (4 MiB) on every GPU that loads the
+ * library, held until the process exits.  Arguments and results are those
+ * of q8d_gqa_decode_attn (the caller still passes q, caches, out, lengths
+ * and the error word); sizes whose scratch would exceed the array,
+ * i.e. q8d_gqa_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, cap)
+ * > q8d_noalloc_scratch_bytes(), are refused with Q8D_ERANGE.
+ * The call allocates nothing.  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and caches it; make that first call before any stream capture.
+ * All calls on a device share the one array, and it keeps the last call's
+ * contents (nothing in it needs to start at zero): calls that overlap on the
+ * GPU (different streams, or concurrent host threads) race on it.
+ * ---------------------------------------------------------------------- */
+size_t q8d_noalloc_scratch_bytes(void);
+int q8d_gqa_decode_attn_noalloc(const float* q, const float* k_new, const float* v_new,
+                                void* kcache, void* vcache, int kv_dtype, float* out, int batch,
+                                int n_heads, int n_kv_heads, int head_dim, int cap,
+                                long long cache_batch_stride, const int* d_lens, float scale,
+                                int* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode step graph ("IV.4: One command buffer per token", "One command
  * buffer": the whole step encoded once and submitted as one unit).
  * The step, per layer: RMSNorm -> q/k/v Q8_0 matvecs -> (q/k/v bias) ->

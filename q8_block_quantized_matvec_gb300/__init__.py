@@ -83,6 +83,11 @@ def lib():
         L.q8d_gqa_decode_attn.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                           i64, vp, f32, vp, sz, vp, vp]
         L.q8d_gqa_decode_attn.restype = i32
+        L.q8d_noalloc_scratch_bytes.argtypes = []
+        L.q8d_noalloc_scratch_bytes.restype = sz
+        L.q8d_gqa_decode_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                  i32, i64, vp, f32, vp, vp]
+        L.q8d_gqa_decode_attn_noalloc.restype = i32
         L.q8d_step_create.argtypes = [C.POINTER(StepDesc), vp, C.POINTER(vp)]
         L.q8d_step_create.restype = i32
         L.q8d_step_launch.argtypes = [vp, vp]
@@ -163,6 +168,23 @@ def q8d_gqa_decode_attn(q, k_new, v_new, kcache, vcache, kv_dtype: int, out, bat
         int(batch), int(n_heads), int(n_kv_heads), int(head_dim), int(cap),
         int(cache_batch_stride), _ptr(d_lens), float(scale), _ptr(workspace), int(ws_bytes),
         _ptr(d_err), _stream(stream)), "q8d_gqa_decode_attn")
+
+
+def q8d_noalloc_scratch_bytes() -> int:
+    return int(lib().q8d_noalloc_scratch_bytes())
+
+
+def q8d_gqa_decode_attn_noalloc(q, k_new, v_new, kcache, vcache, kv_dtype: int, out, batch: int,
+                                n_heads: int, n_kv_heads: int, head_dim: int, cap: int,
+                                cache_batch_stride: int, d_lens, scale: float, d_err,
+                                stream=None) -> int:
+    """q8d_gqa_decode_attn with the scratch in the library's fixed device
+    array (for callers that cannot allocate device memory)."""
+    return _check(lib().q8d_gqa_decode_attn_noalloc(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), int(kv_dtype), _ptr(out),
+        int(batch), int(n_heads), int(n_kv_heads), int(head_dim), int(cap),
+        int(cache_batch_stride), _ptr(d_lens), float(scale), _ptr(d_err), _stream(stream)),
+        "q8d_gqa_decode_attn_noalloc")
 
 
 class Step:
