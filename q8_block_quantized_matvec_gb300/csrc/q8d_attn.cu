@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "q8d_attn.cuh"
+#include "q8d_attn_common.cuh"
 #include "q8d_internal.cuh"
 
 namespace q8d {
@@ -98,6 +99,10 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.n_heads / P.n_kv_heads;
+  if (P.pdl) {
+    griddep_launch_dependents();
+    griddep_wait();
+  }
   const int L = P.d_lens[b];
   if (L < 1 || L > P.cap) {
     if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
@@ -111,22 +116,38 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   KT* kbase = reinterpret_cast<KT*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
   KT* vbase = reinterpret_cast<KT*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
 
-  // In-kernel append of row L-1 by the CTA that owns it.
-  if (P.k_new != nullptr && t_end == L) {
-    const float* kn = P.k_new + (long long)b * kvw + (long long)g * D;
-    const float* vn = P.v_new + (long long)b * kvw + (long long)g * D;
-    for (int j = tid; j < D; j += kAttnThreads) {
-      kbase[(long long)(L - 1) * kvw + j] = to_cache<KT>(kn[j]);
-      vbase[(long long)(L - 1) * kvw + j] = to_cache<KT>(vn[j]);
-    }
+  // In-kernel append of row L-1 by the CTA that owns it (warp 0 the k row
+  // with its bias / norm / RoPE prologue, warp 1 the v row with its bias).
+  const int half = D / 2;
+  const float* cosr = P.rope_cos ? P.rope_cos + (long long)(L - 1) * half : nullptr;
+  const float* sinr = P.rope_sin ? P.rope_sin + (long long)(L - 1) * half : nullptr;
+  if (P.k_new != nullptr && t_end == L && warp < 2) {
+    const float* src = (warp == 0 ? P.k_new : P.v_new) + (long long)b * kvw + (long long)g * D;
+    float v[D / 32];
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) v[t] = src[lane + 32 * t];
+    if (warp == 0)
+      head_prologue<D>(v, lane, P.bk ? P.bk + (long long)g * D : nullptr, P.k_norm, P.eps, cosr, sinr);
+    else
+      head_prologue<D>(v, lane, P.bv ? P.bv + (long long)g * D : nullptr, nullptr, 0.f, nullptr,
+                       nullptr);
+    KT* dst = (warp == 0 ? kbase : vbase) + (long long)(L - 1) * kvw;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = to_cache<KT>(v[t]);
     fence_proxy_async_global();
   }
 
-  // Query rows of the group, pre-scaled into the log2 domain.
+  // Query rows of the group (with the step prologue), scaled into the log2 domain.
   const float qscale = P.scale * kLog2e;
-  for (int e = tid; e < G * D; e += kAttnThreads) {
-    const int hh = e / D, j = e % D;
-    qs[hh * D + j] = P.q[((long long)b * P.n_heads + (long long)g * G + hh) * D + j] * qscale;
+  for (int hh = warp; hh < G; hh += kAttnThreads / 32) {
+    const int hq_ = g * G + hh;
+    float v[D / 32];
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) v[t] = P.q[((long long)b * P.n_heads + hq_) * D + lane + 32 * t];
+    head_prologue<D>(v, lane, P.bq ? P.bq + (long long)hq_ * D : nullptr, P.q_norm, P.eps, cosr,
+                     sinr);
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) qs[hh * D + lane + 32 * t] = v[t] * qscale;
   }
   if (tid < GMAX) {
     m_run[tid] = -INFINITY;
@@ -297,6 +318,10 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
       P.ws_l[hq * P.nc + c] = l_run[h];
     }
   }
+  if (P.tickets) {
+    __syncthreads();  // the reduction buffer is free for the merge's weights
+    ticket_combine<D>(P, L, tpc, b, g, G, smem);
+  }
 }
 
 // Merges the chunk partials of one (sequence, query head):
@@ -387,9 +412,8 @@ int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
     configured[dev] = true;
   }
   dim3 grid(P.nc, P.n_kv_heads, P.batch);
-  fn<<<grid, kAttnThreads, C::kSmem, stream>>>(P);
-  int rc = check_launch();
-  if (rc) return rc;
+  const int rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, P.pdl != 0, P);
+  if (rc || P.tickets) return rc;
   return attn_combine_launch(P, stream);
 }
 

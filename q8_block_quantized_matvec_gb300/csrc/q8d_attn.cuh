@@ -20,6 +20,22 @@ struct AttnParams {
   void* workspace;
   int nc;               // context chunks per (sequence, KV head)
   int* d_err;
+  // Decode-step prologue fused into the f16 kernel (all null / 0 for the
+  // plain C-ABI call): q/k/v biases, per-head q/k RMSNorm gains, RoPE table
+  // [cap][head_dim/2] at position L-1, applied to q and to the appended row.
+  const float* bq;
+  const float* bk;
+  const float* bv;
+  const float* q_norm;
+  const float* k_norm;
+  float eps;
+  const float* rope_cos;
+  const float* rope_sin;
+  // Zero-initialised tickets [batch * n_kv_heads]: when set, the last chunk
+  // CTA of each (sequence, KV head) merges the partials itself (and resets
+  // its ticket); when null a separate combine kernel runs.
+  int* tickets;
+  int pdl;              // launched as a programmatic dependent
   // carved from the workspace by attn_launch
   float* ws_o;
   float* ws_m;

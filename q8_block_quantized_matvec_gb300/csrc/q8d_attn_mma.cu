@@ -14,14 +14,18 @@
 //    f16 hi + lo parts (q = hi + lo to ~2^-22), and so are the
 //    probabilities (scaled by 2^12 first); every product is exact in the f32
 //    accumulator, so the result matches f32 CUDA-core arithmetic.
-//  * Each warp runs its own online softmax over 16 tokens of every 64-token
-//    sub-tile; the four warps' {m, l, O} are merged once at the end of the
-//    chunk and written as the chunk's partial for the combine kernel.
-//  * K/V rows stream through a two-stage ring of bulk copies; rows are padded
-//    by 16 bytes so fragment loads and ldmatrix.trans hit distinct banks.
+//  * Each warp runs its own online softmax over its token groups (groups
+//    w, w+4, w+8, ... of the chunk); the four warps' {m, l, O} are merged once
+//    at the end of the chunk and written as the chunk's partial.
+//  * Every warp streams its own 16-token groups of K/V rows through a
+//    three-stage cp.async ring (16-byte copies; a KV head's row is only 128
+//    or 256 bytes, too small for efficient bulk copies) and never waits for
+//    the other warps until the final merge.  Rows are padded by 16 bytes so
+//    fragment loads and ldmatrix.trans hit distinct banks.
 #include <cuda_fp16.h>
 
 #include "q8d_attn.cuh"
+#include "q8d_attn_common.cuh"
 #include "q8d_internal.cuh"
 
 namespace q8d {
@@ -29,21 +33,33 @@ namespace {
 
 constexpr int kWarpsA = 4;
 constexpr int kThreadsA = kWarpsA * 32;
-constexpr int kTS = 64;                // tokens per sub-tile (16 per warp)
 constexpr float kLog2eA = 1.4426950408889634f;
 constexpr float kPScale = 4096.f;      // probabilities scaled by 2^12 before the f16 split
 
+constexpr int kGroup = 16;             // tokens per warp step
+constexpr int kWStages = 3;            // per-warp cp.async ring depth
+
 template <int D>
 struct MCfg {
-  static constexpr int kRow = D * 2;                // f16 row bytes
-  static constexpr int kStride = kRow + 16;         // padded shared-memory row
-  static constexpr int kStage = 2 * kTS * kStride;  // K rows, then V rows
-  static constexpr int kOffQ = 2 * kStage;          // f32 q [16][D], power-of-two scaled
-  static constexpr int kOffF = kOffQ + 16 * D * 4;  // per-head score factor [16]
-  static constexpr int kOffBar = kOffF + 16 * 4;
-  static constexpr int kSmem = kOffBar + 16;
-  static_assert(kWarpsA * 16 * (D + 2) * 4 <= 2 * kStage, "merge buffer fits the stages");
+  static constexpr int kRow = D * 2;                     // f16 row bytes
+  static constexpr int kStride = kRow + 16;              // padded shared-memory row
+  static constexpr int kStage = 2 * kGroup * kStride;    // 16 K rows, then 16 V rows
+  static constexpr int kWarpRing = kWStages * kStage;    // one warp's ring
+  static constexpr int kOffQ = kWarpsA * kWarpRing;      // f32 q [16][D], power-of-two scaled
+  static constexpr int kOffF = kOffQ + 16 * D * 4;       // per-head score factor [16]
+  static constexpr int kSmem = kOffF + 16 * 4;
+  static_assert(kWarpsA * 16 * (D + 2) * 4 <= kOffQ, "merge buffer fits the rings");
 };
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // v = hi + lo with hi = f16(v), lo = f16(v - hi), for a pair of floats.
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -78,12 +94,15 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   extern __shared__ __align__(128) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
   float* fh = reinterpret_cast<float*>(smem + C::kOffF);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, cq = lane & 3;
   const int G = P.n_heads / P.n_kv_heads;
+  if (P.pdl) {
+    griddep_launch_dependents();
+    griddep_wait();
+  }
   const int L = P.d_lens[b];
   if (L < 1 || L > P.cap) {
     if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
@@ -97,59 +116,77 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   __half* kbase = reinterpret_cast<__half*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
   __half* vbase = reinterpret_cast<__half*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
 
-  // In-kernel append of row L-1 by the CTA that owns it; the bulk copies
-  // below read it back, so attended values are exactly the cached ones.
-  if (P.k_new != nullptr && t_end == L) {
-    const float* kn = P.k_new + (long long)b * kvw + (long long)g * D;
-    const float* vn = P.v_new + (long long)b * kvw + (long long)g * D;
-    for (int j = tid; j < D; j += kThreadsA) {
-      kbase[(long long)(L - 1) * kvw + j] = __float2half_rn(kn[j]);
-      vbase[(long long)(L - 1) * kvw + j] = __float2half_rn(vn[j]);
-    }
-    fence_proxy_async_global();
+  // In-kernel append of row L-1 by the CTA that owns it; the copies below
+  // read it back after the barrier, so attended values are the cached ones.
+  const int half = D / 2;
+  const float* cosr = P.rope_cos ? P.rope_cos + (long long)(L - 1) * half : nullptr;
+  const float* sinr = P.rope_sin ? P.rope_sin + (long long)(L - 1) * half : nullptr;
+  if (P.k_new != nullptr && t_end == L && warp < 2) {
+    // warp 0: k row (bias, norm, RoPE), warp 1: v row (bias)
+    const float* src = (warp == 0 ? P.k_new : P.v_new) + (long long)b * kvw + (long long)g * D;
+    float v[D / 32];
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) v[t] = src[lane + 32 * t];
+    if (warp == 0)
+      head_prologue<D>(v, lane, P.bk ? P.bk + (long long)g * D : nullptr, P.k_norm, P.eps, cosr, sinr);
+    else
+      head_prologue<D>(v, lane, P.bv ? P.bv + (long long)g * D : nullptr, nullptr, 0.f, nullptr,
+                       nullptr);
+    __half* dst = (warp == 0 ? kbase : vbase) + (long long)(L - 1) * kvw;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = __float2half_rn(v[t]);
   }
 
   // Query rows scaled per head by 2^sh so that max|q| < 2^11; the score
   // factor 2^-sh * scale * log2(e) undoes it in the log2 domain.
   for (int hh = warp; hh < 16; hh += kWarpsA) {
-    const float* qrow = P.q + ((long long)b * P.n_heads + (long long)g * G + hh) * D;
-    float mx = 0.f;
+    const int hq_ = g * G + hh;
+    float v[D / 32];
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t)
+      v[t] = (hh < G) ? P.q[((long long)b * P.n_heads + hq_) * D + lane + 32 * t] : 0.f;
     if (hh < G)
-      for (int j = lane; j < D; j += 32) mx = fmaxf(mx, fabsf(qrow[j]));
+      head_prologue<D>(v, lane, P.bq ? P.bq + (long long)hq_ * D : nullptr, P.q_norm, P.eps, cosr,
+                       sinr);
+    float mx = 0.f;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) mx = fmaxf(mx, fabsf(v[t]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     int e = 0;
     if (mx > 0.f) frexpf(mx, &e);
     const int sh = (mx > 0.f) ? 11 - e : 0;
-    for (int j = lane; j < D; j += 32) qs[hh * D + j] = (hh < G) ? ldexpf(qrow[j], sh) : 0.f;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) qs[hh * D + lane + 32 * t] = ldexpf(v[t], sh);
     if (lane == 0) fh[hh] = (hh < G) ? ldexpf(P.scale * kLog2eA, -sh) : 0.f;
   }
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
+  __syncthreads();  // q rows scaled; the appended row is visible to every thread
 
-  const uint64_t pol = policy_evict_first();
-  const int n_sub = (t_end - t_begin + kTS - 1) / kTS;
-  auto issue = [&](int k) {  // warp 0
-    if (k >= n_sub) return;
-    const int r0 = t_begin + k * kTS;
-    const int nr = min(kTS, t_end - r0);
-    uint8_t* st = smem + (k & 1) * C::kStage;
-    if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)(2 * nr * C::kRow));
-    __syncwarp();
-    for (int r = lane; r < nr; r += 32) {
-      const long long row = (long long)(r0 + r) * kvw;
-      bulk_g2s(st + r * C::kStride, kbase + row, C::kRow, &bar[k & 1], pol);
-      bulk_g2s(st + (kTS + r) * C::kStride, vbase + row, C::kRow, &bar[k & 1], pol);
+  // ---- this warp's cp.async ring over its token groups ----
+  const int ngroups = (t_end - t_begin + kGroup - 1) / kGroup;
+  const int my_groups = ngroups > warp ? (ngroups - warp + kWarpsA - 1) / kWarpsA : 0;
+  uint8_t* ring = smem + warp * C::kWarpRing;
+  auto load_group = [&](int i) {  // i-th group of this warp into stage i % kWStages
+    if (i < my_groups) {
+      const int t0 = t_begin + (warp + kWarpsA * i) * kGroup;
+      const int nr = min(kGroup, t_end - t0);
+      uint8_t* st = ring + (i % kWStages) * C::kStage;
+      constexpr int kChunks = C::kRow / 16;  // 16-byte pieces per row
+#pragma unroll
+      for (int e = lane; e < kGroup * kChunks; e += 32) {
+        const int r = e / kChunks, pc = e % kChunks;
+        if (r < nr) {
+          const long long off = (long long)(t0 + r) * kvw * 2 + pc * 16;
+          cp_async16(st + r * C::kStride + pc * 16, reinterpret_cast<const uint8_t*>(kbase) + off);
+          cp_async16(st + (kGroup + r) * C::kStride + pc * 16,
+                     reinterpret_cast<const uint8_t*>(vbase) + off);
+        }
+      }
     }
+    cp_async_commit();  // possibly empty: keeps the group count uniform
   };
-  if (warp == 0) {
-    issue(0);
-    issue(1);
-  }
+#pragma unroll
+  for (int i = 0; i < kWStages - 1; ++i) load_group(i);
 
   // A fragments of q (rows gq and gq + 8, K = head_dim), hi and lo parts.
   uint32_t qh[KS][4], ql[KS][4];
@@ -167,14 +204,14 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
 #pragma unroll
   for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  bool ok = true;
 
-  for (int k = 0; k < n_sub; ++k) {
-    const int nr = min(kTS, t_end - (t_begin + k * kTS));
-    ok = mbar_wait(&bar[k & 1], (uint32_t)(k >> 1) & 1u);
-    if (!__syncthreads_and(ok)) break;
-    const uint8_t* st = smem + (k & 1) * C::kStage;
-    const int base_t = warp * 16;
+  for (int i = 0; i < my_groups; ++i) {
+    load_group(i + kWStages - 1);
+    cp_async_wait<kWStages - 1>();
+    __syncwarp();
+    const int nr = min(kGroup, t_end - (t_begin + (warp + kWarpsA * i) * kGroup));
+    const uint8_t* st = ring + (i % kWStages) * C::kStage;
+    const int base_t = 0;
 
     // ---- S = Q.K^T for this warp's 16 tokens (two n-tiles of 8) ----
     // hi and lo products accumulate in separate chains (4 independent MMA
@@ -259,7 +296,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     {
       const int mi = lane >> 3, r = lane & 7;
       const int tok = min(base_t + (mi & 1) * 8 + r, nr - 1);
-      const uint32_t vrow = smem_u32(st + (kTS + tok) * C::kStride + (mi >> 1) * 16);
+      const uint32_t vrow = smem_u32(st + (kGroup + tok) * C::kStride + (mi >> 1) * 16);
 #pragma unroll
       for (int dn = 0; dn < D / 16; ++dn) {
         uint32_t v0, v1, v2, v3;
@@ -270,9 +307,9 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
         mma16816(o[2 * dn + 1], pl, v2, v3);
       }
     }
-    __syncthreads();
-    if (warp == 0) issue(k + 2);
+    __syncwarp();  // the stage is refilled by the next iteration's load
   }
+  cp_async_wait<0>();
 
   // ---- merge the four warps' {m, l, O}; write the chunk's partial ----
   __syncthreads();
@@ -294,9 +331,6 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     oo[(warp * 16 + gq + 8) * D + col + 1] = o[n][3];
   }
   __syncthreads();
-  if (!ok) {
-    if (tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
-  }
   for (int e = tid; e < G * D; e += kThreadsA) {
     const int h = e / D, j = e % D;
     float M = -INFINITY;
@@ -312,12 +346,15 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
       lsum = fmaf(ll[w * 16 + h], wgt, lsum);
     }
     const long long hq = (long long)b * P.n_heads + (long long)g * G + h;
-    P.ws_o[(hq * P.nc + c) * D + j] = ok ? acc * (1.f / kPScale) : __int_as_float(0x7fc00000);
+    P.ws_o[(hq * P.nc + c) * D + j] = acc * (1.f / kPScale);
     if (j == 0) {
       P.ws_m[hq * P.nc + c] = M;
       P.ws_l[hq * P.nc + c] = lsum;
     }
   }
+  if (!P.tickets) return;
+
+  ticket_combine<D>(P, L, tpc, b, g, G, smem);
 }
 
 template <int D>
@@ -333,9 +370,9 @@ int launch_mma(const AttnParams& P, cudaStream_t stream) {
     configured[dev] = true;
   }
   dim3 grid(P.nc, P.n_kv_heads, P.batch);
-  gqa_mma_kernel<D><<<grid, kThreadsA, C::kSmem, stream>>>(P);
-  const int rc = check_launch();
-  if (rc) return rc;
+  const int rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
+                           P.pdl != 0, P);
+  if (rc || P.tickets) return rc;
   return attn_combine_launch(P, stream);
 }
 

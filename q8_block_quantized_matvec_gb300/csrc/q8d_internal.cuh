@@ -96,6 +96,36 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------
+// Lets the next kernel in the stream start its prologue now.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernels this one depends on have completed and their
+// writes are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kernel` on `stream`, as a programmatic dependent of the previous
+// work in the stream when `pdl` is set.
+template <typename... Args>
+int launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+              bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e == cudaSuccess ? Q8D_OK : record_cuda(e);
+}
+
 // ---- packed f32x2 arithmetic (Blackwell) ---------------------------------
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   uint64_t r;

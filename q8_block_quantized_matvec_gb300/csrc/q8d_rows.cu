@@ -112,9 +112,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Loads the activation pairs of vectors v0..v0+MV-1 for block columns
-// seg*32K + k*32 + lane into registers (zeros past the row end / m).
+// seg*32K + k*32 + lane into registers (zeros past the row end / m),
+// applying the launch's activation transform (m == 1 for the transforms).
 template <int K, int MV>
-__device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int lane,
+__device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int lane, float inv,
                                        uint64_t (&xr)[MV][K][16]) {
 #pragma unroll
   for (int i = 0; i < MV; ++i) {
@@ -122,16 +123,33 @@ __device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int
     for (int k = 0; k < K; ++k) {
       const int b = seg * 32 * K + k * 32 + lane;
       const bool ok = (v0 + i < P.m) && (b < P.bpr);
-      const float4* xp =
-          reinterpret_cast<const float4*>(P.X + (size_t)(v0 + i) * P.ldx + (size_t)b * kQBlock);
+      const size_t base = (size_t)(v0 + i) * P.ldx + (size_t)b * kQBlock;
+      const float4* xp = reinterpret_cast<const float4*>(P.X + base);
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok && P.xmode == kXRmsNorm) {
+          const float4 wv = __ldg(reinterpret_cast<const float4*>(P.xw + base) + t);
+          v.x = v.x * inv * wv.x;
+          v.y = v.y * inv * wv.y;
+          v.z = v.z * inv * wv.z;
+          v.w = v.w * inv * wv.w;
+        } else if (ok && P.xmode == kXSiluMul) {
+          const float4 u = __ldg(reinterpret_cast<const float4*>(P.X + base + P.n) + t);
+          v.x = v.x / (1.0f + expf(-v.x)) * u.x;
+          v.y = v.y / (1.0f + expf(-v.y)) * u.y;
+          v.z = v.z / (1.0f + expf(-v.z)) * u.z;
+          v.w = v.w / (1.0f + expf(-v.w)) * u.w;
+        }
         xr[i][k][2 * t] = pack2(v.x, v.y);
         xr[i][k][2 * t + 1] = pack2(v.z, v.w);
       }
     }
   }
+}
+
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
 }
 
 // One tile of the CTA's contiguous row range: rows [r0, r0 + rows) of
@@ -218,7 +236,34 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
     }
   };
   const bool producer = (warp == 0 && lane == 0);
+  // Weights do not depend on earlier kernels: start streaming them first.
   if (producer) produce(P.nstages);
+  if (P.pdl) {
+    griddep_launch_dependents();
+    griddep_wait();  // activations written by the previous kernel are visible now
+  }
+  // RMSNorm of x (the same sum, in the same order, in every CTA).
+  __shared__ float red_ss[kWarps];
+  float inv_rms = 1.f;
+  if (P.xmode == kXRmsNorm) {
+    float ss = 0.f;
+    const float4* x4 = reinterpret_cast<const float4*>(P.X);
+    for (int i = threadIdx.x; i < P.n / 4; i += kThreads) {
+      const float4 v = __ldg(x4 + i);
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red_ss[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += red_ss[w];
+    inv_rms = 1.0f / sqrtf(tot / (float)P.n + P.eps);
+  }
   {
     // ---------------- consumers ----------------
     const bool x_static = (NS <= kWarps) && (P.m <= MV);
@@ -229,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
     const bool active = (NS <= kWarps) ? (warp < NS * RG) : true;
 
     uint64_t xr[MV][K][16];
-    if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, xr);
+    if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, inv_rms, xr);
 
     if (MV == 1 && x_static) {
       // Matvec fast path: branch-free inner loop.  Lanes past the row end
@@ -306,7 +351,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
         const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
         for (int v0m = 0; v0m < P.m; v0m += MV) {
           for (int seg = my_seg0; seg < NS; seg += seg_step) {
-            if (!x_static) load_x<K, MV>(P, v0m, seg, lane, xr);
+            if (!x_static) load_x<K, MV>(P, v0m, seg, lane, inv_rms, xr);
             for (int rl = first; rl < t.rows; rl += RG) {
               float acc[MV];
 #pragma unroll
@@ -344,6 +389,8 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
     if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
     return;
   }
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
   for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
     const int rc = e / P.m, m = e % P.m;
     float sum = 0.f;
@@ -352,7 +399,40 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
     int sg = 0;
     while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
     float* y = P.seg[sg].y + (size_t)m * P.ldy + (vr - P.vbegin[sg]);
-    *y = P.accumulate ? (*y + sum) : sum;
+    const float out = P.accumulate ? (*y + sum) : sum;
+    *y = out;
+    const int ri = (int)(vr - P.vbegin[sg]);
+    if (!isnan(out) && am_better(out, ri, bv, bi)) {
+      bv = out;
+      bi = ri;
+    }
+  }
+  if (P.am_val) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (am_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    __shared__ float s_bv[kWarps];
+    __shared__ int s_bi[kWarps];
+    if (lane == 0) {
+      s_bv[warp] = bv;
+      s_bi[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kWarps; ++w)
+        if (am_better(s_bv[w], s_bi[w], bv, bi)) {
+          bv = s_bv[w];
+          bi = s_bi[w];
+        }
+      P.am_val[blockIdx.x] = bv;
+      P.am_idx[blockIdx.x] = bi;
+    }
   }
 }
 
@@ -363,7 +443,7 @@ __global__ void fill_zero_kernel(float* y, int ldy, int m, int p) {
 }
 
 template <int K, int MV>
-int launch_rows(RowsParams P, long long R, cudaStream_t stream) {
+int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   auto fn = q8_rows_kernel<K, MV>;
   static int configured[64] = {0};
   int dev = 0;
@@ -395,13 +475,14 @@ int launch_rows(RowsParams P, long long R, cudaStream_t stream) {
   P.rows_per_cta = rows_cta;
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   smem = smem_for(rows_cta);
-  fn<<<(int)grid, kThreads, (size_t)smem, stream>>>(P);
-  return check_launch();
+  if (grid_out) *grid_out = (int)grid;
+  return launch_ex(fn, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, P.pdl != 0,
+                   P);
 }
 
 }  // namespace
 
-int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
+int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   if (P.m <= 0) return Q8D_OK;
   long long p_total = 0;
   for (int s = 0; s < P.nseg; ++s) {
@@ -433,6 +514,7 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   const int NS = (P.bpr + 32 * K - 1) / (32 * K);
   const int MV = (K > 1 || P.m == 1) ? 1 : 2;
   P.segs_per_row = NS;
+  if ((P.xmode != kXPlain || P.am_val) && (P.m != 1 || NS > kWarps)) return Q8D_EUNSUPPORTED;
 
   // Stages of ~36 KB (whole row quads per row group), 2-5 of them; the
   // launcher sizes a single wave of resident CTAs.
@@ -443,10 +525,10 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream) {
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 36 * 1024 ? 3 : 2);
   switch (K * 10 + MV) {
-    case 11: return launch_rows<1, 1>(P, R, stream);
-    case 12: return launch_rows<1, 2>(P, R, stream);
-    case 21: return launch_rows<2, 1>(P, R, stream);
-    case 31: return launch_rows<3, 1>(P, R, stream);
+    case 11: return launch_rows<1, 1>(P, R, stream, grid_out);
+    case 12: return launch_rows<1, 2>(P, R, stream, grid_out);
+    case 21: return launch_rows<2, 1>(P, R, stream, grid_out);
+    case 31: return launch_rows<3, 1>(P, R, stream, grid_out);
     default: return Q8D_EUNSUPPORTED;
   }
 }

@@ -25,6 +25,18 @@ struct RowsParams {
   int m;               // activation rows (1 = matvec)
   int accumulate;      // 1: Y += result (residual add), 0: Y = result
   int* d_err;          // device error word or nullptr
+  // Activation transform applied while x is loaded (m == 1 only):
+  //   kXPlain   x as given
+  //   kXRmsNorm x * (1/sqrt(mean(x^2) + eps)) * xw          (RMSNorm)
+  //   kXSiluMul silu(X[k]) * X[n + k]                        (SwiGLU gate)
+  int xmode;
+  const float* xw;
+  float eps;
+  // Per-CTA argmax of the written rows (m == 1): value and row index at
+  // [blockIdx.x], ties to the lower index, NaN never wins; or nullptr.
+  float* am_val;
+  int* am_idx;
+  int pdl;             // launched as a programmatic dependent of the previous kernel
   // filled by the planner
   int bpr;
   long long row_bytes;
@@ -34,7 +46,10 @@ struct RowsParams {
   int rows_per_tile, stage_bytes, nstages, segs_per_row;
 };
 
-// Plans tiles/stages and launches the kernel on `stream`.  Returns a status.
-int rows_plan_and_launch(RowsParams P, cudaStream_t stream);
+enum { kXPlain = 0, kXRmsNorm = 1, kXSiluMul = 2 };
+
+// Plans tiles/stages and launches the kernel on `stream`.  Returns a status;
+// *grid_out (if given) receives the number of CTAs launched.
+int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out = nullptr);
 
 }  // namespace q8d
