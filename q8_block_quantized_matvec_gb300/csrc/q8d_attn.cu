@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   const int L = P.d_lens[b];
   if (L < 1 || L > P.cap) {
     if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
+    if (P.tickets && c == 0)  // no merge will run: the outputs must not look valid
+      for (int e = tid; e < G * D; e += kAttnThreads)
+        P.out[((long long)b * P.n_heads + (long long)g * G) * D + e] = __int_as_float(0x7fc00000);
     return;
   }
   const int tpc = chunk_rows(L, P.nc);
@@ -374,14 +377,17 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const AttnParams P) {
     s_tot = t;
   }
   __syncthreads();
-  float acc0 = 0.f, acc1 = 0.f;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int c = 0;
-#pragma unroll 4
-  for (; c + 1 < nact; c += 2) {
-    acc0 = fmaf(O[(long long)c * D + j], wsm[c], acc0);
-    acc1 = fmaf(O[(long long)(c + 1) * D + j], wsm[c + 1], acc1);
+  for (; c + 8 <= nact; c += 8) {
+    float o8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o8[u] = O[(long long)(c + u) * D + j];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a[u] = fmaf(o8[u], wsm[c + u], a[u]);
   }
-  if (c < nact) acc0 = fmaf(O[(long long)c * D + j], wsm[c], acc0);
+  for (; c < nact; ++c) a[0] = fmaf(O[(long long)c * D + j], wsm[c], a[0]);
+  const float acc0 = (a[0] + a[1]) + (a[2] + a[3]), acc1 = (a[4] + a[5]) + (a[6] + a[7]);
   o[j] = (acc0 + acc1) / s_tot;
 }
 
@@ -440,7 +446,9 @@ int attn_chunks(int batch, int n_kv_heads, int max_len) {
   const int target = 4 * sm_count();
   int nc = (target + batch * n_kv_heads - 1) / (batch * n_kv_heads);
   const int cap_nc = (std::max(max_len, 1) + kMinChunk - 1) / kMinChunk;
-  return std::max(1, std::min(nc, cap_nc));
+  // at most 256 chunk slots: the in-kernel merge keeps 2 * G * slots floats
+  // in shared memory
+  return std::max(1, std::min(std::min(nc, cap_nc), 256));
 }
 
 size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len) {

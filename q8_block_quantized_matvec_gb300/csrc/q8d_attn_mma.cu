@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   const int L = P.d_lens[b];
   if (L < 1 || L > P.cap) {
     if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
+    if (P.tickets && c == 0)  // no merge will run: the outputs must not look valid
+      for (int e = tid; e < G * D; e += kThreadsA)
+        P.out[((long long)b * P.n_heads + (long long)g * G) * D + e] = __int_as_float(0x7fc00000);
     return;
   }
   const int tpc = chunk_rows(L, P.nc);
@@ -139,26 +142,36 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
 
   // Query rows scaled per head by 2^sh so that max|q| < 2^11; the score
   // factor 2^-sh * scale * log2(e) undoes it in the log2 domain.
-  for (int hh = warp; hh < 16; hh += kWarpsA) {
-    const int hq_ = g * G + hh;
-    float v[D / 32];
+  {
+    // this warp's four query heads: loads first (all in flight), then the
+    // prologue and the power-of-two scaling per head
+    float v[4][D / 32];
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t)
-      v[t] = (hh < G) ? P.q[((long long)b * P.n_heads + hq_) * D + lane + 32 * t] : 0.f;
-    if (hh < G)
-      head_prologue<D>(v, lane, P.bq ? P.bq + (long long)hq_ * D : nullptr, P.q_norm, P.eps, cosr,
-                       sinr);
-    float mx = 0.f;
+    for (int u = 0; u < 4; ++u) {
+      const int hh = warp + kWarpsA * u;
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t) mx = fmaxf(mx, fabsf(v[t]));
+      for (int t = 0; t < D / 32; ++t)
+        v[u][t] = (hh < G) ? P.q[((long long)b * P.n_heads + g * G + hh) * D + lane + 32 * t] : 0.f;
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    int e = 0;
-    if (mx > 0.f) frexpf(mx, &e);
-    const int sh = (mx > 0.f) ? 11 - e : 0;
+    for (int u = 0; u < 4; ++u) {
+      const int hh = warp + kWarpsA * u;
+      const int hq_ = g * G + hh;
+      if (hh < G)
+        head_prologue<D>(v[u], lane, P.bq ? P.bq + (long long)hq_ * D : nullptr, P.q_norm, P.eps,
+                         cosr, sinr);
+      float mx = 0.f;
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t) qs[hh * D + lane + 32 * t] = ldexpf(v[t], sh);
-    if (lane == 0) fh[hh] = (hh < G) ? ldexpf(P.scale * kLog2eA, -sh) : 0.f;
+      for (int t = 0; t < D / 32; ++t) mx = fmaxf(mx, fabsf(v[u][t]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      int e = 0;
+      if (mx > 0.f) frexpf(mx, &e);
+      const int sh = (mx > 0.f) ? 11 - e : 0;
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) qs[hh * D + lane + 32 * t] = ldexpf(v[u][t], sh);
+      if (lane == 0) fh[hh] = (hh < G) ? ldexpf(P.scale * kLog2eA, -sh) : 0.f;
+    }
   }
   __syncthreads();  // q rows scaled; the appended row is visible to every thread
 

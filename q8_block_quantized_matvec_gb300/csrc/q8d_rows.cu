@@ -33,8 +33,8 @@ namespace q8d {
 
 namespace {
 
-constexpr int kWarps = 8;              // warps per CTA, all consume
-constexpr int kThreads = kWarps * 32;  // lane 0 of warp 0 also produces
+constexpr int kWarpsSmall = 8;   // warps per CTA for rows of up to 8 segments
+constexpr int kWarpsLong = 20;   // warps per CTA for rows of 9..20 segments
 
 // Decodes the 32 quants of the block at byte offset `o` of the 4-byte
 // aligned shared buffer `s32` into 16 packed f32x2 pairs, and returns the
@@ -177,9 +177,12 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
 // arrives on); all warps consume.  Each CTA owns a contiguous range of output rows;
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
-template <int K, int MV>
-__global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 168)
+template <int MV, int W>
+__global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 96)
     q8_rows_kernel(const RowsParams P) {
+  constexpr int K = 1;
+  constexpr int kWarps = W;
+  constexpr int kThreads = W * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = P.segs_per_row;
@@ -277,16 +280,34 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
     if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, inv_rms, xr);
 
     if (MV == 1 && x_static) {
-      // Matvec fast path: branch-free inner loop.  Lanes past the row end
-      // read a valid block with zero activations; an odd last row is
-      // computed twice and stored once; two rows are reduced together.
+      // Matvec fast path, branch-free inner loop.  Lanes past the row end read
+      // a valid block with zero activations.  A warp's rows are the CTA rows
+      // r = my_rg (mod RG) in order; their dot products wait in a rotating
+      // buffer and are reduced four at a time with one transposed shuffle
+      // tree (lane 8j ends with the sum of row j), across tile boundaries.
       const uint32_t rowb = (uint32_t)P.row_bytes;
-      uint32_t boff[K];
+      const int bcol = my_seg0 * 32 + lane;
+      const uint32_t boff = (uint32_t)(bcol < P.bpr ? bcol : P.bpr - 1) * kQBlockBytes;
+      float* pcol = part + my_seg0;
+      float q0 = 0.f, q1 = 0.f, q2 = 0.f;
+      int cnt = 0;  // rows of this warp done so far
+      auto push = [&](float v) {
+        const int slot = cnt & 3;
+        if (slot == 0) q0 = v;
+        else if (slot == 1) q1 = v;
+        else if (slot == 2) q2 = v;
+        else {
+          const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+          const float u0 = (b4 ? q2 : q0) + __shfl_xor_sync(0xffffffffu, b4 ? q0 : q2, 16);
+          const float u1 = (b4 ? v : q1) + __shfl_xor_sync(0xffffffffu, b4 ? q1 : v, 16);
+          float w = (b3 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, b3 ? u0 : u1, 8);
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int b = my_seg0 * 32 * K + k * 32 + lane;
-        boff[k] = (uint32_t)(b < P.bpr ? b : P.bpr - 1) * kQBlockBytes;
-      }
+          for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+          const int row = my_rg + (cnt - 3 + (lane >> 3)) * RG;  // CTA row of this lane's sum
+          if ((lane & 7) == 0) pcol[(size_t)row * NS] = w;
+        }
+        ++cnt;
+      };
       long long cur = v0;
       for (int i = 0; cur < v1; ++i) {
         const Tile t = tile_at(P, cur, v0, v1);
@@ -297,44 +318,26 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__((K * MV <= 2) ? 128 : 16
         }
         if (active) {
           const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * s);
-          const uint32_t delta = (uint32_t)((t.r0 * P.row_bytes) & 15LL);
-          const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
-          float* prow = part + (size_t)t.vrow0 * NS + my_seg0;
-          int rl = first;
-          // four rows at a time: independent decode streams, one transposed
-          // shuffle tree (lane 8j ends with the sum of row j)
-          for (; rl + 3 * RG < t.rows; rl += 4 * RG) {
-            float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-#pragma unroll
-            for (int k = 0; k < K; ++k) {
-              const uint32_t o = delta + (uint32_t)rl * rowb + boff[k];
-              const uint32_t st = (uint32_t)RG * rowb;
-              v0 += block_dot_smem(s32, o, xr[0][k]);
-              v1 += block_dot_smem(s32, o + st, xr[0][k]);
-              v2 += block_dot_smem(s32, o + 2 * st, xr[0][k]);
-              v3 += block_dot_smem(s32, o + 3 * st, xr[0][k]);
-            }
-            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-            const float u0 = (b4 ? v2 : v0) + __shfl_xor_sync(0xffffffffu, b4 ? v0 : v2, 16);
-            const float u1 = (b4 ? v3 : v1) + __shfl_xor_sync(0xffffffffu, b4 ? v1 : v3, 16);
-            float w = (b3 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, b3 ? u0 : u1, 8);
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-            if ((lane & 7) == 0) prow[(size_t)(rl + (lane >> 3) * RG) * NS] = w;
+          const uint32_t base = (uint32_t)((t.r0 * P.row_bytes) & 15LL) + boff;
+          int rl = (my_rg - t.vrow0) & (RG - 1);  // RG is a power of two
+          for (; rl + RG < t.rows; rl += 2 * RG) {
+            const float va = block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]);
+            const float vb = block_dot_smem(s32, base + (uint32_t)(rl + RG) * rowb, xr[0][0]);
+            push(va);
+            push(vb);
           }
-          for (; rl < t.rows; rl += RG) {
-            float a = 0.f;
-#pragma unroll
-            for (int k = 0; k < K; ++k)
-              a += block_dot_smem(s32, delta + (uint32_t)rl * rowb + boff[k], xr[0][k]);
-            a = warp_sum(a);
-            if (lane == 0) prow[(size_t)rl * NS] = a;
-          }
+          if (rl < t.rows) push(block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (producer) produce(i + 1 + P.nstages);
         cur += t.rows;
+      }
+      // rows left in the buffer
+      const int rem = cnt & 3;
+      for (int j = 0; j < rem; ++j) {
+        const float w = warp_sum(j == 0 ? q0 : (j == 1 ? q1 : q2));
+        if (lane == 0) pcol[(size_t)(my_rg + (cnt - rem + j) * RG) * NS] = w;
       }
     } else {
     long long cur = v0;
@@ -442,9 +445,10 @@ __global__ void fill_zero_kernel(float* y, int ldy, int m, int p) {
     y[(e / p) * ldy + (e % p)] = 0.f;
 }
 
-template <int K, int MV>
+template <int MV, int W>
 int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
-  auto fn = q8_rows_kernel<K, MV>;
+  auto fn = q8_rows_kernel<MV, W>;
+  constexpr int kThreads = W * 32;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -505,32 +509,28 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.row_bytes = (long long)P.bpr * kQBlockBytes;
   P.total_rows = p_total;
 
-  // Blocks per lane K (1..3): the fewest segments per row that still fit
-  // kWarps warps; with several activation vectors K = 1 (registers).
-  int K = 1;
-  for (K = 1; K < 3; ++K)
-    if ((P.bpr + 32 * K - 1) / (32 * K) <= kWarps) break;
-  if (P.m > 1) K = 1;
-  const int NS = (P.bpr + 32 * K - 1) / (32 * K);
-  const int MV = (K > 1 || P.m == 1) ? 1 : 2;
+  // One 32-block segment of a row per warp (lane l owns block column l of
+  // it, its activations in registers).  Rows of up to 8 segments: 8-warp
+  // CTAs, two per SM; up to 20 segments: 20-warp CTAs; longer rows (or
+  // several activation vectors) reload activations per segment and tile.
+  const int NS = (P.bpr + 31) / 32;
+  const int MV = P.m == 1 ? 1 : 2;
   P.segs_per_row = NS;
-  if ((P.xmode != kXPlain || P.am_val) && (P.m != 1 || NS > kWarps)) return Q8D_EUNSUPPORTED;
+  const int W = (P.m == 1 && NS > kWarpsSmall && NS <= kWarpsLong) ? kWarpsLong : kWarpsSmall;
+  if ((P.xmode != kXPlain || P.am_val) && (P.m != 1 || NS > W)) return Q8D_EUNSUPPORTED;
 
-  // Stages of ~36 KB (whole row quads per row group), 2-5 of them; the
-  // launcher sizes a single wave of resident CTAs.
-  const int RG = NS <= kWarps ? kWarps / NS : 1;
+  // Stages of ~36 KB of whole rows (quads per row group where they fit).
+  const int RG = NS <= W ? W / NS : 1;
   long long R = std::max<long long>(1, 36864 / P.row_bytes);
-  if (R >= 4 * RG) R -= R % (4 * RG);       // whole row quads for every row group
+  if (R >= 4 * RG) R -= R % (4 * RG);
   else if (R >= 2 * RG) R -= R % (2 * RG);
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
-  P.nstages = P.stage_bytes <= 16 * 1024 ? 5 : (P.stage_bytes <= 36 * 1024 ? 3 : 2);
-  switch (K * 10 + MV) {
-    case 11: return launch_rows<1, 1>(P, R, stream, grid_out);
-    case 12: return launch_rows<1, 2>(P, R, stream, grid_out);
-    case 21: return launch_rows<2, 1>(P, R, stream, grid_out);
-    case 31: return launch_rows<3, 1>(P, R, stream, grid_out);
-    default: return Q8D_EUNSUPPORTED;
-  }
+  const int ring = W == kWarpsSmall ? 96 * 1024 : 160 * 1024;  // per-CTA stage budget
+  P.nstages = std::max(2, std::min(8, ring / P.stage_bytes));
+  if (W == kWarpsLong) return MV == 1 ? launch_rows<1, kWarpsLong>(P, R, stream, grid_out)
+                                      : Q8D_EUNSUPPORTED;
+  return MV == 1 ? launch_rows<1, kWarpsSmall>(P, R, stream, grid_out)
+                 : launch_rows<2, kWarpsSmall>(P, R, stream, grid_out);
 }
 
 }  // namespace q8d
