@@ -223,8 +223,31 @@ def run_profile(args):
         cudart.cudaProfilerStop()
         assert ds.step.status() == 0
         ds.close()
-    elif args.profile == "matvec":
-        n, p = 3584, 18944
+    elif args.profile == "matvec_sweep":
+        # the bench's q8d_matvec launches for two 7B-shaped layers + lm_head
+        # (the per-shape traffic scales to the 28-layer sweep by launch counts)
+        shape = synth.MODELS[args.model]
+        mats = []
+        for li in range(2):
+            for nm, n, p in [("wq", shape.hidden, shape.q_width), ("wk", shape.hidden, shape.kv_width),
+                             ("wv", shape.hidden, shape.kv_width), ("wo", shape.q_width, shape.hidden),
+                             ("wg", shape.hidden, shape.ffn), ("wu", shape.hidden, shape.ffn),
+                             ("wd", shape.ffn, shape.hidden)]:
+                mats.append((synth.q8_matrix_torch(0, f"l{li}.{nm}", p, n), n, p))
+        mats.append((synth.q8_matrix_torch(0, "lm_head", shape.vocab, shape.hidden), shape.hidden,
+                     shape.vocab))
+        xs = {n: synth.normal_torch(0, f"x{n}", n, torch.float32) for _, n, _ in mats}
+        y = torch.empty(max(p for _, _, p in mats), device="cuda")
+        for w, n, p in mats:
+            q8d.q8d_matvec(xs[n], w, y, n, p)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStart()
+        for w, n, p in mats:
+            q8d.q8d_matvec(xs[n], w, y, n, p)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStop()
+    elif args.profile in ("matvec", "matvec_down"):
+        n, p = (3584, 18944) if args.profile == "matvec" else (18944, 3584)
         w = synth.q8_matrix_torch(0, "prof.w", p, n)
         x = synth.normal_torch(0, "prof.x", n, torch.float32)
         y = torch.empty(p, device="cuda")
@@ -289,7 +312,8 @@ def main():
     ap.add_argument("--context", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=3)
-    ap.add_argument("--profile", choices=["step", "matvec", "attn"], default=None,
+    ap.add_argument("--profile", choices=["step", "matvec", "matvec_down", "attn", "matvec_sweep"],
+                    default=None,
                     help="run a short fixed workload between cudaProfilerStart/Stop for ncu "
                          "(--profile-from-start off) and print no JSON")
     args = ap.parse_args()
