@@ -152,6 +152,49 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// Sums the lane partials of `nrow` window rows (starting at CTA-range row
+// wbeg) over all segments and lanes, in a fixed order, and writes y (with the
+// launch's accumulate / argmax handling).  part = [row][seg][lane] floats.
+template <int kThreads>
+__device__ __forceinline__ void window_reduce(const RowsParams& P, const float* part, int nrow,
+                                              int NS, long long wbeg, long long v0, float& bv,
+                                              int& bi) {
+  constexpr int kTPR = 8;  // threads per row
+  const int sub = threadIdx.x % kTPR;
+  for (int r = threadIdx.x / kTPR; r < nrow; r += kThreads / kTPR) {
+    const float* pr = part + (size_t)r * NS * 32;
+    float sum = 0.f;
+    for (int e = sub; e < NS * 32; e += kTPR) sum += pr[e];
+#pragma unroll
+    for (int o = kTPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (sub == 0) {
+      const long long vr = wbeg + r;
+      int sg = 0;
+      while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
+      const int ri = (int)(vr - P.vbegin[sg]);
+      float* y = P.seg[sg].y + ri;
+      const float out = P.accumulate ? (*y + sum) : sum;
+      *y = out;
+      if (!isnan(out) && (out > bv || (out == bv && ri < bi))) {
+        bv = out;
+        bi = ri;
+      }
+    }
+  }
+  (void)v0;
+}
+
+// Bounded wait that gives up at once when another warp of the CTA already
+// gave up (so every warp still reaches the CTA's barriers quickly).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
 // One tile of the CTA's contiguous row range: rows [r0, r0 + rows) of
 // segment `seg`, which are rows [vrow0, vrow0 + rows) of the CTA.
 struct Tile {
@@ -194,11 +237,13 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
   const long long v1 = min(P.total_rows, v0 + P.rows_per_cta);
   const int rows_cta = (int)max(0LL, v1 - v0);
 
+  __shared__ int s_abort;
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
     }
+    s_abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -214,8 +259,9 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     while (pi < upto && pcur < v1) {
       const Tile t = tile_at(P, pcur, v0, v1);
       const int s = pi % P.nstages;
-      if (pi >= P.nstages && !mbar_wait(&empty[s], (uint32_t)((pi / P.nstages) - 1) & 1u)) {
+      if (pi >= P.nstages && !wait_or_abort(&empty[s], (uint32_t)((pi / P.nstages) - 1) & 1u, &s_abort)) {
         ok = false;
+        pcur = v1;  // stop producing
         return;
       }
       const RowSeg& S = P.seg[t.seg];
@@ -245,6 +291,8 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     griddep_launch_dependents();
     griddep_wait();  // activations written by the previous kernel are visible now
   }
+  float am_bv = -INFINITY;  // this thread's argmax candidate over written rows
+  int am_bi = 0x7fffffff;
   // RMSNorm of x (the same sum, in the same order, in every CTA).
   __shared__ float red_ss[kWarps];
   float inv_rms = 1.f;
@@ -279,65 +327,52 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     uint64_t xr[MV][K][16];
     if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, inv_rms, xr);
 
-    if (MV == 1 && x_static) {
-      // Matvec fast path, branch-free inner loop.  Lanes past the row end read
-      // a valid block with zero activations.  A warp's rows are the CTA rows
-      // r = my_rg (mod RG) in order; their dot products wait in a rotating
-      // buffer and are reduced four at a time with one transposed shuffle
-      // tree (lane 8j ends with the sum of row j), across tile boundaries.
+    if (MV == 1 && P.fast) {
+      // Matvec fast path.  The hot loop is branch-free: per row and lane one
+      // block dot product and one shared-memory store of the lane's partial
+      // (lanes past the row end read a valid block with zero activations).
+      // Rows are reduced in windows of P.win rows once every warp has
+      // stored its partials: sum over segments and lanes in a fixed order.
       const uint32_t rowb = (uint32_t)P.row_bytes;
       const int bcol = my_seg0 * 32 + lane;
       const uint32_t boff = (uint32_t)(bcol < P.bpr ? bcol : P.bpr - 1) * kQBlockBytes;
-      float* pcol = part + my_seg0;
-      float q0 = 0.f, q1 = 0.f, q2 = 0.f;
-      int cnt = 0;  // rows of this warp done so far
-      auto push = [&](float v) {
-        const int slot = cnt & 3;
-        if (slot == 0) q0 = v;
-        else if (slot == 1) q1 = v;
-        else if (slot == 2) q2 = v;
-        else {
-          const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-          const float u0 = (b4 ? q2 : q0) + __shfl_xor_sync(0xffffffffu, b4 ? q0 : q2, 16);
-          const float u1 = (b4 ? v : q1) + __shfl_xor_sync(0xffffffffu, b4 ? q1 : v, 16);
-          float w = (b3 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, b3 ? u0 : u1, 8);
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-          const int row = my_rg + (cnt - 3 + (lane >> 3)) * RG;  // CTA row of this lane's sum
-          if ((lane & 7) == 0) pcol[(size_t)row * NS] = w;
-        }
-        ++cnt;
-      };
+      float* lanep = part + my_seg0 * 32 + lane;  // + (row in window) * NS * 32
+      const int win = P.win;
       long long cur = v0;
+      long long wbeg = v0;  // first row of the current window
       for (int i = 0; cur < v1; ++i) {
         const Tile t = tile_at(P, cur, v0, v1);
         const int s = i % P.nstages;
-        if (!mbar_wait(&full[s], (uint32_t)(i / P.nstages) & 1u)) {
-          ok = false;
-          break;
-        }
-        if (active) {
+        // on a wait timeout the loop still runs (without computing) so that
+        // every warp reaches the window barriers
+        const bool got = wait_or_abort(&full[s], (uint32_t)(i / P.nstages) & 1u, &s_abort);
+        ok = ok && got;
+        if (active && got) {
           const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * s);
           const uint32_t base = (uint32_t)((t.r0 * P.row_bytes) & 15LL) + boff;
+          const int wrow0 = (int)(cur - wbeg);  // window row of the tile's first row
           int rl = (my_rg - t.vrow0) & (RG - 1);  // RG is a power of two
           for (; rl + RG < t.rows; rl += 2 * RG) {
             const float va = block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]);
             const float vb = block_dot_smem(s32, base + (uint32_t)(rl + RG) * rowb, xr[0][0]);
-            push(va);
-            push(vb);
+            lanep[(size_t)(wrow0 + rl) * NS * 32] = va;
+            lanep[(size_t)(wrow0 + rl + RG) * NS * 32] = vb;
           }
-          if (rl < t.rows) push(block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]));
+          if (rl < t.rows)
+            lanep[(size_t)(wrow0 + rl) * NS * 32] = block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (producer) produce(i + 1 + P.nstages);
         cur += t.rows;
-      }
-      // rows left in the buffer
-      const int rem = cnt & 3;
-      for (int j = 0; j < rem; ++j) {
-        const float w = warp_sum(j == 0 ? q0 : (j == 1 ? q1 : q2));
-        if (lane == 0) pcol[(size_t)(my_rg + (cnt - rem + j) * RG) * NS] = w;
+        if (cur - wbeg >= win || cur >= v1) {
+          // window complete: every warp's partials are in shared memory
+          __syncthreads();
+          const int nrow = (int)(cur - wbeg);
+          window_reduce<kThreads>(P, part, nrow, NS, wbeg, v0, am_bv, am_bi);
+          __syncthreads();
+          wbeg = cur;
+        }
       }
     } else {
     long long cur = v0;
@@ -392,22 +427,25 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
     return;
   }
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
-    const int rc = e / P.m, m = e % P.m;
-    float sum = 0.f;
-    for (int seg = 0; seg < NS; ++seg) sum += part[((size_t)rc * NS + seg) * P.m + m];
-    const long long vr = v0 + rc;
-    int sg = 0;
-    while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
-    float* y = P.seg[sg].y + (size_t)m * P.ldy + (vr - P.vbegin[sg]);
-    const float out = P.accumulate ? (*y + sum) : sum;
-    *y = out;
-    const int ri = (int)(vr - P.vbegin[sg]);
-    if (!isnan(out) && am_better(out, ri, bv, bi)) {
-      bv = out;
-      bi = ri;
+  const bool fast = (MV == 1) && P.fast;
+  float bv = am_bv;
+  int bi = am_bi;
+  if (!fast) {
+    for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
+      const int rc = e / P.m, m = e % P.m;
+      float sum = 0.f;
+      for (int seg = 0; seg < NS; ++seg) sum += part[((size_t)rc * NS + seg) * P.m + m];
+      const long long vr = v0 + rc;
+      int sg = 0;
+      while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
+      float* y = P.seg[sg].y + (size_t)m * P.ldy + (vr - P.vbegin[sg]);
+      const float out = P.accumulate ? (*y + sum) : sum;
+      *y = out;
+      const int ri = (int)(vr - P.vbegin[sg]);
+      if (!isnan(out) && am_better(out, ri, bv, bi)) {
+        bv = out;
+        bi = ri;
+      }
     }
   }
   if (P.am_val) {
@@ -464,8 +502,9 @@ int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   const int sms = sm_count();
   const long long p_total = P.total_rows;
   auto smem_for = [&](long long rows_cta) {
-    return (long long)P.stage_bytes * P.nstages + 16LL * P.nstages +
-           4LL * rows_cta * P.segs_per_row * P.m;
+    const long long part = P.fast ? (long long)(P.win + R) * P.segs_per_row * 32
+                                  : rows_cta * P.segs_per_row * P.m;
+    return (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + 4LL * part;
   };
   long long smem = smem_for((p_total + sms - 1) / sms);
   if (smem > 200 * 1024) return Q8D_EUNSUPPORTED;
@@ -527,6 +566,9 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   const int ring = W == kWarpsSmall ? 96 * 1024 : 160 * 1024;  // per-CTA stage budget
   P.nstages = std::max(2, std::min(8, ring / P.stage_bytes));
+  P.fast = (P.m == 1 && NS <= W) ? 1 : 0;
+  const int win_rows = W == kWarpsSmall ? 32 : 16;
+  P.win = (int)(R * std::max<long long>(1, win_rows / R));
   if (W == kWarpsLong) return MV == 1 ? launch_rows<1, kWarpsLong>(P, R, stream, grid_out)
                                       : Q8D_EUNSUPPORTED;
   return MV == 1 ? launch_rows<1, kWarpsSmall>(P, R, stream, grid_out)

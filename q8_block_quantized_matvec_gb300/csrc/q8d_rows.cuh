@@ -44,6 +44,8 @@ struct RowsParams {
   long long total_rows;    // sum of p
   long long rows_per_cta;  // contiguous virtual rows owned by one CTA
   int rows_per_tile, stage_bytes, nstages, segs_per_row;
+  int win;                 // matvec fast path: rows reduced together (window)
+  int fast;                // 1: matvec fast path (per-lane partials, windows)
 };
 
 enum { kXPlain = 0, kXRmsNorm = 1, kXSiluMul = 2 };
