@@ -292,12 +292,14 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     l1 = l1 * c1 + rs1;
     m0 = mn0;
     m1 = mn1;
+    if (!__all_sync(0xffffffffu, c0 == 1.f && c1 == 1.f)) {  // skipped when no row max moved
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      o[n][0] *= c0;
-      o[n][1] *= c0;
-      o[n][2] *= c1;
-      o[n][3] *= c1;
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= c0;
+        o[n][1] *= c0;
+        o[n][2] *= c1;
+        o[n][3] *= c1;
+      }
     }
     // ---- P (16 heads x 16 tokens) as the A operand, hi/lo ----
     uint32_t ph[4], pl[4];

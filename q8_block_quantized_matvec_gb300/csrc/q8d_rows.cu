@@ -161,13 +161,19 @@ __device__ __forceinline__ void window_reduce(const RowsParams& P, const float* 
                                               int& bi) {
   constexpr int kTPR = 8;  // threads per row
   const int sub = threadIdx.x % kTPR;
-  for (int r = threadIdx.x / kTPR; r < nrow; r += kThreads / kTPR) {
+  // The trip count is the same for all lanes of a warp (the shuffles below
+  // need every lane); lanes past the window's last row add nothing.
+  const int wrow = (threadIdx.x & ~31) / kTPR;  // first row of this warp
+  for (int r0 = wrow; r0 < nrow; r0 += kThreads / kTPR) {
+    const int r = r0 + (threadIdx.x & 31) / kTPR;
+    const bool valid = r < nrow;
     const float* pr = part + (size_t)r * NS * 32;
     float sum = 0.f;
-    for (int e = sub; e < NS * 32; e += kTPR) sum += pr[e];
+    if (valid)
+      for (int e = sub; e < NS * 32; e += kTPR) sum += pr[e];
 #pragma unroll
     for (int o = kTPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (sub == 0) {
+    if (valid && sub == 0) {
       const long long vr = wbeg + r;
       int sg = 0;
       while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
@@ -563,10 +569,13 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   long long R = std::max<long long>(1, 36864 / P.row_bytes);
   if (R >= 4 * RG) R -= R % (4 * RG);
   else if (R >= 2 * RG) R -= R % (2 * RG);
+  P.fast = (P.m == 1 && NS <= W) ? 1 : 0;
+  // The fast path keeps 32 lane partials per (row, segment) for up to two
+  // tiles of rows: short rows get shorter tiles so that this stays <= 64 KB.
+  if (P.fast) R = std::min<long long>(R, std::max<long long>(4 * RG, 128 / NS));
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   const int ring = W == kWarpsSmall ? 96 * 1024 : 160 * 1024;  // per-CTA stage budget
   P.nstages = std::max(2, std::min(8, ring / P.stage_bytes));
-  P.fast = (P.m == 1 && NS <= W) ? 1 : 0;
   const int win_rows = W == kWarpsSmall ? 32 : 16;
   P.win = (int)(R * std::max<long long>(1, win_rows / R));
   if (W == kWarpsLong) return MV == 1 ? launch_rows<1, kWarpsLong>(P, R, stream, grid_out)
