@@ -1,0 +1,539 @@
+// Q8_0 matrix-vector product (one activation vector) on CUDA cores, sm_103a.
+//
+//   y[r] (+)= sum_b scale(r,b) * sum_j q(r,b,j) * x[32b+j]
+// ("IV.4: One command buffer per token", "Eight kernels": q8_matvec), for up
+// to three matrices that share x (q|k|v, gate|up), with the decode step's
+// activation transforms (RMSNorm, SiLU*up), residual accumulation and
+// per-CTA argmax partials folded in.
+//
+// The product reads every weight byte once and does ~2.5 instructions per
+// quant, so at HBM speed it is bound by instruction issue as much as by
+// DRAM.  The layout is chosen to keep the per-block instruction count at the
+// decode's own cost:
+//  * Weight tiles (R whole rows, one contiguous byte range) are streamed into
+//    a ring of shared-memory stages with 1-D bulk copies (TMA) that complete
+//    on mbarriers.  One producer warp issues them, refilling a stage as soon
+//    as every consumer warp has released it; the consumer warps do nothing
+//    but the products, and per-tile bookkeeping is incremental 32-bit
+//    arithmetic.
+//  * A row is covered by NS warps.  For rows of more than 32 blocks the
+//    warps come in pairs that own the even and the odd block columns of a
+//    64-column segment: lane l of the pair's warps owns column 64s + 2l (+1).
+//    Blocks are 34 bytes, so all blocks of one warp then have the same
+//    alignment modulo 4 (the scale in the upper or lower half of a word),
+//    and the 17-word lane stride is free of shared-memory bank conflicts.
+//    Rows of up to 32 blocks use one warp with lane l on column l.
+//  * A lane keeps the 32 activations of its column in registers for every
+//    row it visits; its partial for a row (scale * block dot product) goes
+//    to shared memory, and windows of rows are summed over segments and lanes
+//    in a fixed order (deterministic results).  Windows are double-buffered,
+//    so one barrier of the consumer warps per window suffices.
+//  * Dequantisation: a sign-flipped quant byte is placed in the mantissa of
+//    2^23 with one PRMT, one packed f32x2 add removes the bias exactly, and
+//    packed f32x2 FMAs accumulate in four chains.
+#include <algorithm>
+
+#include "q8d_internal.cuh"
+#include "q8d_rows.cuh"
+
+namespace q8d {
+
+namespace {
+
+constexpr int kMaxWarps = 20;
+
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// scale * sum_j q_j x_j for the block at shared-memory byte address `o`
+// (2-byte aligned).  Alignment modes: AM = 1, the block starts at byte 2 of
+// a word (scale = upper half, quants = the next 8 words); AM = 0, it starts
+// at a word (scale = lower half, quants from byte 2, funnel-shifted); AM = 2,
+// decided per lane from o.
+template <int AM>
+__device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16]) {
+  const uint32_t w0 = o & ~3u;
+  uint32_t a[9];
+  a[0] = lds32<0>(w0);
+  a[1] = lds32<4>(w0);
+  a[2] = lds32<8>(w0);
+  a[3] = lds32<12>(w0);
+  a[4] = lds32<16>(w0);
+  a[5] = lds32<20>(w0);
+  a[6] = lds32<24>(w0);
+  a[7] = lds32<28>(w0);
+  a[8] = lds32<32>(w0);
+  float sc;
+  uint32_t shift = 16;
+  if constexpr (AM == 2) {
+    const bool odd = (o & 2u) != 0;
+    sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
+    shift = odd ? 32u : 16u;
+  } else {
+    const __half2 sh = *reinterpret_cast<const __half2*>(&a[0]);
+    sc = AM ? __high2float(sh) : __low2float(sh);
+  }
+  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
+  uint64_t c[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t w;
+    if constexpr (AM == 1) w = a[k + 1];
+    else if constexpr (AM == 0) w = __funnelshift_r(a[k], a[k + 1], 16);
+    else w = __funnelshift_rc(a[k], a[k + 1], shift);
+    w ^= 0x80808080u;
+    const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
+    const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
+    c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
+    c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
+  }
+  const uint64_t t = add2(add2(c[0], c[1]), add2(c[2], c[3]));
+  float lo, hi;
+  unpack2(t, lo, hi);
+  return sc * (lo + hi);
+}
+
+// Activations of block column `col` (32 floats) with the launch's transform,
+// as 16 packed pairs; zeros when col is past the row end.
+__device__ __forceinline__ void load_x_col(const RowsParams& P, int col, float inv,
+                                           uint64_t (&x2)[16]) {
+  const bool ok = col < P.bpr;
+  const size_t base = (size_t)col * kQBlock;
+  const float4* xp = reinterpret_cast<const float4*>(P.X + base);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok && P.xmode == kXRmsNorm) {
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(P.xw + base) + t);
+      v.x = v.x * inv * wv.x;
+      v.y = v.y * inv * wv.y;
+      v.z = v.z * inv * wv.z;
+      v.w = v.w * inv * wv.w;
+    } else if (ok && P.xmode == kXSiluMul) {
+      const float4 u = __ldg(reinterpret_cast<const float4*>(P.X + base + P.n) + t);
+      v.x = v.x / (1.0f + expf(-v.x)) * u.x;
+      v.y = v.y / (1.0f + expf(-v.y)) * u.y;
+      v.z = v.z / (1.0f + expf(-v.z)) * u.z;
+      v.w = v.w / (1.0f + expf(-v.w)) * u.w;
+    }
+    x2[2 * t] = pack2(v.x, v.y);
+    x2[2 * t + 1] = pack2(v.z, v.w);
+  }
+}
+
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// Bounded wait that gives up at once when another thread of the CTA already
+// gave up, so that every warp still reaches the CTA barriers quickly.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+// Sums the lane partials of `nrow` rows (the window starting at virtual row
+// wbeg) over segments and lanes in a fixed order and writes y.  Eight
+// threads per row, four rows per consumer warp at a time; every lane of a
+// warp runs the same iterations.  part = [row][NS][32] floats, 16-byte
+// aligned rows.
+__device__ __forceinline__ void window_reduce(const RowsParams& P, const float* part, int nrow,
+                                              int NS, int nwarps, int wbeg, float& bv, int& bi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 7;
+  for (int r0 = warp * 4; r0 < nrow; r0 += nwarps * 4) {
+    const int r = r0 + (lane >> 3);
+    const bool valid = r < nrow;
+    const float4* pr = reinterpret_cast<const float4*>(part + (size_t)(valid ? r : r0) * NS * 32) + sub;
+    uint64_t acc0 = pack2(0.f, 0.f), acc1 = acc0;
+    for (int k = 0; k < NS; ++k) {
+      const float4 v = pr[8 * k];
+      acc0 = add2(acc0, pack2(v.x, v.y));
+      acc1 = add2(acc1, pack2(v.z, v.w));
+    }
+    float lo, hi;
+    unpack2(add2(acc0, acc1), lo, hi);
+    float sum = lo + hi;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (valid && sub == 0) {
+      const int vr = wbeg + r;
+      int sg = 0;
+      while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
+      const int ri = vr - (int)P.vbegin[sg];
+      float* y = P.seg[sg].y + ri;
+      const float out = P.accumulate ? (*y + sum) : sum;
+      *y = out;
+      if (!isnan(out) && am_better(out, ri, bv, bi)) {
+        bv = out;
+        bi = ri;
+      }
+    }
+  }
+}
+
+struct Ring {
+  uint8_t* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  float* part;  // [2][win_rows][NS][32] lane partials
+  int* abort_flag;
+};
+
+// Barrier among the consumer warps only (the producer warp runs free).
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Tiles of the CTA's contiguous range of virtual rows (the matrices' rows
+// concatenated): at most R rows each, never across a matrix end.
+struct Cursor {
+  int cur;   // first virtual row of the tile
+  int r0;    // its row within matrix `seg`
+  int seg;
+  int seg_end;  // virtual row where matrix `seg` ends
+  __device__ void start(const RowsParams& P, int v0) {
+    cur = v0;
+    seg = 0;
+    while (seg + 1 < P.nseg && v0 >= P.vbegin[seg + 1]) ++seg;
+    r0 = v0 - (int)P.vbegin[seg];
+    seg_end = (int)P.vbegin[seg] + P.seg[seg].p;
+  }
+  __device__ int rows(int R, int v1) const { return min(R, min(seg_end, v1) - cur); }
+  __device__ void advance(const RowsParams& P, int n) {
+    cur += n;
+    r0 += n;
+    if (cur == seg_end && seg + 1 < P.nseg) {
+      ++seg;
+      r0 = 0;
+      seg_end = cur + P.seg[seg].p;
+    }
+  }
+};
+
+// Producer: one thread issues every tile of the CTA into the ring, waiting
+// for a stage only until all consumer warps have released it.  Returns the
+// number of tiles issued (fewer if a wait timed out).
+__device__ int produce_all(const RowsParams& P, const Ring& ring, int v0, int v1) {
+  const uint64_t pol = policy_evict_first();
+  Cursor c;
+  c.start(P, v0);
+  int s = 0;
+  uint32_t ph = 0;
+  int i = 0;
+  for (; c.cur < v1; ++i) {
+    if (i >= P.nstages && !wait_or_abort(&ring.empty[s], ph ^ 1u, ring.abort_flag)) break;
+    const int rows = c.rows(P.rows_per_tile, v1);
+    const RowSeg& S = P.seg[c.seg];
+    const long long start = (long long)c.r0 * P.row_bytes;
+    const long long end = start + (long long)rows * P.row_bytes;
+    const long long cap16 = ((long long)S.p * P.row_bytes) & ~15LL;
+    const long long a0 = start & ~15LL;
+    long long a1 = (end + 15) & ~15LL;
+    uint8_t* dst = ring.smem + (size_t)P.stage_bytes * s;
+    if (a1 > cap16) {
+      // last tile of a matrix whose size is not a multiple of 16 bytes: the
+      // bytes past the last 16-byte boundary are copied by hand (published
+      // by the arrive below)
+      a1 = cap16 > a0 ? cap16 : a0;
+      for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(S.w + o);
+    }
+    const uint32_t bytes = (uint32_t)(a1 - a0);
+    mbar_arrive_expect_tx(&ring.full[s], bytes);
+    if (bytes) bulk_g2s(dst, S.w + a0, bytes, &ring.full[s], pol);
+    c.advance(P, rows);
+    if (++s == P.nstages) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  return i;
+}
+
+// Consumer loop of one warp.  AM: alignment mode of the warp's blocks.  A
+// warp takes P.np pairs of rows per tile (a tile has R = 2 * RG * np rows).  A tile
+// with fewer rows (the end of a matrix or of the CTA's range) is computed
+// over all R rows of its stage, which the stage's size covers, and only
+// the partials of its real rows are stored.
+template <int AM>
+__device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, uint32_t part32,
+                                        int v0, int v1, int ci, int rg, int RG, int nwarps,
+                                        uint32_t boff, const uint64_t (&x2)[16], float& bv,
+                                        int& bi) {
+  const int lane = threadIdx.x & 31;
+  const int NS = P.segs_per_row;
+  const int n32 = NS * 32;
+  const uint32_t rowb = (uint32_t)P.row_bytes;
+  const uint32_t step = (uint32_t)RG * rowb;        // stage bytes between a warp's rows
+  const uint32_t pstep = (uint32_t)(RG * n32 * 4);  // partial bytes between them
+  const uint32_t rb15 = rowb & 15u;
+  const uint32_t smem32 = smem_u32(ring.smem);
+  const uint32_t lane_part = part32 + (uint32_t)(ci * 32 + lane) * 4u + (uint32_t)(rg * n32) * 4u;
+  const uint32_t buf_bytes = (uint32_t)(P.win_rows * n32 * 4);
+  bool ok = true;
+  Cursor c;
+  c.start(P, v0);
+  uint32_t delta = ((uint32_t)c.r0 * rb15) & 15u;  // tile start mod 16 (matrices are 16-aligned)
+  int s = 0;
+  uint32_t ph = 0;
+  uint32_t stage32 = smem32;
+  int wbeg = v0, wt = 0, wrow = 0;
+  uint32_t buf = 0;  // byte offset of the current window buffer
+  while (c.cur < v1) {
+    const int rows = c.rows(P.rows_per_tile, v1);
+    // On a timeout the loop still runs (over whatever the stage holds; the
+    // launch then reports Q8D_DERR_WAIT) so that every consumer warp reaches
+    // the window barriers.
+    ok = wait_or_abort(&ring.full[s], ph, ring.abort_flag) && ok;
+    uint32_t o = stage32 + delta + boff + (uint32_t)rg * rowb;
+    uint32_t d = lane_part + buf + (uint32_t)(wrow * n32) * 4u;
+    int rl = rg;
+#pragma unroll 1
+    for (int j = 0; j < P.np; ++j) {
+      const float va = block_dot<AM>(o, x2);
+      const float vb = block_dot<AM>(o + step, x2);
+      if (rl < rows) sts32(d, va);
+      if (rl + RG < rows) sts32(d + pstep, vb);
+      o += 2 * step;
+      d += 2 * pstep;
+      rl += 2 * RG;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[s]);
+    stage32 += (uint32_t)P.stage_bytes;
+    if (++s == P.nstages) {
+      s = 0;
+      ph ^= 1u;
+      stage32 = smem32;
+    }
+    const int seg_before = c.seg;
+    c.advance(P, rows);
+    delta = c.seg == seg_before ? (delta + (uint32_t)rows * rb15) & 15u : 0u;
+    wrow += rows;
+    if (++wt == P.win || c.cur >= v1) {
+      // window complete: every consumer warp has stored its partials.  The
+      // other buffer was reduced before this barrier, so the next window may
+      // overwrite it.
+      consumer_sync(nwarps * 32);
+      window_reduce(P, ring.part + buf / 4, wrow, NS, nwarps, wbeg, bv, bi);
+      buf = buf ? 0u : buf_bytes;
+      wt = 0;
+      wrow = 0;
+      wbeg = c.cur;
+    }
+  }
+  return ok;
+}
+
+// Block of W consumer warps plus one producer warp (the last).
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32) q8_gemv_kernel(const RowsParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = (blockDim.x >> 5) - 1;  // consumer warps
+  const int NS = P.segs_per_row;
+  __shared__ int s_abort;
+  __shared__ float s_f[kMaxWarps + 1];
+  __shared__ int s_i[kMaxWarps + 1];
+
+  Ring ring;
+  ring.smem = smem;
+  ring.full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
+  ring.empty = ring.full + P.nstages;
+  ring.abort_flag = &s_abort;
+  ring.part = reinterpret_cast<float*>(ring.empty + P.nstages);
+
+  const int v0 = blockIdx.x * (int)P.rows_per_cta;
+  const int v1 = (int)min(P.total_rows, (long long)v0 + P.rows_per_cta);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.nstages; ++s) {
+      mbar_init(&ring.full[s], 1);
+      mbar_init(&ring.empty[s], W);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  float bv = -INFINITY;  // this thread's argmax candidate over the rows it wrote
+  int bi = 0x7fffffff;
+  bool ok = true;
+  if (warp == W) {
+    // ---- producer warp: weights do not depend on earlier kernels ----
+    if (P.pdl) griddep_launch_dependents();
+    if (lane == 0) {
+      const int issued = produce_all(P, ring, v0, v1);
+      if (*(volatile int*)&s_abort) {
+        // Wait (bounded) for the copies still in flight before the CTA's
+        // shared memory can be released.
+        for (int j = max(0, issued - P.nstages); j < issued; ++j)
+          mbar_wait(&ring.full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
+      }
+    }
+  } else {
+    if (P.pdl) {
+      griddep_launch_dependents();
+      griddep_wait();  // activations written by the previous kernel are visible from here
+    }
+    // RMSNorm scale of x: the same sum, in the same order, in every CTA.
+    float inv_rms = 1.f;
+    if (P.xmode == kXRmsNorm) {
+      float ss = 0.f;
+      const float4* x4 = reinterpret_cast<const float4*>(P.X);
+      for (int i = threadIdx.x; i < P.n / 4; i += W * 32) {
+        const float4 v = __ldg(x4 + i);
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_f[warp] = ss;
+      consumer_sync(W * 32);
+      float tot = 0.f;
+      for (int w = 0; w < W; ++w) tot += s_f[w];
+      inv_rms = 1.0f / sqrtf(tot / (float)P.n + P.eps);
+    }
+
+    // This warp's block column class and row group (W is a multiple of NS).
+    const int ci = warp % NS, rg = warp / NS, RG = W / NS;
+    int col, col_read;
+    if (P.paired) {
+      const int par = ci & 1;
+      col = 64 * (ci >> 1) + 2 * lane + par;
+      // lanes past the row end read the last block of the same parity (so
+      // the warp's alignment holds) with zero activations
+      col_read = min(col, P.bpr - 1 - ((P.bpr - 1 - par) & 1));
+    } else {
+      col = lane;
+      col_read = min(col, P.bpr - 1);
+    }
+    uint64_t x2[16];
+    load_x_col(P, col, inv_rms, x2);
+    const uint32_t boff = (uint32_t)col_read * kQBlockBytes;
+    // With an even number of blocks per row every row starts at a multiple
+    // of 4 bytes, so all blocks of a paired warp start at 2*(col & 1) mod 4.
+    const uint32_t part32 = smem_u32(ring.part);
+    if (P.paired && (P.bpr & 1) == 0) {
+      if (ci & 1)
+        ok = consume<1>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+      else
+        ok = consume<0>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+    } else {
+      ok = consume<2>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+    }
+  }
+
+  if (!__syncthreads_and(ok && !*(volatile int*)&s_abort)) {
+    if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+    return;
+  }
+  if (P.am_val) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (am_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      s_f[warp] = bv;
+      s_i[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w <= W; ++w)
+        if (am_better(s_f[w], s_i[w], bv, bi)) {
+          bv = s_f[w];
+          bi = s_i[w];
+        }
+      P.am_val[blockIdx.x] = bv;
+      P.am_idx[blockIdx.x] = bi;
+    }
+  }
+}
+
+}  // namespace
+
+// Plans and launches the matvec kernel (m == 1, rows of at most 20 warps).
+// Returns Q8D_EUNSUPPORTED when the shape does not fit it.
+int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
+  const int bpr = P.bpr;
+  const bool paired = bpr > 32;
+  const int NS = paired ? 2 * ((bpr + 63) / 64) : 1;  // warps per row
+  if (P.m != 1 || NS > kMaxWarps || P.total_rows > 0x7fffffffLL) return Q8D_EUNSUPPORTED;
+  // One CTA per SM with 16 consumer warps (20 for the longest rows), a
+  // multiple of NS, plus the producer warp; RG rows are in work at once.
+  const int W = NS <= 8 ? NS * (16 / NS) : NS * (kMaxWarps / NS);
+  const int RG = W / NS;
+  const int sms = sm_count();
+  constexpr long long kSmemCta = 220 * 1024;
+
+  // Tiles of R = 2 * RG * NP rows (each warp takes NP pairs of rows per
+  // tile), NP = 4, 2 or 1: the largest whose tile is at most ~64 KB (and
+  // 128 rows) and leaves room for three stages.  Reduction windows are
+  // double-buffered within ~40 KB of partials.
+  long long R = 0, stage = 0, part_bytes = 0;
+  int nst = 0, wt = 0, np = 4;
+  for (;; np /= 2) {
+    R = 2LL * RG * np;
+    const long long win_rows = std::max<long long>(R, 40960 / (2LL * NS * 32 * 4));
+    wt = (int)(win_rows / R);
+    part_bytes = 2LL * wt * R * NS * 32 * 4;
+    stage = ((R * P.row_bytes + 32 + 127) / 128) * 128;
+    nst = (int)std::min<long long>(8, (kSmemCta - part_bytes - 1024) / (stage + 16));
+    if (np == 1 || (R <= 128 && R * P.row_bytes <= 65536 && nst >= 3)) break;
+  }
+  P.paired = paired ? 1 : 0;
+  P.segs_per_row = NS;
+  P.stage_bytes = (int)stage;
+  P.nstages = nst;
+  P.win = wt;
+  P.win_rows = (int)(wt * R);
+  P.np = np;
+  const long long smem = stage * nst + 16LL * nst + part_bytes;
+
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(q8_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         220 * 1024);
+    if (e != cudaSuccess) return record_cuda(e);
+    e = cudaFuncSetAttribute(q8_gemv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return record_cuda(e);
+    configured[dev] = 1;
+  }
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, q8_gemv_kernel, (W + 1) * 32,
+                                                                (size_t)smem);
+  if (e != cudaSuccess) return record_cuda(e);
+  occ = std::max(occ, 1);
+  // One wave of resident CTAs, each owning a contiguous range of rows.
+  long long grid = std::min<long long>(P.total_rows, (long long)sms * occ);
+  const long long rows_cta = (P.total_rows + grid - 1) / grid;
+  grid = (P.total_rows + rows_cta - 1) / rows_cta;
+  P.rows_per_cta = rows_cta;
+  P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
+  if (grid_out) *grid_out = (int)grid;
+  return launch_ex(q8_gemv_kernel, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream,
+                   P.pdl != 0, P);
+}
+
+}  // namespace q8d

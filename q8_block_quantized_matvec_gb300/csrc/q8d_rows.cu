@@ -4,6 +4,8 @@
 //   Y[i][r] (+)= sum_b scale(r,b) * sum_j q(r,b,j) * X[i][32b+j]
 // ("IV.4: One command buffer per token", "Eight kernels": q8_matvec; the
 // batched form is "Metal Backend Optimizations"' nt in [2, 8] matvec).
+// A single vector (m == 1) goes to the matvec kernel of q8d_gemv.cu when its
+// rows fit it; this kernel serves several vectors and very long rows.
 //
 // Design for GB300 (the pages' kernel gives one 32-lane SIMD-group per
 // output row with scalar byte loads; that shape would leave HBM idle here):
@@ -33,8 +35,7 @@ namespace q8d {
 
 namespace {
 
-constexpr int kWarpsSmall = 8;   // warps per CTA for rows of up to 8 segments
-constexpr int kWarpsLong = 20;   // warps per CTA for rows of 9..20 segments
+constexpr int kWarpsSmall = 8;   // warps per CTA
 
 // Decodes the 32 quants of the block at byte offset `o` of the 4-byte
 // aligned shared buffer `s32` into 16 packed f32x2 pairs, and returns the
@@ -76,33 +77,6 @@ __device__ __forceinline__ float block_dot(const uint64_t (&q2)[16], const uint6
   float lo, hi;
   unpack2(s, lo, hi);
   return lo + hi;
-}
-
-// Streams one block straight from shared memory into the dot product with
-// x (no decoded copy is kept): returns scale * sum_j q_j x_j.
-__device__ __forceinline__ float block_dot_smem(const uint32_t* __restrict__ s32, uint32_t o,
-                                                const uint64_t (&x2)[16]) {
-  const uint32_t wi = o >> 2;
-  const bool odd = (o & 2u) != 0;
-  uint32_t a[9];
-#pragma unroll
-  for (int k = 0; k < 9; ++k) a[k] = s32[wi + k];
-  const float sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
-  const uint32_t sh = odd ? 32u : 16u;
-  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
-  uint64_t c[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t w = __funnelshift_rc(a[k], a[k + 1], sh) ^ 0x80808080u;
-    const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
-    const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
-    c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
-    c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
-  }
-  const uint64_t t = add2(add2(c[0], c[1]), add2(c[2], c[3]));
-  float lo, hi;
-  unpack2(t, lo, hi);
-  return sc * (lo + hi);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -152,44 +126,6 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-// Sums the lane partials of `nrow` window rows (starting at CTA-range row
-// wbeg) over all segments and lanes, in a fixed order, and writes y (with the
-// launch's accumulate / argmax handling).  part = [row][seg][lane] floats.
-template <int kThreads>
-__device__ __forceinline__ void window_reduce(const RowsParams& P, const float* part, int nrow,
-                                              int NS, long long wbeg, long long v0, float& bv,
-                                              int& bi) {
-  constexpr int kTPR = 8;  // threads per row
-  const int sub = threadIdx.x % kTPR;
-  // The trip count is the same for all lanes of a warp (the shuffles below
-  // need every lane); lanes past the window's last row add nothing.
-  const int wrow = (threadIdx.x & ~31) / kTPR;  // first row of this warp
-  for (int r0 = wrow; r0 < nrow; r0 += kThreads / kTPR) {
-    const int r = r0 + (threadIdx.x & 31) / kTPR;
-    const bool valid = r < nrow;
-    const float* pr = part + (size_t)r * NS * 32;
-    float sum = 0.f;
-    if (valid)
-      for (int e = sub; e < NS * 32; e += kTPR) sum += pr[e];
-#pragma unroll
-    for (int o = kTPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (valid && sub == 0) {
-      const long long vr = wbeg + r;
-      int sg = 0;
-      while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
-      const int ri = (int)(vr - P.vbegin[sg]);
-      float* y = P.seg[sg].y + ri;
-      const float out = P.accumulate ? (*y + sum) : sum;
-      *y = out;
-      if (!isnan(out) && (out > bv || (out == bv && ri < bi))) {
-        bv = out;
-        bi = ri;
-      }
-    }
-  }
-  (void)v0;
-}
-
 // Bounded wait that gives up at once when another warp of the CTA already
 // gave up (so every warp still reaches the CTA's barriers quickly).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -227,7 +163,7 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int MV, int W>
-__global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 96)
+__global__ void __launch_bounds__(W * 32, 2)
     q8_rows_kernel(const RowsParams P) {
   constexpr int K = 1;
   constexpr int kWarps = W;
@@ -333,54 +269,7 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     uint64_t xr[MV][K][16];
     if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, inv_rms, xr);
 
-    if (MV == 1 && P.fast) {
-      // Matvec fast path.  The hot loop is branch-free: per row and lane one
-      // block dot product and one shared-memory store of the lane's partial
-      // (lanes past the row end read a valid block with zero activations).
-      // Rows are reduced in windows of P.win rows once every warp has
-      // stored its partials: sum over segments and lanes in a fixed order.
-      const uint32_t rowb = (uint32_t)P.row_bytes;
-      const int bcol = my_seg0 * 32 + lane;
-      const uint32_t boff = (uint32_t)(bcol < P.bpr ? bcol : P.bpr - 1) * kQBlockBytes;
-      float* lanep = part + my_seg0 * 32 + lane;  // + (row in window) * NS * 32
-      const int win = P.win;
-      long long cur = v0;
-      long long wbeg = v0;  // first row of the current window
-      for (int i = 0; cur < v1; ++i) {
-        const Tile t = tile_at(P, cur, v0, v1);
-        const int s = i % P.nstages;
-        // on a wait timeout the loop still runs (without computing) so that
-        // every warp reaches the window barriers
-        const bool got = wait_or_abort(&full[s], (uint32_t)(i / P.nstages) & 1u, &s_abort);
-        ok = ok && got;
-        if (active && got) {
-          const uint32_t* s32 = reinterpret_cast<const uint32_t*>(smem + (size_t)P.stage_bytes * s);
-          const uint32_t base = (uint32_t)((t.r0 * P.row_bytes) & 15LL) + boff;
-          const int wrow0 = (int)(cur - wbeg);  // window row of the tile's first row
-          int rl = (my_rg - t.vrow0) & (RG - 1);  // RG is a power of two
-          for (; rl + RG < t.rows; rl += 2 * RG) {
-            const float va = block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]);
-            const float vb = block_dot_smem(s32, base + (uint32_t)(rl + RG) * rowb, xr[0][0]);
-            lanep[(size_t)(wrow0 + rl) * NS * 32] = va;
-            lanep[(size_t)(wrow0 + rl + RG) * NS * 32] = vb;
-          }
-          if (rl < t.rows)
-            lanep[(size_t)(wrow0 + rl) * NS * 32] = block_dot_smem(s32, base + (uint32_t)rl * rowb, xr[0][0]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (producer) produce(i + 1 + P.nstages);
-        cur += t.rows;
-        if (cur - wbeg >= win || cur >= v1) {
-          // window complete: every warp's partials are in shared memory
-          __syncthreads();
-          const int nrow = (int)(cur - wbeg);
-          window_reduce<kThreads>(P, part, nrow, NS, wbeg, v0, am_bv, am_bi);
-          __syncthreads();
-          wbeg = cur;
-        }
-      }
-    } else {
+    {
     long long cur = v0;
     for (int i = 0; cur < v1; ++i) {
       const Tile t = tile_at(P, cur, v0, v1);
@@ -433,10 +322,9 @@ __global__ void __launch_bounds__(W * 32) __maxnreg__(W == kWarpsSmall ? 128 : 9
     if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
     return;
   }
-  const bool fast = (MV == 1) && P.fast;
   float bv = am_bv;
   int bi = am_bi;
-  if (!fast) {
+  {
     for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
       const int rc = e / P.m, m = e % P.m;
       float sum = 0.f;
@@ -508,8 +396,7 @@ int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   const int sms = sm_count();
   const long long p_total = P.total_rows;
   auto smem_for = [&](long long rows_cta) {
-    const long long part = P.fast ? (long long)(P.win + R) * P.segs_per_row * 32
-                                  : rows_cta * P.segs_per_row * P.m;
+    const long long part = rows_cta * P.segs_per_row * P.m;
     return (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + 4LL * part;
   };
   long long smem = smem_for((p_total + sms - 1) / sms);
@@ -553,15 +440,19 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.bpr = P.n / kQBlock;
   P.row_bytes = (long long)P.bpr * kQBlockBytes;
   P.total_rows = p_total;
+  if (P.m == 1) {
+    const int rc = gemv_plan_and_launch(P, stream, grid_out);
+    if (rc != Q8D_EUNSUPPORTED) return rc;
+  }
 
-  // One 32-block segment of a row per warp (lane l owns block column l of
-  // it, its activations in registers).  Rows of up to 8 segments: 8-warp
-  // CTAs, two per SM; up to 20 segments: 20-warp CTAs; longer rows (or
-  // several activation vectors) reload activations per segment and tile.
+  // Several activation vectors (or a row too long for the matvec kernel):
+  // one 32-block segment of a row per warp (lane l owns block column l of
+  // it), 8-warp CTAs.  Rows of up to 8 segments keep the activations in
+  // registers; longer rows reload them per segment and tile.
   const int NS = (P.bpr + 31) / 32;
   const int MV = P.m == 1 ? 1 : 2;
   P.segs_per_row = NS;
-  const int W = (P.m == 1 && NS > kWarpsSmall && NS <= kWarpsLong) ? kWarpsLong : kWarpsSmall;
+  constexpr int W = kWarpsSmall;
   if ((P.xmode != kXPlain || P.am_val) && (P.m != 1 || NS > W)) return Q8D_EUNSUPPORTED;
 
   // Stages of ~36 KB of whole rows (quads per row group where they fit).
@@ -569,17 +460,9 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   long long R = std::max<long long>(1, 36864 / P.row_bytes);
   if (R >= 4 * RG) R -= R % (4 * RG);
   else if (R >= 2 * RG) R -= R % (2 * RG);
-  P.fast = (P.m == 1 && NS <= W) ? 1 : 0;
-  // The fast path keeps 32 lane partials per (row, segment) for up to two
-  // tiles of rows: short rows get shorter tiles so that this stays <= 64 KB.
-  if (P.fast) R = std::min<long long>(R, std::max<long long>(4 * RG, 128 / NS));
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   const int ring = W == kWarpsSmall ? 96 * 1024 : 160 * 1024;  // per-CTA stage budget
   P.nstages = std::max(2, std::min(8, ring / P.stage_bytes));
-  const int win_rows = W == kWarpsSmall ? 32 : 16;
-  P.win = (int)(R * std::max<long long>(1, win_rows / R));
-  if (W == kWarpsLong) return MV == 1 ? launch_rows<1, kWarpsLong>(P, R, stream, grid_out)
-                                      : Q8D_EUNSUPPORTED;
   return MV == 1 ? launch_rows<1, kWarpsSmall>(P, R, stream, grid_out)
                  : launch_rows<2, kWarpsSmall>(P, R, stream, grid_out);
 }

@@ -44,8 +44,11 @@ struct RowsParams {
   long long total_rows;    // sum of p
   long long rows_per_cta;  // contiguous virtual rows owned by one CTA
   int rows_per_tile, stage_bytes, nstages, segs_per_row;
-  int win;                 // matvec fast path: rows reduced together (window)
-  int fast;                // 1: matvec fast path (per-lane partials, windows)
+  // matvec kernel (q8d_gemv.cu) only
+  int paired;              // 1: warp pairs own the even / odd block columns of 64-column segments
+  int win;                 // tiles per reduction window
+  int win_rows;            // rows per window buffer (win * rows_per_tile)
+  int np;                  // row pairs per warp per tile
 };
 
 enum { kXPlain = 0, kXRmsNorm = 1, kXSiluMul = 2 };
@@ -53,5 +56,9 @@ enum { kXPlain = 0, kXRmsNorm = 1, kXSiluMul = 2 };
 // Plans tiles/stages and launches the kernel on `stream`.  Returns a status;
 // *grid_out (if given) receives the number of CTAs launched.
 int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out = nullptr);
+
+// The m == 1 kernel (q8d_gemv.cu); P has bpr, row_bytes, vbegin and
+// total_rows filled.  Q8D_EUNSUPPORTED when the rows are too long for it.
+int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out);
 
 }  // namespace q8d
