@@ -33,6 +33,7 @@
 //    packed f32x2 FMAs accumulate in four chains.
 #include <algorithm>
 
+#include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
 #include "q8d_rows.cuh"
 
@@ -40,66 +41,9 @@ namespace q8d {
 
 namespace {
 
+using namespace mv;
+
 constexpr int kMaxWarps = 20;
-
-template <int OFF>
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void sts32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// scale * sum_j q_j x_j for the block at shared-memory byte address `o`
-// (2-byte aligned).  Alignment modes: AM = 1, the block starts at byte 2 of
-// a word (scale = upper half, quants = the next 8 words); AM = 0, it starts
-// at a word (scale = lower half, quants from byte 2, funnel-shifted); AM = 2,
-// decided per lane from o.
-template <int AM>
-__device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16]) {
-  const uint32_t w0 = o & ~3u;
-  uint32_t a[9];
-  a[0] = lds32<0>(w0);
-  a[1] = lds32<4>(w0);
-  a[2] = lds32<8>(w0);
-  a[3] = lds32<12>(w0);
-  a[4] = lds32<16>(w0);
-  a[5] = lds32<20>(w0);
-  a[6] = lds32<24>(w0);
-  a[7] = lds32<28>(w0);
-  a[8] = lds32<32>(w0);
-  float sc;
-  uint32_t shift = 16;
-  if constexpr (AM == 2) {
-    const bool odd = (o & 2u) != 0;
-    sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
-    shift = odd ? 32u : 16u;
-  } else {
-    const __half2 sh = *reinterpret_cast<const __half2*>(&a[0]);
-    sc = AM ? __high2float(sh) : __low2float(sh);
-  }
-  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
-  uint64_t c[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint32_t w;
-    if constexpr (AM == 1) w = a[k + 1];
-    else if constexpr (AM == 0) w = __funnelshift_r(a[k], a[k + 1], 16);
-    else w = __funnelshift_rc(a[k], a[k + 1], shift);
-    w ^= 0x80808080u;
-    const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
-    const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
-    c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
-    c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
-  }
-  const uint64_t t = add2(add2(c[0], c[1]), add2(c[2], c[3]));
-  float lo, hi;
-  unpack2(t, lo, hi);
-  return sc * (lo + hi);
-}
 
 // Activations of block column `col` (32 floats) with the launch's transform,
 // as 16 packed pairs; zeros when col is past the row end.
@@ -127,22 +71,6 @@ __device__ __forceinline__ void load_x_col(const RowsParams& P, int col, float i
     x2[2 * t] = pack2(v.x, v.y);
     x2[2 * t + 1] = pack2(v.z, v.w);
   }
-}
-
-__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-// Bounded wait that gives up at once when another thread of the CTA already
-// gave up, so that every warp still reaches the CTA barriers quickly.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-  }
-  *abort_flag = 1;
-  return false;
 }
 
 // Sums the lane partials of `nrow` rows (the window starting at virtual row
@@ -192,11 +120,6 @@ struct Ring {
   float* part;  // [2][win_rows][NS][32] lane partials
   int* abort_flag;
 };
-
-// Barrier among the consumer warps only (the producer warp runs free).
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
 
 // Tiles of the CTA's contiguous range of virtual rows (the matrices' rows
 // concatenated): at most R rows each, never across a matrix end.

@@ -1,0 +1,884 @@
+// The whole decode step in one persistent cooperative kernel (sm_103a).
+//
+// What the step computes is the pages' decoder ("IV.4: One command buffer
+// per token": embed_row; per layer RMSNorm, q|k|v matvecs, bias / QK-norm,
+// RoPE, append_kv, attention_decode, o matvec + residual, RMSNorm, gate|up
+// matvecs, SiLU*up, down matvec + residual; final RMSNorm, lm_head matvec,
+// argmax_row).  How it runs is GB300-specific:
+//  * One CTA per SM, 20 consumer warps and one producer warp.  The producer
+//    streams the weight tiles of this CTA's rows of every matvec phase, in
+//    phase order, through a ring of shared-memory stages with 1-D bulk
+//    copies (TMA) completing on mbarriers.  Weights do not depend on
+//    activations, so the stream runs ahead across phase boundaries, grid
+//    barriers and attention: HBM stays busy while the consumers wait.
+//  * Consumers walk the phase table; a grid-wide barrier (a counter in
+//    global memory, bounded spin) separates phases.  Activations written by
+//    other CTAs are read through L2 (ld.global.cg), never through the
+//    non-coherent L1 / read-only path.
+//  * Matvec phases use the layout of the standalone matvec kernel: warp
+//    pairs own the even / odd block columns of 64-column segments, the
+//    lane's 32 activations in registers (RMSNorm or SiLU*up applied while
+//    loading), lane partials reduced in double-buffered row windows.
+//  * Attention: one CTA per (KV head, context chunk) computes the G query
+//    heads' online-softmax partial over its chunk on CUDA cores (f32), the
+//    CTA owning row L-1 first applies bias / QK-norm / RoPE to the new k, v
+//    and appends them; a combine phase merges the chunks per query head.
+#include <algorithm>
+#include <cmath>
+
+#include "q8d_attn_common.cuh"
+#include "q8d_gemv.cuh"
+#include "q8d_internal.cuh"
+#include "q8d_megastep.cuh"
+#include "q8d_rows.cuh"
+
+namespace q8d {
+
+namespace {
+
+using namespace mv;
+
+constexpr int kW = kMsWarps;
+constexpr int kCT = kW * 32;  // consumer threads
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (~1 s with the sleeps)
+
+__device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
+
+// A pointer field of a read-only table.
+template <typename T>
+__device__ __forceinline__ T* ldg_ptr(T* const* p) {
+  return reinterpret_cast<T*>(__ldg(reinterpret_cast<const unsigned long long*>(p)));
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the consumer threads of all CTAs.  Returns false if
+// the step was aborted (a CTA gave up a wait); then every CTA stops.
+__device__ bool grid_sync(const MParams& P, unsigned& target, volatile int* s_abort,
+                          volatile int* s_flag) {
+  consumer_sync(kCT);
+  if (threadIdx.x == 0) {
+    target += gridDim.x;
+    int ok = *s_abort ? 0 : 1;
+    if (!ok) {
+      atomicExch(P.abort, 1);
+    } else {
+      __threadfence();
+      atomicAdd(P.bar, 1u);
+      for (uint32_t i = 0;; ++i) {
+        if ((int)(ld_acquire(P.bar) - target) >= 0) break;
+        if (*(volatile int*)P.abort) {
+          ok = 0;
+          break;
+        }
+        if (i >= kBarSpin) {
+          ok = 0;
+          atomicExch(P.abort, 1);
+          if (P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+          break;
+        }
+        __nanosleep(64);
+      }
+      __threadfence();
+    }
+    if (!ok) *s_abort = 1;
+    *s_flag = ok;
+  }
+  consumer_sync(kCT);
+  return *s_flag != 0;
+}
+
+// ---------------------------------------------------------------- matvec
+// Tiles of the CTA's virtual rows of phase F (at most F.R rows, never across
+// a matrix end).  Fields come from the phase copy in shared memory.
+struct MCursor {
+  int cur, r0, seg, seg_end;
+  __device__ void start(const MPhase& F, int v0) {
+    cur = v0;
+    seg = 0;
+    while (seg + 1 < F.nseg && v0 >= F.vbegin[seg + 1]) ++seg;
+    r0 = v0 - F.vbegin[seg];
+    seg_end = F.vbegin[seg + 1];
+  }
+  __device__ int rows(int R, int v1) const { return min(R, min(seg_end, v1) - cur); }
+  __device__ void advance(const MPhase& F, int n) {
+    cur += n;
+    r0 += n;
+    if (cur == seg_end && seg + 1 < F.nseg) {
+      ++seg;
+      r0 = 0;
+      seg_end = F.vbegin[seg + 1];
+    }
+  }
+};
+
+// Ring position shared by consecutive phases (tile index modulo the stages).
+struct RingPos {
+  int s;
+  uint32_t ph;
+  uint32_t stage32;
+};
+
+// The CTA's virtual row ranges of phase F: one contiguous range, or for a
+// gate|up phase the same rows of both matrices (two ranges).
+__device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int total, int piece,
+                                            int& v0, int& v1) {
+  if (glu) {
+    v0 = blockIdx.x * rpc;
+    v1 = min(nrows0, v0 + rpc);
+    if (v0 > v1) v0 = v1;
+    v0 += piece * nrows0;
+    v1 += piece * nrows0;
+  } else {
+    v0 = blockIdx.x * rpc;
+    v1 = min(total, v0 + rpc);
+  }
+}
+
+// Window reduction (see q8d_gemv.cu): 8 threads per row, fixed order.
+__device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, int wbeg, float& bv,
+                                 int& bi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 7;
+  const int NS = F.NS;
+  for (int r0 = warp * 4; r0 < nrow; r0 += kW * 4) {
+    const int r = r0 + (lane >> 3);
+    const bool valid = r < nrow;
+    const float4* pr =
+        reinterpret_cast<const float4*>(part + (size_t)(valid ? r : r0) * NS * 32) + sub;
+    uint64_t acc0 = pack2(0.f, 0.f), acc1 = acc0;
+    for (int k = 0; k < NS; ++k) {
+      const float4 v = pr[8 * k];
+      acc0 = add2(acc0, pack2(v.x, v.y));
+      acc1 = add2(acc1, pack2(v.z, v.w));
+    }
+    float lo, hi;
+    unpack2(add2(acc0, acc1), lo, hi);
+    float sum = lo + hi;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (valid && sub == 0) {
+      const int vr = wbeg + r;
+      int sg = 0;
+      while (sg + 1 < F.nseg && vr >= F.vbegin[sg + 1]) ++sg;
+      const int ri = vr - F.vbegin[sg];
+      float* y = F.y[sg] + ri;
+      float out = F.accumulate ? (__ldcg(y) + sum) : sum;
+      if (F.glu && sg == 1) {
+        // up row: gate row ri was written by this CTA in an earlier window
+        float* yg = F.y[0] + ri;
+        const float gt = __ldcg(yg);
+        *yg = gt / (1.0f + expf(-gt)) * out;
+      }
+      *y = out;
+      if (F.argmax && !isnan(out) && am_better(out, ri, bv, bi)) {
+        bv = out;
+        bi = ri;
+      }
+    }
+  }
+}
+
+// Consumes up to F.win tiles of the CTA's rows [c.cur, v1) of phase F (one
+// reduction window), storing the lanes' partials at window buffer `buf`
+// (bytes); returns the rows consumed.  AM: alignment mode of this warp.
+template <int AM>
+__device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp, uint64_t* full,
+                                 uint64_t* empty, int* s_abort, uint32_t smem32, MCursor& c,
+                                 uint32_t& delta, int v1, uint32_t lane_buf, int rg, bool active,
+                                 uint32_t boff, const uint64_t (&x2)[16], bool& ok) {
+  const int lane = threadIdx.x & 31;
+  const int RG = F.RG, R = F.R;
+  const int np = R / (2 * RG);
+  const int n32 = F.NS * 32;
+  const uint32_t rowb = (uint32_t)F.row_bytes;
+  const uint32_t step = (uint32_t)RG * rowb;
+  const uint32_t pstep = (uint32_t)(RG * n32 * 4);
+  const uint32_t rb15 = rowb & 15u;
+  int wrow = 0;
+#pragma unroll 1
+  for (int wt = 0; wt < F.win && c.cur < v1; ++wt) {
+    const int rows = c.rows(R, v1);
+    const int rows_st = active ? rows : 0;  // rows whose partials this warp stores
+    ok = wait_or_abort(&full[rp.s], rp.ph, s_abort) && ok;
+    // (warps beyond NS * RG, when NS does not divide the warp count, run the
+    // same code on row group 0's rows and store nothing)
+    uint32_t o = rp.stage32 + delta + boff + (uint32_t)rg * rowb;
+    uint32_t d = lane_buf + (uint32_t)(wrow * n32) * 4u;
+    int rl = rg;
+#pragma unroll 1
+    for (int j = 0; j < np; ++j) {
+      const float va = block_dot<AM>(o, x2);
+      const float vb = block_dot<AM>(o + step, x2);
+      if (rl < rows_st) sts32(d, va);
+      if (rl + RG < rows_st) sts32(d + pstep, vb);
+      o += 2 * step;
+      d += 2 * pstep;
+      rl += 2 * RG;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[rp.s]);
+    rp.stage32 += (uint32_t)P.stage_bytes;
+    if (++rp.s == P.nstages) {
+      rp.s = 0;
+      rp.ph ^= 1u;
+      rp.stage32 = smem32;
+    }
+    const int seg_before = c.seg;
+    c.advance(F, rows);
+    delta = c.seg == seg_before ? (delta + (uint32_t)rows * rb15) & 15u : 0u;
+    wrow += rows;
+  }
+  return wrow;
+}
+
+__device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uint64_t* full,
+                             uint64_t* empty, int* s_abort, uint32_t smem32, uint8_t* region,
+                             float* s_f, int* s_i) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = F.NS, RG = F.RG;
+  const bool active = warp < NS * RG;
+  const int ci = warp % NS, rg = active ? warp / NS : 0;
+  int col, col_read;
+  if (F.paired) {
+    const int par = ci & 1;
+    col = 64 * (ci >> 1) + 2 * lane + par;
+    col_read = min(col, F.bpr - 1 - ((F.bpr - 1 - par) & 1));
+  } else {
+    col = lane;
+    col_read = min(col, F.bpr - 1);
+  }
+  // Activations: every CTA needs all of x, and the warps of a column class
+  // share it, so x (and the RMSNorm weights) pass through shared memory in
+  // chunks of the region, loaded with coalesced 16-byte loads (each CTA
+  // starting at its own offset, so the CTAs released together by the grid
+  // barrier spread over L2 lines).  A lane's column is 8 chunks of 16 bytes
+  // and lanes read columns 256 bytes apart, so chunk t of column c is stored
+  // at position (t + c/2) mod 8 of the column: a warp's reads then cover all
+  // bank groups.
+  uint64_t x2[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) x2[t] = 0;
+  const bool rms = F.xmode == kXRmsNorm;
+  const int pass4 = (rms ? kMsRegion / 32 : kMsRegion / 16);  // float4s of x per pass
+  float inv = 1.f;
+  if (rms && F.n / 4 > pass4) {
+    // x does not fit in one pass: the sum of squares straight from L2
+    float ss = 0.f;
+    const float4* x4 = reinterpret_cast<const float4*>(F.X);
+    for (int i = threadIdx.x; i < F.n / 4; i += kCT) {
+      const float4 v = __ldcg(x4 + i);
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_f[warp] = ss;
+    consumer_sync(kCT);
+    float tot = 0.f;
+    for (int w = 0; w < kW; ++w) tot += s_f[w];
+    inv = 1.0f / sqrtf(tot / (float)F.n + P.eps);
+    consumer_sync(kCT);  // s_f is reused below
+  }
+  float4* xs = reinterpret_cast<float4*>(region);
+  float4* ws = xs + pass4;
+  for (int e0 = 0; e0 < F.n / 4; e0 += pass4) {
+    const int n4 = min(pass4, F.n / 4 - e0);
+    const int rot = (int)((blockIdx.x * 97u) % (unsigned)n4);
+    for (int i = threadIdx.x; i < n4; i += kCT) {
+      int j = i + rot;
+      if (j >= n4) j -= n4;
+      const int ph = (j & ~7) | (((j & 7) + (j >> 4)) & 7);
+      xs[ph] = __ldcg(reinterpret_cast<const float4*>(F.X) + e0 + j);
+      if (rms) ws[ph] = __ldg(reinterpret_cast<const float4*>(F.xw) + e0 + j);
+    }
+    consumer_sync(kCT);
+    if (rms && F.n / 4 <= pass4) {
+      // sum of squares (all of x is in this pass), the same order in every CTA
+      float ss = 0.f;
+      for (int i = threadIdx.x; i < n4; i += kCT) {
+        const float4 v = xs[i];
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_f[warp] = ss;
+      consumer_sync(kCT);
+      float tot = 0.f;
+      for (int w = 0; w < kW; ++w) tot += s_f[w];
+      inv = 1.0f / sqrtf(tot / (float)F.n + P.eps);
+    }
+    const int cl = col - e0 / 8;  // column within this pass
+    if (active && col < F.bpr && cl >= 0 && cl * 8 < n4) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int ph = cl * 8 + ((t + (cl >> 1)) & 7);
+        float4 v = xs[ph];
+        if (rms) {
+          const float4 wv = ws[ph];
+          v.x = v.x * inv * wv.x;
+          v.y = v.y * inv * wv.y;
+          v.z = v.z * inv * wv.z;
+          v.w = v.w * inv * wv.w;
+        }
+        x2[2 * t] = pack2(v.x, v.y);
+        x2[2 * t + 1] = pack2(v.z, v.w);
+      }
+    }
+    consumer_sync(kCT);  // the region is refilled next (or holds window partials)
+  }
+  const uint32_t boff = (uint32_t)col_read * kQBlockBytes;
+  float* part = reinterpret_cast<float*>(region);
+  const uint32_t part32 = smem_u32(region);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  bool ok = true;
+  // With an even number of blocks per row every row starts at a multiple of
+  // 4 bytes, so all blocks of a paired warp start at 2*(col & 1) mod 4.
+  const int am = (F.paired && (F.bpr & 1) == 0) ? (ci & 1) : 2;
+  const uint32_t n32 = (uint32_t)F.NS * 32u;
+  const uint32_t lane_part = part32 + ((uint32_t)(ci * 32 + lane) + (uint32_t)rg * n32) * 4u;
+  const uint32_t buf_bytes = (uint32_t)F.win * (uint32_t)F.R * n32 * 4u;
+  uint32_t buf = 0;
+  const int npieces = F.glu ? 2 : 1;
+  for (int piece = 0; piece < npieces; ++piece) {
+    int v0, v1;
+    piece_range(F.glu, F.vbegin[1], F.rows_per_cta, F.total_rows, piece, v0, v1);
+    MCursor c;
+    c.start(F, v0);
+    uint32_t delta = ((uint32_t)c.r0 * ((uint32_t)F.row_bytes & 15u)) & 15u;
+    while (c.cur < v1) {
+      const int wbeg = c.cur;
+      int nrow;
+      if (am == 0)
+        nrow = ms_consume_window<0>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+                                    lane_part + buf, rg, active, boff, x2, ok);
+      else if (am == 1)
+        nrow = ms_consume_window<1>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+                                    lane_part + buf, rg, active, boff, x2, ok);
+      else
+        nrow = ms_consume_window<2>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+                                    lane_part + buf, rg, active, boff, x2, ok);
+      // window complete: every consumer warp has stored its partials.  The
+      // other buffer was reduced before this barrier, so the next window may
+      // overwrite it.
+      consumer_sync(kCT);
+      ms_window_reduce(F, part + buf / 4, nrow, wbeg, bv, bi);
+      buf = buf ? 0u : buf_bytes;
+    }
+  }
+  if (F.argmax) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (am_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      s_f[warp] = bv;
+      s_i[warp] = bi;
+    }
+    consumer_sync(kCT);
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kW; ++w)
+        if (am_better(s_f[w], s_i[w], bv, bi)) {
+          bv = s_f[w];
+          bi = s_i[w];
+        }
+      P.am_val[blockIdx.x] = bv;
+      P.am_idx[blockIdx.x] = bi;
+    }
+  }
+  return ok;
+}
+
+// ---------------------------------------------------------------- embedding
+__device__ void embed_phase(const MParams& P, int tok, bool len_ok) {
+  const bool bad = tok < 0 || tok >= P.vocab;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && P.d_err) {
+    if (bad) atomicOr(P.d_err, Q8D_DERR_TOKEN_RANGE);
+    if (!len_ok) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
+  }
+  const long long rb = (long long)(P.hidden / kQBlock) * kQBlockBytes;
+  for (int i = blockIdx.x * kCT + threadIdx.x; i < P.hidden; i += gridDim.x * kCT) {
+    if (bad) {
+      P.x[i] = __int_as_float(0x7fc00000);
+      continue;
+    }
+    const uint8_t* blk = P.embed + (long long)tok * rb + (long long)(i / kQBlock) * kQBlockBytes;
+    const float sc = f16_bits_to_f32((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+    P.x[i] = sc * (float)(int8_t)blk[2 + (i % kQBlock)];
+  }
+}
+
+// ---------------------------------------------------------------- attention
+template <typename KT>
+__device__ __forceinline__ KT ms_to_cache(float v);
+template <>
+__device__ __forceinline__ __half ms_to_cache<__half>(float v) {
+  return __float2half_rn(v);
+}
+template <>
+__device__ __forceinline__ float ms_to_cache<float>(float v) {
+  return v;
+}
+
+// DPL consecutive cache elements at p as floats.
+template <typename KT, int DPL>
+__device__ __forceinline__ void ld_row_part(const KT* p, float (&f)[DPL]) {
+  if constexpr (sizeof(KT) == 2) {
+    const __half2* h = reinterpret_cast<const __half2*>(p);
+#pragma unroll
+    for (int j = 0; j < DPL / 2; ++j) {
+      const float2 t = __half22float2(h[j]);
+      f[2 * j] = t.x;
+      f[2 * j + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) f[j] = reinterpret_cast<const float*>(p)[j];
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+template <int D, typename KT>
+struct MsAttnCfg {
+  static constexpr int kST = 8192 / (D * (int)sizeof(KT));  // tokens per sub-tile (8 KB of K)
+  static constexpr int kDPL = D / 32;                        // dims per lane
+  static constexpr int kRowB = D * (int)sizeof(KT);
+  static constexpr int kGMax = 16;
+  static constexpr int kOffQ = 0;                            // f32 [G][D]
+  static constexpr int kOffS = kOffQ + kGMax * D * 4;        // f32 [G][ST]
+  static constexpr int kOffK = kOffS + kGMax * kST * 4;      // KT [ST][D]
+  static constexpr int kOffV = kOffK + kST * kRowB;
+  static constexpr int kBytes = kOffV + kST * kRowB;
+  static_assert(kBytes <= kMsRegion, "attention scratch fits the shared region");
+  static_assert(kST <= 64, "two tokens per lane at most in the softmax");
+};
+
+template <int D, typename KT>
+__device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok,
+                           uint8_t* region) {
+  using C = MsAttnCfg<D, KT>;
+  constexpr int DPL = C::kDPL, ST = C::kST;
+  const int Hk = P.n_kv_heads, G = P.n_heads / Hk, nc = P.nc;
+  const int item = blockIdx.x;
+  if (!len_ok || item >= Hk * nc) return;  // a bad length: the combine writes NaN
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = item / nc, c = item % nc;
+  const MLayer* Ly = P.layers + F.layer;
+  float* pm = P.ws_m + (size_t)item * G;
+  float* pl = P.ws_l + (size_t)item * G;
+  float* po = P.ws_o + (size_t)item * G * D;
+  const int T = (L + nc - 1) / nc;
+  const int t0 = c * T, t1 = min(L, t0 + T);
+  if (t0 >= t1) {
+    if (threadIdx.x < G) {
+      pm[threadIdx.x] = -INFINITY;
+      pl[threadIdx.x] = 0.f;
+    }
+    return;
+  }
+  float* qs = reinterpret_cast<float*>(region + C::kOffQ);
+  float* sc = reinterpret_cast<float*>(region + C::kOffS);
+  uint8_t* Ks = region + C::kOffK;
+  uint8_t* Vs = region + C::kOffV;
+  const int pos = L - 1;
+  const float* cosr = P.rope_cos + (size_t)pos * (D / 2);
+  const float* sinr = P.rope_sin + (size_t)pos * (D / 2);
+  const long long kvw = (long long)Hk * D;
+  KT* kc = reinterpret_cast<KT*>(ldg_ptr(&Ly->kcache));
+  KT* vc = reinterpret_cast<KT*>(ldg_ptr(&Ly->vcache));
+  const float* bq = ldg_ptr(&Ly->bq);
+  const float* bk = ldg_ptr(&Ly->bk);
+  const float* bvp = ldg_ptr(&Ly->bv);
+  const float* qn = ldg_ptr(&Ly->q_norm);
+  const float* kn = ldg_ptr(&Ly->k_norm);
+
+  // query heads of KV head g: bias, QK-norm, RoPE, then scale * log2(e)
+  if (warp < G) {
+    const int hq = g * G + warp;
+    float v[D / 32];
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) v[t] = ldcg(P.q + (size_t)hq * D + lane + 32 * t);
+    head_prologue<D>(v, lane, bq ? bq + (size_t)hq * D : nullptr, qn, P.eps, cosr, sinr);
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) qs[warp * D + lane + 32 * t] = v[t] * (P.scale * kLog2e);
+  }
+  // the CTA owning row L-1 appends the new k (bias, norm, RoPE) and v (bias)
+  if (t1 == L && (warp == G || warp == G + 1)) {
+    const bool isk = warp == G;
+    float v[D / 32];
+    const float* src = (isk ? P.k : P.v) + (size_t)g * D;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) v[t] = ldcg(src + lane + 32 * t);
+    if (isk)
+      head_prologue<D>(v, lane, bk ? bk + (size_t)g * D : nullptr, kn, P.eps, cosr, sinr);
+    else
+      head_prologue<D>(v, lane, bvp ? bvp + (size_t)g * D : nullptr, nullptr, 0.f, nullptr,
+                       nullptr);
+    KT* dst = (isk ? kc : vc) + (long long)pos * kvw + (long long)g * D;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = ms_to_cache<KT>(v[t]);
+  }
+  consumer_sync(kCT);  // q rows in shared memory; the appended row is in the cache
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float o[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+  constexpr int kChunks = C::kRowB / 16;
+  for (int tb = t0; tb < t1; tb += ST) {
+    const int nt = min(ST, t1 - tb);
+    for (int e = threadIdx.x; e < 2 * nt * kChunks; e += kCT) {
+      const int which = e / (nt * kChunks);
+      const int r = (e / kChunks) % nt, pc = e % kChunks;
+      const KT* src = (which ? vc : kc) + (long long)(tb + r) * kvw + (long long)g * D;
+      cp_async16((which ? Vs : Ks) + r * C::kRowB + pc * 16,
+                 reinterpret_cast<const uint8_t*>(src) + pc * 16);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    consumer_sync(kCT);
+    // scores (log2 domain): warp per token, lanes over dims
+    for (int r = warp; r < nt; r += kW) {
+      float kv[DPL];
+      ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Ks + r * C::kRowB) + lane * DPL, kv);
+      for (int h = 0; h < G; ++h) {
+        const float* qh = qs + h * D + lane * DPL;
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) part = fmaf(qh[j], kv[j], part);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) sc[h * ST + r] = part;
+      }
+    }
+    consumer_sync(kCT);
+    if (warp < G) {
+      // online softmax of head `warp` over the sub-tile, then O += P.V
+      float* sh = sc + warp * ST;
+      const float s0 = lane < nt ? sh[lane] : -INFINITY;
+      const float s1 = lane + 32 < nt ? sh[lane + 32] : -INFINITY;
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_run, mx);
+      const float corr = exp2f(m_run - mn);
+      const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
+      __syncwarp();
+      if (lane < nt) sh[lane] = p0;
+      if (lane + 32 < nt) sh[lane + 32] = p1;
+      float ps = p0 + p1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l_run = l_run * corr + ps;
+      m_run = mn;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] *= corr;
+      __syncwarp();
+      for (int r = 0; r < nt; ++r) {
+        const float p = sh[r];
+        float vv[DPL];
+        ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Vs + r * C::kRowB) + lane * DPL, vv);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[j] = fmaf(p, vv[j], o[j]);
+      }
+    }
+    consumer_sync(kCT);  // the sub-tile buffers are refilled next
+  }
+  if (warp < G) {
+    if (lane == 0) {
+      pm[warp] = m_run;
+      pl[warp] = l_run;
+    }
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) po[(size_t)warp * D + lane * DPL + j] = o[j];
+  }
+}
+
+// out[hq] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the chunks
+// of query head hq; warps take chunks w, w + 20, ... and are merged in
+// warp order (deterministic).
+template <int D>
+__device__ void combine_phase(const MParams& P, bool len_ok, uint8_t* region) {
+  constexpr int DPL = D / 32;
+  const int H = P.n_heads, Hk = P.n_kv_heads, G = H / Hk, nc = P.nc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* red = reinterpret_cast<float*>(region);  // [kW][D + 2]
+  for (int hq = blockIdx.x; hq < H; hq += gridDim.x) {
+    float* outp = P.attn + (size_t)hq * D;
+    if (!len_ok) {
+      for (int e = threadIdx.x; e < D; e += kCT) outp[e] = __int_as_float(0x7fc00000);
+      continue;
+    }
+    const int g = hq / G, h = hq % G;
+    float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+    for (int c = warp; c < nc; c += kW) {
+      const size_t it = ((size_t)g * nc + c) * G + h;
+      const float mc = ldcg(P.ws_m + it);
+      if (mc == -INFINITY) continue;  // empty chunk
+      const float lc = ldcg(P.ws_l + it);
+      const float mn = fmaxf(m, mc);
+      const float a = exp2f(m - mn), b = exp2f(mc - mn);
+      l = l * a + lc * b;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] = o[j] * a + ldcg(P.ws_o + it * D + lane * DPL + j) * b;
+      m = mn;
+    }
+    float* rw = red + warp * (D + 2);
+    if (lane == 0) {
+      rw[0] = m;
+      rw[1] = l;
+    }
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) rw[2 + lane * DPL + j] = o[j];
+    consumer_sync(kCT);
+    for (int d = threadIdx.x; d < D; d += kCT) {
+      float M = -INFINITY;
+#pragma unroll 1
+      for (int w = 0; w < kW; ++w) M = fmaxf(M, red[w * (D + 2)]);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll 1
+      for (int w = 0; w < kW; ++w) {
+        const float mw = red[w * (D + 2)];
+        if (mw == -INFINITY) continue;
+        const float wt = exp2f(mw - M);
+        lsum = fmaf(red[w * (D + 2) + 1], wt, lsum);
+        acc = fmaf(red[w * (D + 2) + 2 + d], wt, acc);
+      }
+      outp[d] = acc / lsum;
+    }
+    consumer_sync(kCT);
+  }
+}
+
+// ---------------------------------------------------------------- argmax
+__device__ void argmax_phase(const MParams& P, int pos) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int b = 0; b < (int)gridDim.x; ++b) {
+    const float v = ldcg(P.am_val + b);
+    const int i = __ldcg(P.am_idx + b);
+    if (am_better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+  *P.d_token = bi;
+  *P.d_pos = pos + 1;
+}
+
+// ---------------------------------------------------------------- producer
+// Issues every weight tile of this CTA's rows of all matvec phases, in
+// order, into the ring.  Returns the number of tiles issued (fewer if a
+// wait was abandoned).
+__device__ int produce_all(const MParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                           int* s_abort) {
+  const uint64_t pol = policy_evict_first();
+  int s = 0, issued = 0;
+  uint32_t ph = 0;
+  for (int pi = 0; pi < P.nphases; ++pi) {
+    const MPhase* F = P.phases + pi;
+    if (__ldg(&F->kind) != kPhMatvec) continue;
+    const int nseg = __ldg(&F->nseg), R = __ldg(&F->R), rpc = __ldg(&F->rows_per_cta);
+    const int total = __ldg(&F->total_rows), glu = __ldg(&F->glu);
+    const long long rowb = __ldg(&F->row_bytes);
+    for (int piece = 0; piece < (glu ? 2 : 1); ++piece) {
+    int v0, v1;
+    piece_range(glu, __ldg(&F->vbegin[1]), rpc, total, piece, v0, v1);
+    int cur = v0, seg = 0;
+    while (seg + 1 < nseg && v0 >= __ldg(&F->vbegin[seg + 1])) ++seg;
+    int r0 = v0 - __ldg(&F->vbegin[seg]);
+    int seg_end = __ldg(&F->vbegin[seg + 1]);
+    while (cur < v1) {
+      if (issued >= P.nstages && !wait_or_abort(&empty[s], ph ^ 1u, s_abort)) return issued;
+      const int rows = min(R, min(seg_end, v1) - cur);
+      const uint8_t* w = ldg_ptr(&F->w[seg]);
+      const long long segp = seg_end - __ldg(&F->vbegin[seg]);
+      const long long start = (long long)r0 * rowb;
+      const long long end = start + (long long)rows * rowb;
+      const long long cap16 = (segp * rowb) & ~15LL;
+      const long long a0 = start & ~15LL;
+      long long a1 = (end + 15) & ~15LL;
+      uint8_t* dst = smem + (size_t)P.stage_bytes * s;
+      if (a1 > cap16) {
+        a1 = cap16 > a0 ? cap16 : a0;
+        for (long long o = a1; o < end; ++o) dst[o - a0] = __ldg(w + o);
+      }
+      const uint32_t bytes = (uint32_t)(a1 - a0);
+      mbar_arrive_expect_tx(&full[s], bytes);
+      if (bytes) bulk_g2s(dst, w + a0, bytes, &full[s], pol);
+      cur += rows;
+      r0 += rows;
+      if (cur == seg_end && seg + 1 < nseg) {
+        ++seg;
+        r0 = 0;
+        seg_end = __ldg(&F->vbegin[seg + 1]);
+      }
+      ++issued;
+      if (++s == P.nstages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    }
+  }
+  return issued;
+}
+
+// ---------------------------------------------------------------- kernel
+template <int D, typename KT>
+__global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(16) MPhase s_ph;
+  __shared__ int s_abort, s_flag;
+  __shared__ float s_f[kW];
+  __shared__ int s_i[kW];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
+  uint64_t* empty = full + P.nstages;
+  uint8_t* region = reinterpret_cast<uint8_t*>(empty + P.nstages);  // 16-byte aligned
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.nstages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kW);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kW) {
+    // ---- producer warp ----
+    if (lane == 0) {
+      const int issued = produce_all(P, smem, full, empty, &s_abort);
+      if (*(volatile int*)&s_abort) {
+        // wait (bounded) for copies still in flight before the CTA exits
+        for (int j = max(0, issued - P.nstages); j < issued; ++j)
+          mbar_wait(&full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
+      }
+    }
+  } else {
+    // ---- consumers ----
+    const int tok = *(volatile const int*)P.d_token;
+    const int pos = *(volatile const int*)P.d_pos;
+    const int L = pos + 1;
+    const bool len_ok = pos >= 0 && L <= P.cap;
+    RingPos rp{0, 0u, smem_u32(smem)};
+    const uint32_t smem32 = smem_u32(smem);
+    unsigned target = 0;
+    for (int pi = 0; pi < P.nphases; ++pi) {
+      if (pi > 0 && !grid_sync(P, target, &s_abort, &s_flag)) break;
+      if (threadIdx.x < (int)(sizeof(MPhase) / 4))
+        reinterpret_cast<int*>(&s_ph)[threadIdx.x] =
+            __ldg(reinterpret_cast<const int*>(P.phases + pi) + threadIdx.x);
+      consumer_sync(kCT);
+      const int kind = s_ph.kind;
+      if (kind == kPhMatvec) {
+        if (!matvec_phase(s_ph, P, rp, full, empty, &s_abort, smem32, region, s_f, s_i)) {
+          s_abort = 1;  // seen at the next grid barrier
+        }
+      } else if (kind == kPhAttn) {
+        attn_phase<D, KT>(P, s_ph, L, len_ok, region);
+      } else if (kind == kPhCombine) {
+        combine_phase<D>(P, len_ok, region);
+      } else if (kind == kPhEmbed) {
+        embed_phase(P, tok, len_ok);
+      } else {
+        argmax_phase(P, pos);
+      }
+    }
+    if (s_abort && threadIdx.x == 0) {
+      atomicExch(P.abort, 1);
+      if (P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+    }
+  }
+  __syncthreads();
+}
+
+template <int D, typename KT>
+int launch_typed(const MParams& P, int grid, cudaStream_t st) {
+  auto fn = q8_step_kernel<D, KT>;
+  const size_t smem = megastep_smem(P);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return record_cuda(e);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kMsThreads, smem);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (occ < 1) return Q8D_EUNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kMsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fn, P);
+  return e == cudaSuccess ? Q8D_OK : record_cuda(e);
+}
+
+}  // namespace
+
+bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
+  F.bpr = F.n / kQBlock;
+  F.row_bytes = (long long)F.bpr * kQBlockBytes;
+  F.paired = F.bpr > 32 ? 1 : 0;
+  F.NS = F.paired ? 2 * ((F.bpr + 63) / 64) : 1;
+  if (F.NS > kMsWarps) return false;
+  F.RG = kMsWarps / F.NS;
+  // R = 2 * RG * np rows, np the largest of 4, 2, 1 within the stage target
+  int np = 4;
+  while (np > 1 && 2LL * F.RG * np * F.row_bytes + 32 > stage_target) np /= 2;
+  F.R = 2 * F.RG * np;
+  // window tiles: double-buffered partials within the shared region
+  const long long per_tile = 2LL * F.R * F.NS * 32 * 4;
+  if (per_tile > kMsRegion) return false;
+  F.win = (int)std::max<long long>(1, kMsRegion / per_tile);
+  F.total_rows = F.vbegin[F.nseg];
+  F.rows_per_cta = F.glu ? (F.vbegin[1] + grid - 1) / grid : (F.total_rows + grid - 1) / grid;
+  return true;
+}
+
+int megastep_max_stages(int stage_bytes) {
+  constexpr int kBudget = 224 * 1024;  // dynamic shared memory per CTA (one CTA per SM)
+  return (kBudget - kMsRegion) / (stage_bytes + 16);
+}
+
+size_t megastep_smem(const MParams& P) {
+  return (size_t)P.stage_bytes * P.nstages + 16ull * P.nstages + kMsRegion;
+}
+
+int megastep_launch(const MParams& P, int head_dim, int kv_dtype, int grid, cudaStream_t st) {
+  if (head_dim == 128)
+    return kv_dtype == Q8D_KV_F16 ? launch_typed<128, __half>(P, grid, st)
+                                  : launch_typed<128, float>(P, grid, st);
+  if (head_dim == 64)
+    return kv_dtype == Q8D_KV_F16 ? launch_typed<64, __half>(P, grid, st)
+                                  : launch_typed<64, float>(P, grid, st);
+  return Q8D_EUNSUPPORTED;
+}
+
+}  // namespace q8d

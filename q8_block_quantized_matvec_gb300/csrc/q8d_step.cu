@@ -1,51 +1,24 @@
 // Whole decode step captured as one CUDA graph ("IV.4: One command buffer
 // per token", "One command buffer": every operation of the step encoded
-// once, submitted as one unit, one integer read back).  On GB300 the
-// analogue of the pages' single command buffer is a CUDA graph: the host
-// launches it with one call, the token id and position live in device
-// memory, and the argmax kernel writes the next token and advances the
-// position so the same graph decodes the next token when launched again.
+// once, submitted as one unit, one integer read back).  On GB300 the graph
+// holds one memset (the grid barrier counter) and one persistent
+// cooperative kernel that runs every phase of the step (q8d_megastep.cu);
+// the token id and position live in device memory, and the kernel's last
+// phase writes the next token and advances the position, so the same graph
+// decodes the next token when launched again.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
 
-#include "q8d_attn.cuh"
 #include "q8d_internal.cuh"
+#include "q8d_megastep.cuh"
 #include "q8d_rows.cuh"
 
 namespace q8d {
 namespace {
-
-constexpr int kMaxRowCtas = 1024;  // upper bound on the lm_head launch's CTAs (argmax partials)
-
-// x = dequantised embedding row of *d_token ("The decoder: kernels and
-// helpers": embed_row); also publishes the attended length L = pos + 1.
-__global__ void embed_kernel(const uint8_t* __restrict__ embed, int hidden, int vocab,
-                             const int* d_token, const int* d_pos, int cap, float* x, int* d_len,
-                             int* d_err) {
-  griddep_launch_dependents();
-  griddep_wait();  // the previous step's argmax wrote the token
-  const int tok = *d_token;
-  const bool bad = tok < 0 || tok >= vocab;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (bad && d_err) atomicOr(d_err, Q8D_DERR_TOKEN_RANGE);
-    const int pos = *d_pos;
-    *d_len = pos + 1;  // checked against cap by the append/attention kernels
-    (void)cap;
-  }
-  const long long rb = (long long)(hidden / kQBlock) * kQBlockBytes;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x) {
-    if (bad) {
-      x[i] = __int_as_float(0x7fc00000);
-      continue;
-    }
-    const uint8_t* blk = embed + (long long)tok * rb + (long long)(i / kQBlock) * kQBlockBytes;
-    const float sc = f16_bits_to_f32((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
-    x[i] = sc * (float)(int8_t)blk[2 + (i % kQBlock)];
-  }
-}
 
 // cos/sin of pos * theta^(-i/half) for every cached position, computed in
 // double and rounded once (the RoPE of "Eight kernels": rope_row).
@@ -62,33 +35,6 @@ __global__ void rope_table_kernel(float* cosv, float* sinv, int cap, int half, d
   }
 }
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-// Final argmax over the lm_head CTAs' partial winners (ties to the lowest
-// index; "Eight kernels": argmax_row); writes the next token and advances
-// the position for the next launch of the graph.
-
-__global__ void argmax_final_kernel(const float* pv, const int* pi, int np, int* d_token,
-                                    int* d_pos) {
-  griddep_wait();
-  if (threadIdx.x != 0) return;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int b = 0; b < np; ++b)
-    if (better(pv[b], pi[b], bv, bi)) {
-      bv = pv[b];
-      bi = pi[b];
-    }
-  *d_token = bi;
-  *d_pos = *d_pos + 1;
-}
-
-__global__ void zero_ints(int* p, int n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
-}
-
 }  // namespace
 }  // namespace q8d
 
@@ -97,13 +43,12 @@ using namespace q8d;
 struct q8d_step {
   q8d_step_desc desc;
   std::vector<q8d_layer_desc> layers;
-  // workspace (one allocation)
-  void* ws = nullptr;
+  void* ws = nullptr;  // activations, tables and phase table (one allocation)
   float *x, *q, *k, *v, *attn, *gu, *logits, *rope_cos, *rope_sin, *am_val;
-  int *am_idx, *d_len, *tickets;
-  void* attn_ws;
-  size_t attn_ws_bytes;
-  int attn_nc;
+  int* am_idx;
+  unsigned* bar;  // grid barrier counter and abort flag (two ints)
+  MParams mp;
+  int grid = 0;
   int* h_err = nullptr;  // pinned
   cudaEvent_t ev = nullptr;
   cudaGraph_t graph = nullptr;
@@ -114,140 +59,81 @@ struct q8d_step {
 namespace q8d {
 int step_validate(const q8d_step_desc* d);
 
-// The step, five kernels per layer, each a programmatic dependent of the
-// previous one (its weight stream starts while the previous kernel drains):
-//   q|k|v matvec with RMSNorm folded into the activation load
-//   attention with bias / QK-norm / RoPE / KV append / combine folded in
-//   o matvec accumulating into the residual stream
-//   gate|up matvec with RMSNorm folded in
-//   down matvec with SiLU(gate)*up folded in, accumulating into the residual
-// then the lm_head matvec (final RMSNorm folded in, per-CTA argmax) and the
-// final argmax that writes the next token and advances the position.
+// The step: reset the grid barrier, then the persistent step kernel.
 static int enqueue_step(q8d_step* S, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(S->bar, 0, 2 * sizeof(unsigned), st);
+  if (e != cudaSuccess) return record_cuda(e);
+  return megastep_launch(S->mp, S->desc.head_dim, S->desc.kv_dtype, S->grid, st);
+}
+
+// Phase table of the step: embedding; per layer q|k|v (RMSNorm folded in),
+// attention partials (bias / QK-norm / RoPE / append folded in), combine,
+// o (+ residual), gate|up (RMSNorm folded in; SiLU(gate)*up formed as the
+// up rows complete), down (+ residual); lm_head (RMSNorm folded in, argmax
+// partials); argmax.
+static int build_phases(q8d_step* S, std::vector<MPhase>& ph, int& stage_bytes) {
   const q8d_step_desc& d = S->desc;
-  const int H = d.n_heads, Hk = d.n_kv_heads, D = d.head_dim;
-  const int qw = H * D, kvw = Hk * D;
-  int rc;
-  if ((rc = launch_ex(embed_kernel, dim3((d.hidden + 255) / 256), dim3(256), 0, st, true,
-                      static_cast<const uint8_t*>(d.embed), d.hidden, d.vocab,
-                      (const int*)d.d_token, (const int*)d.d_pos, d.cap, S->x, S->d_len, d.d_err)))
-    return rc;
+  const int qw = d.n_heads * d.head_dim, kvw = d.n_kv_heads * d.head_dim;
+  auto mv = [&](int layer, int n, const float* X, int xmode, const float* xw, int acc,
+                std::initializer_list<std::pair<const void*, std::pair<float*, int>>> segs) {
+    MPhase F{};
+    F.kind = kPhMatvec;
+    F.layer = layer;
+    F.n = n;
+    F.X = X;
+    F.xmode = xmode;
+    F.xw = xw;
+    F.accumulate = acc;
+    int i = 0, tot = 0;
+    for (auto& sg : segs) {
+      F.w[i] = static_cast<const uint8_t*>(sg.first);
+      F.y[i] = sg.second.first;
+      F.vbegin[i] = tot;
+      tot += sg.second.second;
+      ++i;
+    }
+    F.nseg = i;
+    F.vbegin[i] = tot;
+    return F;
+  };
+  MPhase E{};
+  E.kind = kPhEmbed;
+  ph.push_back(E);
   for (int li = 0; li < d.n_layers; ++li) {
     const q8d_layer_desc& L = S->layers[li];
-    {  // q | k | v projections of RMSNorm(x)
-      RowsParams P{};
-      P.seg[0] = {static_cast<const uint8_t*>(L.wq), S->q, qw, 0};
-      P.seg[1] = {static_cast<const uint8_t*>(L.wk), S->k, kvw, 0};
-      P.seg[2] = {static_cast<const uint8_t*>(L.wv), S->v, kvw, 0};
-      P.nseg = 3;
-      P.n = d.hidden;
-      P.X = S->x;
-      P.ldx = d.hidden;
-      P.m = 1;
-      P.xmode = kXRmsNorm;
-      P.xw = L.attn_norm;
-      P.eps = d.rms_eps;
-      P.pdl = 1;
-      P.d_err = d.d_err;
-      if ((rc = rows_plan_and_launch(P, st))) return rc;
-    }
-    {
-      AttnParams A{};
-      A.q = S->q;
-      A.k_new = S->k;
-      A.v_new = S->v;
-      A.kcache = L.kcache;
-      A.vcache = L.vcache;
-      A.kv_dtype = d.kv_dtype;
-      A.out = S->attn;
-      A.batch = 1;
-      A.n_heads = H;
-      A.n_kv_heads = Hk;
-      A.head_dim = D;
-      A.cap = d.cap;
-      A.batch_stride = 0;
-      A.d_lens = S->d_len;
-      A.scale = (float)(1.0 / std::sqrt((double)D));
-      A.workspace = S->attn_ws;
-      A.nc = S->attn_nc;
-      A.d_err = d.d_err;
-      A.bq = d.qkv_bias ? L.bq : nullptr;
-      A.bk = d.qkv_bias ? L.bk : nullptr;
-      A.bv = d.qkv_bias ? L.bv : nullptr;
-      A.q_norm = d.qk_norm ? L.q_norm : nullptr;
-      A.k_norm = d.qk_norm ? L.k_norm : nullptr;
-      A.eps = d.rms_eps;
-      A.rope_cos = S->rope_cos;
-      A.rope_sin = S->rope_sin;
-      A.tickets = S->tickets;
-      A.pdl = 1;
-      if ((rc = attn_launch(A, st))) return rc;
-    }
-    {  // x += Wo . attn
-      RowsParams P{};
-      P.seg[0] = {static_cast<const uint8_t*>(L.wo), S->x, d.hidden, 0};
-      P.nseg = 1;
-      P.n = qw;
-      P.X = S->attn;
-      P.ldx = qw;
-      P.m = 1;
-      P.accumulate = 1;
-      P.pdl = 1;
-      P.d_err = d.d_err;
-      if ((rc = rows_plan_and_launch(P, st))) return rc;
-    }
-    {  // gate | up of RMSNorm(x)
-      RowsParams P{};
-      P.seg[0] = {static_cast<const uint8_t*>(L.wg), S->gu, d.ffn, 0};
-      P.seg[1] = {static_cast<const uint8_t*>(L.wu), S->gu + d.ffn, d.ffn, 0};
-      P.nseg = 2;
-      P.n = d.hidden;
-      P.X = S->x;
-      P.ldx = d.hidden;
-      P.m = 1;
-      P.xmode = kXRmsNorm;
-      P.xw = L.ffn_norm;
-      P.eps = d.rms_eps;
-      P.pdl = 1;
-      P.d_err = d.d_err;
-      if ((rc = rows_plan_and_launch(P, st))) return rc;
-    }
-    {  // x += Wd . (silu(gate) * up)
-      RowsParams P{};
-      P.seg[0] = {static_cast<const uint8_t*>(L.wd), S->x, d.hidden, 0};
-      P.nseg = 1;
-      P.n = d.ffn;
-      P.X = S->gu;
-      P.ldx = d.ffn;
-      P.m = 1;
-      P.accumulate = 1;
-      P.xmode = kXSiluMul;
-      P.pdl = 1;
-      P.d_err = d.d_err;
-      if ((rc = rows_plan_and_launch(P, st))) return rc;
-    }
+    ph.push_back(mv(li, d.hidden, S->x, kXRmsNorm, L.attn_norm, 0,
+                    {{L.wq, {S->q, qw}}, {L.wk, {S->k, kvw}}, {L.wv, {S->v, kvw}}}));
+    MPhase A{};
+    A.kind = kPhAttn;
+    A.layer = li;
+    ph.push_back(A);
+    MPhase Cb{};
+    Cb.kind = kPhCombine;
+    Cb.layer = li;
+    ph.push_back(Cb);
+    ph.push_back(mv(li, qw, S->attn, kXPlain, nullptr, 1, {{L.wo, {S->x, d.hidden}}}));
+    MPhase GU = mv(li, d.hidden, S->x, kXRmsNorm, L.ffn_norm, 0,
+                   {{L.wg, {S->gu, d.ffn}}, {L.wu, {S->gu + d.ffn, d.ffn}}});
+    GU.glu = 1;  // writes h = silu(gate) * up over the gate half of gu
+    ph.push_back(GU);
+    ph.push_back(mv(li, d.ffn, S->gu, kXPlain, nullptr, 1, {{L.wd, {S->x, d.hidden}}}));
   }
-  int np = 0;
-  {  // logits = lm_head . RMSNorm(x), with per-CTA argmax partials
-    RowsParams P{};
-    P.seg[0] = {static_cast<const uint8_t*>(d.lm_head), S->logits, d.vocab, 0};
-    P.nseg = 1;
-    P.n = d.hidden;
-    P.X = S->x;
-    P.ldx = d.hidden;
-    P.m = 1;
-    P.xmode = kXRmsNorm;
-    P.xw = d.out_norm;
-    P.eps = d.rms_eps;
-    P.am_val = S->am_val;
-    P.am_idx = S->am_idx;
-    P.pdl = 1;
-    P.d_err = d.d_err;
-    if ((rc = rows_plan_and_launch(P, st, &np))) return rc;
+  MPhase LM = mv(-1, d.hidden, S->x, kXRmsNorm, d.out_norm, 0, {{d.lm_head, {S->logits, d.vocab}}});
+  LM.argmax = 1;
+  ph.push_back(LM);
+  MPhase AM{};
+  AM.kind = kPhArgmax;
+  ph.push_back(AM);
+  // Stages of ~40 KB: every matvec phase takes the largest tile that fits.
+  constexpr int kStageTarget = 40 * 1024 + 512;
+  stage_bytes = 0;
+  for (auto& F : ph) {
+    if (F.kind != kPhMatvec) continue;
+    if (!megastep_plan_matvec(F, S->grid, kStageTarget)) return Q8D_EUNSUPPORTED;
+    const long long sb = ((F.R * F.row_bytes + 32 + 127) / 128) * 128;
+    stage_bytes = (int)std::max<long long>(stage_bytes, sb);
   }
-  if (np > kMaxRowCtas) return Q8D_EUNSUPPORTED;
-  return launch_ex(argmax_final_kernel, dim3(1), dim3(32), 0, st, true, (const float*)S->am_val,
-                   (const int*)S->am_idx, np, d.d_token, d.d_pos);
+  return Q8D_OK;
 }
 
 }  // namespace q8d
@@ -266,8 +152,9 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   S->layers.assign(desc->layers, desc->layers + desc->n_layers);
   const q8d_step_desc& d = S->desc;
   const int qw = d.n_heads * d.head_dim, kvw = d.n_kv_heads * d.head_dim, half = d.head_dim / 2;
-  S->attn_nc = attn_chunks(1, d.n_kv_heads, d.cap);
-  S->attn_ws_bytes = attn_workspace_bytes(1, d.n_heads, d.n_kv_heads, d.head_dim, d.cap);
+  const int G = d.n_heads / d.n_kv_heads;
+  S->grid = sm_count();
+  const int nc = std::max(1, S->grid / d.n_kv_heads);  // attention chunks per KV head
 
   // carve one allocation (256-byte aligned pieces)
   size_t off = 0;
@@ -276,12 +163,15 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
     off += (bytes + 255) & ~(size_t)255;
     return o;
   };
+  const size_t nphases = 3 + 6ull * d.n_layers;
   const size_t o_x = take(4ull * d.hidden), o_q = take(4ull * qw), o_k = take(4ull * kvw),
                o_v = take(4ull * kvw), o_attn = take(4ull * qw), o_gu = take(8ull * d.ffn),
                o_logits = d.d_logits ? 0 : take(4ull * d.vocab),
                o_cos = take(4ull * d.cap * half), o_sin = take(4ull * d.cap * half),
-               o_amv = take(4ull * kMaxRowCtas), o_ami = take(4ull * kMaxRowCtas),
-               o_len = take(16), o_tk = take(4ull * d.n_kv_heads), o_aws = take(S->attn_ws_bytes);
+               o_amv = take(4ull * S->grid), o_ami = take(4ull * S->grid), o_bar = take(16),
+               o_wm = take(4ull * d.n_kv_heads * nc * G), o_wl = take(4ull * d.n_kv_heads * nc * G),
+               o_wo = take(4ull * d.n_kv_heads * nc * G * d.head_dim),
+               o_ph = take(sizeof(MPhase) * nphases), o_ly = take(sizeof(MLayer) * d.n_layers);
   cudaError_t e = cudaMalloc(&S->ws, off);
   if (e != cudaSuccess) {
     delete S;
@@ -300,22 +190,69 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   S->rope_sin = reinterpret_cast<float*>(base + o_sin);
   S->am_val = reinterpret_cast<float*>(base + o_amv);
   S->am_idx = reinterpret_cast<int*>(base + o_ami);
-  S->d_len = reinterpret_cast<int*>(base + o_len);
-  S->tickets = reinterpret_cast<int*>(base + o_tk);
-  S->attn_ws = base + o_aws;
+  S->bar = reinterpret_cast<unsigned*>(base + o_bar);
 
   auto fail = [&](int code) {
     q8d_step_destroy(S);
     return code;
   };
+  std::vector<MPhase> phases;
+  int stage_bytes = 0;
+  if ((rc = build_phases(S, phases, stage_bytes))) return fail(rc);
+  std::vector<MLayer> mlayers(d.n_layers);
+  for (int li = 0; li < d.n_layers; ++li) {
+    const q8d_layer_desc& L = S->layers[li];
+    mlayers[li] = {L.kcache, L.vcache, d.qkv_bias ? L.bq : nullptr, d.qkv_bias ? L.bk : nullptr,
+                   d.qkv_bias ? L.bv : nullptr, d.qk_norm ? L.q_norm : nullptr,
+                   d.qk_norm ? L.k_norm : nullptr};
+  }
+  MParams& P = S->mp;
+  P = MParams{};
+  P.phases = reinterpret_cast<const MPhase*>(base + o_ph);
+  P.nphases = (int)phases.size();
+  P.layers = reinterpret_cast<const MLayer*>(base + o_ly);
+  P.hidden = d.hidden;
+  P.vocab = d.vocab;
+  P.n_heads = d.n_heads;
+  P.n_kv_heads = d.n_kv_heads;
+  P.cap = d.cap;
+  P.eps = d.rms_eps;
+  P.scale = (float)(1.0 / std::sqrt((double)d.head_dim));
+  P.embed = static_cast<const uint8_t*>(d.embed);
+  P.d_token = d.d_token;
+  P.d_pos = d.d_pos;
+  P.d_err = d.d_err;
+  P.x = S->x;
+  P.q = S->q;
+  P.k = S->k;
+  P.v = S->v;
+  P.attn = S->attn;
+  P.logits = S->logits;
+  P.am_val = S->am_val;
+  P.am_idx = S->am_idx;
+  P.rope_cos = S->rope_cos;
+  P.rope_sin = S->rope_sin;
+  P.ws_m = reinterpret_cast<float*>(base + o_wm);
+  P.ws_l = reinterpret_cast<float*>(base + o_wl);
+  P.ws_o = reinterpret_cast<float*>(base + o_wo);
+  P.nc = nc;
+  P.bar = S->bar;
+  P.abort = reinterpret_cast<int*>(S->bar + 1);
+  P.stage_bytes = stage_bytes;
+  P.nstages = std::min(8, megastep_max_stages(stage_bytes));
+  if (P.nstages < 2) return fail(Q8D_EUNSUPPORTED);
+
   if ((e = cudaMallocHost(&S->h_err, sizeof(int))) != cudaSuccess) return fail(record_cuda(e));
   if ((e = cudaEventCreateWithFlags(&S->ev, cudaEventDisableTiming)) != cudaSuccess)
     return fail(record_cuda(e));
-
+  if ((e = cudaMemcpyAsync(base + o_ph, phases.data(), sizeof(MPhase) * phases.size(),
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return fail(record_cuda(e));
+  if ((e = cudaMemcpyAsync(base + o_ly, mlayers.data(), sizeof(MLayer) * mlayers.size(),
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return fail(record_cuda(e));
   rope_table_kernel<<<256, 256, 0, st>>>(S->rope_cos, S->rope_sin, d.cap, half,
                                          (double)d.rope_theta);
-  if ((rc = check_launch())) return fail(rc);
-  zero_ints<<<1, 32, 0, st>>>(S->tickets, d.n_kv_heads);  // attention tickets start at zero
   if ((rc = check_launch())) return fail(rc);
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(record_cuda(e));
 
