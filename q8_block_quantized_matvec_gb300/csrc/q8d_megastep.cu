@@ -20,9 +20,11 @@
 //    lane's 32 activations in registers (RMSNorm or SiLU*up applied while
 //    loading), lane partials reduced in double-buffered row windows.
 //  * Attention: one CTA per (KV head, context chunk) computes the G query
-//    heads' online-softmax partial over its chunk on CUDA cores (f32), the
-//    CTA owning row L-1 first applies bias / QK-norm / RoPE to the new k, v
-//    and appends them; a combine phase merges the chunks per query head.
+//    heads' online-softmax partial over its chunk on CUDA cores (f32); the
+//    CTA owning row L-1 applies bias / QK-norm / RoPE to the new k, v,
+//    appends them to the cache and patches them into its chunk; a combine
+//    phase (one CTA per query head) merges the chunks.  The producer warp
+//    prefetches each CTA's K/V chunk into L2 a phase ahead.
 #include <algorithm>
 #include <cmath>
 
@@ -458,9 +460,16 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 
+// Context chunks per KV head for attended length L: P.nc (every CTA takes a
+// chunk) unless that leaves chunks of fewer than 16 rows; producer, attention
+// and combine agree on it.
+__device__ __forceinline__ int attn_chunks_for(const MParams& P, int L) {
+  return max(1, min(P.nc, (L + 15) / 16));
+}
+
 template <int D, typename KT>
 struct MsAttnCfg {
-  static constexpr int kST = 8192 / (D * (int)sizeof(KT));  // tokens per sub-tile (8 KB of K)
+  static constexpr int kST = 16384 / (D * (int)sizeof(KT)) < 64 ? 16384 / (D * (int)sizeof(KT)) : 64;  // tokens per sub-tile
   static constexpr int kDPL = D / 32;                        // dims per lane
   static constexpr int kRowB = D * (int)sizeof(KT);
   static constexpr int kGMax = 16;
@@ -478,9 +487,11 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
                            uint8_t* region) {
   using C = MsAttnCfg<D, KT>;
   constexpr int DPL = C::kDPL, ST = C::kST;
-  const int Hk = P.n_kv_heads, G = P.n_heads / Hk, nc = P.nc;
+  const int Hk = P.n_kv_heads, G = P.n_heads / Hk;
   const int item = blockIdx.x;
-  if (!len_ok || item >= Hk * nc) return;  // a bad length: the combine writes NaN
+  if (!len_ok) return;  // the combine writes NaN outputs
+  const int nc = attn_chunks_for(P, L);
+  if (item >= Hk * nc) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = item / nc, c = item % nc;
   const MLayer* Ly = P.layers + F.layer;
@@ -489,13 +500,7 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
   float* po = P.ws_o + (size_t)item * G * D;
   const int T = (L + nc - 1) / nc;
   const int t0 = c * T, t1 = min(L, t0 + T);
-  if (t0 >= t1) {
-    if (threadIdx.x < G) {
-      pm[threadIdx.x] = -INFINITY;
-      pl[threadIdx.x] = 0.f;
-    }
-    return;
-  }
+  // (every chunk is non-empty: nc <= ceil(L / 128))
   float* qs = reinterpret_cast<float*>(region + C::kOffQ);
   float* sc = reinterpret_cast<float*>(region + C::kOffS);
   uint8_t* Ks = region + C::kOffK;
@@ -512,6 +517,24 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
   const float* qn = ldg_ptr(&Ly->q_norm);
   const float* kn = ldg_ptr(&Ly->k_norm);
 
+  constexpr int kChunks = C::kRowB / 16;
+  const bool owner = t1 == L;  // this CTA's chunk ends with the new row L-1
+  // K/V rows [tb, tb + nt) of head g into the sub-tile buffers, except the
+  // new row, which the owner writes in from registers.
+  auto issue = [&](int tb) {
+    const int nt = min(ST, t1 - tb);
+    const int nl = (owner && tb + nt == L) ? nt - 1 : nt;
+    for (int e = threadIdx.x; e < 2 * nl * kChunks; e += kCT) {
+      const int which = e / (nl * kChunks);
+      const int r = (e / kChunks) % nl, pc = e % kChunks;
+      const KT* src = (which ? vc : kc) + (long long)(tb + r) * kvw + (long long)g * D;
+      cp_async16((which ? Vs : Ks) + r * C::kRowB + pc * 16,
+                 reinterpret_cast<const uint8_t*>(src) + pc * 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  issue(t0);  // the loads overlap the prologues below
+
   // query heads of KV head g: bias, QK-norm, RoPE, then scale * log2(e)
   if (warp < G) {
     const int hq = g * G + warp;
@@ -522,52 +545,77 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
 #pragma unroll
     for (int t = 0; t < D / 32; ++t) qs[warp * D + lane + 32 * t] = v[t] * (P.scale * kLog2e);
   }
-  // the CTA owning row L-1 appends the new k (bias, norm, RoPE) and v (bias)
-  if (t1 == L && (warp == G || warp == G + 1)) {
+  // the owner appends the new k (bias, norm, RoPE) and v (bias) to the cache
+  // and keeps them, rounded to the cache type, for its last sub-tile
+  float nv[D / 32];
+  const bool appender = owner && (warp == G || warp == G + 1);
+  if (appender) {
     const bool isk = warp == G;
-    float v[D / 32];
     const float* src = (isk ? P.k : P.v) + (size_t)g * D;
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t) v[t] = ldcg(src + lane + 32 * t);
+    for (int t = 0; t < D / 32; ++t) nv[t] = ldcg(src + lane + 32 * t);
     if (isk)
-      head_prologue<D>(v, lane, bk ? bk + (size_t)g * D : nullptr, kn, P.eps, cosr, sinr);
+      head_prologue<D>(nv, lane, bk ? bk + (size_t)g * D : nullptr, kn, P.eps, cosr, sinr);
     else
-      head_prologue<D>(v, lane, bvp ? bvp + (size_t)g * D : nullptr, nullptr, 0.f, nullptr,
+      head_prologue<D>(nv, lane, bvp ? bvp + (size_t)g * D : nullptr, nullptr, 0.f, nullptr,
                        nullptr);
     KT* dst = (isk ? kc : vc) + (long long)pos * kvw + (long long)g * D;
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = ms_to_cache<KT>(v[t]);
+    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = ms_to_cache<KT>(nv[t]);
   }
-  consumer_sync(kCT);  // q rows in shared memory; the appended row is in the cache
 
   float m_run = -INFINITY, l_run = 0.f;
   float o[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-  constexpr int kChunks = C::kRowB / 16;
   for (int tb = t0; tb < t1; tb += ST) {
     const int nt = min(ST, t1 - tb);
-    for (int e = threadIdx.x; e < 2 * nt * kChunks; e += kCT) {
-      const int which = e / (nt * kChunks);
-      const int r = (e / kChunks) % nt, pc = e % kChunks;
-      const KT* src = (which ? vc : kc) + (long long)(tb + r) * kvw + (long long)g * D;
-      cp_async16((which ? Vs : Ks) + r * C::kRowB + pc * 16,
-                 reinterpret_cast<const uint8_t*>(src) + pc * 16);
+    if (tb != t0) issue(tb);
+    if (appender && tb + nt == L) {
+      KT* row = reinterpret_cast<KT*>((warp == G ? Ks : Vs) + (nt - 1) * C::kRowB);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) row[lane + 32 * t] = ms_to_cache<KT>(nv[t]);
     }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    consumer_sync(kCT);
-    // scores (log2 domain): warp per token, lanes over dims
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    consumer_sync(kCT);  // q rows, this sub-tile's K/V rows and the new row are in place
+    // scores (log2 domain): warp per token, lanes over dims; the lanes'
+    // partial dot products of 4 heads are reduce-scattered across the warp
+    // (lane octet k ends with head k's sum: 6 shuffles instead of 20)
     for (int r = warp; r < nt; r += kW) {
       float kv[DPL];
       ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Ks + r * C::kRowB) + lane * DPL, kv);
-      for (int h = 0; h < G; ++h) {
-        const float* qh = qs + h * D + lane * DPL;
-        float part = 0.f;
+      for (int h0 = 0; h0 < G; h0 += 4) {
+        float v[4];
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) part = fmaf(qh[j], kv[j], part);
+        for (int i = 0; i < 4; ++i) {
+          const float4* qh = reinterpret_cast<const float4*>(qs + min(h0 + i, G - 1) * D + lane * DPL);
+          float part = 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) sc[h * ST + r] = part;
+          for (int j = 0; j < DPL / 4; ++j) {
+            const float4 qq = qh[j];
+            part = fmaf(qq.x, kv[4 * j], part);
+            part = fmaf(qq.y, kv[4 * j + 1], part);
+            part = fmaf(qq.z, kv[4 * j + 2], part);
+            part = fmaf(qq.w, kv[4 * j + 3], part);
+          }
+          if constexpr (DPL % 4 != 0) {
+#pragma unroll
+            for (int j = DPL - DPL % 4; j < DPL; ++j)
+              part = fmaf(qs[min(h0 + i, G - 1) * D + lane * DPL + j], kv[j], part);
+          }
+          v[i] = part;
+        }
+        const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+        float w2[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          w2[i] = (b4 ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 2], 16);
+        float z = (b3 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? w2[0] : w2[1], 8);
+        z += __shfl_xor_sync(0xffffffffu, z, 4);
+        z += __shfl_xor_sync(0xffffffffu, z, 2);
+        z += __shfl_xor_sync(0xffffffffu, z, 1);
+        const int hh = h0 + ((lane >> 3) & 3);
+        if ((lane & 7) == 0 && hh < G) sc[hh * ST + r] = z;
       }
     }
     consumer_sync(kCT);
@@ -590,16 +638,32 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
       for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l_run = l_run * corr + ps;
       m_run = mn;
-#pragma unroll
-      for (int j = 0; j < DPL; ++j) o[j] *= corr;
       __syncwarp();
-      for (int r = 0; r < nt; ++r) {
-        const float p = sh[r];
-        float vv[DPL];
-        ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Vs + r * C::kRowB) + lane * DPL, vv);
+      // P.V with two independent accumulator sets
+      float pa[DPL], pb[DPL];
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) o[j] = fmaf(p, vv[j], o[j]);
+      for (int j = 0; j < DPL; ++j) pa[j] = pb[j] = 0.f;
+      int r = 0;
+      for (; r + 1 < nt; r += 2) {
+        const float p0r = sh[r], p1r = sh[r + 1];
+        float va[DPL], vb[DPL];
+        ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Vs + r * C::kRowB) + lane * DPL, va);
+        ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Vs + (r + 1) * C::kRowB) + lane * DPL, vb);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+          pa[j] = fmaf(p0r, va[j], pa[j]);
+          pb[j] = fmaf(p1r, vb[j], pb[j]);
+        }
       }
+      if (r < nt) {
+        const float p0r = sh[r];
+        float va[DPL];
+        ld_row_part<KT, DPL>(reinterpret_cast<const KT*>(Vs + r * C::kRowB) + lane * DPL, va);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) pa[j] = fmaf(p0r, va[j], pa[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] = fmaf(o[j], corr, pa[j] + pb[j]);
     }
     consumer_sync(kCT);  // the sub-tile buffers are refilled next
   }
@@ -613,15 +677,17 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
   }
 }
 
-// out[hq] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the chunks
-// of query head hq; warps take chunks w, w + 20, ... and are merged in
+// out[hq] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the chunks of
+// query head hq (one CTA per query head).  Warp w takes chunks w, w + 20,
+// ... with all loads issued before use; the warps' partials are merged in
 // warp order (deterministic).
 template <int D>
-__device__ void combine_phase(const MParams& P, bool len_ok, uint8_t* region) {
+__device__ void combine_phase(const MParams& P, int L, bool len_ok, uint8_t* region) {
   constexpr int DPL = D / 32;
-  const int H = P.n_heads, Hk = P.n_kv_heads, G = H / Hk, nc = P.nc;
+  const int H = P.n_heads, Hk = P.n_kv_heads, G = H / Hk;
+  const int nc = attn_chunks_for(P, L);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* red = reinterpret_cast<float*>(region);  // [kW][D + 2]
+  float* red = reinterpret_cast<float*>(region);  // [kW][D + 4]
   for (int hq = blockIdx.x; hq < H; hq += gridDim.x) {
     float* outp = P.attn + (size_t)hq * D;
     if (!len_ok) {
@@ -632,38 +698,47 @@ __device__ void combine_phase(const MParams& P, bool len_ok, uint8_t* region) {
     float m = -INFINITY, l = 0.f, o[DPL];
 #pragma unroll
     for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-    for (int c = warp; c < nc; c += kW) {
-      const size_t it = ((size_t)g * nc + c) * G + h;
-      const float mc = ldcg(P.ws_m + it);
-      if (mc == -INFINITY) continue;  // empty chunk
-      const float lc = ldcg(P.ws_l + it);
-      const float mn = fmaxf(m, mc);
-      const float a = exp2f(m - mn), b = exp2f(mc - mn);
-      l = l * a + lc * b;
+    // at most two chunks per warp for nc <= 40: load both, then merge
+    for (int c0 = warp; c0 < nc; c0 += 2 * kW) {
+      const int c1 = c0 + kW;
+      const size_t i0 = ((size_t)g * nc + c0) * G + h;
+      const size_t i1 = ((size_t)g * nc + min(c1, nc - 1)) * G + h;
+      const float m0 = ldcg(P.ws_m + i0), l0 = ldcg(P.ws_l + i0);
+      const float m1 = c1 < nc ? ldcg(P.ws_m + i1) : -INFINITY;
+      const float l1 = ldcg(P.ws_l + i1);
+      float a0[DPL], a1[DPL];  // through L2: the partials are rewritten every layer
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) o[j] = o[j] * a + ldcg(P.ws_o + it * D + lane * DPL + j) * b;
+      for (int j = 0; j < DPL; ++j) {
+        a0[j] = ldcg(P.ws_o + i0 * D + lane * DPL + j);
+        a1[j] = ldcg(P.ws_o + i1 * D + lane * DPL + j);
+      }
+      const float mn = fmaxf(m, fmaxf(m0, m1));
+      const float s = exp2f(m - mn), w0 = exp2f(m0 - mn), w1 = c1 < nc ? exp2f(m1 - mn) : 0.f;
+      l = l * s + l0 * w0 + l1 * w1;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] = o[j] * s + a0[j] * w0 + (c1 < nc ? a1[j] * w1 : 0.f);
       m = mn;
     }
-    float* rw = red + warp * (D + 2);
+    float* rw = red + warp * (D + 4);
     if (lane == 0) {
       rw[0] = m;
       rw[1] = l;
     }
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) rw[2 + lane * DPL + j] = o[j];
+    for (int j = 0; j < DPL; ++j) rw[4 + lane * DPL + j] = o[j];
     consumer_sync(kCT);
     for (int d = threadIdx.x; d < D; d += kCT) {
       float M = -INFINITY;
 #pragma unroll 1
-      for (int w = 0; w < kW; ++w) M = fmaxf(M, red[w * (D + 2)]);
+      for (int w = 0; w < kW; ++w) M = fmaxf(M, red[w * (D + 4)]);
       float lsum = 0.f, acc = 0.f;
 #pragma unroll 1
       for (int w = 0; w < kW; ++w) {
-        const float mw = red[w * (D + 2)];
+        const float mw = red[w * (D + 4)];
         if (mw == -INFINITY) continue;
         const float wt = exp2f(mw - M);
-        lsum = fmaf(red[w * (D + 2) + 1], wt, lsum);
-        acc = fmaf(red[w * (D + 2) + 2 + d], wt, acc);
+        lsum = fmaf(red[w * (D + 4) + 1], wt, lsum);
+        acc = fmaf(red[w * (D + 4) + 4 + d], wt, acc);
       }
       outp[d] = acc / lsum;
     }
@@ -697,9 +772,34 @@ __device__ int produce_all(const MParams& P, uint8_t* smem, uint64_t* full, uint
   const uint64_t pol = policy_evict_first();
   int s = 0, issued = 0;
   uint32_t ph = 0;
+  const int pos = *(volatile const int*)P.d_pos;
+  const int L = pos + 1;
+  const bool len_ok = pos >= 0 && L <= P.cap;
   for (int pi = 0; pi < P.nphases; ++pi) {
     const MPhase* F = P.phases + pi;
-    if (__ldg(&F->kind) != kPhMatvec) continue;
+    const int kind = __ldg(&F->kind);
+    if (kind == kPhAttn && len_ok && (int)blockIdx.x < P.n_kv_heads * attn_chunks_for(P, L)) {
+      // pull this CTA's K/V chunk (the rows before the new one) into L2 now,
+      // a phase or more before the attention phase reads it
+      const int nc = attn_chunks_for(P, L);
+      const int g = blockIdx.x / nc, c = blockIdx.x % nc;
+      const int T = (L + nc - 1) / nc;
+      const int t0 = c * T, t1 = min(L - 1, t0 + T);
+      const MLayer* Ly = P.layers + __ldg(&F->layer);
+      const uint8_t* kc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->kcache));
+      const uint8_t* vc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->vcache));
+      const long long rowb = (long long)P.head_dim * P.kv_esize;
+      const long long stride = rowb * P.n_kv_heads;
+      for (int t = t0; t < t1; ++t) {
+        const long long off = (long long)t * stride + (long long)g * rowb;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kc + off), "r"((uint32_t)rowb)
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vc + off), "r"((uint32_t)rowb)
+                     : "memory");
+      }
+      continue;
+    }
+    if (kind != kPhMatvec) continue;
     const int nseg = __ldg(&F->nseg), R = __ldg(&F->R), rpc = __ldg(&F->rows_per_cta);
     const int total = __ldg(&F->total_rows), glu = __ldg(&F->glu);
     const long long rowb = __ldg(&F->row_bytes);
@@ -801,7 +901,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
       } else if (kind == kPhAttn) {
         attn_phase<D, KT>(P, s_ph, L, len_ok, region);
       } else if (kind == kPhCombine) {
-        combine_phase<D>(P, len_ok, region);
+        combine_phase<D>(P, L, len_ok, region);
       } else if (kind == kPhEmbed) {
         embed_phase(P, tok, len_ok);
       } else {

@@ -49,7 +49,7 @@ struct MParams {
   const MPhase* phases;
   int nphases;
   const MLayer* layers;
-  int hidden, vocab, n_heads, n_kv_heads, cap;
+  int hidden, vocab, n_heads, n_kv_heads, cap, head_dim, kv_esize;
   float eps, scale;
   const uint8_t* embed;
   int* d_token;
@@ -59,7 +59,7 @@ struct MParams {
   int* am_idx;
   const float *rope_cos, *rope_sin;
   float *ws_m, *ws_l, *ws_o;  // attention partials, [Hk][nc][G] (and [D])
-  int nc;                     // context chunks per KV head
+  int nc;                     // most context chunks per KV head
   unsigned* bar;              // grid barrier counter, zero at launch
   int* abort;                 // set when a CTA gives up a wait, zero at launch
   int stage_bytes, nstages;

@@ -46,7 +46,7 @@ struct q8d_step {
   void* ws = nullptr;  // activations, tables and phase table (one allocation)
   float *x, *q, *k, *v, *attn, *gu, *logits, *rope_cos, *rope_sin, *am_val;
   int* am_idx;
-  unsigned* bar;  // grid barrier counter and abort flag (two ints)
+  unsigned* bar;  // grid barrier counter and abort flag
   MParams mp;
   int grid = 0;
   int* h_err = nullptr;  // pinned
@@ -216,6 +216,8 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   P.n_heads = d.n_heads;
   P.n_kv_heads = d.n_kv_heads;
   P.cap = d.cap;
+  P.head_dim = d.head_dim;
+  P.kv_esize = d.kv_dtype == Q8D_KV_F16 ? 2 : 4;
   P.eps = d.rms_eps;
   P.scale = (float)(1.0 / std::sqrt((double)d.head_dim));
   P.embed = static_cast<const uint8_t*>(d.embed);
