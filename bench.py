@@ -200,8 +200,12 @@ def run_profile(args):
     torch.cuda.set_device(0)
     cudart = torch.cuda.cudart()
     if args.profile == "step":
+        import dataclasses
         from q8_block_quantized_matvec_gb300.device import DeviceStep
         shape = synth.MODELS[args.model]
+        if args.layers:
+            # the same layer shapes with fewer layers: a capture-sized step
+            shape = dataclasses.replace(shape, n_layers=args.layers)
         ctx = args.context
         cap = ctx + 16
         wts = synth.TorchStepWeights(shape, seed=0)
@@ -310,6 +314,8 @@ def main():
     ap.add_argument("--impl", default="q8d", choices=["q8d", "reference"])
     ap.add_argument("--model", default="qwen2.5-7b", choices=["qwen2.5-7b", "qwen3-0.6b", "qwen2.5-0.5b"])
     ap.add_argument("--context", type=int, default=2048)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="--profile step only: use this many layers of the model's shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=3)
     ap.add_argument("--profile", choices=["step", "matvec", "matvec_down", "attn", "matvec_sweep"],

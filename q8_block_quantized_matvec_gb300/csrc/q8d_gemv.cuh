@@ -73,12 +73,28 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-// Bounded wait that gives up at once when another thread of the CTA already
-// gave up, so that every warp still reaches the CTA barriers quickly.
+// try_wait that lets the thread sleep (up to about a microsecond) until the
+// phase completes instead of returning at once: waiting warps stop taking
+// issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (about two seconds) that gives up at once when another
+// thread of the CTA already gave up, so that every warp still reaches the
+// CTA barriers quickly.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < (1u << 21); ++i) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
   }
   *abort_flag = 1;

@@ -213,8 +213,9 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
     uint32_t o = rp.stage32 + delta + boff + (uint32_t)rg * rowb;
     uint32_t d = lane_buf + (uint32_t)(wrow * n32) * 4u;
     int rl = rg;
+    // pairs up to this warp's last row of the tile (a ragged tile stops early)
 #pragma unroll 1
-    for (int j = 0; j < np; ++j) {
+    for (int j = 0; j < np && rl < rows; ++j) {
       const float va = block_dot<AM>(o, x2);
       const float vb = block_dot<AM>(o + step, x2);
       if (rl < rows_st) sts32(d, va);
@@ -950,8 +951,13 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
   if (F.NS > kMsWarps) return false;
   F.RG = kMsWarps / F.NS;
   // R = 2 * RG * np rows, np the largest of 4, 2, 1 within the stage target
+  // that still gives every CTA at least four tiles of the phase
+  const long long rows_cta = F.glu ? ((long long)F.vbegin[1] + grid - 1) / grid * 2
+                                   : ((long long)F.vbegin[F.nseg] + grid - 1) / grid;
   int np = 4;
-  while (np > 1 && 2LL * F.RG * np * F.row_bytes + 32 > stage_target) np /= 2;
+  while (np > 1 && (2LL * F.RG * np * F.row_bytes + 32 > stage_target ||
+                    rows_cta < 4LL * 2 * F.RG * np))
+    np /= 2;
   F.R = 2 * F.RG * np;
   // window tiles: double-buffered partials within the shared region
   const long long per_tile = 2LL * F.R * F.NS * 32 * 4;

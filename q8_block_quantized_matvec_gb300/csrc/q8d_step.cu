@@ -125,7 +125,7 @@ static int build_phases(q8d_step* S, std::vector<MPhase>& ph, int& stage_bytes) 
   AM.kind = kPhArgmax;
   ph.push_back(AM);
   // Stages of ~40 KB: every matvec phase takes the largest tile that fits.
-  constexpr int kStageTarget = 40 * 1024 + 512;
+  constexpr int kStageTarget = 80 * 1024 + 512;
   stage_bytes = 0;
   for (auto& F : ph) {
     if (F.kind != kPhMatvec) continue;
