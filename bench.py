@@ -1,8 +1,9 @@
 """Decode-step throughput of the GB300 Q8_0 decode path.
 
-One step = one launch of the captured decode-step graph: every Q8_0 matvec
-(196 layer matvecs + lm_head), every layer's KV append + split-K attention,
-all glue, argmax; token and position stay in device memory.
+One step = one launch of the captured decode-step graph (a memset and the
+persistent step kernel): every Q8_0 matvec (196 layer matvecs + lm_head),
+every layer's KV append + split-K attention, all glue, argmax; token and
+position stay in device memory.
 
 Workload (default): 7B-shaped model (hidden 3584, 28 layers, 28/4 heads,
 head_dim 128, FFN 18944, vocab 152064, Q8_0 weights = 7.51 GB + 0.58 GB
@@ -125,38 +126,56 @@ def attn_bytes(L, Hk, D, H, esize, append=True):
     return L * Hk * D * 2 * esize + 4 * 2 * H * D + (2 * Hk * D * esize if append else 0)
 
 
+STEP_KERNEL_SOURCES = ("q8d_megastep.cu", "q8d_megastep.cuh", "q8d_gemv.cuh", "q8d_internal.cuh",
+                       "q8d_attn_common.cuh", "q8d_rows.cuh", "q8d_step.cu")
+
+
 def kernel_source_sha():
+    """Hash of the step kernel's sources (ties an ncu summary to a build)."""
     h = hashlib.sha256()
-    for nm in ("q8d_rows.cu", "q8d_internal.cuh", "q8d_rows.cuh"):
+    for nm in STEP_KERNEL_SOURCES:
         with open(os.path.join(ROOT, "q8_block_quantized_matvec_gb300", "csrc", nm), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "q8_matvec_7b_decode_step.md")
+def step_bytes(shape, context: int, esize: int) -> float:
+    """Algorithmic HBM bytes of one decode step at attended length `context`:
+    every weight byte once (layers + lm_head + one embedding row), each
+    layer's K and V rows read once and the new row written."""
+    kv = shape.n_layers * (2 * context * shape.kv_width * esize + 2 * shape.kv_width * esize)
+    return float(shape.weight_bytes() + kv)
+
+
+def ncu_traffic(algorithmic_bytes: float):
+    """DRAM bytes per launch of the step kernel: the committed ncu summary's
+    measured DRAM bytes per algorithmic byte (a 4-layer capture of the same
+    layer shapes) times this launch's algorithmic bytes, if the summary was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "q8_step_kernel_7b_decode.md")
     try:
         txt = open(path).read()
     except OSError:
         return None
-    sha = traffic = None
+    sha = ratio = None
     for ln in txt.splitlines():
         if ln.startswith("kernel_source_sha:"):
             sha = ln.split(":", 1)[1].strip()
-        if ln.startswith(f"{kernel_key}_dram_bytes_per_launch:"):
-            traffic = float(ln.split(":", 1)[1].strip())
-    return traffic if sha == kernel_source_sha() else None
+        if ln.startswith("dram_bytes_per_algorithmic_byte:"):
+            ratio = float(ln.split(":", 1)[1].strip())
+    if sha != kernel_source_sha() or ratio is None:
+        return None
+    return ratio * algorithmic_bytes
 
 
 # ---------------------------------------------------------------------------- oracle
-def oracle_sample(shape_name: str, context: int, seconds_hint: float = 20.0):
+def oracle_sample(shape_name: str, context: int, seconds_hint: float = 12.0):
     """Times the scalar oracle's decode step on a bounded sample of the
     workload: the same shapes truncated to 2 layers (lm_head included), KV
-    at the same context; the full step's time is projected as
-    t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
-    Returns (tokens_per_s, threads, description)."""
+    at the same context, repeated for about `seconds_hint` seconds of CPU
+    work (at least 3 times); with the medians the full step's time is
+    projected as t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
+    Returns (tokens_per_s, threads, description, repetitions)."""
     import numpy as np
 
     import synth
@@ -171,18 +190,23 @@ def oracle_sample(shape_name: str, context: int, seconds_hint: float = 20.0):
     host = orc.HostStep(w, cap, caches)
     threads = orc.default_threads()
     x = synth.normal_f32(0, "bench.x", full.hidden)
-    t0 = time.perf_counter()
-    orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
-    t_head = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    host.step(17, context - 1, threads)
-    t_step2 = time.perf_counter() - t0
+    heads, steps = [], []
+    t_begin = time.perf_counter()
+    while len(steps) < 3 or time.perf_counter() - t_begin < seconds_hint:
+        t0 = time.perf_counter()
+        orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
+        heads.append(time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        host.step(17, context - 1, threads)  # rewrites the same cache row each time
+        steps.append(time.perf_counter() - t0)
+    t_head, t_step2 = statistics.median(heads), statistics.median(steps)
     per_layer = max(t_step2 - t_head, 1e-9) / 2
     t_full = t_head + full.n_layers * per_layer
     desc = (f"oracle decode step of the {full.name}-shaped model truncated to 2 of "
-            f"{full.n_layers} layers (+lm_head, KV context {context}); measured "
-            f"{t_step2:.2f} s, lm_head alone {t_head:.2f} s; projected full step {t_full:.2f} s")
-    return 1.0 / t_full, threads, desc
+            f"{full.n_layers} layers (+lm_head, KV context {context}), {len(steps)} repetitions "
+            f"({time.perf_counter() - t_begin:.1f} s of CPU work); median 2-layer step "
+            f"{t_step2:.3f} s, lm_head alone {t_head:.3f} s; projected full step {t_full:.2f} s")
+    return 1.0 / t_full, threads, desc, len(steps)
 
 
 # ---------------------------------------------------------------------------- profiling
@@ -288,10 +312,10 @@ def run_profile(args):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    tps, threads, desc = oracle_sample(args.model, args.context)
+    tps, threads, desc, reps = oracle_sample(args.model, args.context)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
-        "steps": 1, "warmup": 0, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
+        "steps": reps, "warmup": 0, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(args)},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -473,10 +497,13 @@ def main():
     at_bytes_launch = attn_bytes(ctx, Hk, D, H, esize, append=False)
     at_gbs = at_bytes_launch * shape.n_layers / at_time / 1e9
 
-    traffic = ncu_traffic("q8_rows_kernel")
+    # dominant kernel: the persistent step kernel, one launch per step
+    step_b = statistics.mean(step_bytes(shape, ctx + s, esize) for s in range(args.steps))
+    step_s = t_dev / args.steps
+    traffic = ncu_traffic(step_b)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, threads, desc = oracle_sample(args.model, ctx)
+        tps, threads, desc, _ = oracle_sample(args.model, ctx)
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -491,15 +518,18 @@ def main():
                        "l2": "inputs larger than L2 (7.5 GB of weights streamed per step)"
                        if shape.name == "qwen2.5-7b" else "weights streamed per step exceed L2",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "q8_rows_kernel (q8d_matvec)",
-                         "achieved": mv_launch_bytes / mv_launch_s / 1e9, "peak": hbm,
+            "roofline": {"bound": "hbm", "kernel": "q8_step_kernel (q8d_step_launch)",
+                         "achieved": step_b / step_s / 1e9, "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": mv_launch_bytes / mv_launch_s / 1e9 / hbm, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": mv_launch_bytes,
-                         "avg_launch_us": mv_launch_s * 1e6, "launches": len(mats)},
+                         "frac": step_b / step_s / 1e9 / hbm, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": step_b,
+                         "avg_launch_us": step_s * 1e6, "launches": args.steps},
             "kernels": {
-                "q8_matvec": {"GB_s": mv_gbs, "frac_of_peak": mv_gbs / hbm,
-                              "us_per_step_sum": mv_time * 1e6},
+                "q8_matvec": {"kernel": "q8_gemv_kernel (q8d_matvec, one launch per matrix)",
+                              "GB_s": mv_gbs, "frac_of_peak": mv_gbs / hbm,
+                              "us_per_step_sum": mv_time * 1e6,
+                              "avg_launch_us": mv_launch_s * 1e6,
+                              "algorithmic_bytes_per_launch": mv_launch_bytes},
                 "gqa_decode_attn": {"GB_s": at_gbs, "frac_of_peak": at_gbs / hbm,
                                     "us_per_layer": at_time / shape.n_layers * 1e6,
                                     "context": ctx, "l2": "256 MB flush between layers"},
