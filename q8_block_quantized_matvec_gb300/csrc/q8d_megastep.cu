@@ -44,6 +44,15 @@ constexpr int kW = kMsWarps;
 constexpr int kCT = kW * 32;  // consumer threads
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (~1 s with the sleeps)
+constexpr int kMaxStages = 8;
+
+// Per-CTA state at fixed shared addresses (no registers to hold pointers).
+__shared__ uint64_t ms_full[kMaxStages];   // stage s filled (TMA complete_tx)
+__shared__ uint64_t ms_empty[kMaxStages];  // stage s released by all consumer warps
+__shared__ int ms_abort;                   // a wait of this CTA was abandoned
+__shared__ int ms_flag;
+__shared__ unsigned ms_target;             // grid barrier arrivals to wait for
+__shared__ int ms_L;                       // attended length of this step
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
@@ -61,11 +70,13 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 // Grid-wide barrier of the consumer threads of all CTAs.  Returns false if
 // the step was aborted (a CTA gave up a wait); then every CTA stops.
-__device__ bool grid_sync(const MParams& P, unsigned& target, volatile int* s_abort,
-                          volatile int* s_flag) {
+__device__ bool grid_sync(const MParams& P) {
+  volatile int* s_abort = &ms_abort;
+  volatile int* s_flag = &ms_flag;
   consumer_sync(kCT);
   if (threadIdx.x == 0) {
-    target += gridDim.x;
+    const unsigned target = ms_target + gridDim.x;
+    ms_target = target;
     int ok = *s_abort ? 0 : 1;
     if (!ok) {
       atomicExch(P.abort, 1);
@@ -190,8 +201,8 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
 // reduction window), storing the lanes' partials at window buffer `buf`
 // (bytes); returns the rows consumed.  AM: alignment mode of this warp.
 template <int AM>
-__device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp, uint64_t* full,
-                                 uint64_t* empty, int* s_abort, uint32_t smem32, MCursor& c,
+__device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
+                                 uint32_t smem32, MCursor& c,
                                  uint32_t& delta, int v1, uint32_t lane_buf, int rg, bool active,
                                  uint32_t boff, const uint64_t (&x2)[16], bool& ok) {
   const int lane = threadIdx.x & 31;
@@ -207,25 +218,22 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
   for (int wt = 0; wt < F.win && c.cur < v1; ++wt) {
     const int rows = c.rows(R, v1);
     const int rows_st = active ? rows : 0;  // rows whose partials this warp stores
-    ok = wait_or_abort(&full[rp.s], rp.ph, s_abort) && ok;
+    ok = wait_or_abort(&ms_full[rp.s], rp.ph, &ms_abort) && ok;
     // (warps beyond NS * RG, when NS does not divide the warp count, run the
     // same code on row group 0's rows and store nothing)
     uint32_t o = rp.stage32 + delta + boff + (uint32_t)rg * rowb;
     uint32_t d = lane_buf + (uint32_t)(wrow * n32) * 4u;
-    int rl = rg;
-    // pairs up to this warp's last row of the tile (a ragged tile stops early)
+    // this warp's rows of the tile, one block at a time (a ragged tile stops
+    // at the warp's last row)
 #pragma unroll 1
-    for (int j = 0; j < np && rl < rows; ++j) {
+    for (int rl = rg; rl < rows && rl < 2 * np * RG; rl += RG) {
       const float va = block_dot<AM>(o, x2);
-      const float vb = block_dot<AM>(o + step, x2);
       if (rl < rows_st) sts32(d, va);
-      if (rl + RG < rows_st) sts32(d + pstep, vb);
-      o += 2 * step;
-      d += 2 * pstep;
-      rl += 2 * RG;
+      o += step;
+      d += pstep;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[rp.s]);
+    if (lane == 0) mbar_arrive(&ms_empty[rp.s]);
     rp.stage32 += (uint32_t)P.stage_bytes;
     if (++rp.s == P.nstages) {
       rp.s = 0;
@@ -240,8 +248,8 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
   return wrow;
 }
 
-__device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uint64_t* full,
-                             uint64_t* empty, int* s_abort, uint32_t smem32, uint8_t* region,
+__device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uint32_t smem32,
+                             uint8_t* region,
                              float* s_f, int* s_i) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = F.NS, RG = F.RG;
@@ -364,13 +372,13 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
       const int wbeg = c.cur;
       int nrow;
       if (am == 0)
-        nrow = ms_consume_window<0>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+        nrow = ms_consume_window<0>(F, P, rp, smem32, c, delta, v1,
                                     lane_part + buf, rg, active, boff, x2, ok);
       else if (am == 1)
-        nrow = ms_consume_window<1>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+        nrow = ms_consume_window<1>(F, P, rp, smem32, c, delta, v1,
                                     lane_part + buf, rg, active, boff, x2, ok);
       else
-        nrow = ms_consume_window<2>(F, P, rp, full, empty, s_abort, smem32, c, delta, v1,
+        nrow = ms_consume_window<2>(F, P, rp, smem32, c, delta, v1,
                                     lane_part + buf, rg, active, boff, x2, ok);
       // window complete: every consumer warp has stored its partials.  The
       // other buffer was reduced before this barrier, so the next window may
@@ -768,8 +776,10 @@ __device__ void argmax_phase(const MParams& P, int pos) {
 // Issues every weight tile of this CTA's rows of all matvec phases, in
 // order, into the ring.  Returns the number of tiles issued (fewer if a
 // wait was abandoned).
-__device__ int produce_all(const MParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                           int* s_abort) {
+__device__ int produce_all(const MParams& P, uint8_t* smem) {
+  uint64_t* full = ms_full;
+  uint64_t* empty = ms_empty;
+  int* s_abort = &ms_abort;
   const uint64_t pol = policy_evict_first();
   int s = 0, issued = 0;
   uint32_t ph = 0;
@@ -852,19 +862,17 @@ template <int D, typename KT>
 __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) MPhase s_ph;
-  __shared__ int s_abort, s_flag;
   __shared__ float s_f[kW];
   __shared__ int s_i[kW];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
-  uint64_t* empty = full + P.nstages;
-  uint8_t* region = reinterpret_cast<uint8_t*>(empty + P.nstages);  // 16-byte aligned
+  uint8_t* region = smem + (size_t)P.stage_bytes * P.nstages;  // 128-byte aligned
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kW);
+      mbar_init(&ms_full[s], 1);
+      mbar_init(&ms_empty[s], kW);
     }
-    s_abort = 0;
+    ms_abort = 0;
+    ms_target = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -872,44 +880,46 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
   if (warp == kW) {
     // ---- producer warp ----
     if (lane == 0) {
-      const int issued = produce_all(P, smem, full, empty, &s_abort);
-      if (*(volatile int*)&s_abort) {
+      const int issued = produce_all(P, smem);
+      if (*(volatile int*)&ms_abort) {
         // wait (bounded) for copies still in flight before the CTA exits
         for (int j = max(0, issued - P.nstages); j < issued; ++j)
-          mbar_wait(&full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
+          mbar_wait(&ms_full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
       }
     }
   } else {
     // ---- consumers ----
-    const int tok = *(volatile const int*)P.d_token;
-    const int pos = *(volatile const int*)P.d_pos;
-    const int L = pos + 1;
-    const bool len_ok = pos >= 0 && L <= P.cap;
+    // the step's position: read once, kept in shared memory (fewer live
+    // registers across the phases)
+    if (threadIdx.x == 0) ms_L = *(volatile const int*)P.d_pos + 1;
+    consumer_sync(kCT);
     RingPos rp{0, 0u, smem_u32(smem)};
     const uint32_t smem32 = smem_u32(smem);
-    unsigned target = 0;
     for (int pi = 0; pi < P.nphases; ++pi) {
-      if (pi > 0 && !grid_sync(P, target, &s_abort, &s_flag)) break;
+      if (pi > 0 && !grid_sync(P)) break;
       if (threadIdx.x < (int)(sizeof(MPhase) / 4))
         reinterpret_cast<int*>(&s_ph)[threadIdx.x] =
             __ldg(reinterpret_cast<const int*>(P.phases + pi) + threadIdx.x);
       consumer_sync(kCT);
       const int kind = s_ph.kind;
       if (kind == kPhMatvec) {
-        if (!matvec_phase(s_ph, P, rp, full, empty, &s_abort, smem32, region, s_f, s_i)) {
-          s_abort = 1;  // seen at the next grid barrier
+        if (!matvec_phase(s_ph, P, rp, smem32, region, s_f, s_i)) {
+          ms_abort = 1;  // seen at the next grid barrier
         }
       } else if (kind == kPhAttn) {
-        attn_phase<D, KT>(P, s_ph, L, len_ok, region);
+        const int L = ms_L;
+        attn_phase<D, KT>(P, s_ph, L, L >= 1 && L <= P.cap, region);
       } else if (kind == kPhCombine) {
-        combine_phase<D>(P, L, len_ok, region);
+        const int L = ms_L;
+        combine_phase<D>(P, L, L >= 1 && L <= P.cap, region);
       } else if (kind == kPhEmbed) {
-        embed_phase(P, tok, len_ok);
+        const int L = ms_L;
+        embed_phase(P, *(volatile const int*)P.d_token, L >= 1 && L <= P.cap);
       } else {
-        argmax_phase(P, pos);
+        argmax_phase(P, ms_L - 1);
       }
     }
-    if (s_abort && threadIdx.x == 0) {
+    if (ms_abort && threadIdx.x == 0) {
       atomicExch(P.abort, 1);
       if (P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
     }
@@ -974,7 +984,7 @@ int megastep_max_stages(int stage_bytes) {
 }
 
 size_t megastep_smem(const MParams& P) {
-  return (size_t)P.stage_bytes * P.nstages + 16ull * P.nstages + kMsRegion;
+  return (size_t)P.stage_bytes * P.nstages + kMsRegion;
 }
 
 int megastep_launch(const MParams& P, int head_dim, int kv_dtype, int grid, cudaStream_t st) {
