@@ -24,8 +24,8 @@ __device__ __forceinline__ void sts32(uint32_t addr, float v) {
 // scale * sum_j q_j x_j for the block at shared-memory byte address `o`
 // (2-byte aligned).  Alignment modes: AM = 1, the block starts at byte 2 of
 // a word (scale = upper half, quants = the next 8 words); AM = 0, it starts
-// at a word (scale = lower half, quants from byte 2, funnel-shifted); AM = 2,
-// decided per lane from o.
+// at a word (scale = lower half, quants from byte 2 on); AM = 2, decided
+// per lane from o.
 template <int AM>
 __device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16]) {
   const uint32_t w0 = o & ~3u;
@@ -51,17 +51,33 @@ __device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16])
   }
   const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
   uint64_t c[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
+  if constexpr (AM == 0) {
+    // quants start at byte 2 of word 0: quant 4k+i is byte (2+i) mod 4 of
+    // word k + (2+i)/4, so each is picked straight from its word (no
+    // funnel shift); the sign flip is applied to all nine words once
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint32_t w;
-    if constexpr (AM == 1) w = a[k + 1];
-    else if constexpr (AM == 0) w = __funnelshift_r(a[k], a[k + 1], 16);
-    else w = __funnelshift_rc(a[k], a[k + 1], shift);
-    w ^= 0x80808080u;
-    const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
-    const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
-    c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
-    c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
+    for (int k = 0; k < 9; ++k) a[k] ^= 0x80808080u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t q01 =
+          add2(pack2(magic_byte(a[k], magic_sel(2)), magic_byte(a[k], magic_sel(3))), bias2);
+      const uint64_t q23 =
+          add2(pack2(magic_byte(a[k + 1], magic_sel(0)), magic_byte(a[k + 1], magic_sel(1))), bias2);
+      c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
+      c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t w;
+      if constexpr (AM == 1) w = a[k + 1];
+      else w = __funnelshift_rc(a[k], a[k + 1], shift);
+      w ^= 0x80808080u;
+      const uint64_t q01 = add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2);
+      const uint64_t q23 = add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2);
+      c[(2 * k) & 3] = fma2(q01, x2[2 * k], c[(2 * k) & 3]);
+      c[(2 * k + 1) & 3] = fma2(q23, x2[2 * k + 1], c[(2 * k + 1) & 3]);
+    }
   }
   const uint64_t t = add2(add2(c[0], c[1]), add2(c[2], c[3]));
   float lo, hi;

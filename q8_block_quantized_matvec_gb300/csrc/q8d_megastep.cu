@@ -53,6 +53,12 @@ __shared__ int ms_abort;                   // a wait of this CTA was abandoned
 __shared__ int ms_flag;
 __shared__ unsigned ms_target;             // grid barrier arrivals to wait for
 __shared__ int ms_L;                       // attended length of this step
+// Per-row values of the CTA's rows of a matvec phase: the residual rows it
+// accumulates into (prefetched at the phase start), or its gate rows of a
+// gate|up phase (kept for the up rows): no global round trip in the window
+// reductions.
+constexpr int kRowsMax = 1024;
+__shared__ float ms_rows[kRowsMax];
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
@@ -153,20 +159,24 @@ __device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int to
   }
 }
 
-// Window reduction (see q8d_gemv.cu): 8 threads per row, fixed order.
-__device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, int wbeg, float& bv,
-                                 int& bi) {
+// Window reduction: sums each row's lane partials over segments and lanes
+// in a fixed order and writes the row.
+// rbase: the matrix row held in ms_rows[0] (the CTA's first row), or -1
+// when the CTA's rows do not fit ms_rows (then values go through L2).
+__device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, int wbeg, int rbase,
+                                 float& bv, int& bi) {
+  // 16 threads per row, two rows per warp at a time: a 40-row window keeps
+  // all 20 warps equally busy (the next window barrier waits for the last)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane & 7;
-  const int NS = F.NS;
-  for (int r0 = warp * 4; r0 < nrow; r0 += kW * 4) {
-    const int r = r0 + (lane >> 3);
+  const int sub = lane & 15;
+  const int n4 = F.NS * 8;  // float4s per row
+  for (int r0 = warp * 2; r0 < nrow; r0 += kW * 2) {
+    const int r = r0 + (lane >> 4);
     const bool valid = r < nrow;
-    const float4* pr =
-        reinterpret_cast<const float4*>(part + (size_t)(valid ? r : r0) * NS * 32) + sub;
+    const float4* pr = reinterpret_cast<const float4*>(part + (size_t)(valid ? r : r0) * n4 * 4);
     uint64_t acc0 = pack2(0.f, 0.f), acc1 = acc0;
-    for (int k = 0; k < NS; ++k) {
-      const float4 v = pr[8 * k];
+    for (int k = sub; k < n4; k += 16) {
+      const float4 v = pr[k];
       acc0 = add2(acc0, pack2(v.x, v.y));
       acc1 = add2(acc1, pack2(v.z, v.w));
     }
@@ -174,21 +184,29 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
     unpack2(add2(acc0, acc1), lo, hi);
     float sum = lo + hi;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (valid && sub == 0) {
       const int vr = wbeg + r;
       int sg = 0;
       while (sg + 1 < F.nseg && vr >= F.vbegin[sg + 1]) ++sg;
       const int ri = vr - F.vbegin[sg];
       float* y = F.y[sg] + ri;
-      float out = F.accumulate ? (__ldcg(y) + sum) : sum;
-      if (F.glu && sg == 1) {
-        // up row: gate row ri was written by this CTA in an earlier window
-        float* yg = F.y[0] + ri;
-        const float gt = __ldcg(yg);
-        *yg = gt / (1.0f + expf(-gt)) * out;
+      float out = sum;
+      if (F.accumulate) out += rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(y);
+      if (F.glu) {
+        // gate rows are kept; an up row combines with its gate row (computed
+        // by this CTA in an earlier window) into h = silu(gate) * up, stored
+        // over the gate half (the only half read afterwards)
+        if (sg == 0) {
+          if (rbase >= 0) ms_rows[ri - rbase] = out;
+          else *y = out;
+        } else {
+          const float gt = rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(F.y[0] + ri);
+          F.y[0][ri] = gt / (1.0f + expf(-gt)) * out;
+        }
+      } else {
+        *y = out;
       }
-      *y = out;
       if (F.argmax && !isnan(out) && am_better(out, ri, bv, bi)) {
         bv = out;
         bi = ri;
@@ -298,6 +316,12 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
     inv = 1.0f / sqrtf(tot / (float)F.n + P.eps);
     consumer_sync(kCT);  // s_f is reused below
   }
+  if (F.accumulate && F.rows_per_cta <= kRowsMax) {
+    // the residual rows this CTA adds to (one matrix: rows = virtual rows)
+    const int r0 = blockIdx.x * F.rows_per_cta;
+    const int r1 = min(F.total_rows, r0 + F.rows_per_cta);
+    for (int i = threadIdx.x; i < r1 - r0; i += kCT) ms_rows[i] = __ldcg(F.y[0] + r0 + i);
+  }
   float4* xs = reinterpret_cast<float4*>(region);
   float4* ws = xs + pass4;
   for (int e0 = 0; e0 < F.n / 4; e0 += pass4) {
@@ -361,6 +385,9 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
   const uint32_t lane_part = part32 + ((uint32_t)(ci * 32 + lane) + (uint32_t)rg * n32) * 4u;
   const uint32_t buf_bytes = (uint32_t)F.win * (uint32_t)F.R * n32 * 4u;
   uint32_t buf = 0;
+  const int rbase = (F.accumulate || F.glu) && F.rows_per_cta <= kRowsMax
+                        ? (int)blockIdx.x * F.rows_per_cta
+                        : -1;
   const int npieces = F.glu ? 2 : 1;
   for (int piece = 0; piece < npieces; ++piece) {
     int v0, v1;
@@ -384,7 +411,7 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
       // other buffer was reduced before this barrier, so the next window may
       // overwrite it.
       consumer_sync(kCT);
-      ms_window_reduce(F, part + buf / 4, nrow, wbeg, bv, bi);
+      ms_window_reduce(F, part + buf / 4, nrow, wbeg, rbase, bv, bi);
       buf = buf ? 0u : buf_bytes;
     }
   }
