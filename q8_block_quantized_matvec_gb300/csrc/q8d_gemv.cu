@@ -221,7 +221,7 @@ __device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, u
     // launch then reports Q8D_DERR_WAIT) so that every consumer warp reaches
     // the window barriers.
     ok = wait_or_abort(&ring.full[s], ph, ring.abort_flag) && ok;
-    uint32_t o = stage32 + delta + boff + (uint32_t)rg * rowb;
+    uint32_t o = after_wait(stage32 + delta + boff + (uint32_t)rg * rowb);
     uint32_t d = lane_part + buf + (uint32_t)(wrow * n32) * 4u;
     int rl = rg;
 #pragma unroll 1

@@ -10,10 +10,23 @@
 namespace q8d {
 namespace mv {
 
+// Shared-memory load of a weight word.  Not volatile: the compiler may
+// schedule these loads freely (e.g. the next row's ahead of this row's
+// arithmetic).  Callers make the stage address depend on the mbarrier wait
+// (after_wait) so that no load moves above it, and every loaded value feeds
+// a store that precedes the stage's release.
 template <int OFF>
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF) : "memory");
+  asm("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+
+// Returns v through an opaque instruction ordered after the preceding
+// volatile asm (the mbarrier wait): addresses derived from it cannot be
+// hoisted above the wait.
+__device__ __forceinline__ uint32_t after_wait(uint32_t v) {
+  asm volatile("" : "+r"(v)::"memory");
   return v;
 }
 

@@ -239,7 +239,7 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
     ok = wait_or_abort(&ms_full[rp.s], rp.ph, &ms_abort) && ok;
     // (warps beyond NS * RG, when NS does not divide the warp count, run the
     // same code on row group 0's rows and store nothing)
-    uint32_t o = rp.stage32 + delta + boff + (uint32_t)rg * rowb;
+    uint32_t o = after_wait(rp.stage32 + delta + boff + (uint32_t)rg * rowb);
     uint32_t d = lane_buf + (uint32_t)(wrow * n32) * 4u;
     // this warp's rows of the tile, one block at a time (a ragged tile stops
     // at the warp's last row)
