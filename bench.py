@@ -308,6 +308,22 @@ def run_profile(args):
         assert err.item() == 0
 
 
+# ---------------------------------------------------------------------------- replicas
+def replica_throughput(local_seconds: float, steps: int, dist=None, device="cuda") -> float:
+    """Whole-job steps per second of independent replicas: every rank ran
+    `steps` steps in `local_seconds`; the job takes the slowest rank's time
+    (max over ranks), and the ranks' steps add up."""
+    world = 1
+    t = local_seconds
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        tt = torch.tensor([t], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return world * steps / t
+
+
 # ---------------------------------------------------------------------------- main
 def run_reference(args, rank, world):
     if rank != 0:
@@ -411,11 +427,8 @@ def main():
         barrier()
     t_dev = e0.elapsed_time(e1) / 1e3
     assert ds.step.status(stream) == 0, "device error word set during the timed steps"
-    if dist:
-        tt = torch.tensor([t_dev], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev = float(tt.item())
-    value = world * args.steps / t_dev
+    value = replica_throughput(t_dev, args.steps, dist)
+    t_dev = world * args.steps / value  # the slowest rank's time
 
     # ---- end to end through the public API: H2D token+pos, graph, D2H token ----
     h_in = torch.tensor([17, ctx - 1], dtype=torch.int32).pin_memory()
@@ -432,12 +445,8 @@ def main():
         stream.synchronize()
         h_in[0] = int(h_out[0])
     t_e2e = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": world * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 8,
-           "d2h_bytes_per_step": 4}
+    e2e = {"value": replica_throughput(t_e2e, args.steps, dist), "unit": "tokens/s",
+           "h2d_bytes_per_step": 8, "d2h_bytes_per_step": 4}
 
     # ---- kernel legs: q8_matvec over the step's matrices, attention per layer ----
     mats = []

@@ -88,6 +88,21 @@ def test_step_7b_shape(orc, q8d):
     run_case(orc, synth.QWEN25_7B, pos=2047, cap=2048)
 
 
+def test_step_head_dim_128_f32_cache(orc, q8d):
+    # the step kernel's (head_dim 128, f32 cache) instance
+    shape = synth.ModelShape("d128-f32", 256, 2, 4, 2, 128, 320, 600,
+                             qk_norm=True, qkv_bias=False, kv_dtype=synth.KV_F32)
+    run_case(orc, shape, pos=77, cap=256)
+
+
+def test_step_odd_block_counts(orc, q8d):
+    # rows of 33 and 35 blocks: paired warps whose block alignment changes
+    # from row to row (hidden 1056, ffn 1120), q width 256 (8 blocks)
+    shape = synth.ModelShape("odd-blocks", 1056, 2, 4, 2, 64, 1120, 700,
+                             qk_norm=False, qkv_bias=True, kv_dtype=synth.KV_F16)
+    run_case(orc, shape, pos=300, cap=512)
+
+
 def test_step_position_past_cache_flags_error(orc, q8d):
     shape = synth.tiny_shape(1)
     w = synth.step_weights(shape, seed=1)
