@@ -225,7 +225,6 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
                                  uint32_t boff, const uint64_t (&x2)[16], bool& ok) {
   const int lane = threadIdx.x & 31;
   const int RG = F.RG, R = F.R;
-  const int np = R / (2 * RG);
   const int n32 = F.NS * 32;
   const uint32_t rowb = (uint32_t)F.row_bytes;
   const uint32_t step = (uint32_t)RG * rowb;
@@ -244,7 +243,7 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
     // this warp's rows of the tile, one block at a time (a ragged tile stops
     // at the warp's last row)
 #pragma unroll 1
-    for (int rl = rg; rl < rows && rl < 2 * np * RG; rl += RG) {
+    for (int rl = rg; rl < rows; rl += RG) {
       const float va = block_dot<AM>(o, x2);
       if (rl < rows_st) sts32(d, va);
       o += step;
@@ -987,15 +986,16 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
   F.NS = F.paired ? 2 * ((F.bpr + 63) / 64) : 1;
   if (F.NS > kMsWarps) return false;
   F.RG = kMsWarps / F.NS;
-  // R = 2 * RG * np rows, np the largest of 4, 2, 1 within the stage target
-  // that still gives every CTA at least four tiles of the phase
+  // R = RG * k rows (each warp takes k rows of a tile), k the largest up to
+  // 8 within the stage target that still gives every CTA at least three
+  // tiles of the phase
   const long long rows_cta = F.glu ? ((long long)F.vbegin[1] + grid - 1) / grid * 2
                                    : ((long long)F.vbegin[F.nseg] + grid - 1) / grid;
-  int np = 4;
-  while (np > 1 && (2LL * F.RG * np * F.row_bytes + 32 > stage_target ||
-                    rows_cta < 4LL * 2 * F.RG * np))
-    np /= 2;
-  F.R = 2 * F.RG * np;
+  int k = 8;
+  while (k > 1 && ((long long)F.RG * k * F.row_bytes + 32 > stage_target ||
+                   rows_cta < 3LL * F.RG * k))
+    --k;
+  F.R = F.RG * k;
   // window tiles: double-buffered partials within the shared region
   const long long per_tile = 2LL * F.R * F.NS * 32 * 4;
   if (per_tile > kMsRegion) return false;
@@ -1005,10 +1005,12 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
   return true;
 }
 
-int megastep_max_stages(int stage_bytes) {
-  constexpr int kBudget = 224 * 1024;  // dynamic shared memory per CTA (one CTA per SM)
-  return (kBudget - kMsRegion) / (stage_bytes + 16);
-}
+// dynamic shared memory per CTA (one CTA per SM; the rest is static)
+constexpr int kMsDynamicBudget = 220 * 1024;
+
+int megastep_ring_bytes() { return kMsDynamicBudget - kMsRegion; }
+
+int megastep_max_stages(int stage_bytes) { return megastep_ring_bytes() / stage_bytes; }
 
 size_t megastep_smem(const MParams& P) {
   return (size_t)P.stage_bytes * P.nstages + kMsRegion;

@@ -76,6 +76,9 @@ size_t megastep_smem(const MParams& P);
 // Largest nstages that fits for a given stage size.
 int megastep_max_stages(int stage_bytes);
 
+// Shared memory available to the ring of stages.
+int megastep_ring_bytes();
+
 // Launches the step kernel (cooperative, grid = one CTA per SM) on `st`.
 int megastep_launch(const MParams& P, int head_dim, int kv_dtype, int grid, cudaStream_t st);
 

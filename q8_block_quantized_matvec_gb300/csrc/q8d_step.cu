@@ -125,7 +125,8 @@ static int build_phases(q8d_step* S, std::vector<MPhase>& ph, int& stage_bytes) 
   AM.kind = kPhArgmax;
   ph.push_back(AM);
   // Stages of ~40 KB: every matvec phase takes the largest tile that fits.
-  constexpr int kStageTarget = 80 * 1024 + 512;
+  // (three stages fit the ring: tiles of up to a third of it)
+  const int kStageTarget = (megastep_ring_bytes() / 3) & ~127;
   stage_bytes = 0;
   for (auto& F : ph) {
     if (F.kind != kPhMatvec) continue;
