@@ -214,7 +214,7 @@ def run_profile(args):
     """Fixed workloads for ncu.  step: one decode-step graph launch of the
     bench workload after warm-up.  matvec: q8d_matvec on the 7B gate/up
     shape (3584 -> 18944, 72 MB), 3 launches.  attn: q8d_gqa_decode_attn on
-    7B heads at context 8192 (16.8 MB of KV), 3 launches.  ncu's default
+    7B heads at --context (default 2048: 4.2 MB of KV), 3 launches.  ncu's default
     cache control flushes L2 before every profiled launch."""
     import torch
     from __graft_entry__ import build
@@ -287,7 +287,7 @@ def run_profile(args):
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
     else:
-        H, Hk, D, L = 28, 4, 128, 8192
+        H, Hk, D, L = 28, 4, 128, args.context
         kc = synth.normal_torch(0, "prof.k", (L, Hk * D), torch.float16)
         vc = synth.normal_torch(0, "prof.v", (L, Hk * D), torch.float16)
         q = synth.normal_torch(0, "prof.q", H * D, torch.float32)
