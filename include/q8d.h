@@ -187,13 +187,15 @@ int q8d_gqa_decode_attn_noalloc(const float* q, const float* k_new, const float*
  * the argmax is written back as the next token and the position advanced,
  * so consecutive launches decode consecutive tokens with no host work.
  * All pointers in the descriptors are device pointers owned by the caller
- * and must stay valid until q8d_step_destroy.
+ * and must stay valid until q8d_step_destroy.  Weights, caches and RMSNorm
+ * weights must be 16-byte aligned, the other f32 vectors 4-byte aligned
+ * (Q8D_EALIGN otherwise).
  * ---------------------------------------------------------------------- */
 typedef struct q8d_layer_desc {
   const void *wq, *wk, *wv, *wo, *wg, *wu, *wd; /* Q8_0: [H*hd][hidden], [Hk*hd][hidden] x2,
                                                    [hidden][H*hd], [ffn][hidden] x2,
                                                    [hidden][ffn]                          */
-  const float *attn_norm, *ffn_norm;            /* f32 [hidden]                           */
+  const float *attn_norm, *ffn_norm;            /* f32 [hidden], 16-byte aligned          */
   const float *q_norm, *k_norm;                 /* f32 [head_dim] (qk_norm) or NULL       */
   const float *bq, *bk, *bv;                    /* f32 biases (qkv_bias) or NULL          */
   void *kcache, *vcache;                        /* [cap][Hk*hd] of kv_dtype               */
@@ -207,7 +209,7 @@ typedef struct q8d_step_desc {
   int cap;      /* rows of every KV cache                                      */
   float rms_eps, rope_theta;
   const void* embed;      /* Q8_0 [vocab][hidden]                 */
-  const float* out_norm;  /* f32 [hidden]                         */
+  const float* out_norm;  /* f32 [hidden], 16-byte aligned        */
   const void* lm_head;    /* Q8_0 [vocab][hidden]                 */
   const q8d_layer_desc* layers; /* host array of n_layers (copied at create) */
   int* d_token;           /* device int: input token; receives the argmax     */

@@ -79,7 +79,10 @@ int step_validate(const q8d_step_desc* d) {
   if (d->hidden % 32 || d->ffn % 32) return Q8D_EUNSUPPORTED;
   if (d->kv_dtype != Q8D_KV_F32 && d->kv_dtype != Q8D_KV_F16) return Q8D_EUNSUPPORTED;
   if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f)) return Q8D_EINVAL;
-  if (!aligned(d->embed, 16) || !aligned(d->lm_head, 16)) return Q8D_EALIGN;
+  // the RMSNorm weights are read as 16-byte vectors, the other f32 vectors
+  // element by element
+  if (!aligned(d->embed, 16) || !aligned(d->lm_head, 16) || !aligned(d->out_norm, 16))
+    return Q8D_EALIGN;
   for (int i = 0; i < d->n_layers; ++i) {
     const q8d_layer_desc& L = d->layers[i];
     if (!L.wq || !L.wk || !L.wv || !L.wo || !L.wg || !L.wu || !L.wd || !L.attn_norm ||
@@ -87,9 +90,13 @@ int step_validate(const q8d_step_desc* d) {
       return Q8D_EINVAL;
     if (d->qk_norm && (!L.q_norm || !L.k_norm)) return Q8D_EINVAL;
     if (d->qkv_bias && (!L.bq || !L.bk || !L.bv)) return Q8D_EINVAL;
-    const void* w[] = {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.kcache, L.vcache};
+    const void* w[] = {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.kcache, L.vcache,
+                       L.attn_norm, L.ffn_norm};
     for (const void* p : w)
       if (!aligned(p, 16)) return Q8D_EALIGN;
+    const void* v[] = {L.q_norm, L.k_norm, L.bq, L.bk, L.bv};
+    for (const void* p : v)
+      if (p && !aligned(p, 4)) return Q8D_EALIGN;
   }
   return Q8D_OK;
 }

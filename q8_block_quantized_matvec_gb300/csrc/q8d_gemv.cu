@@ -44,6 +44,8 @@ namespace {
 using namespace mv;
 
 constexpr int kMaxWarps = 20;
+constexpr int kSmallThreads = 17 * 32;              // 16 consumer warps + the producer
+constexpr int kLargeThreads = (kMaxWarps + 1) * 32;  // 20 + 1
 
 // Activations of block column `col` (32 floats) with the launch's transform,
 // as 16 packed pairs; zeros when col is past the row end.
@@ -261,8 +263,11 @@ __device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, u
   return ok;
 }
 
-// Block of W consumer warps plus one producer warp (the last).
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32) q8_gemv_kernel(const RowsParams P) {
+// Block of W consumer warps plus one producer warp (the last), at most
+// NT / 32 warps in all: up to 17 warps (at most five per SM sub-partition)
+// a thread may hold 96 registers, 80 with 21.
+template <int NT>
+__global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = (blockDim.x >> 5) - 1;  // consumer warps
@@ -431,21 +436,21 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.np = np;
   const long long smem = stage * nst + 16LL * nst + part_bytes;
 
-  static int configured[64] = {0};
+  const bool small = (W + 1) * 32 <= kSmallThreads;
+  void (*fn)(const RowsParams) = small ? q8_gemv_kernel<kSmallThreads> : q8_gemv_kernel<kLargeThreads>;
+  static int configured[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(q8_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         220 * 1024);
+  if (dev >= 0 && dev < 64 && !configured[dev][small]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return record_cuda(e);
-    e = cudaFuncSetAttribute(q8_gemv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return record_cuda(e);
-    configured[dev] = 1;
+    configured[dev][small] = 1;
   }
   int occ = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, q8_gemv_kernel, (W + 1) * 32,
-                                                                (size_t)smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, (W + 1) * 32, (size_t)smem);
   if (e != cudaSuccess) return record_cuda(e);
   occ = std::max(occ, 1);
   // One wave of resident CTAs, each owning a contiguous range of rows.
@@ -455,8 +460,7 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.rows_per_cta = rows_cta;
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   if (grid_out) *grid_out = (int)grid;
-  return launch_ex(q8_gemv_kernel, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream,
-                   P.pdl != 0, P);
+  return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, P.pdl != 0, P);
 }
 
 }  // namespace q8d

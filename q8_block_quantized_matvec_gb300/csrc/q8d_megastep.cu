@@ -165,17 +165,18 @@ __device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int to
 // when the CTA's rows do not fit ms_rows (then values go through L2).
 __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, int wbeg, int rbase,
                                  float& bv, int& bi) {
-  // 16 threads per row, two rows per warp at a time: a 40-row window keeps
-  // all 20 warps equally busy (the next window barrier waits for the last)
+  // 8 threads per row, four rows per warp at a time: windows of up to 80
+  // rows take one pass, so no warp carries a second pass into the next
+  // window (stage releases and the next window barrier wait for the last)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane & 15;
+  const int sub = lane & 7;
   const int n4 = F.NS * 8;  // float4s per row
-  for (int r0 = warp * 2; r0 < nrow; r0 += kW * 2) {
-    const int r = r0 + (lane >> 4);
+  for (int r0 = warp * 4; r0 < nrow; r0 += kW * 4) {
+    const int r = r0 + (lane >> 3);
     const bool valid = r < nrow;
     const float4* pr = reinterpret_cast<const float4*>(part + (size_t)(valid ? r : r0) * n4 * 4);
     uint64_t acc0 = pack2(0.f, 0.f), acc1 = acc0;
-    for (int k = sub; k < n4; k += 16) {
+    for (int k = sub; k < n4; k += 8) {
       const float4 v = pr[k];
       acc0 = add2(acc0, pack2(v.x, v.y));
       acc1 = add2(acc1, pack2(v.z, v.w));
@@ -184,7 +185,7 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
     unpack2(add2(acc0, acc1), lo, hi);
     float sum = lo + hi;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (valid && sub == 0) {
       const int vr = wbeg + r;
       int sg = 0;
@@ -802,7 +803,18 @@ __device__ void argmax_phase(const MParams& P, int pos) {
 // Issues every weight tile of this CTA's rows of all matvec phases, in
 // order, into the ring.  Returns the number of tiles issued (fewer if a
 // wait was abandoned).
-__device__ int produce_all(const MParams& P, uint8_t* smem) {
+// Pulls the 128-byte lines of [p, p + bytes) into L2, line j by CTA j mod
+// the grid (small vectors every CTA reads right after a grid barrier).
+__device__ __forceinline__ void prefetch_l2_spread(const void* p, size_t bytes) {
+  if (!p || !bytes) return;
+  const unsigned long long a = reinterpret_cast<unsigned long long>(p), e = a + bytes;
+  for (unsigned long long l = (a >> 7) + blockIdx.x; l <= ((e - 1) >> 7); l += gridDim.x) {
+    const unsigned long long q = (l << 7) > a ? (l << 7) : a;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(q) : "memory");
+  }
+}
+
+__device__ __noinline__ int produce_all(const MParams& P, uint8_t* smem) {
   uint64_t* full = ms_full;
   uint64_t* empty = ms_empty;
   int* s_abort = &ms_abort;
@@ -815,6 +827,20 @@ __device__ int produce_all(const MParams& P, uint8_t* smem) {
   for (int pi = 0; pi < P.nphases; ++pi) {
     const MPhase* F = P.phases + pi;
     const int kind = __ldg(&F->kind);
+    if (kind == kPhAttn && len_ok) {
+      // the layer's biases, QK-norm weights and this position's RoPE row
+      const MLayer* Ly = P.layers + __ldg(&F->layer);
+      const size_t qb = (size_t)P.n_heads * P.head_dim * 4, kb = (size_t)P.n_kv_heads * P.head_dim * 4;
+      prefetch_l2_spread(ldg_ptr(&Ly->bq), qb);
+      prefetch_l2_spread(ldg_ptr(&Ly->bk), kb);
+      prefetch_l2_spread(ldg_ptr(&Ly->bv), kb);
+      prefetch_l2_spread(ldg_ptr(&Ly->q_norm), (size_t)P.head_dim * 4);
+      prefetch_l2_spread(ldg_ptr(&Ly->k_norm), (size_t)P.head_dim * 4);
+      prefetch_l2_spread(P.rope_cos + (size_t)pos * (P.head_dim / 2), (size_t)P.head_dim * 2);
+      prefetch_l2_spread(P.rope_sin + (size_t)pos * (P.head_dim / 2), (size_t)P.head_dim * 2);
+    }
+    if (kind == kPhMatvec && __ldg(&F->xmode) == kXRmsNorm)
+      prefetch_l2_spread(ldg_ptr(&F->xw), (size_t)__ldg(&F->n) * 4);  // the RMSNorm weights
     if (kind == kPhAttn && len_ok && (int)blockIdx.x < P.n_kv_heads * attn_chunks_for(P, L)) {
       // pull this CTA's K/V chunk (the rows before the new one) into L2 now,
       // a phase or more before the attention phase reads it

@@ -124,6 +124,15 @@ def test_step_create_refusals(q8d):
     d.embed = A16 + 2
     assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EALIGN
     d.embed = A16
+    d.out_norm = A16 + 4                                  # RMSNorm weights: float4 loads
+    assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EALIGN
+    d.out_norm = A16
+    layers[0].ffn_norm = A16 + 4
+    assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EALIGN
+    layers[0].ffn_norm = A16
+    layers[0].bk = A16 + 2                                # element loads need 4 bytes
+    assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EALIGN
+    layers[0].bk = A16
     d.qk_norm = 1
     layers[0].q_norm = None
     assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EINVAL
