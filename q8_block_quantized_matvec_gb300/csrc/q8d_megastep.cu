@@ -74,21 +74,35 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier of the consumer threads of all CTAs.  Returns false if
-// the step was aborted (a CTA gave up a wait); then every CTA stops.
-__device__ bool grid_sync(const MParams& P) {
+// Grid-wide barrier of the consumer threads of all CTAs, in two halves:
+// grid_arrive (this CTA is done with the phase) and grid_wait (every CTA
+// is); work that depends on no other CTA may run in between.  grid_wait
+// returns false if the step was aborted (a CTA gave up a wait); then every
+// CTA stops.
+__device__ void grid_arrive(const MParams& P) {
   volatile int* s_abort = &ms_abort;
   volatile int* s_flag = &ms_flag;
   consumer_sync(kCT);
   if (threadIdx.x == 0) {
-    const unsigned target = ms_target + gridDim.x;
-    ms_target = target;
-    int ok = *s_abort ? 0 : 1;
-    if (!ok) {
+    ms_target += gridDim.x;
+    if (*s_abort) {
       atomicExch(P.abort, 1);
+      *s_flag = 0;
     } else {
       __threadfence();
       atomicAdd(P.bar, 1u);
+      *s_flag = 1;
+    }
+  }
+}
+
+__device__ bool grid_wait(const MParams& P) {
+  volatile int* s_abort = &ms_abort;
+  volatile int* s_flag = &ms_flag;
+  if (threadIdx.x == 0) {
+    const unsigned target = ms_target;
+    int ok = *s_flag;
+    if (ok) {
       for (uint32_t i = 0;; ++i) {
         if ((int)(ld_acquire(P.bar) - target) >= 0) break;
         if (*(volatile int*)P.abort) {
@@ -110,6 +124,30 @@ __device__ bool grid_sync(const MParams& P) {
   }
   consumer_sync(kCT);
   return *s_flag != 0;
+}
+
+// Work of matvec phase F that depends on no other CTA, done between the
+// halves of the grid barrier before it: the residual rows this CTA adds to
+// (written by this CTA, or before an earlier barrier) and the RMSNorm
+// weights staged where the activation pass reads them.
+__device__ void matvec_pre(const MPhase& F, uint8_t* region) {
+  if (F.accumulate && F.rows_per_cta <= kRowsMax) {
+    const int r0 = blockIdx.x * F.rows_per_cta;
+    const int r1 = min(F.total_rows, r0 + F.rows_per_cta);
+    for (int i = threadIdx.x; i < r1 - r0; i += kCT) ms_rows[i] = __ldcg(F.y[0] + r0 + i);
+  }
+  const int pass4 = kMsRegion / 32;
+  if (F.xmode == kXRmsNorm && F.n / 4 <= pass4) {
+    float4* ws = reinterpret_cast<float4*>(region) + pass4;
+    const int n4 = F.n / 4;
+    const int rot = (int)((blockIdx.x * 97u) % (unsigned)n4);
+    for (int i = threadIdx.x; i < n4; i += kCT) {
+      int j = i + rot;
+      if (j >= n4) j -= n4;
+      const int ph = (j & ~7) | (((j & 7) + (j >> 4)) & 7);
+      ws[ph] = __ldg(reinterpret_cast<const float4*>(F.xw) + j);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- matvec
@@ -316,12 +354,9 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
     inv = 1.0f / sqrtf(tot / (float)F.n + P.eps);
     consumer_sync(kCT);  // s_f is reused below
   }
-  if (F.accumulate && F.rows_per_cta <= kRowsMax) {
-    // the residual rows this CTA adds to (one matrix: rows = virtual rows)
-    const int r0 = blockIdx.x * F.rows_per_cta;
-    const int r1 = min(F.total_rows, r0 + F.rows_per_cta);
-    for (int i = threadIdx.x; i < r1 - r0; i += kCT) ms_rows[i] = __ldcg(F.y[0] + r0 + i);
-  }
+  // (the residual rows and, for one pass, the RMSNorm weights were staged
+  // by matvec_pre)
+  const bool ws_staged = rms && F.n / 4 <= pass4;
   float4* xs = reinterpret_cast<float4*>(region);
   float4* ws = xs + pass4;
   for (int e0 = 0; e0 < F.n / 4; e0 += pass4) {
@@ -332,7 +367,7 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
       if (j >= n4) j -= n4;
       const int ph = (j & ~7) | (((j & 7) + (j >> 4)) & 7);
       xs[ph] = __ldcg(reinterpret_cast<const float4*>(F.X) + e0 + j);
-      if (rms) ws[ph] = __ldg(reinterpret_cast<const float4*>(F.xw) + e0 + j);
+      if (rms && !ws_staged) ws[ph] = __ldg(reinterpret_cast<const float4*>(F.xw) + e0 + j);
     }
     consumer_sync(kCT);
     if (rms && F.n / 4 <= pass4) {
@@ -948,12 +983,14 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
     RingPos rp{0, 0u, smem_u32(smem)};
     const uint32_t smem32 = smem_u32(smem);
     for (int pi = 0; pi < P.nphases; ++pi) {
-      if (pi > 0 && !grid_sync(P)) break;
+      if (pi > 0) grid_arrive(P);
       if (threadIdx.x < (int)(sizeof(MPhase) / 4))
         reinterpret_cast<int*>(&s_ph)[threadIdx.x] =
             __ldg(reinterpret_cast<const int*>(P.phases + pi) + threadIdx.x);
       consumer_sync(kCT);
       const int kind = s_ph.kind;
+      if (kind == kPhMatvec) matvec_pre(s_ph, region);
+      if (pi > 0 && !grid_wait(P)) break;
       if (kind == kPhMatvec) {
         if (!matvec_phase(s_ph, P, rp, smem32, region, s_f, s_i)) {
           ms_abort = 1;  // seen at the next grid barrier
