@@ -43,7 +43,7 @@ using namespace mv;
 constexpr int kW = kMsWarps;
 constexpr int kCT = kW * 32;  // consumer threads
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (~1 s with the sleeps)
+constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (L2 round trips: ~1 s)
 constexpr int kMaxStages = 8;
 
 // Per-CTA state at fixed shared addresses (no registers to hold pointers).
@@ -89,8 +89,9 @@ __device__ void grid_arrive(const MParams& P) {
       atomicExch(P.abort, 1);
       *s_flag = 0;
     } else {
-      __threadfence();
-      atomicAdd(P.bar, 1u);
+      // release: this CTA's writes of the phase (ordered before by the CTA
+      // barrier above) are visible to every CTA that acquires the count
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.bar) : "memory");
       *s_flag = 1;
     }
   }
@@ -115,7 +116,6 @@ __device__ bool grid_wait(const MParams& P) {
           if (P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
           break;
         }
-        __nanosleep(64);
       }
       __threadfence();
     }
@@ -206,7 +206,9 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
   // 8 threads per row, four rows per warp at a time: windows of up to 80
   // rows take one pass, so no warp carries a second pass into the next
   // window (stage releases and the next window barrier wait for the last)
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // (rows go to the highest warps first: row group 0, the low warps, has
+  // the most rows of a ragged tile)
+  const int lane = threadIdx.x & 31, warp = kW - 1 - (threadIdx.x >> 5);
   const int sub = lane & 7;
   const int n4 = F.NS * 8;  // float4s per row
   for (int r0 = warp * 4; r0 < nrow; r0 += kW * 4) {
