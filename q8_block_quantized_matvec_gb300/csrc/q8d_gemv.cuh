@@ -102,7 +102,7 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-// try_wait that lets the thread sleep (up to about a microsecond) until the
+// try_wait that lets the thread sleep (up to a few microseconds) until the
 // phase completes instead of returning at once: waiting warps stop taking
 // issue slots from the warps that compute.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
@@ -112,14 +112,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(4000u)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait (about two seconds) that gives up at once when another
-// thread of the CTA already gave up, so that every warp still reaches the
-// CTA barriers quickly.
+// Bounded wait (2^21 polls, each sleeping at most the hint: a few seconds)
+// that gives up at once when another thread of the CTA already gave up, so
+// that every warp still reaches the CTA barriers quickly.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag) {
   for (uint32_t i = 0; i < (1u << 21); ++i) {

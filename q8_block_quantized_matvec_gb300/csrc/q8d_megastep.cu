@@ -1052,13 +1052,13 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
   if (F.NS > kMsWarps) return false;
   F.RG = kMsWarps / F.NS;
   // R = RG * k rows (each warp takes k rows of a tile), k the largest up to
-  // 8 within the stage target that still gives every CTA at least three
+  // 8 within the stage target that still gives every CTA at least two
   // tiles of the phase
   const long long rows_cta = F.glu ? ((long long)F.vbegin[1] + grid - 1) / grid * 2
                                    : ((long long)F.vbegin[F.nseg] + grid - 1) / grid;
   int k = 8;
   while (k > 1 && ((long long)F.RG * k * F.row_bytes + 32 > stage_target ||
-                   rows_cta < 3LL * F.RG * k))
+                   rows_cta < 2LL * F.RG * k))
     --k;
   F.R = F.RG * k;
   // window tiles: double-buffered partials within the shared region
