@@ -18,7 +18,8 @@
 //  * Matvec phases use the layout of the standalone matvec kernel: warp
 //    pairs own the even / odd block columns of 64-column segments, the
 //    lane's 32 activations in registers (RMSNorm or SiLU*up applied while
-//    loading), lane partials reduced in double-buffered row windows.
+//    loading), lane partials folded within the warp and reduced in
+//    double-buffered row windows.
 //  * Attention: one CTA per (KV head, context chunk) computes the G query
 //    heads' online-softmax partial over its chunk on CUDA cores (f32); the
 //    CTA owning row L-1 applies bias / QK-norm / RoPE to the new k, v,
@@ -45,6 +46,10 @@ constexpr int kCT = kW * 32;  // consumer threads
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (L2 round trips: ~1 s)
 constexpr int kMaxStages = 8;
+// Partials a warp keeps per row: its 32 lane partials folded to 4 with
+// three shuffles, so a reduction window (a shared buffer) holds 8x the rows
+// (and a row's partials stay whole 16-byte vectors for any NS).
+constexpr int kPW = 4;
 
 // Per-CTA state at fixed shared addresses (no registers to hold pointers).
 __shared__ uint64_t ms_full[kMaxStages];   // stage s filled (TMA complete_tx)
@@ -197,7 +202,7 @@ __device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int to
   }
 }
 
-// Window reduction: sums each row's lane partials over segments and lanes
+// Window reduction: sums each row's warp partials over segments and lanes
 // in a fixed order and writes the row.
 // rbase: the matrix row held in ms_rows[0] (the CTA's first row), or -1
 // when the CTA's rows do not fit ms_rows (then values go through L2).
@@ -210,7 +215,7 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
   // the most rows of a ragged tile)
   const int lane = threadIdx.x & 31, warp = kW - 1 - (threadIdx.x >> 5);
   const int sub = lane & 7;
-  const int n4 = F.NS * 8;  // float4s per row
+  const int n4 = F.NS * kPW / 4;  // float4s per row
   for (int r0 = warp * 4; r0 < nrow; r0 += kW * 4) {
     const int r = r0 + (lane >> 3);
     const bool valid = r < nrow;
@@ -266,10 +271,10 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
                                  uint32_t boff, const uint64_t (&x2)[16], bool& ok) {
   const int lane = threadIdx.x & 31;
   const int RG = F.RG, R = F.R;
-  const int n32 = F.NS * 32;
+  const int nP = F.NS * kPW;  // partials per row
   const uint32_t rowb = (uint32_t)F.row_bytes;
   const uint32_t step = (uint32_t)RG * rowb;
-  const uint32_t pstep = (uint32_t)(RG * n32 * 4);
+  const uint32_t pstep = (uint32_t)(RG * nP * 4);
   const uint32_t rb15 = rowb & 15u;
   int wrow = 0;
 #pragma unroll 1
@@ -280,13 +285,16 @@ __device__ int ms_consume_window(const MPhase& F, const MParams& P, RingPos& rp,
     // (warps beyond NS * RG, when NS does not divide the warp count, run the
     // same code on row group 0's rows and store nothing)
     uint32_t o = after_wait(rp.stage32 + delta + boff + (uint32_t)rg * rowb);
-    uint32_t d = lane_buf + (uint32_t)(wrow * n32) * 4u;
+    uint32_t d = lane_buf + (uint32_t)(wrow * nP) * 4u;
     // this warp's rows of the tile, one block at a time (a ragged tile stops
     // at the warp's last row)
 #pragma unroll 1
     for (int rl = rg; rl < rows; rl += RG) {
-      const float va = block_dot<AM>(o, x2);
-      if (rl < rows_st) sts32(d, va);
+      float va = block_dot<AM>(o, x2);
+      va += __shfl_xor_sync(0xffffffffu, va, 16);
+      va += __shfl_xor_sync(0xffffffffu, va, 8);
+      va += __shfl_xor_sync(0xffffffffu, va, 4);
+      if (rl < rows_st && lane < kPW) sts32(d, va);
       o += step;
       d += pstep;
     }
@@ -418,9 +426,10 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
   // With an even number of blocks per row every row starts at a multiple of
   // 4 bytes, so all blocks of a paired warp start at 2*(col & 1) mod 4.
   const int am = (F.paired && (F.bpr & 1) == 0) ? (ci & 1) : 2;
-  const uint32_t n32 = (uint32_t)F.NS * 32u;
-  const uint32_t lane_part = part32 + ((uint32_t)(ci * 32 + lane) + (uint32_t)rg * n32) * 4u;
-  const uint32_t buf_bytes = (uint32_t)F.win * (uint32_t)F.R * n32 * 4u;
+  const uint32_t nP = (uint32_t)F.NS * kPW;
+  const uint32_t lane_part =
+      part32 + ((uint32_t)(ci * kPW + (lane & (kPW - 1))) + (uint32_t)rg * nP) * 4u;
+  const uint32_t buf_bytes = (uint32_t)F.win * (uint32_t)F.R * nP * 4u;
   uint32_t buf = 0;
   const int rbase = (F.accumulate || F.glu) && F.rows_per_cta <= kRowsMax
                         ? (int)blockIdx.x * F.rows_per_cta
@@ -1062,7 +1071,7 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
     --k;
   F.R = F.RG * k;
   // window tiles: double-buffered partials within the shared region
-  const long long per_tile = 2LL * F.R * F.NS * 32 * 4;
+  const long long per_tile = 2LL * F.R * F.NS * kPW * 4;
   if (per_tile > kMsRegion) return false;
   F.win = (int)std::max<long long>(1, kMsRegion / per_tile);
   F.total_rows = F.vbegin[F.nseg];
