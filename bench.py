@@ -17,7 +17,8 @@ Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica (the decode step does not shard: replicas only) and
 `value` is the sum of the ranks' tokens over the max of their times.
 The reference arm (--impl reference) times the scalar C oracle on the
-host cores on a bounded sample of the same workload.
+host cores: W untimed and K timed steps, each a bounded sample of the same
+workload (2 of the layers plus lm_head, projected to the full step).
 """
 from __future__ import annotations
 
@@ -169,12 +170,14 @@ def ncu_traffic(algorithmic_bytes: float):
 
 
 # ---------------------------------------------------------------------------- oracle
-def oracle_sample(shape_name: str, context: int, seconds_hint: float = 12.0):
+def oracle_sample(shape_name: str, context: int, seconds_hint: float = 12.0,
+                  steps: int | None = None, warmup: int = 0):
     """Times the scalar oracle's decode step on a bounded sample of the
     workload: the same shapes truncated to 2 layers (lm_head included), KV
     at the same context, repeated for about `seconds_hint` seconds of CPU
-    work (at least 3 times); with the medians the full step's time is
-    projected as t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
+    work (at least 3 times), or, with `steps`, `warmup` untimed and then
+    exactly `steps` timed repetitions; with the medians the full step's time
+    is projected as t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
     Returns (tokens_per_s, threads, description, repetitions)."""
     import numpy as np
 
@@ -190,9 +193,14 @@ def oracle_sample(shape_name: str, context: int, seconds_hint: float = 12.0):
     host = orc.HostStep(w, cap, caches)
     threads = orc.default_threads()
     x = synth.normal_f32(0, "bench.x", full.hidden)
+    for _ in range(warmup if steps is not None else 0):
+        orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
+        host.step(17, context - 1, threads)
+    n_steps = steps
     heads, steps = [], []
     t_begin = time.perf_counter()
-    while len(steps) < 3 or time.perf_counter() - t_begin < seconds_hint:
+    while (len(steps) < n_steps if n_steps is not None
+           else len(steps) < 3 or time.perf_counter() - t_begin < seconds_hint):
         t0 = time.perf_counter()
         orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
         heads.append(time.perf_counter() - t0)
@@ -328,10 +336,11 @@ def replica_throughput(local_seconds: float, steps: int, dist=None, device="cuda
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    tps, threads, desc, reps = oracle_sample(args.model, args.context)
+    tps, threads, desc, reps = oracle_sample(args.model, args.context, steps=args.steps,
+                                             warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
-        "steps": reps, "warmup": 0, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
+        "steps": reps, "warmup": args.warmup, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(args)},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
