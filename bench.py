@@ -128,6 +128,7 @@ def attn_bytes(L, Hk, D, H, esize, append=True):
 
 
 STEP_KERNEL_SOURCES = ("q8d_megastep.cu", "q8d_megastep.cuh", "q8d_gemv.cuh", "q8d_internal.cuh",
+                       "q8d_attn.cuh",
                        "q8d_attn_common.cuh", "q8d_rows.cuh", "q8d_step.cu")
 
 
@@ -294,6 +295,15 @@ def run_profile(args):
             q8d.q8d_matvec(x, w, y, n, p)
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
+    elif args.profile == "attn_stress":
+        lens, args_, err = stress_inputs(q8d, 28, 4, 128)
+        q8d.q8d_gqa_decode_attn(*args_)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStart()
+        q8d.q8d_gqa_decode_attn(*args_)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStop()
+        assert err.item() == 0
     else:
         H, Hk, D, L = 28, 4, 128, args.context
         kc = synth.normal_torch(0, "prof.k", (L, Hk * D), torch.float16)
@@ -314,6 +324,58 @@ def run_profile(args):
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
         assert err.item() == 0
+
+
+# ---------------------------------------------------------------------------- attention stress
+STRESS_CAP = 32768
+
+
+def stress_inputs(q8d, H, Hk, D, rank=0):
+    """The long-context attention workload: 8 sequences of the model's heads,
+    lengths drawn uniformly from [1, 32768] (seeded), an f16 cache of 32768
+    rows per sequence, no append."""
+    import torch
+
+    import synth
+    cap, kvw = STRESS_CAP, Hk * D
+    lens = synth.stream(0, "ragged.lens").integers(1, cap + 1, 8).tolist()
+    kc = synth.normal_torch(rank, "stress.k", (8, cap, kvw), torch.float16)
+    vc = synth.normal_torch(rank, "stress.v", (8, cap, kvw), torch.float16)
+    q = synth.normal_torch(rank, "stress.q", (8, H * D), torch.float32)
+    out = torch.empty(8, H * D, device="cuda")
+    wsb = q8d.q8d_gqa_workspace_bytes(8, H, Hk, D, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args_ = (q, None, None, kc, vc, q8d.Q8D_KV_F16, out, 8, H, Hk, D, cap, cap * kvw, lt,
+             1 / math.sqrt(D), ws, wsb, err)
+    return lens, args_, err
+
+
+def attn_stress(q8d, H, Hk, D, reps, stream, flush, rank=0):
+    """q8d_gqa_decode_attn on the stress workload (K/V of all 8 sequences
+    ~0.27 GB, L2 flushed before each timed launch); GB/s of algorithmic
+    bytes (the K/V rows read once, q and the output)."""
+    import torch
+    lens, args_, err = stress_inputs(q8d, H, Hk, D, rank)
+    ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    with torch.cuda.stream(stream):
+        for rep in range(max(reps, 3) + 1):
+            flush.fill_(rep & 0xFF)
+            ev[0].record(stream)
+            q8d.q8d_gqa_decode_attn(*args_, stream)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            if rep:
+                times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    assert err.item() == 0
+    t = statistics.median(times)
+    nbytes = sum(attn_bytes(L, Hk, D, H, 2, append=False) for L in lens)
+    return {"kernel": "gqa_mma_kernel + gqa_combine_kernel (q8d_gqa_decode_attn)",
+            "GB_s": nbytes / t / 1e9, "us_per_launch": t * 1e6, "kv_bytes": nbytes,
+            "batch": 8, "lengths": "seeded uniform in [1, 32768]", "sum_lengths": int(sum(lens)),
+            "l2": "256 MB flush before each launch"}
 
 
 # ---------------------------------------------------------------------------- replicas
@@ -367,7 +429,8 @@ def main():
                     help="--profile step only: use this many layers of the model's shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=3)
-    ap.add_argument("--profile", choices=["step", "matvec", "matvec_down", "attn", "matvec_sweep"],
+    ap.add_argument("--profile",
+                    choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "matvec_sweep"],
                     default=None,
                     help="run a short fixed workload between cudaProfilerStart/Stop for ncu "
                          "(--profile-from-start off) and print no JSON")
@@ -514,6 +577,10 @@ def main():
     at_time = statistics.median(at_times)
     at_bytes_launch = attn_bytes(ctx, Hk, D, H, esize, append=False)
     at_gbs = at_bytes_launch * shape.n_layers / at_time / 1e9
+    stress = attn_stress(q8d, H, Hk, D, args.kernel_reps, stream, flush, rank) \
+        if shape.kv_dtype == synth.KV_F16 else None
+    if stress is not None:
+        stress["frac_of_peak"] = stress["GB_s"] / hbm
 
     # dominant kernel: the persistent step kernel, one launch per step
     step_b = statistics.mean(step_bytes(shape, ctx + s, esize) for s in range(args.steps))
@@ -551,6 +618,7 @@ def main():
                 "gqa_decode_attn": {"GB_s": at_gbs, "frac_of_peak": at_gbs / hbm,
                                     "us_per_layer": at_time / shape.n_layers * 1e6,
                                     "context": ctx, "l2": "256 MB flush between layers"},
+                "gqa_decode_attn_batch8_ragged": stress,
             },
             "e2e": e2e,
             "cpu_baseline": cpu,

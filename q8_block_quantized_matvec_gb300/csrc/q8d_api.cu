@@ -237,6 +237,7 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
   A.scale = scale;
   A.workspace = workspace;
   A.nc = attn_chunks(batch, n_kv_heads, cap);
+  A.nct = attn_ctas_per_head(batch, n_kv_heads, cap);
   A.d_err = d_err;
   return attn_launch(A, static_cast<cudaStream_t>(stream));
 }

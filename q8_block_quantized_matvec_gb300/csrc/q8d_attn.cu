@@ -96,22 +96,21 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   float* corr = l_run + GMAX;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
 
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.n_heads / P.n_kv_heads;
-  if (P.pdl) {
-    griddep_launch_dependents();
-    griddep_wait();
-  }
+  // the combine kernel, launched as a programmatic dependent, may be
+  // scheduled now (it waits for this grid's results before reading them)
+  griddep_launch_dependents();
+  if (P.pdl) griddep_wait();
+  int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
+  if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = P.d_lens[b];
-  if (L < 1 || L > P.cap) {
-    if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
-    if (P.tickets && c == 0)  // no merge will run: the outputs must not look valid
-      for (int e = tid; e < G * D; e += kAttnThreads)
-        P.out[((long long)b * P.n_heads + (long long)g * G) * D + e] = __int_as_float(0x7fc00000);
+  if (!attn_len_ok(P, L)) {  // (the combine writes NaN outputs)
+    if (g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
     return;
   }
-  const int tpc = chunk_rows(L, P.nc);
+  const int tpc = (L + n - 1) / n;
   const int t_begin = c * tpc;
   if (t_begin >= L) return;
   const int t_end = min(L, t_begin + tpc);
@@ -321,10 +320,6 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
       P.ws_l[hq * P.nc + c] = l_run[h];
     }
   }
-  if (P.tickets) {
-    __syncthreads();  // the reduction buffer is free for the merge's weights
-    ticket_combine<D>(P, L, tpc, b, g, G, smem);
-  }
 }
 
 // Merges the chunk partials of one (sequence, query head):
@@ -339,13 +334,16 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const AttnParams P) {
   const int hq = blockIdx.x;  // b * H + h
   const int b = hq / P.n_heads;
   const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  griddep_wait();  // the partials of the attention grid are complete and visible
   const int L = P.d_lens[b];
   float* o = P.out + (long long)hq * D;
-  if (L < 1 || L > P.cap) {
+  if (!attn_len_ok(P, L)) {
     o[j] = __int_as_float(0x7fc00000);
     return;
   }
-  const int tpc = chunk_rows(L, P.nc);
+  // the kernels' split of this sequence (chunks past the rows are unused)
+  const int n = attn_nchunks(P, L, attn_total_rows(P));
+  const int tpc = (L + n - 1) / n;
   const int nact = (L + tpc - 1) / tpc;
   const float* M = P.ws_m + (long long)hq * P.nc;
   const float* S = P.ws_l + (long long)hq * P.nc;
@@ -417,9 +415,9 @@ int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
     if (e != cudaSuccess) return record_cuda(e);
     configured[dev] = true;
   }
-  dim3 grid(P.nc, P.n_kv_heads, P.batch);
+  dim3 grid(P.nct, P.n_kv_heads);
   const int rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, P.pdl != 0, P);
-  if (rc || P.tickets) return rc;
+  if (rc) return rc;
   return attn_combine_launch(P, stream);
 }
 
@@ -435,20 +433,27 @@ int launch_attn_g(const AttnParams& P, cudaStream_t stream) {
 }  // namespace
 
 int attn_combine_launch(const AttnParams& P, cudaStream_t stream) {
+  // a programmatic dependent of the attention grid: its launch overlaps
+  // that grid's tail
+  const dim3 grid((unsigned)(P.batch * P.n_heads));
+  const size_t smem = (size_t)P.nc * sizeof(float);
   if (P.head_dim == 128)
-    gqa_combine_kernel<128><<<P.batch * P.n_heads, 128, P.nc * sizeof(float), stream>>>(P);
-  else
-    gqa_combine_kernel<64><<<P.batch * P.n_heads, 64, P.nc * sizeof(float), stream>>>(P);
-  return check_launch();
+    return launch_ex(gqa_combine_kernel<128>, grid, dim3(128), smem, stream, true, P);
+  return launch_ex(gqa_combine_kernel<64>, grid, dim3(64), smem, stream, true, P);
+}
+
+int attn_ctas_per_head(int batch, int n_kv_heads, int max_len) {
+  const int per_head = (4 * sm_count() + n_kv_heads - 1) / n_kv_heads;
+  // no more than the sequences could use at one chunk per kMinChunk rows
+  const long long by_len = (long long)batch * ((std::max(max_len, 1) + kMinChunk - 1) / kMinChunk);
+  return (int)std::max<long long>(batch, std::min<long long>(per_head, by_len));
 }
 
 int attn_chunks(int batch, int n_kv_heads, int max_len) {
-  const int target = 4 * sm_count();
-  int nc = (target + batch * n_kv_heads - 1) / (batch * n_kv_heads);
-  const int cap_nc = (std::max(max_len, 1) + kMinChunk - 1) / kMinChunk;
-  // at most 256 chunk slots: the in-kernel merge keeps 2 * G * slots floats
-  // in shared memory
-  return std::max(1, std::min(std::min(nc, cap_nc), 256));
+  const int nct = attn_ctas_per_head(batch, n_kv_heads, max_len);
+  const int share = std::max(8, 4 * ((nct + batch - 1) / batch));
+  const int by_len = (std::max(max_len, 1) + kMinChunk - 1) / kMinChunk;
+  return std::max(1, std::min(std::min(nct, share), by_len));
 }
 
 size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len) {

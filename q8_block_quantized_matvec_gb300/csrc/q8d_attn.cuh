@@ -18,7 +18,8 @@ struct AttnParams {
   const int* d_lens;    // [batch]
   float scale;
   void* workspace;
-  int nc;               // context chunks per (sequence, KV head)
+  int nc;               // chunk slots per (sequence, KV head) in the workspace
+  int nct;              // chunk CTAs per KV head (the grid's x)
   int* d_err;
   // Decode-step prologue fused into the f16 kernel (all null / 0 for the
   // plain C-ABI call): q/k/v biases, per-head q/k RMSNorm gains, RoPE table
@@ -31,10 +32,6 @@ struct AttnParams {
   float eps;
   const float* rope_cos;
   const float* rope_sin;
-  // Zero-initialised tickets [batch * n_kv_heads]: when set, the last chunk
-  // CTA of each (sequence, KV head) merges the partials itself (and resets
-  // its ticket); when null a separate combine kernel runs.
-  int* tickets;
   int pdl;              // launched as a programmatic dependent
   // carved from the workspace by attn_launch
   float* ws_o;
@@ -42,14 +39,61 @@ struct AttnParams {
   float* ws_l;
 };
 
-// Context rows per chunk for attended length L with nc chunk slots: at least
-// kMinChunk rows so the partials stay small next to the K/V they summarise.
+// Split-K over a ragged batch.  The host fixes the grid (nct chunk CTAs per
+// KV head) without knowing the lengths, which live in device memory; every
+// CTA (and the combine) derives the same split from them: sequence s gets
+// n_s = 1 + floor((nct - batch) * L_s / sum L) chunks (its share of the
+// batch's rows), at most one per kMinChunk rows and at most nc (the
+// workspace slots), and its rows [0, L_s) go to them in equal parts.  CTA k
+// of a KV head takes chunk k - (n_0 + ... + n_{s-1}) of the sequence s whose
+// range holds k; CTAs past the last chunk have no work.
 constexpr int kMinChunk = 128;
-__host__ __device__ __forceinline__ int chunk_rows(int L, int nc) {
-  const int c = (L + nc - 1) / nc;
-  return c > kMinChunk ? c : kMinChunk;
+
+__device__ __forceinline__ bool attn_len_ok(const AttnParams& P, int L) {
+  return L >= 1 && L <= P.cap;
 }
 
+// Sum of the valid lengths of the batch.
+__device__ __forceinline__ long long attn_total_rows(const AttnParams& P) {
+  long long t = 0;
+  for (int s = 0; s < P.batch; ++s) {
+    const int L = P.d_lens[s];
+    if (attn_len_ok(P, L)) t += L;
+  }
+  return t;
+}
+
+// Chunks of a sequence of length L (1 for an invalid length).
+__device__ __forceinline__ int attn_nchunks(const AttnParams& P, int L, long long total) {
+  if (!attn_len_ok(P, L) || total <= 0) return 1;
+  long long n = 1 + (long long)(P.nct - P.batch) * L / total;
+  n = n < (L + kMinChunk - 1) / kMinChunk ? n : (L + kMinChunk - 1) / kMinChunk;
+  n = n < P.nc ? n : P.nc;
+  return n > 1 ? (int)n : 1;
+}
+
+// Sequence b, chunk c of n for CTA k of a KV head; false if it has no work.
+__device__ __forceinline__ bool attn_chunk_of(const AttnParams& P, int k, int& b, int& c, int& n) {
+  const long long total = attn_total_rows(P);
+  int first = 0;
+  for (int s = 0; s < P.batch; ++s) {
+    const int ns = attn_nchunks(P, P.d_lens[s], total);
+    if (k < first + ns) {
+      b = s;
+      c = k - first;
+      n = ns;
+      return true;
+    }
+    first += ns;
+  }
+  return false;
+}
+
+// Chunk CTAs per KV head (grid.x): about four per SM in all, at least one
+// per sequence, at most one per kMinChunk rows of every cache.
+int attn_ctas_per_head(int batch, int n_kv_heads, int max_len);
+// Workspace chunk slots per (sequence, KV head): up to 4x a sequence's even
+// share of the CTAs (at least 8), one per kMinChunk rows of the cache.
 int attn_chunks(int batch, int n_kv_heads, int max_len);
 int attn_combine_launch(const AttnParams& P, cudaStream_t stream);
 int attn_mma_launch(const AttnParams& P, cudaStream_t stream);  // f16 cache, tensor cores

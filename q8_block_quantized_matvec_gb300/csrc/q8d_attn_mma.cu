@@ -18,10 +18,15 @@
 //    w, w+4, w+8, ... of the chunk); the four warps' {m, l, O} are merged once
 //    at the end of the chunk and written as the chunk's partial.
 //  * Every warp streams its own 16-token groups of K/V rows through a
-//    three-stage cp.async ring (16-byte copies; a KV head's row is only 128
+//    two-stage cp.async ring (16-byte copies; a KV head's row is only 128
 //    or 256 bytes, too small for efficient bulk copies) and never waits for
-//    the other warps until the final merge.  Rows are padded by 16 bytes so
-//    fragment loads and ldmatrix.trans hit distinct banks.
+//    the other warps until the final merge.  Two stages keep a CTA at ~70 KB
+//    of shared memory, so three CTAs (12 warps) share an SM: more loads in
+//    flight per SM than three stages with two CTAs.  Rows are padded by 16
+//    bytes so fragment loads and ldmatrix.trans hit distinct banks.
+//  * The CTAs of a KV head are split over the batch's sequences in
+//    proportion to their lengths (read from device memory by every CTA,
+//    q8d_attn.cuh), so a ragged batch's long sequences do not set the time.
 #include <cuda_fp16.h>
 
 #include "q8d_attn.cuh"
@@ -37,7 +42,7 @@ constexpr float kLog2eA = 1.4426950408889634f;
 constexpr float kPScale = 4096.f;      // probabilities scaled by 2^12 before the f16 split
 
 constexpr int kGroup = 16;             // tokens per warp step
-constexpr int kWStages = 3;            // per-warp cp.async ring depth
+constexpr int kWStages = 2;            // per-warp cp.async ring depth
 
 template <int D>
 struct MCfg {
@@ -95,23 +100,22 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
   float* fh = reinterpret_cast<float*>(smem + C::kOffF);
 
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, cq = lane & 3;
   const int G = P.n_heads / P.n_kv_heads;
-  if (P.pdl) {
-    griddep_launch_dependents();
-    griddep_wait();
-  }
+  // the combine kernel, launched as a programmatic dependent, may be
+  // scheduled now (it waits for this grid's results before reading them)
+  griddep_launch_dependents();
+  if (P.pdl) griddep_wait();
+  int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
+  if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = P.d_lens[b];
-  if (L < 1 || L > P.cap) {
-    if (c == 0 && g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
-    if (P.tickets && c == 0)  // no merge will run: the outputs must not look valid
-      for (int e = tid; e < G * D; e += kThreadsA)
-        P.out[((long long)b * P.n_heads + (long long)g * G) * D + e] = __int_as_float(0x7fc00000);
+  if (!attn_len_ok(P, L)) {  // (the combine writes NaN outputs)
+    if (g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
     return;
   }
-  const int tpc = chunk_rows(L, P.nc);
+  const int tpc = (L + n - 1) / n;
   const int t_begin = c * tpc;
   if (t_begin >= L) return;
   const int t_end = min(L, t_begin + tpc);
@@ -367,9 +371,6 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
       P.ws_l[hq * P.nc + c] = lsum;
     }
   }
-  if (!P.tickets) return;
-
-  ticket_combine<D>(P, L, tpc, b, g, G, smem);
 }
 
 template <int D>
@@ -384,10 +385,10 @@ int launch_mma(const AttnParams& P, cudaStream_t stream) {
     if (e != cudaSuccess) return record_cuda(e);
     configured[dev] = true;
   }
-  dim3 grid(P.nc, P.n_kv_heads, P.batch);
+  dim3 grid(P.nct, P.n_kv_heads);
   const int rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
                            P.pdl != 0, P);
-  if (rc || P.tickets) return rc;
+  if (rc) return rc;
   return attn_combine_launch(P, stream);
 }
 
