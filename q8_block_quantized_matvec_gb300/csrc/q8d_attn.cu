@@ -324,21 +324,26 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
 
 // Merges the chunk partials of one (sequence, query head):
 //   M = max_c m_c,  w_c = 2^(m_c - M),  out = sum_c w_c O_c / sum_c w_c l_c
-// The chunk weights are computed once into shared memory (all chunks'
-// loads in flight together), the sums run in a fixed order: deterministic.
+// kCombGroups groups of D threads (thread j of a group: output element j)
+// take every kCombGroups-th chunk; each thread issues all loads of its
+// chunks before using any (one L2 round trip, up to kCombLoads chunks per
+// pass), merges them, and the groups' {m, l, o} are merged in group order
+// through shared memory.  Fixed order throughout: deterministic.
+constexpr int kCombGroups = 4;
+constexpr int kCombLoads = 8;
+
 template <int D>
-__global__ void __launch_bounds__(D) gqa_combine_kernel(const AttnParams P) {
-  extern __shared__ float wsm[];  // [nc] chunk weights
-  __shared__ float red[D / 32];
-  __shared__ float s_tot;
+__global__ void __launch_bounds__(kCombGroups * D) gqa_combine_kernel(const AttnParams P) {
+  __shared__ float gm[kCombGroups], gl[kCombGroups];
+  __shared__ float go[kCombGroups][D];
   const int hq = blockIdx.x;  // b * H + h
   const int b = hq / P.n_heads;
-  const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  const int j = threadIdx.x % D, grp = threadIdx.x / D;
   griddep_wait();  // the partials of the attention grid are complete and visible
   const int L = P.d_lens[b];
   float* o = P.out + (long long)hq * D;
   if (!attn_len_ok(P, L)) {
-    o[j] = __int_as_float(0x7fc00000);
+    if (grp == 0) o[j] = __int_as_float(0x7fc00000);
     return;
   }
   // the kernels' split of this sequence (chunks past the rows are unused)
@@ -347,46 +352,52 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const AttnParams P) {
   const int nact = (L + tpc - 1) / tpc;
   const float* M = P.ws_m + (long long)hq * P.nc;
   const float* S = P.ws_l + (long long)hq * P.nc;
-  const float* O = P.ws_o + (long long)hq * P.nc * D;
-  float mx = -INFINITY;
-  for (int c = j; c < nact; c += D) mx = fmaxf(mx, M[c]);
+  const float* O = P.ws_o + (long long)hq * P.nc * D + j;
+  float m = -INFINITY, l = 0.f, acc = 0.f;
+  for (int c0 = grp; c0 < nact; c0 += kCombGroups * kCombLoads) {
+    float mc[kCombLoads], sc[kCombLoads], oc[kCombLoads];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  mx = red[0];
+    for (int u = 0; u < kCombLoads; ++u) {
+      const int c = c0 + u * kCombGroups;
+      const bool ok = c < nact;
+      mc[u] = ok ? __ldcg(M + c) : -INFINITY;
+      sc[u] = ok ? __ldcg(S + c) : 0.f;
+      oc[u] = ok ? __ldcg(O + (long long)c * D) : 0.f;
+    }
+    float mn = m;
 #pragma unroll
-  for (int w = 1; w < D / 32; ++w) mx = fmaxf(mx, red[w]);
-  float sl = 0.f;
-  for (int c = j; c < nact; c += D) {
-    const float mc = M[c];
-    const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - mx);
-    wsm[c] = w;
-    sl = fmaf(S[c], w, sl);
+    for (int u = 0; u < kCombLoads; ++u) mn = fmaxf(mn, mc[u]);
+    if (mn == -INFINITY) continue;
+    const float r = exp2f(m - mn);  // 0 when m was -inf
+    l *= r;
+    acc *= r;
+#pragma unroll
+    for (int u = 0; u < kCombLoads; ++u) {
+      const float w = mc[u] == -INFINITY ? 0.f : exp2f(mc[u] - mn);
+      l = fmaf(sc[u], w, l);
+      acc = fmaf(oc[u], w, acc);
+    }
+    m = mn;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, off);
-  __syncthreads();  // red[] reads above are done
-  if (lane == 0) red[warp] = sl;
-  __syncthreads();
   if (j == 0) {
-    float t = 0.f;
-    for (int w = 0; w < D / 32; ++w) t += red[w];
-    s_tot = t;
+    gm[grp] = m;
+    gl[grp] = l;
   }
+  go[grp][j] = acc;
   __syncthreads();
-  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  int c = 0;
-  for (; c + 8 <= nact; c += 8) {
-    float o8[8];
+  if (grp != 0) return;
+  float mx = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) o8[u] = O[(long long)(c + u) * D + j];
+  for (int g = 0; g < kCombGroups; ++g) mx = fmaxf(mx, gm[g]);
+  float lt = 0.f, at = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) a[u] = fmaf(o8[u], wsm[c + u], a[u]);
+  for (int g = 0; g < kCombGroups; ++g) {
+    if (gm[g] == -INFINITY) continue;
+    const float w = exp2f(gm[g] - mx);
+    lt = fmaf(gl[g], w, lt);
+    at = fmaf(go[g][j], w, at);
   }
-  for (; c < nact; ++c) a[0] = fmaf(O[(long long)c * D + j], wsm[c], a[0]);
-  const float acc0 = (a[0] + a[1]) + (a[2] + a[3]), acc1 = (a[4] + a[5]) + (a[6] + a[7]);
-  o[j] = (acc0 + acc1) / s_tot;
+  o[j] = at / lt;
 }
 
 template <typename KT>
@@ -436,10 +447,9 @@ int attn_combine_launch(const AttnParams& P, cudaStream_t stream) {
   // a programmatic dependent of the attention grid: its launch overlaps
   // that grid's tail
   const dim3 grid((unsigned)(P.batch * P.n_heads));
-  const size_t smem = (size_t)P.nc * sizeof(float);
   if (P.head_dim == 128)
-    return launch_ex(gqa_combine_kernel<128>, grid, dim3(128), smem, stream, true, P);
-  return launch_ex(gqa_combine_kernel<64>, grid, dim3(64), smem, stream, true, P);
+    return launch_ex(gqa_combine_kernel<128>, grid, dim3(kCombGroups * 128), 0, stream, true, P);
+  return launch_ex(gqa_combine_kernel<64>, grid, dim3(kCombGroups * 64), 0, stream, true, P);
 }
 
 int attn_ctas_per_head(int batch, int n_kv_heads, int max_len) {
