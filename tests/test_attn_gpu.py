@@ -186,6 +186,45 @@ def test_attention_ragged_batch_32768(q8d, orc):
         assert np.all(np.abs(got[s] - ref) <= TOL * ab), (s, L)
 
 
+@pytest.mark.parametrize("dtype", [synth.KV_F16, synth.KV_F32])
+def test_attention_one_long_sequence_among_short_ones(q8d, orc, dtype):
+    """Length-proportional split at its clamp: one 32768-row sequence next to
+    seven 1-row ones wants ~144 chunks and gets the workspace's slots."""
+    H, Hk, D, cap = 28, 4, 128, 32768
+    kvw = Hk * D
+    lens = [cap, 1, 1, 1, 1, 1, 1, 1]
+    npdt = np.float16 if dtype == synth.KV_F16 else np.float32
+    kc = np.zeros((8, cap, kvw), npdt)
+    vc = np.zeros((8, cap, kvw), npdt)
+    for s_, L in enumerate(lens):
+        kc[s_, :L] = synth.normal_f16(s_, "long.k", (L, kvw)).astype(npdt)
+        vc[s_, :L] = synth.normal_f16(s_, "long.v", (L, kvw)).astype(npdt)
+    q = synth.normal_f32(0, "long.q", (8, H * D))
+    got, err = run_attn(q8d, dev(q), dev(kc), dev(vc), dtype, H, Hk, D, lens, cap,
+                        1 / math.sqrt(D))
+    assert err == 0
+    for s_, L in enumerate(lens):
+        ref, ab = orc.gqa_decode_attn(q[s_], kc[s_], vc[s_], dtype, H, Hk, D, L, 1 / math.sqrt(D))
+        assert np.all(np.abs(got[s_] - ref) <= TOL * ab), (s_, L)
+
+
+def test_attention_batch_larger_than_the_chunk_grid(q8d, orc):
+    """160 sequences (more than the chunk CTAs a KV head would get): one CTA
+    per sequence; lengths 1..160 (seeded order), every output checked."""
+    H, Hk, D, cap = 8, 4, 64, 200
+    kvw = Hk * D
+    batch = 160
+    lens = (synth.stream(0, "wide.lens").permutation(batch) + 1).tolist()
+    kc = synth.normal_f16(0, "wide.k", (batch, cap, kvw))
+    vc = synth.normal_f16(0, "wide.v", (batch, cap, kvw))
+    q = synth.normal_f32(0, "wide.q", (batch, H * D))
+    got, err = run_attn(q8d, dev(q), dev(kc), dev(vc), synth.KV_F16, H, Hk, D, lens, cap, 0.125)
+    assert err == 0
+    for s_, L in enumerate(lens):
+        ref, ab = orc.gqa_decode_attn(q[s_], kc[s_], vc[s_], synth.KV_F16, H, Hk, D, L, 0.125)
+        assert np.all(np.abs(got[s_] - ref) <= TOL * ab), (s_, L)
+
+
 def test_attention_bad_length_sets_error_and_nan(q8d):
     H, Hk, D, cap = 4, 2, 64, 32
     kc = torch.zeros((2, cap, Hk * D), dtype=torch.float16, device="cuda")
