@@ -128,8 +128,7 @@ def attn_bytes(L, Hk, D, H, esize, append=True):
 
 
 STEP_KERNEL_SOURCES = ("q8d_megastep.cu", "q8d_megastep.cuh", "q8d_gemv.cuh", "q8d_internal.cuh",
-                       "q8d_attn.cuh",
-                       "q8d_attn_common.cuh", "q8d_rows.cuh", "q8d_step.cu")
+                       "q8d_attn.cuh", "q8d_attn_common.cuh", "q8d_step.cu")
 
 
 def kernel_source_sha():

@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   // the combine kernel, launched as a programmatic dependent, may be
   // scheduled now (it waits for this grid's results before reading them)
   griddep_launch_dependents();
-  if (P.pdl) griddep_wait();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = P.d_lens[b];
@@ -427,7 +426,7 @@ int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
     configured[dev] = true;
   }
   dim3 grid(P.nct, P.n_kv_heads);
-  const int rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, P.pdl != 0, P);
+  const int rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, false, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

@@ -32,7 +32,6 @@ struct AttnParams {
   float eps;
   const float* rope_cos;
   const float* rope_sin;
-  int pdl;              // launched as a programmatic dependent
   // carved from the workspace by attn_launch
   float* ws_o;
   float* ws_m;

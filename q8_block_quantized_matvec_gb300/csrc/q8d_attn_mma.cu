@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   // the combine kernel, launched as a programmatic dependent, may be
   // scheduled now (it waits for this grid's results before reading them)
   griddep_launch_dependents();
-  if (P.pdl) griddep_wait();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = P.d_lens[b];
@@ -387,7 +386,7 @@ int launch_mma(const AttnParams& P, cudaStream_t stream) {
   }
   dim3 grid(P.nct, P.n_kv_heads);
   const int rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
-                           P.pdl != 0, P);
+                           false, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

@@ -2,9 +2,7 @@
 //
 //   y[r] (+)= sum_b scale(r,b) * sum_j q(r,b,j) * x[32b+j]
 // ("IV.4: One command buffer per token", "Eight kernels": q8_matvec), for up
-// to three matrices that share x (q|k|v, gate|up), with the decode step's
-// activation transforms (RMSNorm, SiLU*up), residual accumulation and
-// per-CTA argmax partials folded in.
+// to three matrices that share x in one launch.
 //
 // The product reads every weight byte once and does ~2.5 instructions per
 // quant, so at HBM speed it is bound by instruction issue as much as by
@@ -47,29 +45,15 @@ constexpr int kMaxWarps = 20;
 constexpr int kSmallThreads = 17 * 32;              // 16 consumer warps + the producer
 constexpr int kLargeThreads = (kMaxWarps + 1) * 32;  // 20 + 1
 
-// Activations of block column `col` (32 floats) with the launch's transform,
-// as 16 packed pairs; zeros when col is past the row end.
-__device__ __forceinline__ void load_x_col(const RowsParams& P, int col, float inv,
-                                           uint64_t (&x2)[16]) {
+// Activations of block column `col` (32 floats) as 16 packed pairs; zeros
+// when col is past the row end.
+__device__ __forceinline__ void load_x_col(const RowsParams& P, int col, uint64_t (&x2)[16]) {
   const bool ok = col < P.bpr;
   const size_t base = (size_t)col * kQBlock;
   const float4* xp = reinterpret_cast<const float4*>(P.X + base);
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
-    float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok && P.xmode == kXRmsNorm) {
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(P.xw + base) + t);
-      v.x = v.x * inv * wv.x;
-      v.y = v.y * inv * wv.y;
-      v.z = v.z * inv * wv.z;
-      v.w = v.w * inv * wv.w;
-    } else if (ok && P.xmode == kXSiluMul) {
-      const float4 u = __ldg(reinterpret_cast<const float4*>(P.X + base + P.n) + t);
-      v.x = v.x / (1.0f + expf(-v.x)) * u.x;
-      v.y = v.y / (1.0f + expf(-v.y)) * u.y;
-      v.z = v.z / (1.0f + expf(-v.z)) * u.z;
-      v.w = v.w / (1.0f + expf(-v.w)) * u.w;
-    }
+    const float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
     x2[2 * t] = pack2(v.x, v.y);
     x2[2 * t + 1] = pack2(v.z, v.w);
   }
@@ -81,7 +65,7 @@ __device__ __forceinline__ void load_x_col(const RowsParams& P, int col, float i
 // warp runs the same iterations.  part = [row][NS][32] floats, 16-byte
 // aligned rows.
 __device__ __forceinline__ void window_reduce(const RowsParams& P, const float* part, int nrow,
-                                              int NS, int nwarps, int wbeg, float& bv, int& bi) {
+                                              int NS, int nwarps, int wbeg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane & 7;
   for (int r0 = warp * 4; r0 < nrow; r0 += nwarps * 4) {
@@ -104,13 +88,7 @@ __device__ __forceinline__ void window_reduce(const RowsParams& P, const float* 
       int sg = 0;
       while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
       const int ri = vr - (int)P.vbegin[sg];
-      float* y = P.seg[sg].y + ri;
-      const float out = P.accumulate ? (*y + sum) : sum;
-      *y = out;
-      if (!isnan(out) && am_better(out, ri, bv, bi)) {
-        bv = out;
-        bi = ri;
-      }
+      P.seg[sg].y[ri] = sum;
     }
   }
 }
@@ -196,8 +174,7 @@ __device__ int produce_all(const RowsParams& P, const Ring& ring, int v0, int v1
 template <int AM>
 __device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, uint32_t part32,
                                         int v0, int v1, int ci, int rg, int RG, int nwarps,
-                                        uint32_t boff, const uint64_t (&x2)[16], float& bv,
-                                        int& bi) {
+                                        uint32_t boff, const uint64_t (&x2)[16]) {
   const int lane = threadIdx.x & 31;
   const int NS = P.segs_per_row;
   const int n32 = NS * 32;
@@ -253,7 +230,7 @@ __device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, u
       // other buffer was reduced before this barrier, so the next window may
       // overwrite it.
       consumer_sync(nwarps * 32);
-      window_reduce(P, ring.part + buf / 4, wrow, NS, nwarps, wbeg, bv, bi);
+      window_reduce(P, ring.part + buf / 4, wrow, NS, nwarps, wbeg);
       buf = buf ? 0u : buf_bytes;
       wt = 0;
       wrow = 0;
@@ -273,8 +250,6 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
   const int W = (blockDim.x >> 5) - 1;  // consumer warps
   const int NS = P.segs_per_row;
   __shared__ int s_abort;
-  __shared__ float s_f[kMaxWarps + 1];
-  __shared__ int s_i[kMaxWarps + 1];
 
   Ring ring;
   ring.smem = smem;
@@ -295,12 +270,9 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
   }
   __syncthreads();
 
-  float bv = -INFINITY;  // this thread's argmax candidate over the rows it wrote
-  int bi = 0x7fffffff;
   bool ok = true;
   if (warp == W) {
-    // ---- producer warp: weights do not depend on earlier kernels ----
-    if (P.pdl) griddep_launch_dependents();
+    // ---- producer warp ----
     if (lane == 0) {
       const int issued = produce_all(P, ring, v0, v1);
       if (*(volatile int*)&s_abort) {
@@ -311,31 +283,6 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
       }
     }
   } else {
-    if (P.pdl) {
-      griddep_launch_dependents();
-      griddep_wait();  // activations written by the previous kernel are visible from here
-    }
-    // RMSNorm scale of x: the same sum, in the same order, in every CTA.
-    float inv_rms = 1.f;
-    if (P.xmode == kXRmsNorm) {
-      float ss = 0.f;
-      const float4* x4 = reinterpret_cast<const float4*>(P.X);
-      for (int i = threadIdx.x; i < P.n / 4; i += W * 32) {
-        const float4 v = __ldg(x4 + i);
-        ss = fmaf(v.x, v.x, ss);
-        ss = fmaf(v.y, v.y, ss);
-        ss = fmaf(v.z, v.z, ss);
-        ss = fmaf(v.w, v.w, ss);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_f[warp] = ss;
-      consumer_sync(W * 32);
-      float tot = 0.f;
-      for (int w = 0; w < W; ++w) tot += s_f[w];
-      inv_rms = 1.0f / sqrtf(tot / (float)P.n + P.eps);
-    }
-
     // This warp's block column class and row group (W is a multiple of NS).
     const int ci = warp % NS, rg = warp / NS, RG = W / NS;
     int col, col_read;
@@ -350,49 +297,23 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
       col_read = min(col, P.bpr - 1);
     }
     uint64_t x2[16];
-    load_x_col(P, col, inv_rms, x2);
+    load_x_col(P, col, x2);
     const uint32_t boff = (uint32_t)col_read * kQBlockBytes;
     // With an even number of blocks per row every row starts at a multiple
     // of 4 bytes, so all blocks of a paired warp start at 2*(col & 1) mod 4.
     const uint32_t part32 = smem_u32(ring.part);
     if (P.paired && (P.bpr & 1) == 0) {
       if (ci & 1)
-        ok = consume<1>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+        ok = consume<1>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2);
       else
-        ok = consume<0>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+        ok = consume<0>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2);
     } else {
-      ok = consume<2>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2, bv, bi);
+      ok = consume<2>(P, ring, part32, v0, v1, ci, rg, RG, W, boff, x2);
     }
   }
 
   if (!__syncthreads_and(ok && !*(volatile int*)&s_abort)) {
     if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
-    return;
-  }
-  if (P.am_val) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (am_better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      s_f[warp] = bv;
-      s_i[warp] = bi;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w <= W; ++w)
-        if (am_better(s_f[w], s_i[w], bv, bi)) {
-          bv = s_f[w];
-          bi = s_i[w];
-        }
-      P.am_val[blockIdx.x] = bv;
-      P.am_idx[blockIdx.x] = bi;
-    }
   }
 }
 
@@ -460,7 +381,7 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.rows_per_cta = rows_cta;
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   if (grid_out) *grid_out = (int)grid;
-  return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, P.pdl != 0, P);
+  return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, false, P);
 }
 
 }  // namespace q8d

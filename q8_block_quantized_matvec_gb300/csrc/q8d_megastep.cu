@@ -33,7 +33,6 @@
 #include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
 #include "q8d_megastep.cuh"
-#include "q8d_rows.cuh"
 
 namespace q8d {
 

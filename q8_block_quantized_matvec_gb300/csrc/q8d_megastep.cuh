@@ -16,6 +16,10 @@ namespace q8d {
 
 enum MPhaseKind { kPhEmbed = 0, kPhMatvec = 1, kPhAttn = 2, kPhCombine = 3, kPhArgmax = 4 };
 
+// Activations of a matvec phase: as stored, or RMSNorm-ed while staged
+// (x * (1/sqrt(mean(x^2) + eps)) * xw).
+enum MXMode { kXPlain = 0, kXRmsNorm = 1 };
+
 constexpr int kMsWarps = 20;                  // consumer warps per CTA
 constexpr int kMsThreads = (kMsWarps + 1) * 32;  // + the producer warp
 constexpr int kMsRegion = 48 * 1024;           // shared region: window partials / attention

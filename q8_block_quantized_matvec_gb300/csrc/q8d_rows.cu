@@ -86,10 +86,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Loads the activation pairs of vectors v0..v0+MV-1 for block columns
-// seg*32K + k*32 + lane into registers (zeros past the row end / m),
-// applying the launch's activation transform (m == 1 for the transforms).
+// seg*32K + k*32 + lane into registers (zeros past the row end / m).
 template <int K, int MV>
-__device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int lane, float inv,
+__device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int lane,
                                        uint64_t (&xr)[MV][K][16]) {
 #pragma unroll
   for (int i = 0; i < MV; ++i) {
@@ -101,29 +100,12 @@ __device__ __forceinline__ void load_x(const RowsParams& P, int v0, int seg, int
       const float4* xp = reinterpret_cast<const float4*>(P.X + base);
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok && P.xmode == kXRmsNorm) {
-          const float4 wv = __ldg(reinterpret_cast<const float4*>(P.xw + base) + t);
-          v.x = v.x * inv * wv.x;
-          v.y = v.y * inv * wv.y;
-          v.z = v.z * inv * wv.z;
-          v.w = v.w * inv * wv.w;
-        } else if (ok && P.xmode == kXSiluMul) {
-          const float4 u = __ldg(reinterpret_cast<const float4*>(P.X + base + P.n) + t);
-          v.x = v.x / (1.0f + expf(-v.x)) * u.x;
-          v.y = v.y / (1.0f + expf(-v.y)) * u.y;
-          v.z = v.z / (1.0f + expf(-v.z)) * u.z;
-          v.w = v.w / (1.0f + expf(-v.w)) * u.w;
-        }
+        const float4 v = ok ? __ldg(xp + t) : make_float4(0.f, 0.f, 0.f, 0.f);
         xr[i][k][2 * t] = pack2(v.x, v.y);
         xr[i][k][2 * t + 1] = pack2(v.z, v.w);
       }
     }
   }
-}
-
-__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
 }
 
 // Bounded wait that gives up at once when another warp of the CTA already
@@ -227,36 +209,7 @@ __global__ void __launch_bounds__(W * 32, 2)
     }
   };
   const bool producer = (warp == 0 && lane == 0);
-  // Weights do not depend on earlier kernels: start streaming them first.
   if (producer) produce(P.nstages);
-  if (P.pdl) {
-    griddep_launch_dependents();
-    griddep_wait();  // activations written by the previous kernel are visible now
-  }
-  float am_bv = -INFINITY;  // this thread's argmax candidate over written rows
-  int am_bi = 0x7fffffff;
-  // RMSNorm of x (the same sum, in the same order, in every CTA).
-  __shared__ float red_ss[kWarps];
-  float inv_rms = 1.f;
-  if (P.xmode == kXRmsNorm) {
-    float ss = 0.f;
-    const float4* x4 = reinterpret_cast<const float4*>(P.X);
-    for (int i = threadIdx.x; i < P.n / 4; i += kThreads) {
-      const float4 v = __ldg(x4 + i);
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red_ss[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += red_ss[w];
-    inv_rms = 1.0f / sqrtf(tot / (float)P.n + P.eps);
-  }
   {
     // ---------------- consumers ----------------
     const bool x_static = (NS <= kWarps) && (P.m <= MV);
@@ -267,7 +220,7 @@ __global__ void __launch_bounds__(W * 32, 2)
     const bool active = (NS <= kWarps) ? (warp < NS * RG) : true;
 
     uint64_t xr[MV][K][16];
-    if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, inv_rms, xr);
+    if (x_static && active) load_x<K, MV>(P, 0, my_seg0, lane, xr);
 
     {
     long long cur = v0;
@@ -284,7 +237,7 @@ __global__ void __launch_bounds__(W * 32, 2)
         const int first = ((my_rg - t.vrow0) % RG + RG) % RG;
         for (int v0m = 0; v0m < P.m; v0m += MV) {
           for (int seg = my_seg0; seg < NS; seg += seg_step) {
-            if (!x_static) load_x<K, MV>(P, v0m, seg, lane, inv_rms, xr);
+            if (!x_static) load_x<K, MV>(P, v0m, seg, lane, xr);
             for (int rl = first; rl < t.rows; rl += RG) {
               float acc[MV];
 #pragma unroll
@@ -322,52 +275,14 @@ __global__ void __launch_bounds__(W * 32, 2)
     if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
     return;
   }
-  float bv = am_bv;
-  int bi = am_bi;
-  {
-    for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
-      const int rc = e / P.m, m = e % P.m;
-      float sum = 0.f;
-      for (int seg = 0; seg < NS; ++seg) sum += part[((size_t)rc * NS + seg) * P.m + m];
-      const long long vr = v0 + rc;
-      int sg = 0;
-      while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
-      float* y = P.seg[sg].y + (size_t)m * P.ldy + (vr - P.vbegin[sg]);
-      const float out = P.accumulate ? (*y + sum) : sum;
-      *y = out;
-      const int ri = (int)(vr - P.vbegin[sg]);
-      if (!isnan(out) && am_better(out, ri, bv, bi)) {
-        bv = out;
-        bi = ri;
-      }
-    }
-  }
-  if (P.am_val) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (am_better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    __shared__ float s_bv[kWarps];
-    __shared__ int s_bi[kWarps];
-    if (lane == 0) {
-      s_bv[warp] = bv;
-      s_bi[warp] = bi;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kWarps; ++w)
-        if (am_better(s_bv[w], s_bi[w], bv, bi)) {
-          bv = s_bv[w];
-          bi = s_bi[w];
-        }
-      P.am_val[blockIdx.x] = bv;
-      P.am_idx[blockIdx.x] = bi;
-    }
+  for (int e = threadIdx.x; e < rows_cta * P.m; e += kThreads) {
+    const int rc = e / P.m, m = e % P.m;
+    float sum = 0.f;
+    for (int seg = 0; seg < NS; ++seg) sum += part[((size_t)rc * NS + seg) * P.m + m];
+    const long long vr = v0 + rc;
+    int sg = 0;
+    while (sg + 1 < P.nseg && vr >= P.vbegin[sg + 1]) ++sg;
+    P.seg[sg].y[(size_t)m * P.ldy + (vr - P.vbegin[sg])] = sum;
   }
 }
 
@@ -412,8 +327,7 @@ int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   smem = smem_for(rows_cta);
   if (grid_out) *grid_out = (int)grid;
-  return launch_ex(fn, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, P.pdl != 0,
-                   P);
+  return launch_ex(fn, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, false, P);
 }
 
 }  // namespace
@@ -427,7 +341,6 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   }
   if (p_total == 0) return Q8D_OK;
   if (P.n == 0) {
-    if (P.accumulate) return Q8D_OK;
     for (int s = 0; s < P.nseg; ++s) {
       if (!P.seg[s].p) continue;
       fill_zero_kernel<<<std::min(1024, (P.m * P.seg[s].p + 255) / 256), 256, 0, stream>>>(
@@ -453,7 +366,6 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   const int MV = P.m == 1 ? 1 : 2;
   P.segs_per_row = NS;
   constexpr int W = kWarpsSmall;
-  if ((P.xmode != kXPlain || P.am_val) && (P.m != 1 || NS > W)) return Q8D_EUNSUPPORTED;
 
   // Stages of ~36 KB of whole rows (quads per row group where they fit).
   const int RG = NS <= W ? W / NS : 1;

@@ -1,5 +1,4 @@
-// Parameters of the CUDA-core Q8_0 row kernels (matvec, small-M, and the
-// multi-matrix launches the decode step uses).
+// Parameters of the CUDA-core Q8_0 row kernels (matvec and small-M).
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,20 +22,7 @@ struct RowsParams {
   int ldx;
   int ldy;
   int m;               // activation rows (1 = matvec)
-  int accumulate;      // 1: Y += result (residual add), 0: Y = result
   int* d_err;          // device error word or nullptr
-  // Activation transform applied while x is loaded (m == 1 only):
-  //   kXPlain   x as given
-  //   kXRmsNorm x * (1/sqrt(mean(x^2) + eps)) * xw          (RMSNorm)
-  //   kXSiluMul silu(X[k]) * X[n + k]                        (SwiGLU gate)
-  int xmode;
-  const float* xw;
-  float eps;
-  // Per-CTA argmax of the written rows (m == 1): value and row index at
-  // [blockIdx.x], ties to the lower index, NaN never wins; or nullptr.
-  float* am_val;
-  int* am_idx;
-  int pdl;             // launched as a programmatic dependent of the previous kernel
   // filled by the planner
   int bpr;
   long long row_bytes;
@@ -50,8 +36,6 @@ struct RowsParams {
   int win_rows;            // rows per window buffer (win * rows_per_tile)
   int np;                  // row pairs per warp per tile
 };
-
-enum { kXPlain = 0, kXRmsNorm = 1, kXSiluMul = 2 };
 
 // Plans tiles/stages and launches the kernel on `stream`.  Returns a status;
 // *grid_out (if given) receives the number of CTAs launched.

@@ -15,7 +15,6 @@
 
 #include "q8d_internal.cuh"
 #include "q8d_megastep.cuh"
-#include "q8d_rows.cuh"
 
 namespace q8d {
 namespace {
