@@ -205,8 +205,13 @@ __device__ __forceinline__ bool consume(const RowsParams& P, const Ring& ring, u
     int rl = rg;
 #pragma unroll 1
     for (int j = 0; j < P.np; ++j) {
-      const float va = block_dot<AM>(o, x2);
-      const float vb = block_dot<AM>(o + step, x2);
+      // both rows' words first: the two decodes are independent work for
+      // the scheduler to interleave
+      uint32_t wa[9], wb[9];
+      block_words(o, wa);
+      block_words(o + step, wb);
+      const float va = block_dot_words<AM>(wa, o, x2);
+      const float vb = block_dot_words<AM>(wb, o + step, x2);
       if (rl < rows) sts32(d, va);
       if (rl + RG < rows) sts32(d + pstep, vb);
       o += 2 * step;

@@ -34,15 +34,10 @@ __device__ __forceinline__ void sts32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// scale * sum_j q_j x_j for the block at shared-memory byte address `o`
-// (2-byte aligned).  Alignment modes: AM = 1, the block starts at byte 2 of
-// a word (scale = upper half, quants = the next 8 words); AM = 0, it starts
-// at a word (scale = lower half, quants from byte 2 on); AM = 2, decided
-// per lane from o.
-template <int AM>
-__device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16]) {
+// The nine shared-memory words holding the block at byte address `o`
+// (2-byte aligned): the 34 bytes of the block start in the first word.
+__device__ __forceinline__ void block_words(uint32_t o, uint32_t (&a)[9]) {
   const uint32_t w0 = o & ~3u;
-  uint32_t a[9];
   a[0] = lds32<0>(w0);
   a[1] = lds32<4>(w0);
   a[2] = lds32<8>(w0);
@@ -52,6 +47,16 @@ __device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16])
   a[6] = lds32<24>(w0);
   a[7] = lds32<28>(w0);
   a[8] = lds32<32>(w0);
+}
+
+// scale * sum_j q_j x_j for the block at byte address `o` whose words are
+// `a` (block_words).  Alignment modes: AM = 1, the block starts at byte 2
+// of a word (scale = upper half, quants = the next 8 words); AM = 0, it
+// starts at a word (scale = lower half, quants from byte 2 on); AM = 2,
+// decided per lane from o.
+template <int AM>
+__device__ __forceinline__ float block_dot_words(uint32_t (&a)[9], uint32_t o,
+                                                 const uint64_t (&x2)[16]) {
   float sc;
   uint32_t shift = 16;
   if constexpr (AM == 2) {
@@ -96,6 +101,14 @@ __device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16])
   float lo, hi;
   unpack2(t, lo, hi);
   return sc * (lo + hi);
+}
+
+// scale * sum_j q_j x_j for the block at shared-memory byte address `o`.
+template <int AM>
+__device__ __forceinline__ float block_dot(uint32_t o, const uint64_t (&x2)[16]) {
+  uint32_t a[9];
+  block_words(o, a);
+  return block_dot_words<AM>(a, o, x2);
 }
 
 __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
