@@ -114,8 +114,11 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
 int q8d_kv_append(const float* k, const float* v, void* kcache, void* vcache, int kv_dtype,
                   int kv_width, int cap, const int* d_pos, int* d_err, void* stream);
 
-/* Bytes of scratch q8d_gqa_decode_attn needs for these sizes (split-K
- * partials).  max_len is the largest length any call will see (<= cap). */
+/* Bytes of scratch q8d_gqa_decode_attn needs for these sizes: the split-K
+ * partials {m, l, O} of up to a fixed number of chunk slots per sequence
+ * and query head (chunk CTAs are split over a batch in proportion to the
+ * lengths, on the device).  Pass the cache capacity `cap` as max_len: the
+ * call checks ws_bytes against the size for its cap. */
 size_t q8d_gqa_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len);
 
 /* ------------------------------------------------------------------------
