@@ -17,9 +17,10 @@
 //    non-coherent L1 / read-only path.
 //  * Matvec phases use the layout of the standalone matvec kernel: warp
 //    pairs own the even / odd block columns of 64-column segments, the
-//    lane's 32 activations in registers (RMSNorm or SiLU*up applied while
-//    loading), lane partials folded within the warp and reduced in
-//    double-buffered row windows.
+//    lane's 32 activations in registers (RMSNorm applied while loading),
+//    lane partials folded within the warp and reduced in double-buffered
+//    row windows; the gate|up phase forms SiLU(gate) * up as it writes the
+//    up rows.
 //  * Attention: one CTA per (KV head, context chunk) computes the G query
 //    heads' online-softmax partial over its chunk on CUDA cores (f32); the
 //    CTA owning row L-1 applies bias / QK-norm / RoPE to the new k, v,
