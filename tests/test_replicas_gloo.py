@@ -51,3 +51,21 @@ def test_reference_arm_other_ranks_do_nothing(capsys):
         context = 2048
     bench.run_reference(A(), rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_runs_the_requested_steps(capsys):
+    """Rank 0 of the reference arm times W untimed and exactly K timed oracle
+    sample steps and prints one JSON line with K, W and the sample."""
+    import json
+
+    class A:
+        model = "qwen2.5-0.5b"
+        context = 64
+        steps = 2
+        warmup = 1
+        gpus = 1
+    bench.run_reference(A(), rank=0, world=1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert "2 repetitions" in line["cpu_baseline"]["sample"]
