@@ -452,7 +452,8 @@ int attn_combine_launch(const AttnParams& P, cudaStream_t stream) {
 }
 
 int attn_ctas_per_head(int batch, int n_kv_heads, int max_len) {
-  const int per_head = (4 * sm_count() + n_kv_heads - 1) / n_kv_heads;
+  // two per SM in all: one wave at the f16 kernel's two resident CTAs per SM
+  const int per_head = (2 * sm_count() + n_kv_heads - 1) / n_kv_heads;
   // no more than the sequences could use at one chunk per kMinChunk rows
   const long long by_len = (long long)batch * ((std::max(max_len, 1) + kMinChunk - 1) / kMinChunk);
   return (int)std::max<long long>(batch, std::min<long long>(per_head, by_len));

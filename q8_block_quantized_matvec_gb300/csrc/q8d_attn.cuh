@@ -88,7 +88,7 @@ __device__ __forceinline__ bool attn_chunk_of(const AttnParams& P, int k, int& b
   return false;
 }
 
-// Chunk CTAs per KV head (grid.x): about four per SM in all, at least one
+// Chunk CTAs per KV head (grid.x): about two per SM in all, at least one
 // per sequence, at most one per kMinChunk rows of every cache.
 int attn_ctas_per_head(int batch, int n_kv_heads, int max_len);
 // Workspace chunk slots per (sequence, KV head): up to 4x a sequence's even
