@@ -294,6 +294,15 @@ def run_profile(args):
             q8d.q8d_matvec(x, w, y, n, p)
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
+    elif args.profile in ("mma16", "mma64"):
+        m = 16 if args.profile == "mma16" else 64
+        w, x, y, n, p = small_m_inputs(m)
+        q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStart()
+        q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStop()
     elif args.profile == "attn_stress":
         lens, args_, err = stress_inputs(q8d, 28, 4, 128)
         q8d.q8d_gqa_decode_attn(*args_)
@@ -377,6 +386,52 @@ def attn_stress(q8d, H, Hk, D, reps, stream, flush, rank=0):
             "l2": "256 MB flush before each launch"}
 
 
+# ---------------------------------------------------------------------------- small M
+SMALL_M = (1, 4, 16, 64)
+
+
+def small_m_inputs(m, rank=0):
+    """The 7B gate/up shape (3584 -> 18944, 72 MB of Q8_0) against m
+    activation rows."""
+    import torch
+
+    import synth
+    n, p = 3584, 18944
+    w = synth.q8_matrix_torch(rank, "smallm.w", p, n)
+    x = synth.normal_torch(rank, f"smallm.x{m}", (m, n), torch.float32)
+    y = torch.empty(m, p, device="cuda")
+    return w, x, y, n, p
+
+
+def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
+    """q8d_matmul_small_m on the 7B gate/up shape at m = 1, 4, 16, 64 (m >= 16
+    on tcgen05), L2 flushed before each timed launch; GB/s of algorithmic
+    bytes (weights once, X and Y)."""
+    import torch
+    out = {}
+    ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for m in SMALL_M:
+        w, x, y, n, p = small_m_inputs(m, rank)
+        times = []
+        with torch.cuda.stream(stream):
+            for rep in range(max(reps, 3) + 1):
+                flush.fill_(rep & 0xFF)
+                ev[0].record(stream)
+                q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p, stream)
+                ev[1].record(stream)
+                ev[1].synchronize()
+                if rep:
+                    times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+        t = statistics.median(times)
+        nbytes = p * n // 32 * 34 + 4 * m * n + 4 * m * p
+        out[f"m{m}"] = {"us": t * 1e6, "GB_s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / hbm,
+                        "TFLOP_s": 2.0 * m * n * p / t / 1e12,
+                        "kernel": "q8_mma_kernel (tcgen05)" if m >= 16 else "q8_gemv_kernel / q8_rows_kernel"}
+        del w, x, y
+    out["shape"] = "3584 -> 18944 (7B gate/up), L2 flushed before each launch"
+    return out
+
+
 # ---------------------------------------------------------------------------- replicas
 def replica_throughput(local_seconds: float, steps: int, dist=None, device="cuda") -> float:
     """Whole-job steps per second of independent replicas: every rank ran
@@ -429,7 +484,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=3)
     ap.add_argument("--profile",
-                    choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "matvec_sweep"],
+                    choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "mma16", "mma64",
+                             "matvec_sweep"],
                     default=None,
                     help="run a short fixed workload between cudaProfilerStart/Stop for ncu "
                          "(--profile-from-start off) and print no JSON")
@@ -580,6 +636,8 @@ def main():
         if shape.kv_dtype == synth.KV_F16 else None
     if stress is not None:
         stress["frac_of_peak"] = stress["GB_s"] / hbm
+    small_m = small_m_leg(q8d, args.kernel_reps, stream, flush, hbm, rank) \
+        if shape.name == "qwen2.5-7b" else None
 
     # dominant kernel: the persistent step kernel, one launch per step
     step_b = statistics.mean(step_bytes(shape, ctx + s, esize) for s in range(args.steps))
@@ -618,6 +676,7 @@ def main():
                                     "us_per_layer": at_time / shape.n_layers * 1e6,
                                     "context": ctx, "l2": "256 MB flush between layers"},
                 "gqa_decode_attn_batch8_ragged": stress,
+                "q8_matmul_small_m": small_m,
             },
             "e2e": e2e,
             "cpu_baseline": cpu,

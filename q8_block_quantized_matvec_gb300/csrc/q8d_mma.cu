@@ -12,7 +12,11 @@
 //    partials through distributed shared memory in rank order
 //    (deterministic, no global scratch, no atomics).
 //  * Raw Q8_0 bytes (8 blocks = 272 bytes per row per 256-element chunk) are
-//    streamed with 1-D bulk copies into a ring of stages.  All threads
+//    streamed into a ring of stages, a chunk's 128 rows by one 2-D tensor
+//    copy (TMA: the rows are a weight-row stride apart in global memory;
+//    the 272 bytes are 68 32-bit elements, so the box stays within TMA's 256
+//    elements per dimension and every x coordinate is a multiple of 16
+//    bytes; rows past the matrix are zero-filled).  All threads
 //    dequantise scale*q exactly in f32, round once to bf16 and store the A
 //    tile in the canonical K-major 128-byte-swizzled layout; X rows are
 //    rounded to bf16 into the B tile the same way.
@@ -22,6 +26,7 @@
 //    be overwritten.  The epilogue reads TMEM with tcgen05.ld.
 // Accuracy: one bf16 rounding of each weight and activation, f32
 // accumulation: |error| <= ~2^-8 * sum|terms| per output.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,8 +44,10 @@ constexpr int kRawStage = kM * kRawRow;         // 34816 bytes
 constexpr int kAtomBytes = kM * 128;            // one 64-element K atom of A
 constexpr int kATile = 4 * kAtomBytes;          // 65536 bytes
 constexpr int kMaxN = 128;
+constexpr int kBGroup = 4;                      // B-tile pieces a thread loads at once
 
 struct MmaParams {
+  CUtensorMap wmap;  // the weights as [p][row_bytes / 4] 32-bit elements, box [128][68]
   const float* X;
   int ldx;
   const uint8_t* w;
@@ -130,7 +137,17 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c, int atom_bytes) {
   return (uint32_t)(atom * atom_bytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const MmaParams P) {
+// 2-D tensor copy of the box at element (x, y) of the map into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_constant__ MmaParams P) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled atoms
   const uint32_t base_s = smem_u32(smem_raw);
@@ -170,16 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const MmaParams P) 
   const uint64_t pol = policy_evict_first();
   const int valid_rows = min(kM, P.p - r0);
 
-  auto issue = [&](int i) {  // warp 0
-    if (i >= nloc) return;
+  auto issue = [&](int i) {  // warp 0: one tensor copy of the chunk's 128 rows
+    if (i >= nloc || lane != 0) return;
     const int c = c_begin + i;
     uint64_t* bar = &raw_bar[i % P.raw_stages];
     uint8_t* dst = raw + (size_t)(i % P.raw_stages) * kRawStage;
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(valid_rows * kRawRow));
-    __syncwarp();
-    for (int rr = lane; rr < valid_rows; rr += 32)
-      bulk_g2s(dst + rr * kRawRow, P.w + (long long)(r0 + rr) * P.row_bytes + (long long)c * kRawRow,
-               kRawRow, bar, pol);
+    mbar_arrive_expect_tx(bar, (uint32_t)kRawStage);  // the whole box (zero-filled past p)
+    tma_load_2d(dst, &P.wmap, c * (kRawRow / 4), r0, bar, pol);
   };
   if (warp == 0)
     for (int i = 0; i < P.raw_stages; ++i) issue(i);
@@ -188,21 +202,48 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const MmaParams P) 
                          ((uint32_t)(kM >> 4) << 24);
   bool ok = true;
 
-  for (int i = 0; i < nloc; ++i) {
-    const int c = c_begin + i;
-    // (a) the previous chunk's MMAs must have finished reading A and B
-    if (i > 0) ok = ok && mbar_wait(mma_bar, (uint32_t)(i - 1) & 1u);
-    // (b) B tile: X[0..m) rows, K elements [c*256, c*256+256), rounded to bf16
-    for (int e = tid; e < P.npad * 32; e += kThreads) {
+  // B tile pieces: thread tid takes pieces tid + k * kThreads (k < nit), 8
+  // K elements of one X row each, loaded kBGroup at a time (one L2 round
+  // trip per group) before they are rounded and stored
+  const int nit = P.npad * 32 / kThreads;
+  auto b_load = [&](int c, int k0, float4 (&va)[kBGroup], float4 (&vb)[kBGroup]) {
+#pragma unroll
+    for (int u = 0; u < kBGroup; ++u) {
+      const int e = tid + (k0 + u) * kThreads;
       const int row = e & 7 | ((e >> 8) << 3), cch = (e >> 3) & 31;  // 8 rows per quarter-warp
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < P.m) {
+      va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k0 + u < nit && row < P.m) {
         const float4* xp = reinterpret_cast<const float4*>(P.X + (long long)row * P.ldx +
                                                            (long long)c * kKC + cch * 8);
-        const float4 a = __ldg(xp), b = __ldg(xp + 1);
-        v = make_uint4(bf16x2(a.x, a.y), bf16x2(a.z, a.w), bf16x2(b.x, b.y), bf16x2(b.z, b.w));
+        va[u] = __ldg(xp);
+        vb[u] = __ldg(xp + 1);
       }
+    }
+  };
+  auto b_store = [&](int k0, const float4 (&va)[kBGroup], const float4 (&vb)[kBGroup]) {
+#pragma unroll
+    for (int u = 0; u < kBGroup; ++u) {
+      if (k0 + u >= nit) break;
+      const int e = tid + (k0 + u) * kThreads;
+      const int row = e & 7 | ((e >> 8) << 3), cch = (e >> 3) & 31;
+      const uint4 v = make_uint4(bf16x2(va[u].x, va[u].y), bf16x2(va[u].z, va[u].w),
+                                 bf16x2(vb[u].x, vb[u].y), bf16x2(vb[u].z, vb[u].w));
       *reinterpret_cast<uint4*>(B + sw128_offset(row, cch, b_atom)) = v;
+    }
+  };
+
+  for (int i = 0; i < nloc; ++i) {
+    const int c = c_begin + i;
+    // (b) B tile: X[0..m) rows, K elements [c*256, c*256+256), rounded to
+    // bf16; the first group's loads are in flight while (a) waits
+    float4 va[kBGroup], vb[kBGroup];
+    b_load(c, 0, va, vb);
+    // (a) the previous chunk's MMAs must have finished reading A and B
+    if (i > 0) ok = ok && mbar_wait(mma_bar, (uint32_t)(i - 1) & 1u);
+    b_store(0, va, vb);
+    for (int k0 = kBGroup; k0 < nit; k0 += kBGroup) {
+      b_load(c, k0, va, vb);
+      b_store(k0, va, vb);
     }
     // (c) raw weight bytes of this chunk
     ok = ok && mbar_wait(&raw_bar[i % P.raw_stages], (uint32_t)(i / P.raw_stages) & 1u);
@@ -308,11 +349,47 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const MmaParams P) 
 
 }  // namespace
 
+// cuTensorMapEncodeTiled from the driver (looked up once, no link-time
+// dependency on libcuda); null if unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
 // Runs the tensor-core path; Q8D_EUNSUPPORTED for shapes it does not take
-// (n not a multiple of 256), which the caller routes to the CUDA-core path.
+// (n not a multiple of 256, or no tensor-map encoder), which the caller
+// routes to the CUDA-core path.
 int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int ldy, int m, int n,
                        int p, cudaStream_t stream) {
   if (n % kKC != 0) return Q8D_EUNSUPPORTED;
+  const EncodeTiledFn encode = encode_tiled();
+  if (!encode) return Q8D_EUNSUPPORTED;
+  // the weights as p rows of row_bytes / 4 32-bit elements (row_bytes is a
+  // multiple of 272, so of 16), box = one chunk of 128 rows
+  const long long row_bytes = (long long)(n / kQBlock) * kQBlockBytes;
+  CUtensorMap wmap;
+  {
+    const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)p};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(kRawRow / 4), (cuuint32_t)kM};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(w), gdim, gstride, box,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return Q8D_EUNSUPPORTED;
+  }
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -327,6 +404,7 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
   const int sms = sm_count();
   for (int i0 = 0; i0 < m; i0 += kMaxN) {
     MmaParams P{};
+    P.wmap = wmap;
     P.m = std::min(kMaxN, m - i0);
     P.npad = (P.m + 15) / 16 * 16;
     P.X = X + (long long)i0 * ldx;
@@ -337,7 +415,7 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
     P.n = n;
     P.p = p;
     P.nchunks = nchunks;
-    P.row_bytes = (long long)(n / kQBlock) * kQBlockBytes;
+    P.row_bytes = row_bytes;
     P.ksplit = std::max(1, std::min({8, sms / row_tiles, nchunks}));
     const int fixed = kATile + 4 * P.npad * 128 + 1024 + 64;
     P.raw_stages = (fixed + 3 * kRawStage <= 227 * 1024) ? 3 : 2;
