@@ -36,7 +36,7 @@
 namespace q8d {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kM = 128;                         // weight rows per CTA (MMA M)
 constexpr int kKC = 256;                        // K elements per chunk
 constexpr int kRawRow = (kKC / kQBlock) * kQBlockBytes;  // 272 bytes
