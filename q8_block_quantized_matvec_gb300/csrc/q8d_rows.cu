@@ -145,7 +145,7 @@ __device__ __forceinline__ Tile tile_at(const RowsParams& P, long long cur, long
 // per-(row, segment) partials wait in shared memory and are reduced in a
 // fixed order once, at the end, so no CTA-wide barrier runs per tile.
 template <int MV, int W>
-__global__ void __launch_bounds__(W * 32, 2)
+__global__ void __launch_bounds__(W * 32, MV >= 4 ? 1 : 2)
     q8_rows_kernel(const RowsParams P) {
   constexpr int K = 1;
   constexpr int kWarps = W;
@@ -363,7 +363,9 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   // it), 8-warp CTAs.  Rows of up to 8 segments keep the activations in
   // registers; longer rows reload them per segment and tile.
   const int NS = (P.bpr + 31) / 32;
-  const int MV = P.m == 1 ? 1 : 2;
+  // activation rows held in registers per pass (four: one CTA per SM, up
+  // to 255 registers a thread; each block is decoded once for all of them)
+  const int MV = P.m == 1 ? 1 : (P.m == 2 ? 2 : 4);
   P.segs_per_row = NS;
   constexpr int W = kWarpsSmall;
 
@@ -375,8 +377,9 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.stage_bytes = (int)(((R * P.row_bytes + 32 + 127) / 128) * 128);
   const int ring = W == kWarpsSmall ? 96 * 1024 : 160 * 1024;  // per-CTA stage budget
   P.nstages = std::max(2, std::min(8, ring / P.stage_bytes));
-  return MV == 1 ? launch_rows<1, kWarpsSmall>(P, R, stream, grid_out)
-                 : launch_rows<2, kWarpsSmall>(P, R, stream, grid_out);
+  if (MV == 1) return launch_rows<1, kWarpsSmall>(P, R, stream, grid_out);
+  if (MV == 2) return launch_rows<2, kWarpsSmall>(P, R, stream, grid_out);
+  return launch_rows<4, kWarpsSmall>(P, R, stream, grid_out);
 }
 
 }  // namespace q8d
