@@ -232,19 +232,22 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
     }
   };
 
+  // the first group of chunk i's B pieces is loaded during chunk i - 1 (all
+  // of a thread's pieces for m <= 64): its L2 latency overlaps the previous
+  // chunk's dequantisation and MMAs
+  float4 va[kBGroup], vb[kBGroup];
+  if (nloc > 0) b_load(c_begin, 0, va, vb);
   for (int i = 0; i < nloc; ++i) {
     const int c = c_begin + i;
-    // (b) B tile: X[0..m) rows, K elements [c*256, c*256+256), rounded to
-    // bf16; the first group's loads are in flight while (a) waits
-    float4 va[kBGroup], vb[kBGroup];
-    b_load(c, 0, va, vb);
     // (a) the previous chunk's MMAs must have finished reading A and B
     if (i > 0) ok = ok && mbar_wait(mma_bar, (uint32_t)(i - 1) & 1u);
+    // (b) B tile: X[0..m) rows, K elements [c*256, c*256+256), rounded to bf16
     b_store(0, va, vb);
     for (int k0 = kBGroup; k0 < nit; k0 += kBGroup) {
       b_load(c, k0, va, vb);
       b_store(k0, va, vb);
     }
+    if (i + 1 < nloc) b_load(c + 1, 0, va, vb);
     // (c) raw weight bytes of this chunk
     ok = ok && mbar_wait(&raw_bar[i % P.raw_stages], (uint32_t)(i / P.raw_stages) & 1u);
     if (!__syncthreads_and(ok)) break;
