@@ -238,6 +238,16 @@ int q8d_step_launch(q8d_step* step, void* stream);
  * limit ran out. */
 int q8d_step_status(q8d_step* step, void* stream, int timeout_ms, int* err);
 
+/* Sets how many polls a grid-wide barrier wait inside the step kernel makes
+ * before the step gives up (polls == 0 restores the default, 2^21 polls,
+ * about a second).  On expiry the step sets Q8D_DERR_WAIT in the error
+ * word, every CTA of the step leaves at its next barrier, the remaining
+ * phases are skipped (the token and position are not advanced) and the
+ * CUDA context stays usable.  The value is written in stream order on
+ * `stream` and applies to later launches.  A small value is a way to check
+ * that a caller's error handling sees an abandoned step. */
+int q8d_step_set_wait_limit(q8d_step* step, unsigned polls, void* stream);
+
 /* Number of kernel nodes one launch runs. */
 int q8d_step_kernel_count(const q8d_step* step);
 

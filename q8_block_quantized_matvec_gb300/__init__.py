@@ -94,6 +94,8 @@ def lib():
         L.q8d_step_launch.restype = i32
         L.q8d_step_status.argtypes = [vp, vp, i32, C.POINTER(i32)]
         L.q8d_step_status.restype = i32
+        L.q8d_step_set_wait_limit.argtypes = [vp, C.c_uint, vp]
+        L.q8d_step_set_wait_limit.restype = i32
         L.q8d_step_kernel_count.argtypes = [vp]
         L.q8d_step_kernel_count.restype = i32
         L.q8d_step_logits.argtypes = [vp]
@@ -205,6 +207,10 @@ class Step:
         _check(lib().q8d_step_status(self.handle, _stream(stream), int(timeout_ms), C.byref(err)),
                "q8d_step_status")
         return err.value
+
+    def set_wait_limit(self, polls: int, stream=None) -> int:
+        return _check(lib().q8d_step_set_wait_limit(self.handle, int(polls), _stream(stream)),
+                      "q8d_step_set_wait_limit")
 
     def kernel_count(self) -> int:
         return lib().q8d_step_kernel_count(self.handle)

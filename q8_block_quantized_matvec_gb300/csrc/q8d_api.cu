@@ -6,7 +6,10 @@
 #include <chrono>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+#include <set>
 #include <thread>
+#include <utility>
 
 #include "q8d_attn.cuh"
 #include "q8d_internal.cuh"
@@ -24,6 +27,25 @@ int record_cuda(cudaError_t e) {
 int check_launch() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? Q8D_OK : record_cuda(e);
+}
+
+int configure_kernel(const void* fn, int smem_bytes, bool max_carveout) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return record_cuda(ge);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({fn, dev})) return Q8D_OK;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (max_carveout) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  done.insert({fn, dev});
+  return Q8D_OK;
 }
 
 int sm_count() {

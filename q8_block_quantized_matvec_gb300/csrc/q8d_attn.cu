@@ -417,16 +417,10 @@ template <int D, typename KT, int GMAX>
 int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
   using C = AttnCfg<D, KT, GMAX>;
   auto fn = gqa_split_kernel<D, KT, GMAX>;
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return record_cuda(e);
-    configured[dev] = true;
-  }
+  int rc = configure_kernel(reinterpret_cast<const void*>(fn), C::kSmem, false);
+  if (rc) return rc;
   dim3 grid(P.nct, P.n_kv_heads);
-  const int rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, false, P);
+  rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, false, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

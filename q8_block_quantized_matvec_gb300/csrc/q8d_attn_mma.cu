@@ -375,17 +375,10 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
 template <int D>
 int launch_mma(const AttnParams& P, cudaStream_t stream) {
   using C = MCfg<D>;
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_mma_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return record_cuda(e);
-    configured[dev] = true;
-  }
+  int rc = configure_kernel(reinterpret_cast<const void*>(gqa_mma_kernel<D>), C::kSmem, false);
+  if (rc) return rc;
   dim3 grid(P.nct, P.n_kv_heads);
-  const int rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
+  rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
                            false, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);

@@ -364,17 +364,8 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
 
   const bool small = (W + 1) * 32 <= kSmallThreads;
   void (*fn)(const RowsParams) = small ? q8_gemv_kernel<kSmallThreads> : q8_gemv_kernel<kLargeThreads>;
-  static int configured[64][2] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev][small]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return record_cuda(e);
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return record_cuda(e);
-    configured[dev][small] = 1;
-  }
+  const int rc = configure_kernel(reinterpret_cast<const void*>(fn), 220 * 1024, true);
+  if (rc) return rc;
   int occ = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, (W + 1) * 32, (size_t)smem);
   if (e != cudaSuccess) return record_cuda(e);

@@ -25,6 +25,11 @@ constexpr uint32_t kWaitLimit = 1u << 24;
 int record_cuda(cudaError_t e);  // stores e for q8d_last_cuda_error, returns Q8D_ECUDA
 int sm_count();                  // SMs of the current device (cached per device)
 int check_launch();              // cudaGetLastError -> status
+// Sets a kernel's dynamic shared-memory limit to smem_bytes (and, with
+// max_carveout, prefers the largest shared-memory carveout) the first time
+// it is called for that kernel on the current device.  Thread-safe; returns
+// a status (Q8D_ECUDA if cudaGetDevice or an attribute call fails).
+int configure_kernel(const void* fn, int smem_bytes, bool max_carveout);
 // Polls `ev` for at most timeout_ms (<= 0: 10 s); then *dst = *src.
 int wait_event_bounded(cudaEvent_t ev, int timeout_ms, const int* src, int* dst);
 

@@ -44,7 +44,6 @@ using namespace mv;
 constexpr int kW = kMsWarps;
 constexpr int kCT = kW * 32;  // consumer threads
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kBarSpin = 1u << 21;  // grid barrier polls (L2 round trips: ~1 s)
 constexpr int kMaxStages = 8;
 // Partials a warp keeps per row: its 32 lane partials folded to 4 with
 // three shuffles, so a reduction window (a shared buffer) holds 8x the rows
@@ -57,6 +56,7 @@ __shared__ uint64_t ms_empty[kMaxStages];  // stage s released by all consumer w
 __shared__ int ms_abort;                   // a wait of this CTA was abandoned
 __shared__ int ms_flag;
 __shared__ unsigned ms_target;             // grid barrier arrivals to wait for
+__shared__ unsigned ms_spin;               // grid barrier polls before giving up
 __shared__ int ms_L;                       // attended length of this step
 // Per-row values of the CTA's rows of a matvec phase: the residual rows it
 // accumulates into (prefetched at the phase start), or its gate rows of a
@@ -115,7 +115,7 @@ __device__ bool grid_wait(const MParams& P) {
           ok = 0;
           break;
         }
-        if (i >= kBarSpin) {
+        if (i >= ms_spin) {
           ok = 0;
           atomicExch(P.abort, 1);
           if (P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
@@ -582,7 +582,10 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
   float* po = P.ws_o + (size_t)item * G * D;
   const int T = (L + nc - 1) / nc;
   const int t0 = c * T, t1 = min(L, t0 + T);
-  // (every chunk is non-empty: nc <= ceil(L / 128))
+  // (chunks of T = ceil(L / nc) rows: for some L the last chunk is empty,
+  // t0 >= L; it then writes m = -inf, l = 0, which the combine skips, and
+  // it also takes the owner branch below, appending the same rounded row
+  // as the chunk that holds row L-1)
   float* qs = reinterpret_cast<float*>(region + C::kOffQ);
   float* sc = reinterpret_cast<float*>(region + C::kOffS);
   uint8_t* Ks = region + C::kOffK;
@@ -971,20 +974,15 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
     }
     ms_abort = 0;
     ms_target = 0;
+    ms_spin = *(volatile const unsigned*)P.wait_limit;
     fence_barrier_init();
   }
   __syncthreads();
 
+  int issued = 0;
   if (warp == kW) {
     // ---- producer warp ----
-    if (lane == 0) {
-      const int issued = produce_all(P, smem);
-      if (*(volatile int*)&ms_abort) {
-        // wait (bounded) for copies still in flight before the CTA exits
-        for (int j = max(0, issued - P.nstages); j < issued; ++j)
-          mbar_wait(&ms_full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
-      }
-    }
+    if (lane == 0) issued = produce_all(P, smem);
   } else {
     // ---- consumers ----
     // the step's position: read once, kept in shared memory (fewer live
@@ -1025,6 +1023,13 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
     }
   }
   __syncthreads();
+  if (warp == kW && lane == 0 && ms_abort) {
+    // the step was abandoned: tiles issued but never consumed may still be
+    // in flight; wait (bounded) for the last copy of every stage before the
+    // CTA's shared memory is released
+    for (int j = max(0, issued - P.nstages); j < issued; ++j)
+      mbar_wait(&ms_full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
+  }
 }
 
 template <int D, typename KT>

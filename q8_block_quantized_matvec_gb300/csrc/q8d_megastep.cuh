@@ -66,6 +66,7 @@ struct MParams {
   int nc;                     // most context chunks per KV head
   unsigned* bar;              // grid barrier counter, zero at launch
   int* abort;                 // set when a CTA gives up a wait, zero at launch
+  const unsigned* wait_limit; // polls a grid barrier wait makes before the step gives up
   int stage_bytes, nstages;
 };
 

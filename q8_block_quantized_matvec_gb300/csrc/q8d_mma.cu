@@ -393,15 +393,8 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return Q8D_EUNSUPPORTED;
   }
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(q8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return record_cuda(e);
-    configured[dev] = true;
-  }
+  const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), 227 * 1024, false);
+  if (crc) return crc;
   const int row_tiles = (p + kM - 1) / kM;
   const int nchunks = n / kKC;
   const int sms = sm_count();

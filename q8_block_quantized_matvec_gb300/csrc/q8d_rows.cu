@@ -296,17 +296,8 @@ template <int MV, int W>
 int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   auto fn = q8_rows_kernel<MV, W>;
   constexpr int kThreads = W * 32;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return record_cuda(e);
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return record_cuda(e);
-    configured[dev] = 1;
-  }
+  const int rc = configure_kernel(reinterpret_cast<const void*>(fn), 200 * 1024, true);
+  if (rc) return rc;
   // One wave of resident CTAs, each owning a contiguous row range.
   const int sms = sm_count();
   const long long p_total = P.total_rows;

@@ -45,7 +45,7 @@ struct q8d_step {
   void* ws = nullptr;  // activations, tables and phase table (one allocation)
   float *x, *q, *k, *v, *attn, *gu, *logits, *rope_cos, *rope_sin, *am_val;
   int* am_idx;
-  unsigned* bar;  // grid barrier counter and abort flag
+  unsigned* bar;  // grid barrier counter, abort flag (both reset per launch), wait limit
   MParams mp;
   int grid = 0;
   int* h_err = nullptr;  // pinned
@@ -57,6 +57,10 @@ struct q8d_step {
 
 namespace q8d {
 int step_validate(const q8d_step_desc* d);
+
+// Default number of polls a grid-barrier wait of the step kernel makes
+// before the step gives up (each poll is an L2 round trip: about a second).
+constexpr unsigned kStepWaitPolls = 1u << 21;
 
 // The step: reset the grid barrier, then the persistent step kernel.
 static int enqueue_step(q8d_step* S, cudaStream_t st) {
@@ -240,6 +244,7 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   P.nc = nc;
   P.bar = S->bar;
   P.abort = reinterpret_cast<int*>(S->bar + 1);
+  P.wait_limit = S->bar + 2;
   P.stage_bytes = stage_bytes;
   P.nstages = std::min(8, megastep_max_stages(stage_bytes));
   if (P.nstages < 2) return fail(Q8D_EUNSUPPORTED);
@@ -252,6 +257,10 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
     return fail(record_cuda(e));
   if ((e = cudaMemcpyAsync(base + o_ly, mlayers.data(), sizeof(MLayer) * mlayers.size(),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return fail(record_cuda(e));
+  const unsigned polls = kStepWaitPolls;
+  if ((e = cudaMemcpyAsync(S->bar + 2, &polls, sizeof(polls), cudaMemcpyHostToDevice, st)) !=
+      cudaSuccess)
     return fail(record_cuda(e));
   rope_table_kernel<<<256, 256, 0, st>>>(S->rope_cos, S->rope_sin, d.cap, half,
                                          (double)d.rope_theta);
@@ -303,6 +312,15 @@ int q8d_step_status(q8d_step* S, void* stream, int timeout_ms, int* err) {
   if (e != cudaSuccess) return record_cuda(e);
   if ((e = cudaEventRecord(S->ev, st)) != cudaSuccess) return record_cuda(e);
   return wait_event_bounded(S->ev, timeout_ms, S->h_err, err);
+}
+
+int q8d_step_set_wait_limit(q8d_step* S, unsigned polls, void* stream) {
+  if (!S) return Q8D_EINVAL;
+  const unsigned v = polls ? polls : kStepWaitPolls;
+  // (a pageable source: the value is staged before the call returns)
+  const cudaError_t e = cudaMemcpyAsync(S->bar + 2, &v, sizeof(v), cudaMemcpyHostToDevice,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q8D_OK : record_cuda(e);
 }
 
 int q8d_step_kernel_count(const q8d_step* S) { return S ? S->kernel_nodes : 0; }

@@ -161,3 +161,44 @@ def test_small_m_tensor_parity(q8d, orc, m, n, p):
     assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
     # the norm-wise error is reported, and is far inside the bar
     assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) < 1e-2
+
+
+@pytest.mark.parametrize("m", [16, 64])
+@pytest.mark.parametrize("n,p", [(3584, 33), (3584, 200), (512, 300)])
+def test_small_m_tensor_ragged_row_tile(q8d, orc, m, n, p):
+    """p not a multiple of the 128-row tile: the last tile's rows past p come
+    from the tensor map's zero fill and are not stored."""
+    w = synth.q8_matrix(6, f"tr.w{n}.{p}", p, n)
+    X = synth.normal_f32(6, f"tr.X{n}.{m}", (m, n))
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    got = gpu_small_m(q8d, w, X, n, p, ldy=p + 5)
+    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+
+
+@pytest.mark.parametrize("m", [65, 80, 128, 129, 200, 256])
+def test_small_m_tensor_large_m(q8d, orc, m):
+    """m up to the entry point's 256: above 128 rows the activations go
+    through the kernel in more than one pass."""
+    n, p = 1024, 300
+    w = synth.q8_matrix(7, "lm.w", p, n)
+    X = synth.normal_f32(7, f"lm.X{m}", (m, n))
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    got = gpu_small_m(q8d, w, X, n, p)
+    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+
+
+@pytest.mark.parametrize("m", [1, 4, 16, 64])
+def test_small_m_bench_shape_sampled(q8d, orc, m):
+    """The launch the bench times: 7B gate/up (3584 -> 18944) at m rows;
+    257 sampled output rows per activation row against the oracle."""
+    n, p = 3584, 18944
+    w = synth.q8_matrix(0, "7b.gate/up", p, n)
+    X = synth.normal_f32(8, f"bs.X{m}", (m, n))
+    got = gpu_small_m(q8d, w, X, n, p)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, p - 1], rng.integers(0, p, 255)])).astype(np.int64)
+    tol = TOL if m <= 8 else TOL_BF16
+    for i in range(m):
+        ref, ab = orc.q8_matvec_rows(w, X[i], n, rows)
+        assert np.all(np.abs(got[i, rows] - ref) <= tol * ab), i
+    assert np.isfinite(got).all()
