@@ -16,9 +16,13 @@ step (7.5 GB) are 58x the 129 MB L2, so no flush is needed between steps.
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
 independent replica (the decode step does not shard: replicas only) and
 `value` is the sum of the ranks' tokens over the max of their times.
-The reference arm (--impl reference) times the scalar C oracle on the
-host cores: W untimed and K timed steps, each a bounded sample of the same
-workload (2 of the layers plus lm_head, projected to the full step).
+Besides the workload's own step the line carries kernel legs through the
+C ABI (q8d_matvec over the step's matrices, q8d_gqa_decode_attn per layer
+at the context and at 8192, the batch-8 ragged stress, q8d_matmul_small_m)
+and, under "configs", decode steps of the other configurations
+(Qwen3-0.6B at 2048, Qwen2.5-0.5B at 512/2048/4096, 7B at 2048/8192).
+The reference arm (--impl reference) times the scalar C oracle on all host
+cores: W untimed and exactly K timed whole decode steps of the workload.
 """
 from __future__ import annotations
 
@@ -50,14 +54,17 @@ def peaks():
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clock and throttle reasons during a region
+    (every 20 ms; samples are kept with their host arrival time so that the
+    summary covers the timed window only)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 20):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
 
@@ -65,20 +72,22 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            time.sleep(0.3)  # the first sample is in before the region starts
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
+            time.sleep(2 * self.period_ms / 1e3)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -86,10 +95,22 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons of the samples taken
+        in [t0, t1] (host monotonic time; the whole run if not given).  A
+        window shorter than the sampling period keeps the nearest sample
+        on each side."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = self.lines
+        if t0 is not None and rows:
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+            if not inside:
+                before = [r for r in rows if r[0] < t0][-1:]
+                after = [r for r in rows if r[0] > t1][:1]
+                inside = before + after
+            rows = inside
+        for _, ln in rows:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -104,7 +125,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "period_ms": self.period_ms}
 
 
 def gpu_index():
@@ -170,51 +191,99 @@ def ncu_traffic(algorithmic_bytes: float):
 
 
 # ---------------------------------------------------------------------------- oracle
-def oracle_sample(shape_name: str, context: int, seconds_hint: float = 12.0,
-                  steps: int | None = None, warmup: int = 0):
-    """Times the scalar oracle's decode step on a bounded sample of the
-    workload: the same shapes truncated to 2 layers (lm_head included), KV
-    at the same context, repeated for about `seconds_hint` seconds of CPU
-    work (at least 3 times), or, with `steps`, `warmup` untimed and then
-    exactly `steps` timed repetitions; with the medians the full step's time
-    is projected as t(lm_head) + n_layers/2 * (t(2-layer step) - t(lm_head)).
-    Returns (tokens_per_s, threads, description, repetitions)."""
-    import numpy as np
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
+
+def oracle_model(shape_name: str, context: int, n_layers: int = 0):
+    """Host weights and caches of the workload for the oracle: the model's
+    shapes (optionally truncated to n_layers), KV filled to context - 1
+    rows; every timed step appends row context - 1 and attends `context`."""
     import synth
     from oracle import oracle as orc
     full = synth.MODELS[shape_name]
-    sample = synth.ModelShape(full.name + "-2layer", full.hidden, 2, full.n_heads, full.n_kv_heads,
-                              full.head_dim, full.ffn, full.vocab, full.qk_norm, full.qkv_bias,
-                              full.kv_dtype, full.rms_eps, full.rope_theta)
-    w = synth.step_weights(sample, seed=0)
-    cap = context
-    caches = [synth.kv_prefix(sample, 0, li, cap, context - 1) for li in range(2)]
-    host = orc.HostStep(w, cap, caches)
-    threads = orc.default_threads()
-    x = synth.normal_f32(0, "bench.x", full.hidden)
-    for _ in range(warmup if steps is not None else 0):
-        orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
+    shape = full
+    if n_layers:
+        shape = synth.ModelShape(full.name + f"-{n_layers}layer", full.hidden, n_layers,
+                                 full.n_heads, full.n_kv_heads, full.head_dim, full.ffn,
+                                 full.vocab, full.qk_norm, full.qkv_bias, full.kv_dtype,
+                                 full.rms_eps, full.rope_theta)
+    w = synth.step_weights(shape, seed=0)
+    caches = [synth.kv_prefix(shape, 0, li, context, context - 1) for li in range(shape.n_layers)]
+    return w, orc.HostStep(w, context, caches)
+
+
+def oracle_full_steps(shape_name: str, context: int, steps: int, warmup: int, threads: int):
+    """Wall times of `steps` whole decode steps of the oracle (every layer,
+    lm_head, argmax) after `warmup` untimed ones, on `threads` host threads."""
+    _, host = oracle_model(shape_name, context)
+    for _ in range(warmup):
         host.step(17, context - 1, threads)
-    n_steps = steps
-    heads, steps = [], []
-    t_begin = time.perf_counter()
-    while (len(steps) < n_steps if n_steps is not None
-           else len(steps) < 3 or time.perf_counter() - t_begin < seconds_hint):
+    times = []
+    for _ in range(steps):
         t0 = time.perf_counter()
-        orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, threads)
+        host.step(17, context - 1, threads)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def oracle_single_thread(shape_name: str, context: int, runs: int = 5):
+    """One host thread, a bounded sample: the model truncated to 2 layers
+    (lm_head included), median of `runs` steps after one warm-up, with the
+    lm_head timed alone so that the full step projects as
+    t(lm_head) + n_layers / 2 * (t(2-layer step) - t(lm_head))."""
+    import synth
+    from oracle import oracle as orc
+    full = synth.MODELS[shape_name]
+    w, host = oracle_model(shape_name, context, n_layers=2)
+    x = synth.normal_f32(0, "bench.x", full.hidden)
+    host.step(17, context - 1, 1)
+    heads, steps = [], []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        orc.q8_matvec(w.lm_head, x, full.hidden, full.vocab, 1)
         heads.append(time.perf_counter() - t0)
         t0 = time.perf_counter()
-        host.step(17, context - 1, threads)  # rewrites the same cache row each time
+        host.step(17, context - 1, 1)
         steps.append(time.perf_counter() - t0)
     t_head, t_step2 = statistics.median(heads), statistics.median(steps)
-    per_layer = max(t_step2 - t_head, 1e-9) / 2
-    t_full = t_head + full.n_layers * per_layer
-    desc = (f"oracle decode step of the {full.name}-shaped model truncated to 2 of "
-            f"{full.n_layers} layers (+lm_head, KV context {context}), {len(steps)} repetitions "
-            f"({time.perf_counter() - t_begin:.1f} s of CPU work); median 2-layer step "
-            f"{t_step2:.3f} s, lm_head alone {t_head:.3f} s; projected full step {t_full:.2f} s")
-    return 1.0 / t_full, threads, desc, len(steps)
+    t_full = t_head + full.n_layers * max(t_step2 - t_head, 1e-9) / 2
+    return {"value": 1.0 / t_full, "unit": "tokens/s", "cores": 1,
+            "sample": (f"2 of {full.n_layers} layers (+lm_head, KV context {context}), median of "
+                       f"{runs} steps: {t_step2:.3f} s, lm_head alone {t_head:.3f} s; projected "
+                       f"full step {t_full:.2f} s")}
+
+
+def cpu_baseline_leg(shape_name: str, context: int, runs: int = 5):
+    """The oracle as it stands on this host: all cores on whole decode steps
+    (median of `runs` after one warm-up), plus the single-thread mode on a
+    2-layer sample; the CPU model is recorded."""
+    from oracle import oracle as orc
+    threads = orc.default_threads()
+    t0 = time.perf_counter()
+    times = oracle_full_steps(shape_name, context, runs, 1, threads)
+    t_all = time.perf_counter() - t0
+    single = oracle_single_thread(shape_name, context, runs)
+    med = statistics.median(times)
+    return {"value": 1.0 / med, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": (f"whole {shape_name}-shaped decode steps (every layer + lm_head, KV context "
+                       f"{context}), median of {runs} after one warm-up: {med:.3f} s per step "
+                       f"({t_all:.1f} s of wall time incl. the warm-up)"),
+            "cpu_model": cpu_model(), "single_thread": single}
 
 
 # ---------------------------------------------------------------------------- profiling
@@ -450,17 +519,26 @@ def replica_throughput(local_seconds: float, steps: int, dist=None, device="cuda
 
 # ---------------------------------------------------------------------------- main
 def run_reference(args, rank, world):
+    """The reference arm: the oracle as it stands, whole decode steps of the
+    workload (every layer, lm_head, argmax) on all host cores, W untimed and
+    exactly K timed; rank 0 only."""
     if rank != 0:
         return
-    tps, threads, desc, reps = oracle_sample(args.model, args.context, steps=args.steps,
-                                             warmup=args.warmup)
+    from oracle import oracle as orc
+    threads = orc.default_threads()
+    times = oracle_full_steps(args.model, args.context, args.steps, args.warmup, threads)
+    total = sum(times)
+    tps = args.steps / total
+    desc = (f"whole {args.model}-shaped decode steps (every layer + lm_head + argmax, KV context "
+            f"{args.context}): {args.warmup} untimed, {args.steps} timed, {total:.1f} s; median "
+            f"{statistics.median(times):.3f} s per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
-        "steps": reps, "warmup": args.warmup, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(args)},
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_name(args)},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -469,6 +547,104 @@ def run_reference(args, rank, world):
 def workload_name(args):
     return (f"{args.model}-shaped decode step, Q8_0 weights, "
             f"{'f16' if args.model != 'qwen2.5-0.5b' else 'f32'} KV cache, context {args.context}")
+
+
+def device_caches(shape, ctx, cap, rank):
+    """Per-layer KV caches of `cap` rows with ctx - 1 seeded rows."""
+    import torch
+
+    import synth
+    kdt = torch.float16 if shape.kv_dtype == synth.KV_F16 else torch.float32
+    caches = []
+    for li in range(shape.n_layers):
+        kc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
+        vc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
+        kc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.kprefix", (ctx - 1, shape.kv_width), kdt)
+        vc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.vprefix", (ctx - 1, shape.kv_width), kdt)
+        caches.append((kc, vc))
+    return caches
+
+
+def config_leg(shape, wts, ctx, steps, warmup, stream, hbm, rank):
+    """Decode steps of another configuration (graph launches, everything
+    resident), CUDA-event timed on the launching stream."""
+    import torch
+
+    import synth
+    from q8_block_quantized_matvec_gb300.device import DeviceStep
+    cap = ctx + warmup + steps + 64
+    caches = device_caches(shape, ctx, cap, rank)
+    ds = DeviceStep(wts, cap, caches, stream=stream)
+    with torch.cuda.stream(stream):
+        ds.set_state(17, ctx - 1)
+        for _ in range(warmup):
+            ds.launch(stream)
+        ds.set_state(17, ctx - 1)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        ds.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    assert ds.step.status(stream) == 0, "device error word set"
+    ds.close()
+    del caches
+    esize = 2 if shape.kv_dtype == synth.KV_F16 else 4
+    b = statistics.mean(step_bytes(shape, ctx + s, esize) for s in range(steps))
+    return {"tokens_s": steps / t, "ms_per_step": 1e3 * t / steps, "steps": steps,
+            "context_first_step": ctx, "kv": "f16" if esize == 2 else "f32",
+            "weight_bytes_per_step": shape.weight_bytes(),
+            "roofline": {"bound": "hbm", "achieved_GB_s": b / (t / steps) / 1e9,
+                         "frac": b / (t / steps) / 1e9 / hbm,
+                         "algorithmic_bytes_per_launch": b}}
+
+
+def attn_layer_leg(q8d, shape, caches, ctx, cap, reps, stream, flush, rank):
+    """q8d_gqa_decode_attn over every layer's cache at attended length ctx,
+    one launch per layer with an L2 flush (256 MB) between layers; returns
+    the median over reps of the per-step sum."""
+    import torch
+
+    import synth
+    esize = 2 if shape.kv_dtype == synth.KV_F16 else 4
+    H, Hk, D = shape.n_heads, shape.n_kv_heads, shape.head_dim
+    qv = synth.normal_torch(rank, "bench.q", H * D, torch.float32)
+    aout = torch.empty(H * D, device="cuda")
+    wsb = q8d.q8d_gqa_workspace_bytes(1, H, Hk, D, cap)
+    aws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+    aerr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    at_times = []
+    with torch.cuda.stream(stream):
+        for rep in range(reps + 1):
+            tot = 0.0
+            for li in range(shape.n_layers):
+                flush.fill_(li & 0xFF)  # evict the previous layer's KV from L2 (same stream)
+                a.record(stream)
+                q8d.q8d_gqa_decode_attn(qv, None, None, caches[li][0], caches[li][1],
+                                        shape.kv_dtype, aout, 1, H, Hk, D, cap, 0, lens,
+                                        1 / math.sqrt(D), aws, wsb, aerr, stream)
+                b.record(stream)
+                b.synchronize()
+                tot += a.elapsed_time(b) / 1e3
+            if rep:
+                at_times.append(tot)
+    assert aerr.item() == 0
+    t = statistics.median(at_times)
+    nbytes = attn_bytes(ctx, Hk, D, H, esize, append=False)
+    return {"kernel": "gqa_mma_kernel + gqa_combine_kernel (q8d_gqa_decode_attn)"
+            if esize == 2 else "gqa_split_kernel + gqa_combine_kernel (q8d_gqa_decode_attn)",
+            "GB_s": nbytes * shape.n_layers / t / 1e9, "us_per_layer": t / shape.n_layers * 1e6,
+            "bytes_per_layer": nbytes, "context": ctx, "l2": "256 MB flush between layers"}
+
+
+# The other configurations of the workload set, measured as extra keys:
+# (model, context) pairs; the line's own workload is skipped.
+CONFIG_LEGS = [("qwen3-0.6b", 2048), ("qwen2.5-0.5b", 512), ("qwen2.5-0.5b", 2048),
+               ("qwen2.5-0.5b", 4096), ("qwen2.5-7b", 2048), ("qwen2.5-7b", 8192)]
 
 
 def main():
@@ -482,6 +658,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="--profile step only: use this many layers of the model's shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations")
     ap.add_argument("--kernel-reps", type=int, default=3)
     ap.add_argument("--profile",
                     choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "mma16", "mma64",
@@ -520,14 +697,7 @@ def main():
     ctx = args.context
     cap = ctx + args.warmup + 2 * args.steps + 64
     wts = synth.TorchStepWeights(shape, seed=rank)
-    kdt = torch.float16 if shape.kv_dtype == synth.KV_F16 else torch.float32
-    caches = []
-    for li in range(shape.n_layers):
-        kc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
-        vc = torch.zeros((cap, shape.kv_width), dtype=kdt, device="cuda")
-        kc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.kprefix", (ctx - 1, shape.kv_width), kdt)
-        vc[:ctx - 1] = synth.normal_torch(rank, f"l{li}.vprefix", (ctx - 1, shape.kv_width), kdt)
-        caches.append((kc, vc))
+    caches = device_caches(shape, ctx, cap, rank)
     stream = torch.cuda.Stream()
     ds = DeviceStep(wts, cap, caches, stream=stream)
     torch.cuda.synchronize()
@@ -547,11 +717,13 @@ def main():
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_index()) as clk:
+        h0 = time.monotonic()
         e0.record(stream)
         for _ in range(args.steps):
             ds.launch(stream)
         e1.record(stream)
         barrier()
+        h1 = time.monotonic()
     t_dev = e0.elapsed_time(e1) / 1e3
     assert ds.step.status(stream) == 0, "device error word set during the timed steps"
     value = replica_throughput(t_dev, args.steps, dist)
@@ -574,6 +746,7 @@ def main():
     t_e2e = time.perf_counter() - t0
     e2e = {"value": replica_throughput(t_e2e, args.steps, dist), "unit": "tokens/s",
            "h2d_bytes_per_step": 8, "d2h_bytes_per_step": 4}
+    ds.close()
 
     # ---- kernel legs: q8_matvec over the step's matrices, attention per layer ----
     mats = []
@@ -587,7 +760,7 @@ def main():
     xin = {n: synth.normal_torch(rank, f"bench.x{n}", n, torch.float32) for _, n, _ in mats}
     yout = torch.empty(max(p for _, _, p in mats), device="cuda")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in mats]
-    mv_times = []
+    mv_times, mv_big = [], []
     for rep in range(args.kernel_reps + 1):
         torch.cuda.synchronize()
         for (w, n, p), (a, b) in zip(mats, ev):
@@ -597,41 +770,27 @@ def main():
         torch.cuda.synchronize()
         if rep:
             mv_times.append(sum(a.elapsed_time(b) for a, b in ev) / 1e3)
+            mv_big.append(sum(a.elapsed_time(b) for (w, n, p), (a, b) in zip(mats, ev)
+                              if p == shape.ffn or n == shape.ffn) / 1e3)
     mv_time = statistics.median(mv_times)
     mv_bytes = sum(matvec_bytes(n, p) for _, n, p in mats)
-    mv_launch_bytes = mv_bytes / len(mats)
-    mv_launch_s = mv_time / len(mats)
+    big_bytes = sum(matvec_bytes(n, p) for _, n, p in mats if p == shape.ffn or n == shape.ffn)
     hbm, peak_kind = peaks()
     mv_gbs = mv_bytes / mv_time / 1e9
+    big_gbs = big_bytes / statistics.median(mv_big) / 1e9
 
-    esize = 2 if shape.kv_dtype == synth.KV_F16 else 4
-    H, Hk, D = shape.n_heads, shape.n_kv_heads, shape.head_dim
-    qv = synth.normal_torch(rank, "bench.q", H * D, torch.float32)
-    aout = torch.empty(H * D, device="cuda")
-    wsb = q8d.q8d_gqa_workspace_bytes(1, H, Hk, D, cap)
-    aws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
-    aerr = torch.zeros(1, dtype=torch.int32, device="cuda")
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-    at_times = []
-    with torch.cuda.stream(stream):
-        for rep in range(args.kernel_reps + 1):
-            tot = 0.0
-            for li in range(shape.n_layers):
-                flush.fill_(li & 0xFF)  # evict the previous layer's KV from L2 (same stream)
-                a, b = ev[0]
-                a.record(stream)
-                q8d.q8d_gqa_decode_attn(qv, None, None, caches[li][0], caches[li][1], shape.kv_dtype,
-                                        aout, 1, H, Hk, D, cap, 0, lens, 1 / math.sqrt(D), aws, wsb,
-                                        aerr, stream)
-                b.record(stream)
-                b.synchronize()
-                tot += a.elapsed_time(b) / 1e3
-            if rep:
-                at_times.append(tot)
-    at_time = statistics.median(at_times)
-    at_bytes_launch = attn_bytes(ctx, Hk, D, H, esize, append=False)
-    at_gbs = at_bytes_launch * shape.n_layers / at_time / 1e9
+    attn = attn_layer_leg(q8d, shape, caches, ctx, cap, args.kernel_reps, stream, flush, rank)
+    attn["frac_of_peak"] = attn["GB_s"] / hbm
+    attn_long = None
+    H, Hk, D = shape.n_heads, shape.n_kv_heads, shape.head_dim
+    if shape.name == "qwen2.5-7b" and ctx != 8192:
+        del caches
+        caches = device_caches(shape, 8192, 8192, rank)
+        attn_long = attn_layer_leg(q8d, shape, caches, 8192, 8192, args.kernel_reps, stream, flush,
+                                   rank)
+        attn_long["frac_of_peak"] = attn_long["GB_s"] / hbm
+    del caches
     stress = attn_stress(q8d, H, Hk, D, args.kernel_reps, stream, flush, rank) \
         if shape.kv_dtype == synth.KV_F16 else None
     if stress is not None:
@@ -639,14 +798,29 @@ def main():
     small_m = small_m_leg(q8d, args.kernel_reps, stream, flush, hbm, rank) \
         if shape.name == "qwen2.5-7b" else None
 
+    # ---- the other configurations (decode steps, extra keys) ----
+    configs = {}
+    if not args.no_configs:
+        csteps = max(args.steps, 20)
+        for mname, cctx in CONFIG_LEGS:
+            if (mname, cctx) == (args.model, ctx):
+                continue
+            cshape = synth.MODELS[mname]
+            cw = wts if mname == args.model else synth.TorchStepWeights(cshape, seed=rank)
+            configs[f"{mname}@{cctx}"] = config_leg(cshape, cw, cctx, csteps, args.warmup, stream,
+                                                    hbm, rank)
+            if cw is not wts:
+                del cw
+            torch.cuda.empty_cache()
+
     # dominant kernel: the persistent step kernel, one launch per step
+    esize = 2 if shape.kv_dtype == synth.KV_F16 else 4
     step_b = statistics.mean(step_bytes(shape, ctx + s, esize) for s in range(args.steps))
     step_s = t_dev / args.steps
     traffic = ncu_traffic(step_b)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, threads, desc, _ = oracle_sample(args.model, ctx)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline_leg(args.model, ctx)
 
     if rank == 0:
         line = {
@@ -670,21 +844,21 @@ def main():
                 "q8_matvec": {"kernel": "q8_gemv_kernel (q8d_matvec, one launch per matrix)",
                               "GB_s": mv_gbs, "frac_of_peak": mv_gbs / hbm,
                               "us_per_step_sum": mv_time * 1e6,
-                              "avg_launch_us": mv_launch_s * 1e6,
-                              "algorithmic_bytes_per_launch": mv_launch_bytes},
-                "gqa_decode_attn": {"GB_s": at_gbs, "frac_of_peak": at_gbs / hbm,
-                                    "us_per_layer": at_time / shape.n_layers * 1e6,
-                                    "context": ctx, "l2": "256 MB flush between layers"},
+                              "avg_launch_us": mv_time / len(mats) * 1e6,
+                              "algorithmic_bytes_per_launch": mv_bytes / len(mats),
+                              "ffn_matrices_GB_s": big_gbs, "ffn_matrices_frac_of_peak": big_gbs / hbm},
+                "gqa_decode_attn": attn,
+                "gqa_decode_attn_ctx8192": attn_long,
                 "gqa_decode_attn_batch8_ragged": stress,
                 "q8_matmul_small_m": small_m,
             },
+            "configs": configs,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": kernels_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clk.summary(h0, h1),
         }
         print(json.dumps(line), flush=True)
-    ds.close()
     if dist:
         dist.destroy_process_group()
 
