@@ -35,6 +35,7 @@
 
 #define ORC_KV_F32 0
 #define ORC_KV_F16 1
+#define ORC_KV_Q8_0 2  /* packed: rows of kvw/32 Q8_0 blocks */
 
 /* ------------------------------------------------------------------------ */
 /* IEEE 754 binary16 <-> binary32, written from the format's definition.    */
@@ -272,8 +273,56 @@ void orc_q8_matmul(const uint8_t* w, const float* X, int ldx, int m, int n, int 
 /* even.  Pinned by tests (row placement, untouched neighbours, RNE).       */
 /* ------------------------------------------------------------------------ */
 
+/* ------------------------------------------------------------------------ */
+/* Packed Q8_0 KV cache ([P1] "Execution dispatch", packed q8_0 KV: a store */
+/* byte-identical to the CPU quantizer, and attention that reads the 34-byte */
+/* blocks natively).  A cache row of kvw elements is kvw/32 consecutive      */
+/* Q8_0 blocks in the weight matrices' layout: row t starts at byte          */
+/* t * (kvw/32) * 34, element i of the row is quant i%32 of block i/32.      */
+/* The pages name the CPU quantizer without restating it; it is read as the  */
+/* Q8_0 format's reference quantizer, computed in f32 as that quantizer is:  */
+/*   amax = max_j |x_j|,  d = amax / 127,  id = (d != 0) ? 1 / d : 0,        */
+/*   q_j = x_j * id rounded to the nearest integer, halves away from zero,   */
+/*   stored scale = d rounded to binary16 (nearest even).                    */
+/* Inputs are finite.  Pinned by tests: an all-zero block, exact multiples   */
+/* of a power of two, halves rounding away from zero, the round-trip bound   */
+/* and sign symmetry on random blocks.                                       */
+/* ------------------------------------------------------------------------ */
+void orc_q8_0_quantize_block(const float* x, uint8_t* blk) {
+  float amax = 0.0f;
+  for (int j = 0; j < ORC_QBLOCK; ++j) {
+    float a = fabsf(x[j]);
+    if (a > amax) amax = a;
+  }
+  float d = amax / 127.0f;
+  float id = d != 0.0f ? 1.0f / d : 0.0f;
+  uint16_t sb = orc_f32_to_f16(d);
+  blk[0] = (uint8_t)(sb & 0xff);
+  blk[1] = (uint8_t)(sb >> 8);
+  for (int j = 0; j < ORC_QBLOCK; ++j) {
+    float v = x[j] * id;          /* one f32 product (no contraction: -ffp-contract=off) */
+    int q = (int)roundf(v);       /* nearest, halves away from zero */
+    blk[2 + j] = (uint8_t)(int8_t)q;
+  }
+}
+
+static size_t orc_kv_row_bytes(int kv_dtype, int kvw) {
+  if (kv_dtype == ORC_KV_F32) return 4 * (size_t)kvw;
+  if (kv_dtype == ORC_KV_F16) return 2 * (size_t)kvw;
+  return (size_t)(kvw / ORC_QBLOCK) * ORC_QBLOCK_BYTES;
+}
+
 void orc_kv_append(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,
                    int64_t pos) {
+  if (kv_dtype == ORC_KV_Q8_0) {
+    uint8_t* kb = (uint8_t*)kc + (size_t)pos * orc_kv_row_bytes(kv_dtype, kvw);
+    uint8_t* vb = (uint8_t*)vc + (size_t)pos * orc_kv_row_bytes(kv_dtype, kvw);
+    for (int b = 0; b < kvw / ORC_QBLOCK; ++b) {
+      orc_q8_0_quantize_block(k + (int64_t)b * ORC_QBLOCK, kb + (size_t)b * ORC_QBLOCK_BYTES);
+      orc_q8_0_quantize_block(v + (int64_t)b * ORC_QBLOCK, vb + (size_t)b * ORC_QBLOCK_BYTES);
+    }
+    return;
+  }
   if (kv_dtype == ORC_KV_F32) {
     float* kf = (float*)kc + pos * kvw;
     float* vf = (float*)vc + pos * kvw;
@@ -291,8 +340,14 @@ void orc_kv_append(const float* k, const float* v, void* kc, void* vc, int kv_dt
   }
 }
 
+/* Element idx = t * kvw + i of a cache (kvw a multiple of 32 for Q8_0:
+ * block idx / 32 of the packed rows, which start at multiples of kvw/32). */
 static double orc_kv_read(const void* c, int kv_dtype, int64_t idx) {
   if (kv_dtype == ORC_KV_F32) return (double)((const float*)c)[idx];
+  if (kv_dtype == ORC_KV_Q8_0) {
+    const uint8_t* blk = (const uint8_t*)c + (size_t)(idx / ORC_QBLOCK) * ORC_QBLOCK_BYTES;
+    return orc_block_scale(blk) * (double)orc_block_quant(blk, (int)(idx % ORC_QBLOCK));
+  }
   return (double)orc_f16_to_f32(((const uint16_t*)c)[idx]);
 }
 

@@ -19,6 +19,7 @@ _lib = None
 
 KV_F32 = 0
 KV_F16 = 1
+KV_Q8_0 = 2  # packed rows of kv_width/32 Q8_0 blocks (34 bytes each)
 
 
 def build(force: bool = False) -> str:
@@ -69,6 +70,7 @@ def _declare(L):
     L.orc_q8_matvec_rows.argtypes = [vp, vp, i32, vp, i32, vp, vp]
     L.orc_q8_matmul.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, i32]
     L.orc_kv_append.argtypes = [vp, vp, vp, vp, i32, i32, i64]
+    L.orc_q8_0_quantize_block.argtypes = [vp, vp]
     L.orc_gqa_decode_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     L.orc_gqa_decode_attn.restype = i32
     L.orc_rmsnorm.argtypes = [vp, vp, i32, C.c_double, vp]
@@ -137,6 +139,23 @@ def q8_matmul(w: np.ndarray, X: np.ndarray, n: int, p: int, nthreads: int | None
     lib().orc_q8_matmul(_p(w), _p(X), X.shape[1], m, n, p, _p(Y), p, _p(ab),
                         nthreads or default_threads())
     return Y, ab
+
+
+def q8_0_quantize_block(x) -> np.ndarray:
+    """The packed-KV store's quantizer on 32 values: 34 bytes (uint8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == 32
+    out = np.empty(34, dtype=np.uint8)
+    lib().orc_q8_0_quantize_block(_p(x), _p(out))
+    return out
+
+
+def kv_row_bytes(kv_dtype: int, kv_width: int) -> int:
+    if kv_dtype == KV_F32:
+        return 4 * kv_width
+    if kv_dtype == KV_F16:
+        return 2 * kv_width
+    return kv_width // 32 * 34
 
 
 def kv_append(k, v, kc: np.ndarray, vc: np.ndarray, kv_dtype: int, pos: int):

@@ -26,6 +26,7 @@ QBLOCK_BYTES = 34    # 2-byte little-endian f16 scale + 32 int8 quants
 
 KV_F32 = 0
 KV_F16 = 1
+KV_Q8_0 = 2  # packed cache: rows of kv_width/32 Q8_0 blocks
 
 
 def stream(seed: int, name: str) -> np.random.Generator:
@@ -227,10 +228,25 @@ def step_weights(shape: ModelShape, seed: int = 0) -> StepWeights:
                        lm_head=lm_head)
 
 
+def q8_kv_cache(seed: int, name: str, cap: int, kv_width: int, rows: int | None = None):
+    """A packed Q8_0 cache [cap, kv_width/32*34] (uint8) whose first `rows`
+    rows (all if None) hold random blocks: quants uniform on [-127, 127],
+    scales uniform on [4e-3, 3e-2] (the range of N(0, 1) rows' blocks);
+    the other rows are zero."""
+    rows = cap if rows is None else rows
+    out = np.zeros((cap, kv_width // QBLOCK * QBLOCK_BYTES), dtype=np.uint8)
+    if rows > 0:
+        out[:rows] = q8_matrix(seed, name, rows, kv_width, 4e-3, 3e-2)
+    return out
+
+
 def kv_prefix(shape: ModelShape, seed: int, layer: int, cap: int, rows: int):
     """Cache contents for `rows` already-decoded positions: N(0,1) in the cache
     dtype; rows past `rows` are zero.  Returns (kcache, vcache) arrays
     [cap, kv_width] of float16 or float32."""
+    if shape.kv_dtype == KV_Q8_0:
+        return (q8_kv_cache(seed, f"l{layer}.kprefix", cap, shape.kv_width, rows),
+                q8_kv_cache(seed, f"l{layer}.vprefix", cap, shape.kv_width, rows))
     dt = np.float16 if shape.kv_dtype == KV_F16 else np.float32
     kc = np.zeros((cap, shape.kv_width), dtype=dt)
     vc = np.zeros((cap, shape.kv_width), dtype=dt)

@@ -397,3 +397,104 @@ def test_decode_step_pos0_attention_is_v(orc):
     c = orc.HostStep(w3, 4)
     lc, _ = c.step(3, 0)
     assert not np.array_equal(la, lc)
+
+
+# --------------------------------------------------------------------------- packed Q8_0 KV
+def q8kv_parts(blk):
+    """(scale as float64, quants as int) of one 34-byte block."""
+    return float(blk[0:2].copy().view("<f2")[0]), blk[2:].view(np.int8).astype(np.int64)
+
+
+def test_q8kv_quantize_zero_block(orc):
+    assert np.array_equal(orc.q8_0_quantize_block(np.zeros(32, np.float32)), np.zeros(34, np.uint8))
+
+
+def test_q8kv_quantize_exact_multiples_of_a_power_of_two(orc):
+    """x = k * 2^-3 with integer k, max |k| = 127: d = 2^-3 exactly, so the
+    block is the scale 0x3000 and the quants k."""
+    k = synth.stream(0, "q8kv.k").integers(-127, 128, 32)
+    k[5] = -127
+    b = orc.q8_0_quantize_block((k * 0.125).astype(np.float32))
+    assert b[0] == 0x00 and b[1] == 0x30
+    assert np.array_equal(b[2:].view(np.int8), k.astype(np.int8))
+
+
+def test_q8kv_quantize_halves_round_away_from_zero(orc):
+    """amax = 127 makes d = 1: x * id is x itself, so halves show the rounding."""
+    x = np.zeros(32, np.float32)
+    x[:9] = [127, 2.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5, 0.49999997]
+    b = orc.q8_0_quantize_block(x)
+    assert b[0] == 0x00 and b[1] == 0x3C
+    assert list(b[2:11].view(np.int8)) == [127, 3, -3, 1, -1, 2, -2, 127, 0]
+
+
+@pytest.mark.parametrize("sigma", [1e-3, 1.0, 300.0])
+def test_q8kv_quantize_round_trip_and_symmetry(orc, sigma):
+    """Random blocks: the largest |x| maps to +-127; every element comes back
+    within half a step of d = amax/127 plus the scale's f16 rounding; -x
+    gives the same scale and negated quants."""
+    X = (synth.normal_f32(3, f"q8kv.rt{sigma}", (64, 32)) * np.float32(sigma)).astype(np.float32)
+    for x in X:
+        b = orc.q8_0_quantize_block(x)
+        s, q = q8kv_parts(b)
+        d = np.max(np.abs(x.astype(np.float64))) / 127
+        assert abs(s - d) <= 2.0 ** -11 * d + 2.0 ** -25  # (binary16 subnormals below 2^-14)
+        assert np.max(np.abs(q)) == 127
+        assert np.all(np.abs(x - s * q) <= 0.5 * d * (1 + 1e-6) + np.abs(s - d) * np.abs(q))
+        bn = orc.q8_0_quantize_block(-x)
+        assert np.array_equal(bn[:2], b[:2]) and np.array_equal(bn[2:].view(np.int8), -q)
+
+
+def test_q8kv_pages_memory_ratio(orc):
+    """The pages' 3.76x memory win of the packed cache over f32: 128 bytes of
+    f32 per 32 elements against one 34-byte block."""
+    g = GOLDEN["packed_kv_memory_ratio"]
+    kvw = 512
+    ratio = orc.kv_row_bytes(synth.KV_F32, kvw) / orc.kv_row_bytes(synth.KV_Q8_0, kvw)
+    assert round(ratio, g["digits"]) == g["ratio"]
+
+
+def test_q8kv_append_row(orc):
+    g = GOLDEN["append_test_shape"]
+    w, pos, cap = 2 * g["width"], g["pos"], g["cap"]
+    lcg = synth.PagesLCG(g["seed"])
+    k = np.array([lcg.next_f32() for _ in range(w)], np.float32) * np.float32(300.0)
+    v = np.array([lcg.next_f32() for _ in range(w)], np.float32)
+    rb = w // 32 * 34
+    kc = np.full((cap, rb), 7, np.uint8)
+    vc = np.full((cap, rb), 7, np.uint8)
+    orc.kv_append(k, v, kc, vc, synth.KV_Q8_0, pos)
+    for c, x in ((kc, k), (vc, v)):
+        want = np.concatenate([orc.q8_0_quantize_block(x[32 * i:32 * i + 32]) for i in range(w // 32)])
+        assert np.array_equal(c[pos], want)
+        assert np.all(np.delete(c, pos, axis=0) == 7)
+
+
+@pytest.mark.parametrize("H,Hk,d,L", [(4, 2, 32, 9), (14, 2, 64, 33), (28, 4, 128, 17)])
+def test_q8kv_attention_equals_dequantized_cache(orc, H, Hk, d, L):
+    """Attention over a packed cache equals, bit for bit, attention over an
+    f32 cache holding its dequantised values (exact in f32), and matches
+    numpy brute force."""
+    cap = L + 2
+    q = synth.normal_f32(5, "q8kv.q", H * d)
+    kc = synth.q8_kv_cache(5, "q8kv.kc", cap, Hk * d)
+    vc = synth.q8_kv_cache(5, "q8kv.vc", cap, Hk * d)
+    kf = np_dequant(kc, cap, Hk * d).astype(np.float32)
+    vf = np_dequant(vc, cap, Hk * d).astype(np.float32)
+    out, ab = orc.gqa_decode_attn(q, kc, vc, synth.KV_Q8_0, H, Hk, d, L, 1 / math.sqrt(d))
+    out2, ab2 = orc.gqa_decode_attn(q, kf, vf, synth.KV_F32, H, Hk, d, L, 1 / math.sqrt(d))
+    assert np.array_equal(out, out2) and np.array_equal(ab, ab2)
+    ref = np_attention(q, kf, vf, H, Hk, d, L, 1 / math.sqrt(d))
+    assert np.all(np.abs(out - ref) <= 1e-7 * ab)
+
+
+def test_q8kv_attention_single_position_returns_dequantized_v(orc):
+    H, Hk, d = 6, 2, 64
+    q = synth.normal_f32(6, "q8kv.q1", H * d) * 10
+    kc = synth.q8_kv_cache(6, "q8kv.k1", 3, Hk * d)
+    vc = synth.q8_kv_cache(6, "q8kv.v1", 3, Hk * d)
+    out, _ = orc.gqa_decode_attn(q, kc, vc, synth.KV_Q8_0, H, Hk, d, 1, 0.125)
+    v0 = np_dequant(vc, 3, Hk * d)[0].astype(np.float32)
+    for h in range(H):
+        g = h // (H // Hk)
+        assert np.array_equal(out[h * d:(h + 1) * d], v0[g * d:(g + 1) * d])

@@ -54,8 +54,9 @@ def test_reference_arm_other_ranks_do_nothing(capsys):
 
 
 def test_reference_arm_runs_the_requested_steps(capsys):
-    """Rank 0 of the reference arm times W untimed and exactly K timed oracle
-    sample steps and prints one JSON line with K, W and the sample."""
+    """Rank 0 of the reference arm times W untimed and exactly K timed whole
+    oracle decode steps and prints one JSON line whose ms_per_step * steps
+    is the timed wall time."""
     import json
 
     class A:
@@ -68,4 +69,6 @@ def test_reference_arm_runs_the_requested_steps(capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
-    assert "2 repetitions" in line["cpu_baseline"]["sample"]
+    assert "1 untimed, 2 timed" in line["cpu_baseline"]["sample"]
+    assert line["cpu_baseline"]["cpu_model"]
+    assert abs(line["ms_per_step"] * line["steps"] / 1e3 - line["steps"] / line["value"]) < 1e-6
