@@ -455,6 +455,44 @@ def attn_stress(q8d, H, Hk, D, reps, stream, flush, rank=0):
             "l2": "256 MB flush before each launch"}
 
 
+def attn_stress_q8(q8d, H, Hk, D, reps, stream, flush, rank=0):
+    """The same batch-8 ragged workload over a packed Q8_0 cache (34 bytes
+    per 32 elements: 0.53x the f16 bytes), L2 flushed before each launch."""
+    import torch
+
+    import synth
+    cap, kvw = STRESS_CAP, Hk * D
+    lens = synth.stream(0, "ragged.lens").integers(1, cap + 1, 8).tolist()
+    kc = synth.q8_matrix_torch(rank, "stress.kq8", 8 * cap, kvw, scale_lo=4e-3, scale_hi=3e-2)
+    vc = synth.q8_matrix_torch(rank, "stress.vq8", 8 * cap, kvw, scale_lo=4e-3, scale_hi=3e-2)
+    q = synth.normal_torch(rank, "stress.q", (8, H * D), torch.float32)
+    out = torch.empty(8, H * D, device="cuda")
+    wsb = q8d.q8d_gqa_workspace_bytes(8, H, Hk, D, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    with torch.cuda.stream(stream):
+        for rep in range(max(reps, 3) + 1):
+            flush.fill_(rep & 0xFF)
+            ev[0].record(stream)
+            q8d.q8d_gqa_decode_attn(q, None, None, kc, vc, q8d.Q8D_KV_Q8_0, out, 8, H, Hk, D, cap,
+                                    cap * kvw, lt, 1 / math.sqrt(D), ws, wsb, err, stream)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            if rep:
+                times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    assert err.item() == 0
+    t = statistics.median(times)
+    row_bytes = kvw // 32 * 34
+    nbytes = sum(2 * L * row_bytes + 4 * 2 * H * D for L in lens)
+    return {"kernel": "gqa_q8kv_kernel + gqa_combine_kernel (q8d_gqa_decode_attn, packed Q8_0 KV)",
+            "GB_s": nbytes / t / 1e9, "us_per_launch": t * 1e6, "kv_bytes": nbytes,
+            "batch": 8, "lengths": "seeded uniform in [1, 32768]", "sum_lengths": int(sum(lens)),
+            "l2": "256 MB flush before each launch"}
+
+
 # ---------------------------------------------------------------------------- small M
 SMALL_M = (1, 4, 16, 64)
 
@@ -795,6 +833,10 @@ def main():
         if shape.kv_dtype == synth.KV_F16 else None
     if stress is not None:
         stress["frac_of_peak"] = stress["GB_s"] / hbm
+    stress_q8 = attn_stress_q8(q8d, H, Hk, D, args.kernel_reps, stream, flush, rank) \
+        if shape.kv_dtype == synth.KV_F16 else None
+    if stress_q8 is not None:
+        stress_q8["frac_of_peak"] = stress_q8["GB_s"] / hbm
     small_m = small_m_leg(q8d, args.kernel_reps, stream, flush, hbm, rank) \
         if shape.name == "qwen2.5-7b" else None
 
@@ -850,6 +892,7 @@ def main():
                 "gqa_decode_attn": attn,
                 "gqa_decode_attn_ctx8192": attn_long,
                 "gqa_decode_attn_batch8_ragged": stress,
+                "gqa_decode_attn_batch8_ragged_q8_0_kv": stress_q8,
                 "q8_matmul_small_m": small_m,
             },
             "configs": configs,

@@ -36,6 +36,15 @@
  *               [g*head_dim, (g+1)*head_dim) of every row ("minfer Metal
  *               Backend Design" / "Metal Backend Optimizations", the
  *               [nkv][nk*hd] layout shared with llama.cpp).
+ *   Packed KV   Q8D_KV_Q8_0 ("minfer Metal Backend Design", "Execution
+ *               dispatch": packed q8_0 KV): the same [cap][kv_width] cache
+ *               stored as a Q8_0 matrix, row t = kv_width/32 consecutive
+ *               34-byte blocks starting at byte t * kv_width/32 * 34, so
+ *               KV head g is blocks [g*head_dim/32, (g+1)*head_dim/32).
+ *               Rows are written by the Q8_0 quantizer: per block
+ *               d = max|x| / 127, q_j = x_j * (1/d) rounded to nearest with
+ *               halves away from zero, scale = d rounded to binary16, all in
+ *               f32 (an all-zero block stores zeros); inputs must be finite.
  */
 #ifndef Q8D_H
 #define Q8D_H
@@ -58,6 +67,7 @@ extern "C" {
 
 #define Q8D_KV_F32 0
 #define Q8D_KV_F16 1
+#define Q8D_KV_Q8_0 2 /* packed: every cache row is kv_width/32 Q8_0 blocks */
 
 /* Bits of the device-side error word. */
 #define Q8D_DERR_POS_RANGE 0x1   /* append position outside [0, cap)          */
@@ -105,11 +115,14 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
  * q8d_kv_append — write one token's K and V rows into the caches
  * ("IV.4: One command buffer per token", "Eight kernels": append_kv).
  *   kcache[pos][i] = cvt(k[i]), vcache[pos][i] = cvt(v[i]), i < kv_width
- * cvt is the identity for an f32 cache and round-to-nearest-even to binary16
- * for an f16 cache.  pos is read from device memory (*d_pos) so a captured
- * graph replays unchanged; pos outside [0, cap) sets Q8D_DERR_POS_RANGE in
- * *d_err and writes nothing.  k, v: device f32[kv_width]; caches: device,
- * [cap][kv_width]; d_err: device int (OR-ed into, never cleared).
+ * cvt is the identity for an f32 cache, round-to-nearest-even to binary16
+ * for an f16 cache and the Q8_0 quantizer of each 32-element block for a
+ * packed cache (kv_width % 32 == 0, else Q8D_EUNSUPPORTED; the stored bytes
+ * equal a scalar CPU quantizer's).  pos is read from device memory (*d_pos)
+ * so a captured graph replays unchanged; pos outside [0, cap) sets
+ * Q8D_DERR_POS_RANGE in *d_err and writes nothing.  k, v: device
+ * f32[kv_width]; caches: device, cap rows (a packed cache 16-byte aligned,
+ * else Q8D_EALIGN); d_err: device int (OR-ed into, never cleared).
  * ---------------------------------------------------------------------- */
 int q8d_kv_append(const float* k, const float* v, void* kcache, void* vcache, int kv_dtype,
                   int kv_width, int cap, const int* d_pos, int* d_err, void* stream);

@@ -26,6 +26,7 @@ Q8D_ENOMEM = -7
 
 Q8D_KV_F32 = 0
 Q8D_KV_F16 = 1
+Q8D_KV_Q8_0 = 2
 
 Q8D_DERR_POS_RANGE = 0x1
 Q8D_DERR_LEN_RANGE = 0x2

@@ -205,11 +205,14 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
 int q8d_kv_append(const float* k, const float* v, void* kcache, void* vcache, int kv_dtype,
                   int kv_width, int cap, const int* d_pos, int* d_err, void* stream) {
   if (!k || !v || !kcache || !vcache || !d_pos || kv_width <= 0 || cap <= 0) return Q8D_EINVAL;
-  if (kv_dtype != Q8D_KV_F32 && kv_dtype != Q8D_KV_F16) return Q8D_EUNSUPPORTED;
-  const size_t es = kv_dtype == Q8D_KV_F16 ? 2 : 4;
+  if (kv_dtype != Q8D_KV_F32 && kv_dtype != Q8D_KV_F16 && kv_dtype != Q8D_KV_Q8_0)
+    return Q8D_EUNSUPPORTED;
+  if (kv_dtype == Q8D_KV_Q8_0 && kv_width % 32) return Q8D_EUNSUPPORTED;
+  // (a packed cache's blocks are written with 16-bit scale stores)
+  const size_t es = kv_dtype == Q8D_KV_F32 ? 4 : (kv_dtype == Q8D_KV_F16 ? 2 : 16);
   if (!aligned(kcache, es) || !aligned(vcache, es) || !aligned(k, 4) || !aligned(v, 4))
     return Q8D_EALIGN;
-  const size_t cb = es * (size_t)kv_width * cap;
+  const size_t cb = kv_dtype == Q8D_KV_Q8_0 ? q8_bytes(cap, kv_width) : es * (size_t)kv_width * cap;
   if (overlap(kcache, cb, vcache, cb)) return Q8D_EINVAL;
   return kv_append_launch(k, v, kcache, vcache, kv_dtype, kv_width, cap, d_pos, d_err,
                           static_cast<cudaStream_t>(stream));
@@ -230,14 +233,19 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
   if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || cap <= 0) return Q8D_EINVAL;
   if (head_dim != 64 && head_dim != 128) return Q8D_EUNSUPPORTED;
   if (n_heads % n_kv_heads || n_heads / n_kv_heads > 16) return Q8D_EUNSUPPORTED;
-  if (kv_dtype != Q8D_KV_F32 && kv_dtype != Q8D_KV_F16) return Q8D_EUNSUPPORTED;
+  if (kv_dtype != Q8D_KV_F32 && kv_dtype != Q8D_KV_F16 && kv_dtype != Q8D_KV_Q8_0)
+    return Q8D_EUNSUPPORTED;
   if (!std::isfinite(scale)) return Q8D_EINVAL;
   const long long kvw = (long long)n_kv_heads * head_dim;
-  const int es = kv_dtype == Q8D_KV_F16 ? 2 : 4;
   if (batch > 1 && cache_batch_stride < kvw * cap) return Q8D_EINVAL;
   if (cache_batch_stride < 0) return Q8D_EINVAL;
-  if (!aligned(kcache, 16) || !aligned(vcache, 16) || ((cache_batch_stride * es) % 16))
-    return Q8D_EALIGN;
+  // sequence starts 16-byte aligned: for a packed cache the stride (in
+  // elements) is a whole number of blocks, 34 bytes per 32 elements
+  const long long stride_bytes =
+      kv_dtype == Q8D_KV_Q8_0
+          ? (cache_batch_stride % 32 ? 1 : cache_batch_stride / 32 * 34)
+          : cache_batch_stride * (kv_dtype == Q8D_KV_F16 ? 2 : 4);
+  if (!aligned(kcache, 16) || !aligned(vcache, 16) || (stride_bytes % 16)) return Q8D_EALIGN;
   if (!aligned(q, 4) || !aligned(out, 4) || !aligned(workspace, 16)) return Q8D_EALIGN;
   if (ws_bytes < attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, cap))
     return Q8D_ERANGE;

@@ -413,6 +413,27 @@ __global__ void kv_append_kernel(const float* k, const float* v, KT* kc, KT* vc,
   }
 }
 
+// Packed Q8_0 store: one warp per 32-element block, the k blocks then the
+// v blocks of the row.
+__global__ void kv_append_q8_kernel(const float* k, const float* v, uint8_t* kc, uint8_t* vc,
+                                    int kvw, int cap, const int* d_pos, int* d_err) {
+  const int pos = *d_pos;
+  if (pos < 0 || pos >= cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && d_err) atomicOr(d_err, Q8D_DERR_POS_RANGE);
+    return;
+  }
+  const int nb = kvw / kQBlock, lane = threadIdx.x & 31;
+  const long long rowb = (long long)nb * kQBlockBytes;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < 2 * nb; w += nwarps) {
+    const bool isv = w >= nb;
+    const int b = isv ? w - nb : w;
+    const float x = (isv ? v : k)[b * kQBlock + lane];
+    quantize_q8_0_warp(x, (isv ? vc : kc) + (long long)pos * rowb + (long long)b * kQBlockBytes,
+                       lane);
+  }
+}
+
 template <int D, typename KT, int GMAX>
 int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
   using C = AttnCfg<D, KT, GMAX>;
@@ -472,6 +493,7 @@ int attn_launch(AttnParams P, cudaStream_t stream) {
   P.ws_m = ws + (size_t)P.batch * P.n_heads * nc * P.head_dim;
   P.ws_l = P.ws_m + (size_t)P.batch * P.n_heads * nc;
   if (P.kv_dtype == Q8D_KV_F16) return attn_mma_launch(P, stream);
+  if (P.kv_dtype == Q8D_KV_Q8_0) return attn_q8kv_launch(P, stream);
   if (P.head_dim == 128) return launch_attn_g<128, float>(P, stream);
   return launch_attn_g<64, float>(P, stream);
 }
@@ -479,6 +501,13 @@ int attn_launch(AttnParams P, cudaStream_t stream) {
 int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,
                      int cap, const int* d_pos, int* d_err, cudaStream_t stream) {
   const int threads = 256, blocks = std::max(1, std::min(64, (kvw + threads - 1) / threads));
+  if (kv_dtype == Q8D_KV_Q8_0) {
+    const int qblocks = std::max(1, std::min(64, (2 * (kvw / kQBlock) * 32 + threads - 1) / threads));
+    kv_append_q8_kernel<<<qblocks, threads, 0, stream>>>(k, v, static_cast<uint8_t*>(kc),
+                                                         static_cast<uint8_t*>(vc), kvw, cap,
+                                                         d_pos, d_err);
+    return check_launch();
+  }
   if (kv_dtype == Q8D_KV_F16)
     kv_append_kernel<__half><<<blocks, threads, 0, stream>>>(
         k, v, reinterpret_cast<__half*>(kc), reinterpret_cast<__half*>(vc), kvw, cap, d_pos, d_err);

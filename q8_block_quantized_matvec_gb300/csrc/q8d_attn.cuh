@@ -96,6 +96,7 @@ int attn_ctas_per_head(int batch, int n_kv_heads, int max_len);
 int attn_chunks(int batch, int n_kv_heads, int max_len);
 int attn_combine_launch(const AttnParams& P, cudaStream_t stream);
 int attn_mma_launch(const AttnParams& P, cudaStream_t stream);  // f16 cache, tensor cores
+int attn_q8kv_launch(const AttnParams& P, cudaStream_t stream);  // packed Q8_0 cache
 size_t attn_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim, int max_len);
 int attn_launch(AttnParams P, cudaStream_t stream);
 int kv_append_launch(const float* k, const float* v, void* kc, void* vc, int kv_dtype, int kvw,

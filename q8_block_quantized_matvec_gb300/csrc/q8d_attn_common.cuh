@@ -40,4 +40,26 @@ __device__ __forceinline__ void head_prologue(float (&v)[D / 32], int lane, cons
   }
 }
 
+// Q8_0 store of one 32-element block held by a warp (lane j holds element
+// j): the packed KV cache's quantizer ("minfer Metal Backend Design",
+// "Execution dispatch": the store is byte-identical to the CPU quantizer,
+// read as the Q8_0 format's reference quantizer in f32):
+//   amax = max |x|, d = amax / 127, id = d != 0 ? 1 / d : 0,
+//   q_j = x_j * id rounded to nearest with halves away from zero (roundf),
+//   scale = d rounded to binary16 (nearest even).
+// Every operation is a correctly rounded f32 operation (IEEE division, a
+// single product, no contraction), so the bytes match a scalar CPU
+// quantizer bit for bit.  blk: the block's 34 bytes in global memory, at
+// an even address (the scale is written with one 16-bit store).
+__device__ __forceinline__ void quantize_q8_0_warp(float x, uint8_t* blk, int lane) {
+  float amax = fabsf(x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float id = d != 0.f ? __fdiv_rn(1.0f, d) : 0.f;
+  const int q = (int)roundf(__fmul_rn(x, id));
+  blk[2 + lane] = (uint8_t)(int8_t)q;
+  if (lane == 0) *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(__float2half_rn(d));
+}
+
 }  // namespace q8d

@@ -81,6 +81,10 @@ def test_kv_append_refusals(q8d):
     assert L.q8d_kv_append(None, B16, C16, C16 + 4096, 1, 64, 8, A16, A16, None) == q8d.Q8D_EINVAL
     assert L.q8d_kv_append(A16, B16, C16, C16 + 4096, 1, 64, 8, None, A16, None) == q8d.Q8D_EINVAL
     assert L.q8d_kv_append(A16, B16, C16, C16 + 64, 1, 64, 8, A16, A16, None) == q8d.Q8D_EINVAL  # caches overlap
+    # packed Q8_0: rows must be whole blocks; caches of cap * kv_width/32 * 34 bytes
+    assert L.q8d_kv_append(A16, B16, C16, C16 + 4096, 2, 48, 8, A16, A16, None) == q8d.Q8D_EUNSUPPORTED
+    assert L.q8d_kv_append(A16, B16, C16, C16 + 496, 2, 64, 8, A16, A16, None) == q8d.Q8D_EINVAL
+    assert L.q8d_kv_append(A16, B16, C16 + 2, C16 + 4096, 2, 64, 8, A16, A16, None) == q8d.Q8D_EALIGN
 
 
 def attn(q8d, **kw):
@@ -105,6 +109,10 @@ def test_attention_refusals(q8d):
     assert attn(q8d, batch=2, stride=100) == q8d.Q8D_EINVAL        # sequences would overlap
     assert attn(q8d, wsb=16) == q8d.Q8D_ERANGE
     assert attn(q8d, scale=float("inf")) == q8d.Q8D_EINVAL
+    # packed cache: sequence starts (stride / 32 * 34 bytes) must be 16-byte aligned
+    big = 64 * 1024 * 128
+    assert attn(q8d, dt=2, batch=2, stride=big + 32) == q8d.Q8D_EALIGN
+    assert attn(q8d, dt=2, batch=2, stride=big + 8) == q8d.Q8D_EALIGN
 
 
 def test_step_create_refusals(q8d):
