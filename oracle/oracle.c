@@ -405,6 +405,46 @@ int orc_gqa_decode_attn(const float* q, const void* kc, const void* vc, int kv_d
 }
 
 /* ------------------------------------------------------------------------ */
+/* Windowed decode attention ([P1] "Execution dispatch", window modes: an    */
+/* explicit [lo, hi) span, or a map of up to four (cell, len) runs per       */
+/* query, e.g. a shared prefix plus a private run).  The query attends to    */
+/* exactly the cells of its runs: the plain definition is the attention     */
+/* above over the cache rows of the runs gathered in run order (a softmax    */
+/* over a set; the order changes rounding only).  runs: nruns (cell, len)   */
+/* pairs; every run inside [0, cap) and at least one row in all, else -1.    */
+/* Pinned by tests: one run [0, L) equals the causal attention bitwise, a   */
+/* one-cell window returns that cell's V row bitwise, brute force over     */
+/* gathered rows, and a window shifted by one cell changes the output.     */
+/* ------------------------------------------------------------------------ */
+int orc_gqa_decode_attn_runs(const float* q, const void* kc, const void* vc, int kv_dtype,
+                             int n_heads, int n_kv_heads, int head_dim, int cap, const int* runs,
+                             int nruns, float scale, float* out, double* absterm) {
+  int kvw = n_kv_heads * head_dim;
+  if (kv_dtype == ORC_KV_Q8_0 && kvw % ORC_QBLOCK) return -1;
+  size_t rb = orc_kv_row_bytes(kv_dtype, kvw);
+  int64_t total = 0;
+  for (int r = 0; r < nruns; ++r) {
+    int cell = runs[2 * r], len = runs[2 * r + 1];
+    if (cell < 0 || len < 0 || (int64_t)cell + len > cap) return -1;
+    total += len;
+  }
+  if (total < 1) return -1;
+  uint8_t* kg = (uint8_t*)malloc(rb * (size_t)total);
+  uint8_t* vg = (uint8_t*)malloc(rb * (size_t)total);
+  int64_t w = 0;
+  for (int r = 0; r < nruns; ++r)
+    for (int t = 0; t < runs[2 * r + 1]; ++t, ++w) {
+      memcpy(kg + (size_t)w * rb, (const uint8_t*)kc + (size_t)(runs[2 * r] + t) * rb, rb);
+      memcpy(vg + (size_t)w * rb, (const uint8_t*)vc + (size_t)(runs[2 * r] + t) * rb, rb);
+    }
+  int rc = orc_gqa_decode_attn(q, kg, vg, kv_dtype, n_heads, n_kv_heads, head_dim, (int)total,
+                               scale, out, absterm);
+  free(kg);
+  free(vg);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Decode-step glue ([P3] "Eight kernels": rms_norm_row, rope_row,           */
 /* add_inplace, silu_hadamard, argmax_row; "The decoder": embed_row).       */
 /* ------------------------------------------------------------------------ */

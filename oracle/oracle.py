@@ -73,6 +73,9 @@ def _declare(L):
     L.orc_q8_0_quantize_block.argtypes = [vp, vp]
     L.orc_gqa_decode_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     L.orc_gqa_decode_attn.restype = i32
+    L.orc_gqa_decode_attn_runs.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, f32, vp,
+                                           vp]
+    L.orc_gqa_decode_attn_runs.restype = i32
     L.orc_rmsnorm.argtypes = [vp, vp, i32, C.c_double, vp]
     L.orc_rope_head.argtypes = [vp, i32, i64, C.c_double]
     L.orc_silu_mul.argtypes = [C.c_double, C.c_double]
@@ -179,6 +182,25 @@ def gqa_decode_attn(q, kc, vc, kv_dtype: int, n_heads: int, n_kv_heads: int, hea
                                    int(L), float(scale), _p(out), _p(ab))
     if rc != 0:
         raise ValueError("oracle attention: bad arguments")
+    return out, ab
+
+
+def gqa_decode_attn_runs(q, kc, vc, kv_dtype: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                         runs, scale: float):
+    """Windowed attention of one query: the cache rows of `runs` ((cell, len)
+    pairs over a cache of kc.shape[0] rows).  Returns (out f32[H*d],
+    absterm f64[H*d])."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    kc = np.ascontiguousarray(kc)
+    vc = np.ascontiguousarray(vc)
+    r = np.ascontiguousarray(np.asarray(runs, dtype=np.int32).reshape(-1, 2))
+    out = np.empty(n_heads * head_dim, dtype=np.float32)
+    ab = np.empty(n_heads * head_dim, dtype=np.float64)
+    rc = lib().orc_gqa_decode_attn_runs(_p(q), _p(kc), _p(vc), kv_dtype, n_heads, n_kv_heads,
+                                        head_dim, kc.shape[0], _p(r), r.shape[0], float(scale),
+                                        _p(out), _p(ab))
+    if rc != 0:
+        raise ValueError("oracle windowed attention: bad runs")
     return out, ab
 
 

@@ -498,3 +498,59 @@ def test_q8kv_attention_single_position_returns_dequantized_v(orc):
     for h in range(H):
         g = h // (H // Hk)
         assert np.array_equal(out[h * d:(h + 1) * d], v0[g * d:(g + 1) * d])
+
+
+# --------------------------------------------------------------------------- windowed attention
+@pytest.mark.parametrize("dtype", [synth.KV_F32, synth.KV_F16, synth.KV_Q8_0])
+def test_window_full_span_is_causal_attention(orc, dtype):
+    H, Hk, d, L, cap = 6, 2, 64, 37, 50
+    q = synth.normal_f32(11, "w.q", H * d)
+    if dtype == synth.KV_Q8_0:
+        kc, vc = synth.q8_kv_cache(11, "w.k", cap, Hk * d), synth.q8_kv_cache(11, "w.v", cap, Hk * d)
+    else:
+        dt = np.float16 if dtype == synth.KV_F16 else np.float32
+        kc = synth.normal_f32(11, "w.k", (cap, Hk * d)).astype(dt)
+        vc = synth.normal_f32(11, "w.v", (cap, Hk * d)).astype(dt)
+    a, aa = orc.gqa_decode_attn(q, kc, vc, dtype, H, Hk, d, L, 0.125)
+    b, bb = orc.gqa_decode_attn_runs(q, kc, vc, dtype, H, Hk, d, [(0, L)], 0.125)
+    assert np.array_equal(a, b) and np.array_equal(aa, bb)
+
+
+@pytest.mark.parametrize("cell", [0, 17, 49])
+def test_window_one_cell_returns_that_v_row(orc, cell):
+    """The pages' one-cell window gate: the named cell's V row, bitwise."""
+    H, Hk, d, cap = 6, 3, 32, 50
+    q = synth.normal_f32(12, "w1.q", H * d) * 20
+    kc = synth.normal_f16(12, "w1.k", (cap, Hk * d))
+    vc = synth.normal_f16(12, "w1.v", (cap, Hk * d))
+    out, _ = orc.gqa_decode_attn_runs(q, kc, vc, synth.KV_F16, H, Hk, d, [(cell, 1), (0, 0)], 0.3)
+    for h in range(H):
+        g = h // (H // Hk)
+        assert np.array_equal(out[h * d:(h + 1) * d], vc[cell, g * d:(g + 1) * d].astype(np.float32))
+
+
+def test_window_runs_brute_force_and_shift_control(orc):
+    """A shared prefix run plus a gapped private run against numpy over the
+    gathered rows; shifting the private run by one cell changes the output;
+    swapping the runs' order changes only rounding."""
+    H, Hk, d, cap = 8, 2, 64, 120
+    q = synth.normal_f32(13, "wr.q", H * d)
+    kc = synth.normal_f32(13, "wr.k", (cap, Hk * d))
+    vc = synth.normal_f32(13, "wr.v", (cap, Hk * d))
+    runs = [(0, 20), (60, 15)]
+    out, ab = orc.gqa_decode_attn_runs(q, kc, vc, synth.KV_F32, H, Hk, d, runs, 0.125)
+    rows = list(range(0, 20)) + list(range(60, 75))
+    ref = np_attention(q, kc[rows], vc[rows], H, Hk, d, len(rows), 0.125)
+    assert np.all(np.abs(out - ref) <= 1e-7 * ab)
+    shifted, _ = orc.gqa_decode_attn_runs(q, kc, vc, synth.KV_F32, H, Hk, d, [(0, 20), (61, 15)], 0.125)
+    assert not np.array_equal(out, shifted)
+    swapped, _ = orc.gqa_decode_attn_runs(q, kc, vc, synth.KV_F32, H, Hk, d, runs[::-1], 0.125)
+    assert np.all(np.abs(out - swapped) <= 1e-7 * ab)
+
+
+def test_window_refuses_bad_runs(orc):
+    q = np.zeros(64, np.float32)
+    kc = np.zeros((10, 64), np.float32)
+    for runs in ([(0, 0)], [(-1, 3)], [(8, 3)], [(0, 5), (9, 2)]):
+        with pytest.raises(ValueError):
+            orc.gqa_decode_attn_runs(q, kc, kc, synth.KV_F32, 1, 1, 64, runs, 1.0)
