@@ -165,6 +165,36 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
                         int* d_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * q8d_gqa_decode_attn_window — q8d_gqa_decode_attn over explicit KV windows
+ * ("minfer Metal Backend Design", "Execution dispatch", window modes: an
+ * explicit [lo, hi) span per query, or a map of up to four (cell, len) runs
+ * per query, e.g. a prefix shared by several sequences plus a private run).
+ * Sequence s attends exactly the cache rows of its runs, in run order:
+ *   d_runs:  device int [batch][Q8D_MAX_RUNS][2], run r of sequence s is
+ *            (cell, len) = (d_runs[s][r][0], d_runs[s][r][1]), the rows
+ *            [cell, cell + len) of sequence s's cache; unused runs have
+ *            len 0.  A span [lo, hi) is the single run (lo, hi - lo).
+ *            Every run must lie in [0, cap) (0 <= cell, 0 <= len,
+ *            cell + len <= cap) and the runs must hold at least one row in
+ *            all, else Q8D_DERR_LEN_RANGE is set in *d_err and the
+ *            sequence's outputs are NaN.
+ *   cache_batch_stride: as for q8d_gqa_decode_attn, or 0: every sequence
+ *            reads the same cache (shared cells, e.g. a common prefix).
+ * With k_new/v_new the rounded new rows are first written at the LAST row
+ * of each sequence's window (the last row of its last non-empty run) and
+ * attended to; that row must not be read by another sequence of the same
+ * call (the calls' writes and reads would race).
+ * Other arguments, the workspace and the results are those of
+ * q8d_gqa_decode_attn (f32, f16 and packed Q8_0 caches).
+ * ---------------------------------------------------------------------- */
+#define Q8D_MAX_RUNS 4
+int q8d_gqa_decode_attn_window(const float* q, const float* k_new, const float* v_new,
+                               void* kcache, void* vcache, int kv_dtype, float* out, int batch,
+                               int n_heads, int n_kv_heads, int head_dim, int cap,
+                               long long cache_batch_stride, const int* d_runs, float scale,
+                               void* workspace, size_t ws_bytes, int* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * q8d_gqa_decode_attn_noalloc — q8d_gqa_decode_attn without a caller
  * workspace.  The pages have no counterpart to this entry point.
  * It exists for callers that cannot allocate device memory: code whose

@@ -28,6 +28,8 @@ Q8D_KV_F32 = 0
 Q8D_KV_F16 = 1
 Q8D_KV_Q8_0 = 2
 
+Q8D_MAX_RUNS = 4
+
 Q8D_DERR_POS_RANGE = 0x1
 Q8D_DERR_LEN_RANGE = 0x2
 Q8D_DERR_TOKEN_RANGE = 0x4
@@ -84,6 +86,9 @@ def lib():
         L.q8d_gqa_decode_attn.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                           i64, vp, f32, vp, sz, vp, vp]
         L.q8d_gqa_decode_attn.restype = i32
+        L.q8d_gqa_decode_attn_window.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                 i32, i64, vp, f32, vp, sz, vp, vp]
+        L.q8d_gqa_decode_attn_window.restype = i32
         L.q8d_noalloc_scratch_bytes.argtypes = []
         L.q8d_noalloc_scratch_bytes.restype = sz
         L.q8d_gqa_decode_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
@@ -171,6 +176,17 @@ def q8d_gqa_decode_attn(q, k_new, v_new, kcache, vcache, kv_dtype: int, out, bat
         int(batch), int(n_heads), int(n_kv_heads), int(head_dim), int(cap),
         int(cache_batch_stride), _ptr(d_lens), float(scale), _ptr(workspace), int(ws_bytes),
         _ptr(d_err), _stream(stream)), "q8d_gqa_decode_attn")
+
+
+def q8d_gqa_decode_attn_window(q, k_new, v_new, kcache, vcache, kv_dtype: int, out, batch: int,
+                               n_heads: int, n_kv_heads: int, head_dim: int, cap: int,
+                               cache_batch_stride: int, d_runs, scale: float, workspace,
+                               ws_bytes: int, d_err, stream=None) -> int:
+    return _check(lib().q8d_gqa_decode_attn_window(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), int(kv_dtype), _ptr(out),
+        int(batch), int(n_heads), int(n_kv_heads), int(head_dim), int(cap),
+        int(cache_batch_stride), _ptr(d_runs), float(scale), _ptr(workspace), int(ws_bytes),
+        _ptr(d_err), _stream(stream)), "q8d_gqa_decode_attn_window")
 
 
 def q8d_noalloc_scratch_bytes() -> int:

@@ -223,12 +223,17 @@ size_t q8d_gqa_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_
   return attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, max_len);
 }
 
-int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, void* kcache,
-                        void* vcache, int kv_dtype, float* out, int batch, int n_heads,
-                        int n_kv_heads, int head_dim, int cap, long long cache_batch_stride,
-                        const int* d_lens, float scale, void* workspace, size_t ws_bytes,
-                        int* d_err, void* stream) {
-  if (!q || !kcache || !vcache || !out || !d_lens || !workspace) return Q8D_EINVAL;
+}  // extern "C"
+
+namespace q8d {
+// Shared checks and launch of the causal (d_lens) and windowed (d_runs)
+// decode attention; shared_cache: sequences may share one cache (stride 0).
+static int attn_entry(const float* q, const float* k_new, const float* v_new, void* kcache,
+                      void* vcache, int kv_dtype, float* out, int batch, int n_heads,
+                      int n_kv_heads, int head_dim, int cap, long long cache_batch_stride,
+                      const int* d_lens, const int* d_runs, float scale, void* workspace,
+                      size_t ws_bytes, int* d_err, cudaStream_t stream) {
+  if (!q || !kcache || !vcache || !out || !(d_lens || d_runs) || !workspace) return Q8D_EINVAL;
   if ((k_new == nullptr) != (v_new == nullptr)) return Q8D_EINVAL;
   if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || cap <= 0) return Q8D_EINVAL;
   if (head_dim != 64 && head_dim != 128) return Q8D_EUNSUPPORTED;
@@ -237,8 +242,10 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
     return Q8D_EUNSUPPORTED;
   if (!std::isfinite(scale)) return Q8D_EINVAL;
   const long long kvw = (long long)n_kv_heads * head_dim;
-  if (batch > 1 && cache_batch_stride < kvw * cap) return Q8D_EINVAL;
   if (cache_batch_stride < 0) return Q8D_EINVAL;
+  // sequences own disjoint caches, or (run maps only) share one cache
+  if (batch > 1 && cache_batch_stride < kvw * cap && !(d_runs && cache_batch_stride == 0))
+    return Q8D_EINVAL;
   // sequence starts 16-byte aligned: for a packed cache the stride (in
   // elements) is a whole number of blocks, 34 bytes per 32 elements
   const long long stride_bytes =
@@ -247,6 +254,7 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
           : cache_batch_stride * (kv_dtype == Q8D_KV_F16 ? 2 : 4);
   if (!aligned(kcache, 16) || !aligned(vcache, 16) || (stride_bytes % 16)) return Q8D_EALIGN;
   if (!aligned(q, 4) || !aligned(out, 4) || !aligned(workspace, 16)) return Q8D_EALIGN;
+  if (d_runs && !aligned(d_runs, 4)) return Q8D_EALIGN;
   if (ws_bytes < attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, cap))
     return Q8D_ERANGE;
   AttnParams A{};
@@ -264,12 +272,38 @@ int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, 
   A.cap = cap;
   A.batch_stride = cache_batch_stride;
   A.d_lens = d_lens;
+  A.d_runs = d_runs;
   A.scale = scale;
   A.workspace = workspace;
   A.nc = attn_chunks(batch, n_kv_heads, cap);
   A.nct = attn_ctas_per_head(batch, n_kv_heads, cap);
   A.d_err = d_err;
-  return attn_launch(A, static_cast<cudaStream_t>(stream));
+  return attn_launch(A, stream);
+}
+}  // namespace q8d
+
+extern "C" {
+
+int q8d_gqa_decode_attn(const float* q, const float* k_new, const float* v_new, void* kcache,
+                        void* vcache, int kv_dtype, float* out, int batch, int n_heads,
+                        int n_kv_heads, int head_dim, int cap, long long cache_batch_stride,
+                        const int* d_lens, float scale, void* workspace, size_t ws_bytes,
+                        int* d_err, void* stream) {
+  if (!d_lens) return Q8D_EINVAL;
+  return attn_entry(q, k_new, v_new, kcache, vcache, kv_dtype, out, batch, n_heads, n_kv_heads,
+                    head_dim, cap, cache_batch_stride, d_lens, nullptr, scale, workspace,
+                    ws_bytes, d_err, static_cast<cudaStream_t>(stream));
+}
+
+int q8d_gqa_decode_attn_window(const float* q, const float* k_new, const float* v_new,
+                               void* kcache, void* vcache, int kv_dtype, float* out, int batch,
+                               int n_heads, int n_kv_heads, int head_dim, int cap,
+                               long long cache_batch_stride, const int* d_runs, float scale,
+                               void* workspace, size_t ws_bytes, int* d_err, void* stream) {
+  if (!d_runs) return Q8D_EINVAL;
+  return attn_entry(q, k_new, v_new, kcache, vcache, kv_dtype, out, batch, n_heads, n_kv_heads,
+                    head_dim, cap, cache_batch_stride, nullptr, d_runs, scale, workspace,
+                    ws_bytes, d_err, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   float* l_run = m_run + GMAX;
   float* corr = l_run + GMAX;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  __shared__ AttnWindow s_win;  // this sequence's window (row t -> cache row)
 
   const int g = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -104,8 +105,8 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   griddep_launch_dependents();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
-  const int L = P.d_lens[b];
-  if (!attn_len_ok(P, L)) {  // (the combine writes NaN outputs)
+  const int L = attn_window_len(P, b);
+  if (L < 1) {  // (the combine writes NaN outputs)
     if (g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
     return;
   }
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   const int t_begin = c * tpc;
   if (t_begin >= L) return;
   const int t_end = min(L, t_begin + tpc);
+  if (tid == 0) attn_window_store(P, b, &s_win);  // (read after the barrier before the loads)
   const long long kvw = (long long)P.n_kv_heads * D;
   KT* kbase = reinterpret_cast<KT*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
   KT* vbase = reinterpret_cast<KT*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
     else
       head_prologue<D>(v, lane, P.bv ? P.bv + (long long)g * D : nullptr, nullptr, 0.f, nullptr,
                        nullptr);
-    KT* dst = (warp == 0 ? kbase : vbase) + (long long)(L - 1) * kvw;
+    KT* dst = (warp == 0 ? kbase : vbase) + (long long)attn_cell(P, b, L - 1) * kvw;
 #pragma unroll
     for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = to_cache<KT>(v[t]);
     fence_proxy_async_global();
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
     if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)(2 * nr * C::kRowBytes));
     __syncwarp();
     for (int r = lane; r < nr; r += 32) {
-      const long long row = (long long)(r0 + r) * kvw;
+      const long long row = (long long)s_win.cell_of(r0 + r) * kvw;
       bulk_g2s(st + r * C::kKStride, kbase + row, C::kRowBytes, &bar[k & 1], pol);
       bulk_g2s(st + C::kTS * C::kKStride + r * C::kRowBytes, vbase + row, C::kRowBytes,
                &bar[k & 1], pol);
@@ -339,9 +341,9 @@ __global__ void __launch_bounds__(kCombGroups * D) gqa_combine_kernel(const Attn
   const int b = hq / P.n_heads;
   const int j = threadIdx.x % D, grp = threadIdx.x / D;
   griddep_wait();  // the partials of the attention grid are complete and visible
-  const int L = P.d_lens[b];
+  const int L = attn_window_len(P, b);
   float* o = P.out + (long long)hq * D;
-  if (!attn_len_ok(P, L)) {
+  if (L < 1) {
     if (grp == 0) o[j] = __int_as_float(0x7fc00000);
     return;
   }

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   extern __shared__ __align__(128) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
   float* fh = reinterpret_cast<float*>(smem + C::kOffF);
+  __shared__ AttnWindow s_win;  // this sequence's window (row t -> cache row)
 
   const int g = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -109,8 +110,8 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   griddep_launch_dependents();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
-  const int L = P.d_lens[b];
-  if (!attn_len_ok(P, L)) {  // (the combine writes NaN outputs)
+  const int L = attn_window_len(P, b);
+  if (L < 1) {  // (the combine writes NaN outputs)
     if (g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
     return;
   }
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   const int t_begin = c * tpc;
   if (t_begin >= L) return;
   const int t_end = min(L, t_begin + tpc);
+  if (tid == 0) attn_window_store(P, b, &s_win);  // (read after the barrier before the loads)
   const long long kvw = (long long)P.n_kv_heads * D;
   __half* kbase = reinterpret_cast<__half*>(P.kcache) + (long long)b * P.batch_stride + (long long)g * D;
   __half* vbase = reinterpret_cast<__half*>(P.vcache) + (long long)b * P.batch_stride + (long long)g * D;
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     else
       head_prologue<D>(v, lane, P.bv ? P.bv + (long long)g * D : nullptr, nullptr, 0.f, nullptr,
                        nullptr);
-    __half* dst = (warp == 0 ? kbase : vbase) + (long long)(L - 1) * kvw;
+    __half* dst = (warp == 0 ? kbase : vbase) + (long long)attn_cell(P, b, L - 1) * kvw;
 #pragma unroll
     for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = __float2half_rn(v[t]);
   }
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
       for (int e = lane; e < kGroup * kChunks; e += 32) {
         const int r = e / kChunks, pc = e % kChunks;
         if (r < nr) {
-          const long long off = (long long)(t0 + r) * kvw * 2 + pc * 16;
+          const long long off = (long long)s_win.cell_of(t0 + r) * kvw * 2 + pc * 16;
           cp_async16(st + r * C::kStride + pc * 16, reinterpret_cast<const uint8_t*>(kbase) + off);
           cp_async16(st + (kGroup + r) * C::kStride + pc * 16,
                      reinterpret_cast<const uint8_t*>(vbase) + off);

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
   extern __shared__ __align__(128) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
   float* fh = reinterpret_cast<float*>(smem + C::kOffF);
+  __shared__ AttnWindow s_win;  // this sequence's window (row t -> cache row)
 
   const int g = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -148,8 +149,8 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
   griddep_launch_dependents();  // the combine may be scheduled now
   int b, c, n;
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
-  const int L = P.d_lens[b];
-  if (!attn_len_ok(P, L)) {
+  const int L = attn_window_len(P, b);
+  if (L < 1) {
     if (g == 0 && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_LEN_RANGE);
     return;
   }
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
   const int t_begin = c * tpc;
   if (t_begin >= L) return;
   const int t_end = min(L, t_begin + tpc);
+  if (tid == 0) attn_window_store(P, b, &s_win);  // (read after the barrier before the loads)
   const long long rowb = (long long)P.n_kv_heads * C::kRowB;  // packed cache row
   // sequence b's cache starts at its element offset b * stride, i.e. at
   // block b * stride / 32
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
     else
       head_prologue<D>(v, lane, P.bv ? P.bv + (long long)g * D : nullptr, nullptr, 0.f, nullptr,
                        nullptr);
-    uint8_t* dst = (warp == 0 ? kbase : vbase) + (long long)(L - 1) * rowb;
+    uint8_t* dst = (warp == 0 ? kbase : vbase) + (long long)attn_cell(P, b, L - 1) * rowb;
 #pragma unroll
     for (int t = 0; t < NB; ++t) quantize_q8_0_warp(v[t], dst + t * kQBlockBytes, lane);
   }
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
       for (int e = lane; e < kGroupQ * C::kPer; e += 32) {
         const int r = e / C::kPer, pc = e % C::kPer;
         if (r < nr) {
-          const long long off = (long long)(t0 + r) * rowb + pc * C::kCopy;
+          const long long off = (long long)s_win.cell_of(t0 + r) * rowb + pc * C::kCopy;
           cp_async_n<C::kCopy>(st + r * C::kRS + pc * C::kCopy, kbase + off);
           cp_async_n<C::kCopy>(st + (kGroupQ + r) * C::kRS + pc * C::kCopy, vbase + off);
         }

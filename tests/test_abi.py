@@ -115,6 +115,22 @@ def test_attention_refusals(q8d):
     assert attn(q8d, dt=2, batch=2, stride=big + 8) == q8d.Q8D_EALIGN
 
 
+def test_window_attention_refusals(q8d):
+    L = q8d.lib()
+
+    def win(**kw):
+        a = dict(runs=A16 + 0x300000, stride=0, batch=2, dt=1, kc=B16)
+        a.update(kw)
+        return L.q8d_gqa_decode_attn_window(A16, None, None, a["kc"], C16, a["dt"], A16 + 0x100000,
+                                            a["batch"], 16, 8, 128, 64, a["stride"], a["runs"],
+                                            0.088, A16 + 0x200000, 1 << 30, A16, None)
+    assert win(runs=None) == q8d.Q8D_EINVAL
+    assert win(stride=100) == q8d.Q8D_EINVAL        # overlapping per-sequence caches
+    assert win(runs=A16 + 0x300002) == q8d.Q8D_EALIGN
+    assert win(kc=B16 + 8) == q8d.Q8D_EALIGN
+    assert win(dt=5) == q8d.Q8D_EUNSUPPORTED
+
+
 def test_step_create_refusals(q8d):
     L = q8d.lib()
     h = C.c_void_p()
