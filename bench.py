@@ -43,6 +43,15 @@ sys.path.insert(0, ROOT)
 METRIC = "q8_matvec & gqa_decode_attn HBM GB/s (% of GB300 peak); decode-step tokens/s"
 
 
+def bf16_peak():
+    """Measured dense bf16 TFLOP/s (cuBLAS burst), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -493,8 +502,55 @@ def attn_stress_q8(q8d, H, Hk, D, reps, stream, flush, rank=0):
             "l2": "256 MB flush before each launch"}
 
 
+def attn_window_leg(q8d, H, Hk, D, reps, stream, flush, rank=0):
+    """q8d_gqa_decode_attn_window on a shared-prefix batch: 8 sequences read
+    one f16 cache (stride 0), each a 8192-row shared prefix run plus its own
+    1024-row run; L2 flushed before each launch.  GB/s over the rows the
+    sequences attend (the prefix counted once per sequence) and over the
+    distinct rows."""
+    import torch
+
+    import synth
+    pre, own, B = 8192, 1024, 8
+    cap, kvw = pre + B * own, Hk * D
+    kc = synth.normal_torch(rank, "win.k", (cap, kvw), torch.float16)
+    vc = synth.normal_torch(rank, "win.v", (cap, kvw), torch.float16)
+    q = synth.normal_torch(rank, "win.q", (B, H * D), torch.float32)
+    runs = torch.zeros((B, 4, 2), dtype=torch.int32)
+    for s in range(B):
+        runs[s, 0] = torch.tensor([0, pre])
+        runs[s, 1] = torch.tensor([pre + s * own, own])
+    runs = runs.cuda()
+    out = torch.empty(B, H * D, device="cuda")
+    wsb = q8d.q8d_gqa_workspace_bytes(B, H, Hk, D, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    with torch.cuda.stream(stream):
+        for rep in range(max(reps, 3) + 1):
+            flush.fill_(rep & 0xFF)
+            ev[0].record(stream)
+            q8d.q8d_gqa_decode_attn_window(q, None, None, kc, vc, q8d.Q8D_KV_F16, out, B, H, Hk, D,
+                                           cap, 0, runs, 1 / math.sqrt(D), ws, wsb, err, stream)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            if rep:
+                times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    assert err.item() == 0
+    t = statistics.median(times)
+    attended = B * attn_bytes(pre + own, Hk, D, H, 2, append=False)
+    distinct = 2 * cap * kvw * 2 + B * 8 * H * D
+    return {"kernel": "gqa_mma_kernel + gqa_combine_kernel (q8d_gqa_decode_attn_window)",
+            "us_per_launch": t * 1e6, "attended_GB_s": attended / t / 1e9,
+            "distinct_GB_s": distinct / t / 1e9, "attended_bytes": attended,
+            "distinct_bytes": distinct,
+            "workload": "8 sequences, one f16 cache: shared 8192-row prefix + own 1024-row run each",
+            "l2": "256 MB flush before each launch"}
+
+
 # ---------------------------------------------------------------------------- small M
-SMALL_M = (1, 4, 16, 64)
+SMALL_M = (1, 4, 16, 64, 128, 256)
 
 
 def small_m_inputs(m, rank=0):
@@ -533,7 +589,8 @@ def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
         nbytes = p * n // 32 * 34 + 4 * m * n + 4 * m * p
         out[f"m{m}"] = {"us": t * 1e6, "GB_s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / hbm,
                         "TFLOP_s": 2.0 * m * n * p / t / 1e12,
-                        "kernel": "q8_mma_kernel (tcgen05)" if m >= 16 else "q8_gemv_kernel / q8_rows_kernel"}
+                        "kernel": "q8_mma_kernel (tcgen05)" if m >= 16 else "q8_gemv_kernel / q8_rows_kernel",
+                        "bf16_tensor_frac_of_measured": 2.0 * m * n * p / t / 1e12 / bf16_peak()}
         del w, x, y
     out["shape"] = "3584 -> 18944 (7B gate/up), L2 flushed before each launch"
     return out
@@ -833,6 +890,10 @@ def main():
         if shape.kv_dtype == synth.KV_F16 else None
     if stress is not None:
         stress["frac_of_peak"] = stress["GB_s"] / hbm
+    window = attn_window_leg(q8d, H, Hk, D, args.kernel_reps, stream, flush, rank) \
+        if shape.kv_dtype == synth.KV_F16 else None
+    if window is not None:
+        window["distinct_frac_of_peak"] = window["distinct_GB_s"] / hbm
     stress_q8 = attn_stress_q8(q8d, H, Hk, D, args.kernel_reps, stream, flush, rank) \
         if shape.kv_dtype == synth.KV_F16 else None
     if stress_q8 is not None:
@@ -893,6 +954,7 @@ def main():
                 "gqa_decode_attn_ctx8192": attn_long,
                 "gqa_decode_attn_batch8_ragged": stress,
                 "gqa_decode_attn_batch8_ragged_q8_0_kv": stress_q8,
+                "gqa_decode_attn_window_shared_prefix": window,
                 "q8_matmul_small_m": small_m,
             },
             "configs": configs,
