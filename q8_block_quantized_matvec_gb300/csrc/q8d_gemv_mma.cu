@@ -1,0 +1,369 @@
+// Q8_0 matrix-vector product with the block dot products on the tensor
+// cores (mma.sync m16n8k16, f16 operands, f32 accumulation), sm_103a.
+//
+//   y[r] = sum_b scale(r,b) * sum_j q(r,b,j) * x[32b+j]
+// ("IV.4: One command buffer per token", "Eight kernels": q8_matvec; the
+// per-block product is summed inside the block and scaled once, as the
+// pages' kernel does).
+//
+// Why: on CUDA cores every quant costs a byte permute, a bias add and an FMA
+// (half of them on the half-rate ALU pipe), which holds the matvec near 50 %
+// issue and 0.5 of HBM.  Here a quant pair costs one PRMT and one sub.f16x2,
+// and the products go to the tensor pipe:
+//  * A (16 x 16 per MMA): quants as exact f16 (a sign-flipped byte under the
+//    exponent byte 0x64 is 1152 + q; one sub.f16x2 removes the 1152).  The
+//    16 A rows are 8 weight rows x 2 column halves, so a unit of work is 8
+//    rows x 4 blocks of the same byte alignment (blocks base, base+2,
+//    base+4, base+6; half 0 = {base, base+4}, half 1 = {base+2, base+6}),
+//    and 8-row granularity keeps the rows of a matrix evenly spread over
+//    the CTAs.  Each thread feeds one 32-bit word of quants per MMA (its
+//    contraction indices are permuted to match: 4 consecutive bytes).
+//  * B (16 x 8): the 8 columns are 4 blocks x (x_hi, x_lo), x = hi + lo in
+//    f16 after one power-of-two scale of the whole vector (max|x| scaled
+//    into [2^14, 2^15)), so every product is exact in f32 and the sum
+//    matches f32 arithmetic; columns that pair a row half with the other
+//    half's blocks are zero.  The fragments are built once per launch in
+//    shared memory, in the permuted byte order of each block's words.
+//  * D: every thread ends a unit with the (hi, lo) partials of one (row,
+//    block) pair, scales them by that block's f16 scale and accumulates in
+//    f32; 4 lanes share a row and the warps' row partials are summed in a
+//    fixed order (deterministic).
+//  * Weights stream in through a ring of shared-memory stages filled with
+//    1-D bulk copies (TMA) by one producer warp: a tile is 8 rows x up to
+//    ~150 blocks (long rows are cut into slices), one copy per row into a
+//    row slot padded so that the lanes' word reads hit distinct banks.
+// Blocks of odd index start two bytes after a word boundary, so their quants
+// are word aligned; for even blocks the words at +4 .. +28 hold quants 2..29
+// and the last word is assembled from the block's first and last words.
+#include <algorithm>
+
+#include "q8d_gemv.cuh"
+#include "q8d_internal.cuh"
+#include "q8d_rows.cuh"
+
+namespace q8d {
+namespace {
+
+using namespace mv;
+
+constexpr int kMvMaxWarps = 16;                         // consumer warps (at most)
+constexpr int kMvThreads = (kMvMaxWarps + 1) * 32;      // + the producer warp
+constexpr int kXfBlock = 144;                           // x fragment bytes per block (128 + pad)
+constexpr int kSetRows = 8;                             // rows per unit
+constexpr int kWinSets = 4;                             // row sets per reduction window
+
+struct MvParams {
+  const uint8_t* w;
+  float* y;
+  const float* x;
+  int n, bpr, p;
+  int row_bytes;     // bpr * 34, a multiple of 272
+  int rows_per_cta;  // a multiple of 8
+  int S, nslices;    // blocks per slice (a multiple of 8), slices per row
+  int SR;            // shared-memory row slot (bytes, multiple of 16)
+  int stage_bytes, nstages;
+  int W;             // consumer warps
+  int* d_err;
+};
+
+__device__ __forceinline__ uint32_t lds32a(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64a(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16a(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Four signed quants (one word) -> two exact f16 pairs: bytes (0, 1), (2, 3).
+__device__ __forceinline__ void quant_pairs(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  const uint32_t f = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(f, 0x64646464u, 0x5140);
+  const uint32_t b = __byte_perm(f, 0x64646464u, 0x7362);
+  const uint32_t bias = 0x64806480u;  // (1152, 1152)
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(a), "r"(bias));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(bias));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Quant index of byte k of word w of a block (the order the A side reads).
+__device__ __forceinline__ int word_quant(bool even_block, int w, int k) {
+  if (!even_block) return 4 * w + k;
+  if (w < 7) return 4 * w + 2 + k;
+  return k < 2 ? k : 28 + k;
+}
+
+// Word w of the block starting at shared byte address `blk` (a block of the
+// slice: even blocks start on a word boundary, odd ones two bytes past it).
+template <bool kEven>
+__device__ __forceinline__ uint32_t block_word(uint32_t blk, int w) {
+  if constexpr (kEven) {
+    if (w < 7) return lds32a(blk + 4 + 4 * w);
+    return __byte_perm(lds32a(blk), lds32a(blk + 32), 0x5432);
+  } else {
+    return lds32a(blk + 2 + 4 * w);
+  }
+}
+
+// One unit: 8 rows x 4 blocks (base, base+2, base+4, base+6) of the tile.
+// row32: shared address of this thread's row gq in the stage; xf_b: the x
+// fragment address of this thread's B block (or the zero pad), per word.
+template <bool kEven>
+__device__ __forceinline__ float unit_dot(uint32_t row32, int ub, int cq, uint32_t xf_lane,
+                                          bool bmatch) {
+  const int j = cq & 1, wsel = cq >> 1;
+  const uint32_t blk0 = row32 + (uint32_t)(ub + 4 * j) * kQBlockBytes;      // half 0
+  const uint32_t blk1 = row32 + (uint32_t)(ub + 2 + 4 * j) * kQBlockBytes;  // half 1
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int w = 2 * i + wsel;
+    uint32_t a0, a1, a2, a3;
+    quant_pairs(block_word<kEven>(blk0, w), a0, a2);
+    quant_pairs(block_word<kEven>(blk1, w), a1, a3);
+    uint2 b = make_uint2(0u, 0u);
+    if (bmatch) b = lds64a(xf_lane + (uint32_t)(w * 16));
+    mma_f16(acc, a0, a1, a2, a3, b.x, b.y);
+  }
+  // (row gq, block b_cq): half 0 for cq < 2 (rows 0..7 of the MMA), half 1
+  // for cq >= 2 (rows 8..15); its hi and lo columns
+  const float part = cq < 2 ? acc[0] + acc[1] : acc[2] + acc[3];
+  const int sb = cq < 2 ? ub + 4 * cq : ub + 2 + 4 * (cq - 2);
+  const float sc = __half2float(__ushort_as_half((unsigned short)lds16a(row32 + (uint32_t)sb * kQBlockBytes)));
+  return sc * part;
+}
+
+__device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                          int* abort_flag, int v0, int v1) {
+  const uint64_t pol = policy_evict_first();
+  int s = 0, issued = 0;
+  uint32_t ph = 0;
+  for (int r0 = v0; r0 < v1; r0 += kSetRows) {
+    const int nrows = min(kSetRows, v1 - r0);
+    for (int sl = 0; sl < P.nslices; ++sl) {
+      if (issued >= P.nstages && !wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) return issued;
+      const int c0 = sl * P.S;
+      const int nb = min(P.S, P.bpr - c0);
+      const uint32_t bytes = (uint32_t)nb * kQBlockBytes;
+      uint8_t* dst = smem + (size_t)P.stage_bytes * s;
+      mbar_arrive_expect_tx(&full[s], bytes * nrows);
+      for (int r = 0; r < nrows; ++r)
+        bulk_g2s(dst + r * P.SR, P.w + (long long)(r0 + r) * P.row_bytes + (long long)c0 * kQBlockBytes,
+                 bytes, &full[s], pol);
+      ++issued;
+      if (++s == P.nstages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  return issued;
+}
+
+__global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+  __shared__ float s_red[kMvMaxWarps];
+  __shared__ int s_exp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = P.W;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
+  uint64_t* empty = full + P.nstages;
+  uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);
+  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // 64 zero bytes
+  float* part = reinterpret_cast<float*>(zpad + 64);             // [2][kWinSets*8][W]
+  const int v0 = blockIdx.x * P.rows_per_cta;
+  const int v1 = min(P.p, v0 + P.rows_per_cta);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.nstages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], W);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  int issued = 0;
+  bool ok = true;
+  if (warp == W) {
+    if (lane == 0) issued = mv_produce(P, smem, full, empty, &s_abort, v0, v1);
+  } else {
+    const int nct = W * 32;
+    // ---- the vector's power-of-two scale: max|x| * 2^e in [2^14, 2^15) ----
+    float mx = 0.f;
+    const float4* x4 = reinterpret_cast<const float4*>(P.x);
+    for (int i = threadIdx.x; i < P.n / 4; i += nct) {
+      const float4 v = __ldg(x4 + i);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[warp] = mx;
+    consumer_sync(nct);
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+      for (int w = 0; w < W; ++w) m = fmaxf(m, s_red[w]);
+      int ex = 0;
+      if (m > 0.f) frexpf(m, &ex);
+      s_exp = m > 0.f ? 15 - ex : 0;
+    }
+    consumer_sync(nct);
+    const int e = s_exp;
+    // ---- x fragments: block bb, word w, hi / lo: the 4 values of the
+    // word's bytes, hi = f16(x 2^e), lo = f16(x 2^e - hi) ----
+    for (int it = threadIdx.x; it < P.bpr * 8; it += nct) {
+      const int bb = it >> 3, w = it & 7;
+      const bool even = (bb & 1) == 0;
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = ldexpf(__ldg(P.x + bb * kQBlock + word_quant(even, w, k)), e);
+      const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
+      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+      const __half2 l01 = __floats2half2_rn(v[0] - f01.x, v[1] - f01.y);
+      const __half2 l23 = __floats2half2_rn(v[2] - f23.x, v[3] - f23.y);
+      uint2* dst = reinterpret_cast<uint2*>(xf + (size_t)bb * kXfBlock + w * 16);
+      dst[0] = make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+      dst[1] = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+    }
+    if (threadIdx.x < 16) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
+    consumer_sync(nct);
+
+    // ---- main loop ----
+    const int gq = lane >> 2, cq = lane & 3;
+    // this thread's B column: n = gq = 4h + 2jb + hl; nonzero when its block
+    // (jb) is the one this thread's contraction words belong to (cq & 1)
+    const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
+    const bool bmatch = bjb == (cq & 1);
+    const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
+    const uint32_t smem32 = smem_u32(smem);
+    const float inv = ldexpf(1.f, -e);
+    int s = 0;
+    uint32_t ph = 0;
+    int set = 0, buf = 0;
+    float yacc = 0.f;
+    for (int r0 = v0; r0 < v1; r0 += kSetRows, ++set) {
+      for (int sl = 0; sl < P.nslices; ++sl) {
+        ok = wait_or_abort(&full[s], ph, &s_abort) && ok;
+        const uint32_t row32 = after_wait(smem32 + (uint32_t)(P.stage_bytes * s) + (uint32_t)(gq * P.SR));
+        const int c0 = sl * P.S;
+        const int units = min(P.S, P.bpr - c0) / 4;
+        for (int u = warp; u < units; u += W) {
+          const int ub = 8 * (u >> 1) + (u & 1);  // first block of the unit in the slice
+          const int bblk = c0 + ub + 2 * bh + 4 * bjb;
+          const uint32_t xl = bmatch ? xf32 + (uint32_t)bblk * kXfBlock + (uint32_t)bhl * 8 : z32;
+          yacc += (u & 1) ? unit_dot<false>(row32, ub, cq, xl, bmatch)
+                          : unit_dot<true>(row32, ub, cq, xl, bmatch);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == P.nstages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      // the row set is complete: the warp's partial of row r0 + gq
+      yacc += __shfl_xor_sync(0xffffffffu, yacc, 1);
+      yacc += __shfl_xor_sync(0xffffffffu, yacc, 2);
+      const int slot = set % kWinSets;
+      if (cq == 0) part[((buf * kWinSets + slot) * kSetRows + gq) * W + warp] = yacc;
+      yacc = 0.f;
+      if (slot == kWinSets - 1 || r0 + kSetRows >= v1) {
+        consumer_sync(nct);
+        // window reduction: rows of the window's sets, warp partials in order
+        const int wr0 = r0 - slot * kSetRows;
+        for (int t = threadIdx.x; t < (slot + 1) * kSetRows; t += nct) {
+          const int row = wr0 + t;
+          if (row < v1) {
+            const float* pr = part + ((size_t)buf * kWinSets * kSetRows + t) * W;
+            float sum = 0.f;
+            for (int w = 0; w < W; ++w) sum += pr[w];
+            P.y[row] = sum * inv;
+          }
+        }
+        buf ^= 1;
+      }
+    }
+  }
+  if (!__syncthreads_and(ok && !*(volatile int*)&s_abort)) {
+    if (threadIdx.x == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
+  }
+  if (warp == W && lane == 0 && *(volatile int*)&s_abort) {
+    for (int j = max(0, issued - P.nstages); j < issued; ++j)
+      mbar_wait(&full[j % P.nstages], (uint32_t)(j / P.nstages) & 1u);
+  }
+}
+
+}  // namespace
+
+// Plans and launches the tensor-core matvec.  Q8D_EUNSUPPORTED when the
+// shape does not suit it (one matrix, n % 256 == 0, enough rows to give
+// every SM two 8-row sets); the caller then runs the CUDA-core kernel.
+int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid_out) {
+  if (R.m != 1 || R.nseg != 1 || R.bpr % 8 || R.bpr < 8) return Q8D_EUNSUPPORTED;
+  const int sms = sm_count();
+  const long long p = R.seg[0].p;
+  if (p < 2LL * kSetRows * sms || p > 0x7fffffffLL) return Q8D_EUNSUPPORTED;
+  MvParams P{};
+  P.w = R.seg[0].w;
+  P.y = R.seg[0].y;
+  P.x = R.X;
+  P.n = R.n;
+  P.bpr = R.bpr;
+  P.p = (int)p;
+  P.row_bytes = R.bpr * kQBlockBytes;
+  P.d_err = R.d_err;
+  // slices of at most ~4.6 KB per row (8 rows: ~37 KB a stage)
+  const int max_blocks = 136;
+  P.nslices = (P.bpr + max_blocks - 1) / max_blocks;
+  P.S = ((P.bpr + P.nslices - 1) / P.nslices + 7) / 8 * 8;
+  P.nslices = (P.bpr + P.S - 1) / P.S;
+  // row slot: >= the slice, 16-byte multiple, 4 banks apart row to row
+  int SR = (P.S * kQBlockBytes + 15) / 16 * 16;
+  while ((SR / 4) % 32 != 4) SR += 16;
+  P.SR = SR;
+  P.stage_bytes = kSetRows * SR;
+  // consumer warps: the count in [8, 16] that splits a slice's units most evenly
+  const int U = P.S / 4;
+  int bestW = kMvMaxWarps;
+  double best = 0.0;
+  for (int w = kMvMaxWarps; w >= 8; --w) {
+    const double eff = (double)U / (w * ((U + w - 1) / w));
+    if (eff > best + 1e-9) {
+      best = eff;
+      bestW = w;
+    }
+  }
+  P.W = bestW;
+  const long long fixed = (long long)P.bpr * kXfBlock + 64 + 2LL * kWinSets * kSetRows * P.W * 4;
+  const long long budget = 220 * 1024;
+  P.nstages = (int)std::min<long long>(8, (budget - fixed) / (P.stage_bytes + 16));
+  if (P.nstages < 3) return Q8D_EUNSUPPORTED;
+  const long long smem = (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + fixed;
+  // 8-row sets spread evenly over one wave of CTAs (one per SM)
+  const long long sets = (p + kSetRows - 1) / kSetRows;
+  const long long sets_cta = (sets + sms - 1) / sms;
+  P.rows_per_cta = (int)(sets_cta * kSetRows);
+  const int grid = (int)((p + P.rows_per_cta - 1) / P.rows_per_cta);
+  const int rc = configure_kernel(reinterpret_cast<const void*>(q8_gemv_mma_kernel), 220 * 1024, true);
+  if (rc) return rc;
+  if (grid_out) *grid_out = grid;
+  return launch_ex(q8_gemv_mma_kernel, dim3(grid), dim3((P.W + 1) * 32), (size_t)smem, stream, false, P);
+}
+
+}  // namespace q8d

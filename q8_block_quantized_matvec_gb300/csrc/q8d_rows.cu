@@ -345,7 +345,9 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.row_bytes = (long long)P.bpr * kQBlockBytes;
   P.total_rows = p_total;
   if (P.m == 1) {
-    const int rc = gemv_plan_and_launch(P, stream, grid_out);
+    int rc = gemv_mma_plan_and_launch(P, stream, grid_out);
+    if (rc != Q8D_EUNSUPPORTED) return rc;
+    rc = gemv_plan_and_launch(P, stream, grid_out);
     if (rc != Q8D_EUNSUPPORTED) return rc;
   }
 

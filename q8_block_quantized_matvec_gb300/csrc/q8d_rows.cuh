@@ -45,4 +45,8 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out = null
 // total_rows filled.  Q8D_EUNSUPPORTED when the rows are too long for it.
 int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out);
 
+// The m == 1 tensor-core kernel (q8d_gemv_mma.cu) for one matrix with
+// n % 256 == 0 and enough rows; Q8D_EUNSUPPORTED otherwise.
+int gemv_mma_plan_and_launch(const RowsParams& P, cudaStream_t stream, int* grid_out);
+
 }  // namespace q8d

@@ -202,3 +202,80 @@ def test_small_m_bench_shape_sampled(q8d, orc, m):
         ref, ab = orc.q8_matvec_rows(w, X[i], n, rows)
         assert np.all(np.abs(got[i, rows] - ref) <= tol * ab), i
     assert np.isfinite(got).all()
+
+
+# ---------------------------------------------------------------------------- tensor-core matvec
+# q8d_matvec runs its tensor-core kernel (mma.sync, f16 hi/lo activations)
+# for one matrix with n % 256 == 0 and p >= 16 * SMs rows; these shapes
+# reach it (and its sliced-row path for n > 4352), including row counts
+# that are not multiples of the 8-row unit.
+MMA_SHAPES = [(1024, 3072), (3584, 3584), (3584, 2437), (18944, 3584), (4864, 2500), (256, 5000),
+              (8192, 3001)]
+
+
+@pytest.mark.parametrize("n,p", MMA_SHAPES)
+def test_matvec_mma_parity(q8d, orc, n, p):
+    w = synth.q8_matrix(11, f"mm.w{n}x{p}", p, n)
+    x = synth.normal_f32(11, f"mm.x{n}", n)
+    ref, ab = orc.q8_matvec(w, x, n, p)
+    got = gpu_matvec(q8d, w, x, n, p)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= TOL * ab), (err / ab).max()
+
+
+@pytest.mark.parametrize("n,p", [(256, 2500), (3584, 2440), (18944, 2432)])
+def test_matvec_mma_exact_integer_sums(q8d, n, p):
+    w = synth.q8_from_parts(5, "mmw", p, n, 0x3C00)
+    q = w.reshape(p, n // 32, 34)[:, :, 2:].view(np.int8).astype(np.int64).reshape(p, n)
+    got = gpu_matvec(q8d, w, np.ones(n, np.float32), n, p)
+    assert np.array_equal(got.astype(np.int64), q.sum(axis=1))
+
+
+def test_matvec_mma_one_hot_columns(q8d):
+    """One-hot x at columns covering every byte position of even and odd
+    blocks (the permuted word order of both alignments)."""
+    n, p = 512, 2432
+    w = synth.q8_matrix(12, "mmoh", p, n)
+    blk = w.reshape(p, n // 32, 34)
+    sc = blk[:, :, 0:2].copy().view("<f2").astype(np.float32).reshape(p, n // 32)
+    q = blk[:, :, 2:].view(np.int8).astype(np.float32).reshape(p, n)
+    for j in list(range(0, 64)) + [97, 130, 255, 256, 319, 480, 511]:
+        x = np.zeros(n, np.float32)
+        x[j] = np.float32(3.0)
+        want = (sc[:, j // 32] * q[:, j]).astype(np.float32) * np.float32(3.0)
+        assert np.array_equal(gpu_matvec(q8d, w, x, n, p, canary=False), want), j
+
+
+def test_matvec_mma_minus_128_and_sum_of_x(q8d):
+    n, p = 1024, 2432
+    w = synth.q8_const_matrix(p, n, 0x3C00, -128)
+    assert np.array_equal(gpu_matvec(q8d, w, np.ones(n, np.float32), n, p),
+                          np.full(p, -128.0 * n, np.float32))
+    w1 = synth.q8_const_matrix(p, n, 0x3C00, 1)
+    x = synth.normal_f32(13, "mms", n)
+    got = gpu_matvec(q8d, w1, x, n, p)
+    assert np.all(np.abs(got - np.sum(x, dtype=np.float64)) <= TOL * np.abs(x).sum())
+
+
+def test_matvec_mma_wide_dynamic_range_and_determinism(q8d, orc):
+    """x spanning 2^-20 .. 2^10 (the f16 split after the vector's power-of-two
+    scale) within the bar; two launches agree bitwise."""
+    n, p = 3584, 2600
+    w = synth.q8_matrix(14, "mmr", p, n)
+    x = synth.normal_f32(14, "mmrx", n) * np.exp2(synth.stream(14, "mmre").integers(-20, 11, n)).astype(np.float32)
+    ref, ab = orc.q8_matvec(w, x, n, p)
+    a = gpu_matvec(q8d, w, x, n, p)
+    b = gpu_matvec(q8d, w, x, n, p)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert np.all(np.abs(a.astype(np.float64) - ref) <= TOL * ab), (np.abs(a - ref) / ab).max()
+
+
+def test_matvec_mma_control_perturbed_byte(q8d):
+    n, p = 2048, 2432
+    w = synth.q8_matrix(15, "mmc", p, n)
+    x = synth.normal_f32(15, "mmcx", n)
+    a = gpu_matvec(q8d, w, x, n, p)
+    w2 = w.copy()
+    w2[1000, 34 * 37 + 9] ^= 0x11
+    b = gpu_matvec(q8d, w2, x, n, p)
+    assert a[1000] != b[1000] and np.array_equal(np.delete(a, 1000), np.delete(b, 1000))
