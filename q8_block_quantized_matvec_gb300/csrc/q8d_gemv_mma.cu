@@ -63,6 +63,7 @@ struct MvParams {
   int SR;            // shared-memory row slot (bytes, multiple of 16)
   int stage_bytes, nstages;
   int W;             // consumer warps
+  int T;             // 8-row sets per tile (1 or 2)
   int* d_err;
 };
 
@@ -108,44 +109,68 @@ __device__ __forceinline__ int word_quant(bool even_block, int w, int k) {
   return k < 2 ? k : 28 + k;
 }
 
-// Word w of the block starting at shared byte address `blk` (a block of the
-// slice: even blocks start on a word boundary, odd ones two bytes past it).
-template <bool kEven>
-__device__ __forceinline__ uint32_t block_word(uint32_t blk, int w) {
-  if constexpr (kEven) {
-    if (w < 7) return lds32a(blk + 4 + 4 * w);
-    return __byte_perm(lds32a(blk), lds32a(blk + 32), 0x5432);
-  } else {
-    return lds32a(blk + 2 + 4 * w);
-  }
+// Per-lane constants of the unit loop (byte offsets within a pair of units:
+// 8 consecutive blocks 8k .. 8k+7 of a tile row; the even unit is blocks
+// 8k + {0, 2, 4, 6}, the odd unit 8k + {1, 3, 5, 7}; half 0 of a unit is
+// its blocks +0 and +4, half 1 its blocks +2 and +6).
+struct LaneOffs {
+  uint32_t e0, e1;    // even unit, halves 0 / 1: this lane's word 2i + wsel, i < 3 (+ 8 i)
+  uint32_t e3a, e3b;  // even unit, i = 3: the two words the last word comes from (half 0)
+  uint32_t sel3;      // their byte selector (word 6 as is, or bytes {2,3} + {32,33})
+  uint32_t o0, o1;    // odd unit, halves 0 / 1: word 2i + wsel (+ 8 i)
+  uint32_t s_even;    // this lane's (row, block) scale of the even unit (odd: + 34)
+};
+
+__device__ __forceinline__ LaneOffs lane_offsets(int cq) {
+  const int j = cq & 1, wsel = cq >> 1;
+  LaneOffs L;
+  // even blocks start on a word: words +4 .. +28 hold quants 2 .. 29, the
+  // last word is quants {0, 1} (bytes 2, 3) and {30, 31} (bytes 32, 33)
+  L.e0 = 136u * j + 4u + 4u * wsel;
+  L.e1 = L.e0 + 68u;
+  L.e3a = wsel ? 136u * j : 136u * j + 28u;
+  L.e3b = 136u * j + 32u;
+  L.sel3 = wsel ? 0x5432u : 0x3210u;
+  // odd blocks start two bytes past a word: quants are word aligned
+  L.o0 = 34u + 136u * j + 2u + 4u * wsel;
+  L.o1 = L.o0 + 68u;
+  L.s_even = (uint32_t)(cq < 2 ? 4 * cq : 2 + 4 * (cq - 2)) * kQBlockBytes;
+  return L;
 }
 
-// One unit: 8 rows x 4 blocks (base, base+2, base+4, base+6) of the tile.
-// row32: shared address of this thread's row gq in the stage; xf_b: the x
-// fragment address of this thread's B block (or the zero pad), per word.
-template <bool kEven>
-__device__ __forceinline__ float unit_dot(uint32_t row32, int ub, int cq, uint32_t xf_lane,
-                                          bool bmatch) {
-  const int j = cq & 1, wsel = cq >> 1;
-  const uint32_t blk0 = row32 + (uint32_t)(ub + 4 * j) * kQBlockBytes;      // half 0
-  const uint32_t blk1 = row32 + (uint32_t)(ub + 2 + 4 * j) * kQBlockBytes;  // half 1
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+// Two units (8 rows x blocks 8k .. 8k+7) at row32 + base; xb: this lane's x
+// fragments of the pair (its B block of the even unit, word wsel; the odd
+// unit's are 144 bytes on; the zero pad for lanes whose B column is zero).
+__device__ __forceinline__ float pair_dot(uint32_t rb, uint32_t xb, uint32_t xstep, const LaneOffs& L,
+                                          bool lo_half) {
+  float ae[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int w = 2 * i + wsel;
+    uint32_t we0, we1;
+    if (i < 3) {
+      we0 = lds32a(rb + L.e0 + 8 * i);
+      we1 = lds32a(rb + L.e1 + 8 * i);
+    } else {
+      we0 = __byte_perm(lds32a(rb + L.e3a), lds32a(rb + L.e3b), L.sel3);
+      we1 = __byte_perm(lds32a(rb + L.e3a + 68), lds32a(rb + L.e3b + 68), L.sel3);
+    }
+    const uint32_t wo0 = lds32a(rb + L.o0 + 8 * i), wo1 = lds32a(rb + L.o1 + 8 * i);
+    const uint2 be = lds64a(xb + 32 * i);
+    const uint2 bo = lds64a(xb + xstep + 32 * i);
     uint32_t a0, a1, a2, a3;
-    quant_pairs(block_word<kEven>(blk0, w), a0, a2);
-    quant_pairs(block_word<kEven>(blk1, w), a1, a3);
-    uint2 b = make_uint2(0u, 0u);
-    if (bmatch) b = lds64a(xf_lane + (uint32_t)(w * 16));
-    mma_f16(acc, a0, a1, a2, a3, b.x, b.y);
+    quant_pairs(we0, a0, a2);
+    quant_pairs(we1, a1, a3);
+    mma_f16(ae, a0, a1, a2, a3, be.x, be.y);
+    quant_pairs(wo0, a0, a2);
+    quant_pairs(wo1, a1, a3);
+    mma_f16(ao, a0, a1, a2, a3, bo.x, bo.y);
   }
-  // (row gq, block b_cq): half 0 for cq < 2 (rows 0..7 of the MMA), half 1
-  // for cq >= 2 (rows 8..15); its hi and lo columns
-  const float part = cq < 2 ? acc[0] + acc[1] : acc[2] + acc[3];
-  const int sb = cq < 2 ? ub + 4 * cq : ub + 2 + 4 * (cq - 2);
-  const float sc = __half2float(__ushort_as_half((unsigned short)lds16a(row32 + (uint32_t)sb * kQBlockBytes)));
-  return sc * part;
+  // (row gq, block b_cq) of each unit: half 0 for cq < 2, half 1 otherwise
+  const float pe = lo_half ? ae[0] + ae[1] : ae[2] + ae[3];
+  const float po = lo_half ? ao[0] + ao[1] : ao[2] + ao[3];
+  const float se = __half2float(__ushort_as_half((unsigned short)lds16a(rb + L.s_even)));
+  const float so = __half2float(__ushort_as_half((unsigned short)lds16a(rb + L.s_even + 34)));
+  return fmaf(se, pe, so * po);
 }
 
 __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
@@ -153,8 +178,9 @@ __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint
   const uint64_t pol = policy_evict_first();
   int s = 0, issued = 0;
   uint32_t ph = 0;
-  for (int r0 = v0; r0 < v1; r0 += kSetRows) {
-    const int nrows = min(kSetRows, v1 - r0);
+  const int tile_rows = kSetRows * P.T;
+  for (int r0 = v0; r0 < v1; r0 += tile_rows) {
+    const int nrows = min(tile_rows, v1 - r0);
     for (int sl = 0; sl < P.nslices; ++sl) {
       if (issued >= P.nstages && !wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) return issued;
       const int c0 = sl * P.S;
@@ -185,8 +211,8 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
   uint64_t* empty = full + P.nstages;
   uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);
-  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // 64 zero bytes
-  float* part = reinterpret_cast<float*>(zpad + 64);             // [2][kWinSets*8][W]
+  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // 128 zero bytes
+  float* part = reinterpret_cast<float*>(zpad + 128);            // [2][kWinSets*8][W]
   const int v0 = blockIdx.x * P.rows_per_cta;
   const int v1 = min(P.p, v0 + P.rows_per_cta);
   if (threadIdx.x == 0) {
@@ -241,62 +267,75 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
       dst[0] = make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
       dst[1] = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
     }
-    if (threadIdx.x < 16) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
+    if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
     consumer_sync(nct);
 
     // ---- main loop ----
     const int gq = lane >> 2, cq = lane & 3;
+    const LaneOffs LO = lane_offsets(cq);
     // this thread's B column: n = gq = 4h + 2jb + hl; nonzero when its block
     // (jb) is the one this thread's contraction words belong to (cq & 1)
     const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
     const bool bmatch = bjb == (cq & 1);
+    const uint32_t xlane = bmatch ? (uint32_t)((2 * bh + 4 * bjb) * kXfBlock + bhl * 8 + (cq >> 1) * 16) : 0u;
     const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
+    const uint32_t xstep = bmatch ? (uint32_t)kXfBlock : 0u;
     const uint32_t smem32 = smem_u32(smem);
+    const bool lo_half = cq < 2;
     const float inv = ldexpf(1.f, -e);
+    const int S = P.S, bpr = P.bpr, nslices = P.nslices, nst = P.nstages;
+    const uint32_t stage_b = (uint32_t)P.stage_bytes, rowoff = (uint32_t)(gq * P.SR);
+    const int T = P.T;
+    const uint32_t set_b = (uint32_t)(kSetRows * P.SR);  // bytes between the row sets of a tile
     int s = 0;
     uint32_t ph = 0;
     int set = 0, buf = 0;
-    float yacc = 0.f;
-    for (int r0 = v0; r0 < v1; r0 += kSetRows, ++set) {
-      for (int sl = 0; sl < P.nslices; ++sl) {
+    for (int r0 = v0; r0 < v1; r0 += kSetRows * T) {
+      float yacc[2] = {0.f, 0.f};  // this thread's row gq of the tile's sets
+      for (int sl = 0; sl < nslices; ++sl) {
         ok = wait_or_abort(&full[s], ph, &s_abort) && ok;
-        const uint32_t row32 = after_wait(smem32 + (uint32_t)(P.stage_bytes * s) + (uint32_t)(gq * P.SR));
-        const int c0 = sl * P.S;
-        const int units = min(P.S, P.bpr - c0) / 4;
-        for (int u = warp; u < units; u += W) {
-          const int ub = 8 * (u >> 1) + (u & 1);  // first block of the unit in the slice
-          const int bblk = c0 + ub + 2 * bh + 4 * bjb;
-          const uint32_t xl = bmatch ? xf32 + (uint32_t)bblk * kXfBlock + (uint32_t)bhl * 8 : z32;
-          yacc += (u & 1) ? unit_dot<false>(row32, ub, cq, xl, bmatch)
-                          : unit_dot<true>(row32, ub, cq, xl, bmatch);
+        const uint32_t row32 = after_wait(smem32 + stage_b * (uint32_t)s + rowoff);
+        const int c0 = sl * S;
+        const int pairs = min(S, bpr - c0) / 8;
+        for (int k = warp; k < pairs; k += W) {
+          const uint32_t xb = bmatch ? xf32 + (uint32_t)(c0 + 8 * k) * kXfBlock + xlane : z32;
+          const uint32_t rb = row32 + 272u * (uint32_t)k;
+          yacc[0] += pair_dot(rb, xb, xstep, LO, lo_half);
+          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, xstep, LO, lo_half);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == P.nstages) {
+        if (++s == nst) {
           s = 0;
           ph ^= 1u;
         }
       }
-      // the row set is complete: the warp's partial of row r0 + gq
-      yacc += __shfl_xor_sync(0xffffffffu, yacc, 1);
-      yacc += __shfl_xor_sync(0xffffffffu, yacc, 2);
-      const int slot = set % kWinSets;
-      if (cq == 0) part[((buf * kWinSets + slot) * kSetRows + gq) * W + warp] = yacc;
-      yacc = 0.f;
-      if (slot == kWinSets - 1 || r0 + kSetRows >= v1) {
-        consumer_sync(nct);
-        // window reduction: rows of the window's sets, warp partials in order
-        const int wr0 = r0 - slot * kSetRows;
-        for (int t = threadIdx.x; t < (slot + 1) * kSetRows; t += nct) {
-          const int row = wr0 + t;
-          if (row < v1) {
-            const float* pr = part + ((size_t)buf * kWinSets * kSetRows + t) * W;
-            float sum = 0.f;
-            for (int w = 0; w < W; ++w) sum += pr[w];
-            P.y[row] = sum * inv;
+      // the tile's row sets are complete: the warp's partials of rows r0 + 8t + gq
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t >= T || r0 + kSetRows * t >= v1) break;
+        const int rs0 = r0 + kSetRows * t;
+        float y = yacc[t];
+        y += __shfl_xor_sync(0xffffffffu, y, 1);
+        y += __shfl_xor_sync(0xffffffffu, y, 2);
+        const int slot = set % kWinSets;
+        if (cq == 0) part[((buf * kWinSets + slot) * kSetRows + gq) * W + warp] = y;
+        if (slot == kWinSets - 1 || rs0 + kSetRows >= v1) {
+          consumer_sync(nct);
+          // window reduction: rows of the window's sets, warp partials in order
+          const int wr0 = rs0 - slot * kSetRows;
+          for (int i = threadIdx.x; i < (slot + 1) * kSetRows; i += nct) {
+            const int row = wr0 + i;
+            if (row < v1) {
+              const float* pr = part + ((size_t)buf * kWinSets * kSetRows + i) * W;
+              float sum = 0.f;
+              for (int w = 0; w < W; ++w) sum += pr[w];
+              P.y[row] = sum * inv;
+            }
           }
+          buf ^= 1;
         }
-        buf ^= 1;
+        ++set;
       }
     }
   }
@@ -312,10 +351,11 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
 }  // namespace
 
 // Plans and launches the tensor-core matvec.  Q8D_EUNSUPPORTED when the
-// shape does not suit it (one matrix, n % 256 == 0, enough rows to give
-// every SM two 8-row sets); the caller then runs the CUDA-core kernel.
+// shape does not suit it (one matrix, n % 256 == 0 and n >= 2048, enough
+// rows to give every SM two 8-row sets); the caller then runs the
+// CUDA-core kernel.
 int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid_out) {
-  if (R.m != 1 || R.nseg != 1 || R.bpr % 8 || R.bpr < 8) return Q8D_EUNSUPPORTED;
+  if (R.m != 1 || R.nseg != 1 || R.bpr % 8 || R.bpr < 64) return Q8D_EUNSUPPORTED;
   const int sms = sm_count();
   const long long p = R.seg[0].p;
   if (p < 2LL * kSetRows * sms || p > 0x7fffffffLL) return Q8D_EUNSUPPORTED;
@@ -338,8 +378,9 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   while ((SR / 4) % 32 != 4) SR += 16;
   P.SR = SR;
   P.stage_bytes = kSetRows * SR;
-  // consumer warps: the count in [8, 16] that splits a slice's units most evenly
-  const int U = P.S / 4;
+  // consumer warps: the count in [8, 16] that splits a slice's unit pairs
+  // (8 blocks of 8 rows) most evenly
+  const int U = P.S / 8;
   int bestW = kMvMaxWarps;
   double best = 0.0;
   for (int w = kMvMaxWarps; w >= 8; --w) {
@@ -350,15 +391,19 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
     }
   }
   P.W = bestW;
-  const long long fixed = (long long)P.bpr * kXfBlock + 64 + 2LL * kWinSets * kSetRows * P.W * 4;
+  const long long fixed = (long long)P.bpr * kXfBlock + 128 + 2LL * kWinSets * kSetRows * P.W * 4;
   const long long budget = 220 * 1024;
+  // two row sets per tile (each warp's per-tile work twice as long) when
+  // three such stages fit
+  P.T = (budget - fixed) / (2LL * P.stage_bytes + 16) >= 3 ? 2 : 1;
+  P.stage_bytes *= P.T;
   P.nstages = (int)std::min<long long>(8, (budget - fixed) / (P.stage_bytes + 16));
   if (P.nstages < 3) return Q8D_EUNSUPPORTED;
   const long long smem = (long long)P.stage_bytes * P.nstages + 16LL * P.nstages + fixed;
   // 8-row sets spread evenly over one wave of CTAs (one per SM)
   const long long sets = (p + kSetRows - 1) / kSetRows;
   const long long sets_cta = (sets + sms - 1) / sms;
-  P.rows_per_cta = (int)(sets_cta * kSetRows);
+  P.rows_per_cta = (int)(sets_cta * kSetRows);  // (a CTA's last tile may hold one set)
   const int grid = (int)((p + P.rows_per_cta - 1) / P.rows_per_cta);
   const int rc = configure_kernel(reinterpret_cast<const void*>(q8_gemv_mma_kernel), 220 * 1024, true);
   if (rc) return rc;

@@ -206,10 +206,10 @@ def test_small_m_bench_shape_sampled(q8d, orc, m):
 
 # ---------------------------------------------------------------------------- tensor-core matvec
 # q8d_matvec runs its tensor-core kernel (mma.sync, f16 hi/lo activations)
-# for one matrix with n % 256 == 0 and p >= 16 * SMs rows; these shapes
+# for one matrix with n % 256 == 0, n >= 2048 and p >= 16 * SMs rows; these shapes
 # reach it (and its sliced-row path for n > 4352), including row counts
 # that are not multiples of the 8-row unit.
-MMA_SHAPES = [(1024, 3072), (3584, 3584), (3584, 2437), (18944, 3584), (4864, 2500), (256, 5000),
+MMA_SHAPES = [(2048, 3072), (3584, 3584), (3584, 2437), (18944, 3584), (4864, 2500), (2048, 5000),
               (8192, 3001)]
 
 
@@ -223,7 +223,7 @@ def test_matvec_mma_parity(q8d, orc, n, p):
     assert np.all(err <= TOL * ab), (err / ab).max()
 
 
-@pytest.mark.parametrize("n,p", [(256, 2500), (3584, 2440), (18944, 2432)])
+@pytest.mark.parametrize("n,p", [(2048, 2500), (3584, 2440), (18944, 2432)])
 def test_matvec_mma_exact_integer_sums(q8d, n, p):
     w = synth.q8_from_parts(5, "mmw", p, n, 0x3C00)
     q = w.reshape(p, n // 32, 34)[:, :, 2:].view(np.int8).astype(np.int64).reshape(p, n)
@@ -234,12 +234,12 @@ def test_matvec_mma_exact_integer_sums(q8d, n, p):
 def test_matvec_mma_one_hot_columns(q8d):
     """One-hot x at columns covering every byte position of even and odd
     blocks (the permuted word order of both alignments)."""
-    n, p = 512, 2432
+    n, p = 2048, 2432
     w = synth.q8_matrix(12, "mmoh", p, n)
     blk = w.reshape(p, n // 32, 34)
     sc = blk[:, :, 0:2].copy().view("<f2").astype(np.float32).reshape(p, n // 32)
     q = blk[:, :, 2:].view(np.int8).astype(np.float32).reshape(p, n)
-    for j in list(range(0, 64)) + [97, 130, 255, 256, 319, 480, 511]:
+    for j in list(range(0, 64)) + [97, 130, 255, 256, 319, 480, 511, 1024, 2047]:
         x = np.zeros(n, np.float32)
         x[j] = np.float32(3.0)
         want = (sc[:, j // 32] * q[:, j]).astype(np.float32) * np.float32(3.0)
@@ -247,7 +247,7 @@ def test_matvec_mma_one_hot_columns(q8d):
 
 
 def test_matvec_mma_minus_128_and_sum_of_x(q8d):
-    n, p = 1024, 2432
+    n, p = 2048, 2432
     w = synth.q8_const_matrix(p, n, 0x3C00, -128)
     assert np.array_equal(gpu_matvec(q8d, w, np.ones(n, np.float32), n, p),
                           np.full(p, -128.0 * n, np.float32))
