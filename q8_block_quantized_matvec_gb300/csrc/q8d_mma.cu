@@ -11,19 +11,21 @@
 //    of `ksplit` CTAs along K shares one output tile and reduces the fp32
 //    partials through distributed shared memory in rank order
 //    (deterministic, no global scratch, no atomics).
-//  * Raw Q8_0 bytes (8 blocks = 272 bytes per row per 256-element chunk) are
-//    streamed into a ring of stages, a chunk's 128 rows by one 2-D tensor
-//    copy (TMA: the rows are a weight-row stride apart in global memory;
-//    the 272 bytes are 68 32-bit elements, so the box stays within TMA's 256
-//    elements per dimension and every x coordinate is a multiple of 16
-//    bytes; rows past the matrix are zero-filled).  All threads
-//    dequantise scale*q exactly in f32, round once to bf16 and store the A
-//    tile in the canonical K-major 128-byte-swizzled layout; X rows are
-//    rounded to bf16 into the B tile the same way.
-//  * One thread issues tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 ->
-//    f32, M = 128, N = m rounded up to 16, K = 16 per instruction) into a
-//    TMEM accumulator; tcgen05.commit signals an mbarrier when the tiles may
-//    be overwritten.  The epilogue reads TMEM with tcgen05.ld.
+//  * Warp roles, so that dequantisation, weight streaming and MMAs overlap:
+//    one producer warp streams raw Q8_0 bytes (8 blocks = 272 bytes per row
+//    per 256-element chunk, the 128 rows a weight-row stride apart) by one
+//    2-D tensor copy per chunk (TMA: 68 32-bit elements x 128 rows; every x
+//    coordinate a multiple of 16 bytes; rows past the matrix zero-filled)
+//    into a ring of stages; 16 dequantising warps turn each half chunk (128
+//    K elements) into bf16 A and B tiles in the canonical K-major
+//    128-byte-swizzled layout (a thread: one (row, block) of scale * q,
+//    computed exactly in f32 and rounded once, and its share of the X rows
+//    rounded to bf16), double-buffered; one MMA warp issues
+//    tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> f32, M = 128,
+//    N = m rounded up to 16, K = 16 per instruction) on a buffer as soon as
+//    it is written and commits to that buffer's mbarrier, which frees it
+//    for the half chunk after next.  The epilogue reads TMEM with
+//    tcgen05.ld.
 // Accuracy: one bf16 rounding of each weight and activation, f32
 // accumulation: |error| <= ~2^-8 * sum|terms| per output.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
@@ -31,20 +33,26 @@
 
 #include <algorithm>
 
+#include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
 
 namespace q8d {
 namespace {
 
-constexpr int kThreads = 512;
+using mv::wait_or_abort;
+
+constexpr int kDeqWarps = 16;                   // dequantising warps
+constexpr int kDeqThreads = kDeqWarps * 32;
+constexpr int kThreads = kDeqThreads + 64;      // + the TMA producer warp + the MMA warp
 constexpr int kM = 128;                         // weight rows per CTA (MMA M)
-constexpr int kKC = 256;                        // K elements per chunk
+constexpr int kKC = 256;                        // K elements per raw chunk (one tensor copy)
+constexpr int kHalfK = 128;                     // K elements per A/B tile (half a chunk)
 constexpr int kRawRow = (kKC / kQBlock) * kQBlockBytes;  // 272 bytes
 constexpr int kRawStage = kM * kRawRow;         // 34816 bytes
 constexpr int kAtomBytes = kM * 128;            // one 64-element K atom of A
-constexpr int kATile = 4 * kAtomBytes;          // 65536 bytes
+constexpr int kAHalf = 2 * kAtomBytes;          // an A tile of 128 K elements: 32 KB
 constexpr int kMaxN = 128;
-constexpr int kBGroup = 4;                      // B-tile pieces a thread loads at once
+constexpr int kMaxPieces = kMaxN * (kHalfK / 8) / kDeqThreads;  // B pieces per thread (<= 4)
 
 struct MmaParams {
   CUtensorMap wmap;  // the weights as [p][row_bytes / 4] 32-bit elements, box [128][68]
@@ -152,13 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   // 1024-byte alignment for the swizzled atoms
   const uint32_t base_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (base_s & 1023)) & 1023);
-  uint8_t* A = smem;
-  uint8_t* B = A + kATile;
-  const int b_atom = P.npad * 128;
-  uint8_t* raw = B + 4 * b_atom;
-  uint64_t* raw_bar = reinterpret_cast<uint64_t*>(raw + (size_t)P.raw_stages * kRawStage);
-  uint64_t* mma_bar = raw_bar + P.raw_stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  const int b_atom = P.npad * 128;             // one 64-element K atom of B
+  uint8_t* A = smem;                           // [2][2 atoms][128 rows][128 B]
+  uint8_t* B = A + 2 * kAHalf;                 // [2][2 atoms][npad rows][128 B]
+  uint8_t* raw = B + 2 * 2 * b_atom;           // [raw_stages][128 rows][272 B]
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(raw + (size_t)P.raw_stages * kRawStage);
+  uint64_t* raw_empty = raw_full + P.raw_stages;
+  uint64_t* ab_full = raw_empty + P.raw_stages;  // [2]: half-chunk tiles written
+  uint64_t* ab_empty = ab_full + 2;              // [2]: their MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_empty + 2);
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -166,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   const int c_begin = (int)((long long)rank * P.nchunks / P.ksplit);
   const int c_end = (int)((long long)(rank + 1) * P.nchunks / P.ksplit);
   const int nloc = c_end - c_begin;
+  const int nhalf = 2 * nloc;
   const uint32_t ncols = P.npad <= 32 ? 32u : (P.npad <= 64 ? 64u : 128u);
 
   if (warp == 0) {
@@ -176,89 +188,94 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int s = 0; s < P.raw_stages; ++s) mbar_init(&raw_bar[s], 1);
-    mbar_init(mma_bar, 1);
+    for (int s = 0; s < P.raw_stages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kDeqWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ab_full[b], kDeqWarps);
+      mbar_init(&ab_empty[b], 1);
+    }
+    s_abort = 0;
     fence_barrier_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint64_t pol = policy_evict_first();
   const int valid_rows = min(kM, P.p - r0);
-
-  auto issue = [&](int i) {  // warp 0: one tensor copy of the chunk's 128 rows
-    if (i >= nloc || lane != 0) return;
-    const int c = c_begin + i;
-    uint64_t* bar = &raw_bar[i % P.raw_stages];
-    uint8_t* dst = raw + (size_t)(i % P.raw_stages) * kRawStage;
-    mbar_arrive_expect_tx(bar, (uint32_t)kRawStage);  // the whole box (zero-filled past p)
-    tma_load_2d(dst, &P.wmap, c * (kRawRow / 4), r0, bar, pol);
-  };
-  if (warp == 0)
-    for (int i = 0; i < P.raw_stages; ++i) issue(i);
-
-  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(P.npad >> 3) << 17) |
-                         ((uint32_t)(kM >> 4) << 24);
   bool ok = true;
+  int issued = 0;
 
-  // B tile pieces: thread tid takes pieces tid + k * kThreads (k < nit), 8
-  // K elements of one X row each, loaded kBGroup at a time (one L2 round
-  // trip per group) before they are rounded and stored
-  const int nit = P.npad * 32 / kThreads;
-  auto b_load = [&](int c, int k0, float4 (&va)[kBGroup], float4 (&vb)[kBGroup]) {
-#pragma unroll
-    for (int u = 0; u < kBGroup; ++u) {
-      const int e = tid + (k0 + u) * kThreads;
-      const int row = e & 7 | ((e >> 8) << 3), cch = (e >> 3) & 31;  // 8 rows per quarter-warp
-      va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k0 + u < nit && row < P.m) {
-        const float4* xp = reinterpret_cast<const float4*>(P.X + (long long)row * P.ldx +
-                                                           (long long)c * kKC + cch * 8);
-        va[u] = __ldg(xp);
-        vb[u] = __ldg(xp + 1);
+  if (warp == kDeqWarps) {
+    // ---- producer: one 2-D tensor copy per 8-block chunk of the 128 rows ----
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (int i = 0; i < nloc; ++i) {
+        const int st = i % P.raw_stages;
+        if (i >= P.raw_stages &&
+            !wait_or_abort(&raw_empty[st], (uint32_t)((i / P.raw_stages) - 1) & 1u, &s_abort))
+          break;
+        mbar_arrive_expect_tx(&raw_full[st], (uint32_t)kRawStage);  // the whole box (zero-filled past p)
+        tma_load_2d(raw + (size_t)st * kRawStage, &P.wmap, (c_begin + i) * (kRawRow / 4), r0,
+                    &raw_full[st], pol);
+        ++issued;
       }
     }
-  };
-  auto b_store = [&](int k0, const float4 (&va)[kBGroup], const float4 (&vb)[kBGroup]) {
+  } else if (warp == kDeqWarps + 1) {
+    // ---- MMA issuer: 8 UMMAs (K = 16 each) per half-chunk, then commit ----
+    if (lane == 0) {
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                             ((uint32_t)(P.npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+      for (int j = 0; j < nhalf; ++j) {
+        const int b = j & 1;
+        if (!wait_or_abort(&ab_full[b], (uint32_t)(j >> 1) & 1u, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(A + b * kAHalf), b0 = smem_u32(B + b * 2 * b_atom);
 #pragma unroll
-    for (int u = 0; u < kBGroup; ++u) {
-      if (k0 + u >= nit) break;
-      const int e = tid + (k0 + u) * kThreads;
-      const int row = e & 7 | ((e >> 8) << 3), cch = (e >> 3) & 31;
-      const uint4 v = make_uint4(bf16x2(va[u].x, va[u].y), bf16x2(va[u].z, va[u].w),
-                                 bf16x2(vb[u].x, vb[u].y), bf16x2(vb[u].z, vb[u].w));
-      *reinterpret_cast<uint4*>(B + sw128_offset(row, cch, b_atom)) = v;
+        for (int s = 0; s < kHalfK / 16; ++s) {
+          const uint32_t koff = (uint32_t)((s & 3) * 32);
+          umma_bf16(tmem, sw128_desc(a0 + (s >> 2) * kAtomBytes + koff),
+                    sw128_desc(b0 + (s >> 2) * b_atom + koff), idesc, (j > 0 || s > 0) ? 1u : 0u);
+        }
+        umma_commit(&ab_empty[b]);
+      }
     }
-  };
-
-  // the first group of chunk i's B pieces is loaded during chunk i - 1 (all
-  // of a thread's pieces for m <= 64): its L2 latency overlaps the previous
-  // chunk's dequantisation and MMAs
-  float4 va[kBGroup], vb[kBGroup];
-  if (nloc > 0) b_load(c_begin, 0, va, vb);
-  for (int i = 0; i < nloc; ++i) {
-    const int c = c_begin + i;
-    // (a) the previous chunk's MMAs must have finished reading A and B
-    if (i > 0) ok = ok && mbar_wait(mma_bar, (uint32_t)(i - 1) & 1u);
-    // (b) B tile: X[0..m) rows, K elements [c*256, c*256+256), rounded to bf16
-    b_store(0, va, vb);
-    for (int k0 = kBGroup; k0 < nit; k0 += kBGroup) {
-      b_load(c, k0, va, vb);
-      b_store(k0, va, vb);
-    }
-    if (i + 1 < nloc) b_load(c + 1, 0, va, vb);
-    // (c) raw weight bytes of this chunk
-    ok = ok && mbar_wait(&raw_bar[i % P.raw_stages], (uint32_t)(i / P.raw_stages) & 1u);
-    if (!__syncthreads_and(ok)) break;
-    // (d) dequantise 128 rows x 8 blocks into the A tile
-    const uint8_t* rs = raw + (size_t)(i % P.raw_stages) * kRawStage;
-    for (int f = tid; f < kM * 8; f += kThreads) {
-      const int rr = (f & 7) | (((f >> 5) & 15) << 3);
-      const int blk = ((f >> 3) & 3) | ((f >> 9) << 2);
-      uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0, o2 = o0, o3 = o0;
+  } else {
+    // ---- dequantisation warps: one (row, block) item and up to npad/32 B
+    // pieces per thread and half-chunk ----
+    const int rr = (tid & 7) | ((tid >> 5) << 3);
+    const int blk = (tid >> 3) & 3;
+    const int nb = P.npad * (kHalfK / 8) / kDeqThreads;  // B pieces per thread (may be 0 or fractional)
+    const int npieces = P.npad * (kHalfK / 8);
+    for (int j = 0; j < nhalf; ++j) {
+      const int i = j >> 1, h = j & 1, b = j & 1, c = c_begin + i;
+      const int st = i % P.raw_stages;
+      // B pieces of this half: X rows, K elements c*256 + h*128 + [8 cch, 8 cch + 8)
+      float4 xa[kMaxPieces], xb[kMaxPieces];
+#pragma unroll
+      for (int u = 0; u < kMaxPieces; ++u) {
+        const int e = tid + u * kDeqThreads;
+        const int row = (e & 7) | ((e >> 7) << 3), cch = (e >> 3) & 15;
+        xa[u] = xb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u <= nb && e < npieces && row < P.m) {
+          const float4* xp = reinterpret_cast<const float4*>(
+              P.X + (long long)row * P.ldx + (long long)c * kKC + h * kHalfK + cch * 8);
+          xa[u] = __ldg(xp);
+          xb[u] = __ldg(xp + 1);
+        }
+      }
+      if (h == 0) ok = wait_or_abort(&raw_full[st], (uint32_t)(i / P.raw_stages) & 1u, &s_abort) && ok;
+      // the item's block (raw row rr, block 4h + blk) as bf16 of scale * q
+      const uint8_t* rs = raw + (size_t)st * kRawStage;
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) pk[k] = 0u;
       if (rr < valid_rows) {
-        const uint32_t off = (uint32_t)(rr * kRawRow + blk * kQBlockBytes);
+        const uint32_t off = (uint32_t)(rr * kRawRow + (4 * h + blk) * kQBlockBytes);
         const uint32_t* s32 = reinterpret_cast<const uint32_t*>(rs);
         const uint32_t wi = off >> 2;
         const bool odd = (off & 2u) != 0;
@@ -267,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
         for (int k = 0; k < 9; ++k) a[k] = s32[wi + k];
         const float sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
         const uint32_t sh = odd ? 32u : 16u;
-        uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t wq = __funnelshift_rc(a[k], a[k + 1], sh) ^ 0x80808080u;
@@ -278,40 +294,48 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
           pk[2 * k] = bf16x2(q0 * sc, q1 * sc);
           pk[2 * k + 1] = bf16x2(q2 * sc, q3 * sc);
         }
-        o0 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        o1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        o2 = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-        o3 = make_uint4(pk[12], pk[13], pk[14], pk[15]);
       }
-      const int c0 = blk * 4;  // 16-byte chunk index of the block's first 8 elements
-      *reinterpret_cast<uint4*>(A + sw128_offset(rr, c0 + 0, kAtomBytes)) = o0;
-      *reinterpret_cast<uint4*>(A + sw128_offset(rr, c0 + 1, kAtomBytes)) = o1;
-      *reinterpret_cast<uint4*>(A + sw128_offset(rr, c0 + 2, kAtomBytes)) = o2;
-      *reinterpret_cast<uint4*>(A + sw128_offset(rr, c0 + 3, kAtomBytes)) = o3;
-    }
-    // generic-proxy smem writes -> visible to the tensor core (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (warp == 0) {
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+      // (the raw stage is read: release it after the chunk's second half)
+      if (h == 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[st]);
+      }
+      // tiles of buffer b are free once the MMAs of half j - 2 completed
+      if (j >= 2) ok = wait_or_abort(&ab_empty[b], (uint32_t)((j >> 1) - 1) & 1u, &s_abort) && ok;
+      uint8_t* Ab = A + b * kAHalf;
+      const int c0 = blk * 4;  // 16-byte chunk index of the block's first 8 elements (in the half)
+      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 0, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 1, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 2, kAtomBytes)) = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 3, kAtomBytes)) = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+      uint8_t* Bb = B + b * 2 * b_atom;
 #pragma unroll
-        for (int s = 0; s < kKC / 16; ++s) {
-          const uint32_t koff = (uint32_t)((s & 3) * 32);
-          umma_bf16(tmem, sw128_desc(a0 + (s >> 2) * kAtomBytes + koff),
-                    sw128_desc(b0 + (s >> 2) * b_atom + koff), idesc, (i > 0 || s > 0) ? 1u : 0u);
+      for (int u = 0; u < kMaxPieces; ++u) {
+        const int e = tid + u * kDeqThreads;
+        if (u <= nb && e < npieces) {
+          const int row = (e & 7) | ((e >> 7) << 3), cch = (e >> 3) & 15;
+          *reinterpret_cast<uint4*>(Bb + sw128_offset(row, cch, b_atom)) =
+              make_uint4(bf16x2(xa[u].x, xa[u].y), bf16x2(xa[u].z, xa[u].w),
+                         bf16x2(xb[u].x, xb[u].y), bf16x2(xb[u].z, xb[u].w));
         }
-        umma_commit(mma_bar);
       }
+      // generic-proxy shared writes -> visible to the tensor core (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      issue(i + P.raw_stages);  // the raw stage just consumed is free again
+      if (lane == 0) mbar_arrive(&ab_full[b]);
     }
   }
 
+  // every MMA of the CTA has completed once the last half's commit arrives
+  if (nhalf > 0)
+    ok = wait_or_abort(&ab_empty[(nhalf - 1) & 1], (uint32_t)((nhalf - 1) >> 1) & 1u, &s_abort) && ok;
+  ok = __syncthreads_and(ok && !*(volatile int*)&s_abort);
+  if (!ok && warp == kDeqWarps && lane == 0) {
+    // copies issued but never consumed may still be in flight
+    for (int k = max(0, issued - P.raw_stages); k < issued; ++k)
+      mbar_wait(&raw_full[k % P.raw_stages], (uint32_t)(k / P.raw_stages) & 1u);
+  }
   // ---- epilogue: TMEM -> shared partial tile [npad][128] (reusing A) ----
-  if (nloc > 0) ok = ok && mbar_wait(mma_bar, (uint32_t)(nloc - 1) & 1u);
-  ok = __syncthreads_and(ok);
   tc_fence_after();
   float* part = reinterpret_cast<float*>(A);
   if (warp < 4) {
@@ -393,7 +417,7 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return Q8D_EUNSUPPORTED;
   }
-  const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), 227 * 1024, false);
+  const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), 224 * 1024, false);
   if (crc) return crc;
   const int row_tiles = (p + kM - 1) / kM;
   const int nchunks = n / kKC;
@@ -413,8 +437,8 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
     P.nchunks = nchunks;
     P.row_bytes = row_bytes;
     P.ksplit = std::max(1, std::min({8, sms / row_tiles, nchunks}));
-    const int fixed = kATile + 4 * P.npad * 128 + 1024 + 64;
-    P.raw_stages = (fixed + 3 * kRawStage <= 227 * 1024) ? 3 : 2;
+    const int fixed = 2 * kAHalf + 2 * 2 * P.npad * 128 + 1024 + 128;
+    P.raw_stages = (fixed + 3 * kRawStage <= 224 * 1024) ? 3 : 2;
     const int smem = fixed + P.raw_stages * kRawStage;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(row_tiles, P.ksplit, 1);
