@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
 
   const uint64_t pol = policy_evict_first();
   const int n_sub = (t_end - t_begin + C::kTS - 1) / C::kTS;
+  // the window's first run in registers (a causal window is only that run)
+  const int run0_len = s_win.len[0], run0_cell = s_win.cell[0];
   auto issue = [&](int k) {  // warp 0 only
     if (k >= n_sub) return;
     const int r0 = t_begin + k * C::kTS;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
     if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)(2 * nr * C::kRowBytes));
     __syncwarp();
     for (int r = lane; r < nr; r += 32) {
-      const long long row = (long long)s_win.cell_of(r0 + r) * kvw;
+      const long long row = (long long)(r0 + r < run0_len ? run0_cell + r0 + r : s_win.cell_of(r0 + r)) * kvw;
       bulk_g2s(st + r * C::kKStride, kbase + row, C::kRowBytes, &bar[k & 1], pol);
       bulk_g2s(st + C::kTS * C::kKStride + r * C::kRowBytes, vbase + row, C::kRowBytes,
                &bar[k & 1], pol);

@@ -179,6 +179,8 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     }
   }
   __syncthreads();  // q rows scaled; the appended row is visible to every thread
+  // the window's first run in registers (a causal window is only that run)
+  const int run0_len = s_win.len[0], run0_cell = s_win.cell[0];
 
   // ---- this warp's cp.async ring over its token groups ----
   const int ngroups = (t_end - t_begin + kGroup - 1) / kGroup;
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
       for (int e = lane; e < kGroup * kChunks; e += 32) {
         const int r = e / kChunks, pc = e % kChunks;
         if (r < nr) {
-          const long long off = (long long)s_win.cell_of(t0 + r) * kvw * 2 + pc * 16;
+          const long long off = (long long)(t0 + r < run0_len ? run0_cell + t0 + r : s_win.cell_of(t0 + r)) * kvw * 2 + pc * 16;
           cp_async16(st + r * C::kStride + pc * 16, reinterpret_cast<const uint8_t*>(kbase) + off);
           cp_async16(st + (kGroup + r) * C::kStride + pc * 16,
                      reinterpret_cast<const uint8_t*>(vbase) + off);

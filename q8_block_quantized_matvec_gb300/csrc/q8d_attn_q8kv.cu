@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
     }
   }
   __syncthreads();  // q rows scaled; the appended row is in the cache
+  // the window's first run in registers (a causal window is only that run)
+  const int run0_len = s_win.len[0], run0_cell = s_win.cell[0];
 
   // ---- this warp's cp.async ring over its token groups ----
   const int ngroups = (t_end - t_begin + kGroupQ - 1) / kGroupQ;
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
       for (int e = lane; e < kGroupQ * C::kPer; e += 32) {
         const int r = e / C::kPer, pc = e % C::kPer;
         if (r < nr) {
-          const long long off = (long long)s_win.cell_of(t0 + r) * rowb + pc * C::kCopy;
+          const long long off = (long long)(t0 + r < run0_len ? run0_cell + t0 + r : s_win.cell_of(t0 + r)) * rowb + pc * C::kCopy;
           cp_async_n<C::kCopy>(st + r * C::kRS + pc * C::kCopy, kbase + off);
           cp_async_n<C::kCopy>(st + (kGroupQ + r) * C::kRS + pc * C::kCopy, vbase + off);
         }
