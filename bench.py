@@ -381,6 +381,16 @@ def run_profile(args):
         q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p)
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
+    elif args.profile in ("attn_stress_q8", "attn_window"):
+        s = torch.cuda.Stream()
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+        fn = attn_stress_q8 if args.profile == "attn_stress_q8" else attn_window_leg
+        fn(q8d, 28, 4, 128, 1, s, flush)  # warm-up launches (not profiled)
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStart()
+        fn(q8d, 28, 4, 128, 0, s, flush)  # four launches
+        torch.cuda.synchronize()
+        cudart.cudaProfilerStop()
     elif args.profile == "attn_stress":
         lens, args_, err = stress_inputs(q8d, 28, 4, 128)
         q8d.q8d_gqa_decode_attn(*args_)
@@ -757,7 +767,7 @@ def main():
     ap.add_argument("--kernel-reps", type=int, default=3)
     ap.add_argument("--profile",
                     choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "mma16", "mma64",
-                             "matvec_sweep"],
+                             "matvec_sweep", "attn_stress_q8", "attn_window"],
                     default=None,
                     help="run a short fixed workload between cudaProfilerStart/Stop for ncu "
                          "(--profile-from-start off) and print no JSON")
