@@ -9,47 +9,31 @@
 // Why: on CUDA cores every quant costs a byte permute, a bias add and an FMA
 // (half of them on the half-rate ALU pipe), which holds the matvec near 50 %
 // issue and 0.5 of HBM.  Here a quant pair costs one PRMT and one sub.f16x2,
-// and the products go to the tensor pipe:
-//  * A (16 x 16 per MMA): quants as exact f16 (a sign-flipped byte under the
-//    exponent byte 0x64 is 1152 + q; one sub.f16x2 removes the 1152).  The
-//    16 A rows are 8 weight rows x 2 column halves, so a unit of work is 8
-//    rows x 4 blocks of the same byte alignment (blocks base, base+2,
-//    base+4, base+6; half 0 = {base, base+4}, half 1 = {base+2, base+6}),
-//    and 8-row granularity keeps the rows of a matrix evenly spread over
-//    the CTAs.  Each thread feeds one 32-bit word of quants per MMA (its
-//    contraction indices are permuted to match: 4 consecutive bytes).
-//  * B (16 x 8): the 8 columns are 4 blocks x (x_hi, x_lo), x = hi + lo in
-//    f16 after one power-of-two scale of the whole vector (max|x| scaled
-//    into [2^14, 2^15)), so every product is exact in f32 and the sum
-//    matches f32 arithmetic; columns that pair a row half with the other
-//    half's blocks are zero.  The fragments are built once per launch in
-//    shared memory, in the permuted byte order of each block's words.
-//  * D: every thread ends a unit with the (hi, lo) partials of one (row,
-//    block) pair, scales them by that block's f16 scale and accumulates in
-//    f32; 4 lanes share a row and the warps' row partials are summed in a
-//    fixed order (deterministic).
+// and the products go to the tensor pipe (the operand layout is in
+// q8d_mma_frag.cuh).  This kernel scales the whole vector by one power of
+// two (max|x| into [2^14, 2^15)) before the f16 hi/lo split, and builds the
+// x fragments once per launch in shared memory.
 //  * Weights stream in through a ring of shared-memory stages filled with
 //    1-D bulk copies (TMA) by one producer warp: a tile is 8 rows x up to
 //    ~150 blocks (long rows are cut into slices), one copy per row into a
 //    row slot padded so that the lanes' word reads hit distinct banks.
-// Blocks of odd index start two bytes after a word boundary, so their quants
-// are word aligned; for even blocks the words at +4 .. +28 hold quants 2..29
-// and the last word is assembled from the block's first and last words.
+//  * 4 lanes share a row; the warps' row partials are summed in a fixed
+//    order (deterministic).
 #include <algorithm>
 
 #include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
+#include "q8d_mma_frag.cuh"
 #include "q8d_rows.cuh"
 
 namespace q8d {
 namespace {
 
 using namespace mv;
+using namespace tc;
 
 constexpr int kMvMaxWarps = 16;                         // consumer warps (at most)
 constexpr int kMvThreads = (kMvMaxWarps + 1) * 32;      // + the producer warp
-constexpr int kXfBlock = 144;                           // x fragment bytes per block (128 + pad)
-constexpr int kSetRows = 8;                             // rows per unit
 constexpr int kWinSets = 4;                             // row sets per reduction window
 
 struct MvParams {
@@ -66,112 +50,6 @@ struct MvParams {
   int T;             // 8-row sets per tile (1 or 2)
   int* d_err;
 };
-
-__device__ __forceinline__ uint32_t lds32a(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64a(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds16a(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-
-// Four signed quants (one word) -> two exact f16 pairs: bytes (0, 1), (2, 3).
-__device__ __forceinline__ void quant_pairs(uint32_t w, uint32_t& h01, uint32_t& h23) {
-  const uint32_t f = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(f, 0x64646464u, 0x5140);
-  const uint32_t b = __byte_perm(f, 0x64646464u, 0x7362);
-  const uint32_t bias = 0x64806480u;  // (1152, 1152)
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(a), "r"(bias));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(bias));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Quant index of byte k of word w of a block (the order the A side reads).
-__device__ __forceinline__ int word_quant(bool even_block, int w, int k) {
-  if (!even_block) return 4 * w + k;
-  if (w < 7) return 4 * w + 2 + k;
-  return k < 2 ? k : 28 + k;
-}
-
-// Per-lane constants of the unit loop (byte offsets within a pair of units:
-// 8 consecutive blocks 8k .. 8k+7 of a tile row; the even unit is blocks
-// 8k + {0, 2, 4, 6}, the odd unit 8k + {1, 3, 5, 7}; half 0 of a unit is
-// its blocks +0 and +4, half 1 its blocks +2 and +6).
-struct LaneOffs {
-  uint32_t e0, e1;    // even unit, halves 0 / 1: this lane's word 2i + wsel, i < 3 (+ 8 i)
-  uint32_t e3a, e3b;  // even unit, i = 3: the two words the last word comes from (half 0)
-  uint32_t sel3;      // their byte selector (word 6 as is, or bytes {2,3} + {32,33})
-  uint32_t o0, o1;    // odd unit, halves 0 / 1: word 2i + wsel (+ 8 i)
-  uint32_t s_even;    // this lane's (row, block) scale of the even unit (odd: + 34)
-};
-
-__device__ __forceinline__ LaneOffs lane_offsets(int cq) {
-  const int j = cq & 1, wsel = cq >> 1;
-  LaneOffs L;
-  // even blocks start on a word: words +4 .. +28 hold quants 2 .. 29, the
-  // last word is quants {0, 1} (bytes 2, 3) and {30, 31} (bytes 32, 33)
-  L.e0 = 136u * j + 4u + 4u * wsel;
-  L.e1 = L.e0 + 68u;
-  L.e3a = wsel ? 136u * j : 136u * j + 28u;
-  L.e3b = 136u * j + 32u;
-  L.sel3 = wsel ? 0x5432u : 0x3210u;
-  // odd blocks start two bytes past a word: quants are word aligned
-  L.o0 = 34u + 136u * j + 2u + 4u * wsel;
-  L.o1 = L.o0 + 68u;
-  L.s_even = (uint32_t)(cq < 2 ? 4 * cq : 2 + 4 * (cq - 2)) * kQBlockBytes;
-  return L;
-}
-
-// Two units (8 rows x blocks 8k .. 8k+7) at row32 + base; xb: this lane's x
-// fragments of the pair (its B block of the even unit, word wsel; the odd
-// unit's are 144 bytes on; the zero pad for lanes whose B column is zero).
-__device__ __forceinline__ float pair_dot(uint32_t rb, uint32_t xb, uint32_t xstep, const LaneOffs& L,
-                                          bool lo_half) {
-  float ae[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t we0, we1;
-    if (i < 3) {
-      we0 = lds32a(rb + L.e0 + 8 * i);
-      we1 = lds32a(rb + L.e1 + 8 * i);
-    } else {
-      we0 = __byte_perm(lds32a(rb + L.e3a), lds32a(rb + L.e3b), L.sel3);
-      we1 = __byte_perm(lds32a(rb + L.e3a + 68), lds32a(rb + L.e3b + 68), L.sel3);
-    }
-    const uint32_t wo0 = lds32a(rb + L.o0 + 8 * i), wo1 = lds32a(rb + L.o1 + 8 * i);
-    const uint2 be = lds64a(xb + 32 * i);
-    const uint2 bo = lds64a(xb + xstep + 32 * i);
-    uint32_t a0, a1, a2, a3;
-    quant_pairs(we0, a0, a2);
-    quant_pairs(we1, a1, a3);
-    mma_f16(ae, a0, a1, a2, a3, be.x, be.y);
-    quant_pairs(wo0, a0, a2);
-    quant_pairs(wo1, a1, a3);
-    mma_f16(ao, a0, a1, a2, a3, bo.x, bo.y);
-  }
-  // (row gq, block b_cq) of each unit: half 0 for cq < 2, half 1 otherwise
-  const float pe = lo_half ? ae[0] + ae[1] : ae[2] + ae[3];
-  const float po = lo_half ? ao[0] + ao[1] : ao[2] + ao[3];
-  const float se = __half2float(__ushort_as_half((unsigned short)lds16a(rb + L.s_even)));
-  const float so = __half2float(__ushort_as_half((unsigned short)lds16a(rb + L.s_even + 34)));
-  return fmaf(se, pe, so * po);
-}
 
 __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
                           int* abort_flag, int v0, int v1) {
@@ -259,13 +137,7 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
       float v[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) v[k] = ldexpf(__ldg(P.x + bb * kQBlock + word_quant(even, w, k)), e);
-      const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
-      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-      const __half2 l01 = __floats2half2_rn(v[0] - f01.x, v[1] - f01.y);
-      const __half2 l23 = __floats2half2_rn(v[2] - f23.x, v[3] - f23.y);
-      uint2* dst = reinterpret_cast<uint2*>(xf + (size_t)bb * kXfBlock + w * 16);
-      dst[0] = make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
-      dst[1] = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+      store_x_word(xf + (size_t)bb * kXfBlock + w * 16, v);
     }
     if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
     consumer_sync(nct);

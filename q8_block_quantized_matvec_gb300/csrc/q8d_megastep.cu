@@ -34,6 +34,7 @@
 #include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
 #include "q8d_megastep.cuh"
+#include "q8d_mma_frag.cuh"
 
 namespace q8d {
 
@@ -62,7 +63,7 @@ __shared__ int ms_L;                       // attended length of this step
 // accumulates into (prefetched at the phase start), or its gate rows of a
 // gate|up phase (kept for the up rows): no global round trip in the window
 // reductions.
-constexpr int kRowsMax = 1024;
+constexpr int kRowsMax = 512;
 __shared__ float ms_rows[kRowsMax];
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
@@ -131,6 +132,11 @@ __device__ bool grid_wait(const MParams& P) {
   return *s_flag != 0;
 }
 
+// Whether a tensor-core phase's RMSNorm weights fit behind its fragments.
+__device__ __forceinline__ bool tc_weights_staged(const MPhase& F) {
+  return F.bpr * 276 + 128 <= kMsRegion;  // bpr * (144 + 4) + 128 + n * 4
+}
+
 // Work of matvec phase F that depends on no other CTA, done between the
 // halves of the grid barrier before it: the residual rows this CTA adds to
 // (written by this CTA, or before an earlier barrier) and the RMSNorm
@@ -140,6 +146,16 @@ __device__ void matvec_pre(const MPhase& F, uint8_t* region) {
     const int r0 = blockIdx.x * F.rows_per_cta;
     const int r1 = min(F.total_rows, r0 + F.rows_per_cta);
     for (int i = threadIdx.x; i < r1 - r0; i += kCT) ms_rows[i] = __ldcg(F.y[0] + r0 + i);
+  }
+  if (F.tc) {
+    // tensor-core phase: the RMSNorm weights at the end of the region
+    // (clear of the fragments the activation pass writes)
+    if (F.xmode == kXRmsNorm && tc_weights_staged(F)) {
+      float4* ws = reinterpret_cast<float4*>(region + kMsRegion) - F.n / 4;
+      for (int i = threadIdx.x; i < F.n / 4; i += kCT)
+        ws[i] = __ldg(reinterpret_cast<const float4*>(F.xw) + i);
+    }
+    return;
   }
   const int pass4 = kMsRegion / 32;
   if (F.xmode == kXRmsNorm && F.n / 4 <= pass4) {
@@ -202,10 +218,40 @@ __device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int to
   }
 }
 
-// Window reduction: sums each row's warp partials over segments and lanes
-// in a fixed order and writes the row.
+// Writes the dot product `sum` of virtual row vr of phase F: adds the
+// residual, forms SiLU(gate) * up, tracks the argmax.
 // rbase: the matrix row held in ms_rows[0] (the CTA's first row), or -1
 // when the CTA's rows do not fit ms_rows (then values go through L2).
+__device__ __forceinline__ void ms_store_row(const MPhase& F, int vr, float sum, int rbase,
+                                             float& bv, int& bi) {
+  int sg = 0;
+  while (sg + 1 < F.nseg && vr >= F.vbegin[sg + 1]) ++sg;
+  const int ri = vr - F.vbegin[sg];
+  float* y = F.y[sg] + ri;
+  float out = sum;
+  if (F.accumulate) out += rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(y);
+  if (F.glu) {
+    // gate rows are kept; an up row combines with its gate row (computed
+    // by this CTA in an earlier window) into h = silu(gate) * up, stored
+    // over the gate half (the only half read afterwards)
+    if (sg == 0) {
+      if (rbase >= 0) ms_rows[ri - rbase] = out;
+      else *y = out;
+    } else {
+      const float gt = rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(F.y[0] + ri);
+      F.y[0][ri] = gt / (1.0f + expf(-gt)) * out;
+    }
+  } else {
+    *y = out;
+  }
+  if (F.argmax && !isnan(out) && am_better(out, ri, bv, bi)) {
+    bv = out;
+    bi = ri;
+  }
+}
+
+// Window reduction: sums each row's warp partials over segments and lanes
+// in a fixed order and writes the row.
 __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, int wbeg, int rbase,
                                  float& bv, int& bi) {
   // 8 threads per row, four rows per warp at a time: windows of up to 80
@@ -231,33 +277,36 @@ __device__ void ms_window_reduce(const MPhase& F, const float* part, int nrow, i
     float sum = lo + hi;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (valid && sub == 0) {
-      const int vr = wbeg + r;
-      int sg = 0;
-      while (sg + 1 < F.nseg && vr >= F.vbegin[sg + 1]) ++sg;
-      const int ri = vr - F.vbegin[sg];
-      float* y = F.y[sg] + ri;
-      float out = sum;
-      if (F.accumulate) out += rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(y);
-      if (F.glu) {
-        // gate rows are kept; an up row combines with its gate row (computed
-        // by this CTA in an earlier window) into h = silu(gate) * up, stored
-        // over the gate half (the only half read afterwards)
-        if (sg == 0) {
-          if (rbase >= 0) ms_rows[ri - rbase] = out;
-          else *y = out;
-        } else {
-          const float gt = rbase >= 0 ? ms_rows[ri - rbase] : __ldcg(F.y[0] + ri);
-          F.y[0][ri] = gt / (1.0f + expf(-gt)) * out;
-        }
-      } else {
-        *y = out;
-      }
-      if (F.argmax && !isnan(out) && am_better(out, ri, bv, bi)) {
-        bv = out;
-        bi = ri;
-      }
+    if (valid && sub == 0) ms_store_row(F, wbeg + r, sum, rbase, bv, bi);
+  }
+}
+
+// The CTA's argmax candidate (over the threads' (bv, bi)) to P.am_val /
+// P.am_idx[blockIdx.x].
+__device__ void ms_argmax_cta(const MParams& P, float bv, int bi, float* s_f, int* s_i) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (am_better(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
     }
+  }
+  if (lane == 0) {
+    s_f[warp] = bv;
+    s_i[warp] = bi;
+  }
+  consumer_sync(kCT);
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kW; ++w)
+      if (am_better(s_f[w], s_i[w], bv, bi)) {
+        bv = s_f[w];
+        bi = s_i[w];
+      }
+    P.am_val[blockIdx.x] = bv;
+    P.am_idx[blockIdx.x] = bi;
   }
 }
 
@@ -461,31 +510,224 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
       buf = buf ? 0u : buf_bytes;
     }
   }
-  if (F.argmax) {
+  if (F.argmax) ms_argmax_cta(P, bv, bi, s_f, s_i);
+  return ok;
+}
+
+// ---------------------------------------------------------------- tensor-core matvec
+// Matvec phases whose rows are whole pairs of 8 blocks (n % 256 == 0) and
+// whose x fragments fit the shared region: the block dot products run on
+// mma.sync (layout in q8d_mma_frag.cuh).  A tile is 8 consecutive rows of
+// the CTA's range (the last one may hold fewer), each in a row slot of F.SR
+// bytes; the unit pairs of all the CTA's tiles are dealt to the warps in
+// turn (pair k of the CTA's t-th tile goes to warp (t * pairs + k) mod 20),
+// so no warp waits for another within a window.  Each 32-element block of
+// the activation vector gets its own power-of-two scale before the f16
+// hi/lo split (the 8 threads that build a block's fragment share its max),
+// and the block's inverse scale multiplies its partial with the weight
+// scale: no CTA-wide reduction is needed for it.
+//
+// Region layout: x fragments [bpr][144], a 128-byte zero pad, the blocks'
+// inverse scales [bpr] (f32), then the double-buffered window partials
+// [2][win * 8][kW].
+
+// The 4 values of word w of block bb (in word_quant order) from v + 32 bb.
+// kMode 0: L2 loads (activations other CTAs wrote), 1: read-only global
+// loads, 2: shared memory.
+template <int kMode>
+__device__ __forceinline__ void load_word(const float* v, int bb, int w, float (&o)[4]) {
+  const float* b = v + (size_t)bb * kQBlock;
+  auto ld2 = [](const float* p) {
+    const float2* q = reinterpret_cast<const float2*>(p);
+    return kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
+  };
+  if (bb & 1) {
+    const float4* q = reinterpret_cast<const float4*>(b + 4 * w);
+    const float4 a = kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  } else {
+    const float2 a = ld2(b + (w < 7 ? 4 * w + 2 : 0));
+    const float2 c = ld2(b + (w < 7 ? 4 * w + 4 : 30));
+    o[0] = a.x; o[1] = a.y; o[2] = c.x; o[3] = c.y;
+  }
+}
+
+constexpr int kTcItems = 4;  // (block, word) items per consumer thread: bpr <= 320
+
+__device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uint32_t smem32,
+                                uint8_t* region, float* s_f, int* s_i) {
+  using namespace tc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bpr = F.bpr;
+  uint8_t* xf = region;
+  uint8_t* zpad = xf + (size_t)bpr * kXfBlock;
+  float* xinv = reinterpret_cast<float*>(zpad + 128);
+  float* part = xinv + bpr;
+  // ---- x fragments (RMSNorm applied first where the phase has it) ----
+  const bool rms = F.xmode == kXRmsNorm;
+  const int nit = bpr * 8;
+  float v[kTcItems][4];
+  float ss = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (am_better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
+  for (int k = 0; k < kTcItems; ++k) {
+    const int it = threadIdx.x + k * kCT;
+    if (it < nit) {
+      load_word<0>(F.X, it >> 3, it & 7, v[k]);
+    } else {
+      v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.f;
     }
-    if (lane == 0) {
-      s_f[warp] = bv;
-      s_i[warp] = bi;
-    }
+    ss = fmaf(v[k][0], v[k][0], ss);
+    ss = fmaf(v[k][1], v[k][1], ss);
+    ss = fmaf(v[k][2], v[k][2], ss);
+    ss = fmaf(v[k][3], v[k][3], ss);
+  }
+  if (rms) {
+    // (every element is in exactly one (block, word) item; the sum's order
+    // is the same in every CTA)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_f[warp] = ss;
     consumer_sync(kCT);
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kW; ++w)
-        if (am_better(s_f[w], s_i[w], bv, bi)) {
-          bv = s_f[w];
-          bi = s_i[w];
-        }
-      P.am_val[blockIdx.x] = bv;
-      P.am_idx[blockIdx.x] = bi;
+    float tot = 0.f;
+    for (int w = 0; w < kW; ++w) tot += s_f[w];
+    const float inv = 1.0f / sqrtf(tot / (float)F.n + P.eps);
+    const bool staged = tc_weights_staged(F);  // (by matvec_pre)
+    const float* wsm = reinterpret_cast<const float*>(region + kMsRegion) - F.n;
+#pragma unroll
+    for (int k = 0; k < kTcItems; ++k) {
+      const int it = threadIdx.x + k * kCT;
+      float wv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (it < nit) {
+        if (staged) load_word<2>(wsm, it >> 3, it & 7, wv);
+        else load_word<1>(F.xw, it >> 3, it & 7, wv);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[k][j] = v[k][j] * inv * wv[j];
     }
   }
+#pragma unroll
+  for (int k = 0; k < kTcItems; ++k) {
+    const int it = threadIdx.x + k * kCT;
+    if (k * kCT >= nit) break;  // (uniform over the CTA)
+    // the block's max |x| over its 8 words (8 consecutive lanes)
+    float m = fmaxf(fmaxf(fabsf(v[k][0]), fabsf(v[k][1])), fmaxf(fabsf(v[k][2]), fabsf(v[k][3])));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    int ex = 0;
+    if (m > 0.f) frexpf(m, &ex);
+    // m * 2^e in [2^14, 2^15) (e >= -113 for any finite m; e <= 125 keeps
+    // 2^e and 2^-e normal floats, blocks below 2^-110 scale to less)
+    const int e = m > 0.f ? min(125, 15 - ex) : 0;
+    if (it < nit) {
+      const float sc = __int_as_float((127 + e) << 23);
+      float t[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j] = v[k][j] * sc;
+      store_x_word(xf + (size_t)(it >> 3) * kXfBlock + (it & 7) * 16, t);
+      if ((it & 7) == 0) xinv[it >> 3] = __int_as_float((127 - e) << 23);
+    }
+  }
+  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
+  consumer_sync(kCT);
+
+  // ---- units ----
+  const int gq = lane >> 2, cq = lane & 3;
+  const LaneOffs LO = lane_offsets(cq);
+  // this thread's B column: n = gq = 4h + 2jb + hl; nonzero when its block
+  // (jb) is the one this thread's contraction words belong to (cq & 1)
+  const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
+  const bool bmatch = bjb == (cq & 1);
+  const uint32_t xlane =
+      bmatch ? (uint32_t)((2 * bh + 4 * bjb) * kXfBlock + bhl * 8 + (cq >> 1) * 16) : 0u;
+  const uint32_t xstep = bmatch ? (uint32_t)kXfBlock : 0u;
+  const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
+  const uint32_t xi32 = smem_u32(xinv) + 4u * (uint32_t)lane_block(cq);
+  const bool lo_half = cq < 2;
+  const int P8 = bpr / 8;  // unit pairs per row
+  const int T = F.T;
+  // this lane's row gq of a set: groups of 1 << gsh rows, 16 bytes apart
+  const uint32_t rowoff = (uint32_t)(gq * F.row_bytes) + (uint32_t)((gq >> F.gsh) << 4);
+  const uint32_t part32 = smem_u32(part);
+  const int tile_rows = kSetRows * T;
+  const uint32_t buf_bytes = (uint32_t)(F.win * tile_rows * kW) * 4u;
+  const int rbase = (F.accumulate || F.glu) && F.rows_per_cta <= kRowsMax
+                        ? (int)blockIdx.x * F.rows_per_cta
+                        : -1;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  bool ok = true;
+  uint32_t buf = 0;
+  int first = warp;  // this warp's first pair of the next tile
+  const int npieces = F.glu ? 2 : 1;
+  for (int piece = 0; piece < npieces; ++piece) {
+    int v0, v1;
+    piece_range(F.glu, F.vbegin[1], F.rows_per_cta, F.total_rows, piece, v0, v1);
+    int wt = 0, wbeg = v0;
+    for (int r0 = v0; r0 < v1; r0 += tile_rows) {
+      const int nsets = min(T, (v1 - r0 + kSetRows - 1) / kSetRows);
+      const int items = nsets * P8;
+      ok = wait_or_abort(&ms_full[rp.s], rp.ph, &ms_abort) && ok;
+      const uint32_t row32 = after_wait(rp.stage32 + rowoff);
+      float y0 = 0.f, y1 = 0.f;  // row gq of the tile's sets 0 / 1
+      for (int j = first; j < items; j += kW) {
+        const int sl = j >= P8 ? 1 : 0;  // (T <= 2)
+        const int k = j - sl * P8;
+        const uint32_t rb = row32 + (uint32_t)(sl * F.SR) + 272u * (uint32_t)k;
+        const uint32_t xb = bmatch ? xf32 + (uint32_t)(8 * k) * kXfBlock + xlane : z32;
+        float pe, po;
+        pair_units(rb, xb, xstep, LO, lo_half, pe, po);
+        const float se = unit_scale(rb, LO, false) * lds32f(xi32 + 32u * (uint32_t)k);
+        const float so = unit_scale(rb, LO, true) * lds32f(xi32 + 32u * (uint32_t)k + 4u);
+        const float d = fmaf(se, pe, so * po);
+        if (sl) y1 += d;
+        else y0 += d;
+      }
+      first = ((first - items) % kW + kW) % kW;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms_empty[rp.s]);
+      rp.stage32 += (uint32_t)P.stage_bytes;
+      if (++rp.s == P.nstages) {
+        rp.s = 0;
+        rp.ph ^= 1u;
+        rp.stage32 = smem32;
+      }
+      // the warp's partials of rows r0 + gq and r0 + 8 + gq (4 lanes per row)
+      y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+      y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+      y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+      y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+      if (cq == 0) {
+        const uint32_t a = part32 + buf + (uint32_t)(((wt * tile_rows + gq) * kW + warp) * 4);
+        sts32(a, y0);
+        if (T > 1) sts32(a + (uint32_t)(kSetRows * kW * 4), y1);
+      }
+      ++wt;
+      if (wt == F.win || r0 + tile_rows >= v1) {
+        // window complete: sum each row's warp partials (4 threads a row,
+        // 5 warps each, in a fixed order) and write the rows
+        consumer_sync(kCT);
+        const int nrow = min(wt * tile_rows, v1 - wbeg);
+        const float* pw = part + buf / 4;
+        for (int i0 = 0; i0 < nrow; i0 += kCT / 4) {
+          const int i = i0 + (threadIdx.x >> 2), sub = threadIdx.x & 3;
+          float sum = 0.f;
+          if (i < nrow) {
+            const float* pr = pw + (size_t)i * kW;
+#pragma unroll
+            for (int w = 0; w < kW / 4; ++w) sum += pr[sub + 4 * w];
+          }
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          if (i < nrow && sub == 0) ms_store_row(F, wbeg + i, sum, rbase, bv, bi);
+        }
+        buf = buf ? 0u : buf_bytes;
+        wt = 0;
+        wbeg = r0 + tile_rows;
+      }
+    }
+  }
+  if (F.argmax) ms_argmax_cta(P, bv, bi, s_f, s_i);
   return ok;
 }
 
@@ -915,6 +1157,52 @@ __device__ __noinline__ int produce_all(const MParams& P, uint8_t* smem) {
     const int nseg = __ldg(&F->nseg), R = __ldg(&F->R), rpc = __ldg(&F->rows_per_cta);
     const int total = __ldg(&F->total_rows), glu = __ldg(&F->glu);
     const long long rowb = __ldg(&F->row_bytes);
+    if (__ldg(&F->tc)) {
+      // tiles of T sets of 8 rows (fewer at the end of a range); a set is
+      // groups of consecutive rows, one bulk copy per group (per row where
+      // a group crosses into the next matrix); rows are 16-byte multiples
+      // at 16-byte aligned addresses (n % 256 == 0)
+      const uint32_t SR = (uint32_t)__ldg(&F->SR);
+      const int gsh = __ldg(&F->gsh), gsz = 1 << gsh, T = __ldg(&F->T);
+      const uint32_t gbytes = (uint32_t)(gsz * rowb) + 16u;
+      for (int piece = 0; piece < (glu ? 2 : 1); ++piece) {
+        int v0, v1;
+        piece_range(glu, __ldg(&F->vbegin[1]), rpc, total, piece, v0, v1);
+        int seg = 0;
+        while (seg + 1 < nseg && v0 >= __ldg(&F->vbegin[seg + 1])) ++seg;
+        int seg_beg = __ldg(&F->vbegin[seg]), seg_end = __ldg(&F->vbegin[seg + 1]);
+        const uint8_t* wseg = ldg_ptr(&F->w[seg]);
+        for (int r0 = v0; r0 < v1; r0 += 8 * T) {
+          if (issued >= P.nstages && !wait_or_abort(&empty[s], ph ^ 1u, s_abort)) return issued;
+          const int nrows = min(8 * T, v1 - r0);
+          uint8_t* dst = smem + (size_t)P.stage_bytes * s;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(nrows * rowb));
+          for (int a = 0; a < nrows; a += gsz) {
+            const int b = min(a + gsz, nrows);
+            uint8_t* gd = dst + (a >> 3) * SR + ((a & 7) >> gsh) * gbytes;
+            for (int r = a; r < b;) {
+              const int vr = r0 + r;
+              while (vr >= seg_end) {  // (the next matrix of the phase)
+                ++seg;
+                seg_beg = seg_end;
+                seg_end = __ldg(&F->vbegin[seg + 1]);
+                wseg = ldg_ptr(&F->w[seg]);
+              }
+              const int nr = min(b, r + (seg_end - vr)) - r;
+              bulk_g2s(gd + (r - a) * rowb, wseg + (long long)(vr - seg_beg) * rowb,
+                       (uint32_t)(nr * rowb), &full[s], pol);
+              r += nr;
+            }
+          }
+          ++issued;
+          if (++s == P.nstages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      continue;
+    }
     for (int piece = 0; piece < (glu ? 2 : 1); ++piece) {
     int v0, v1;
     piece_range(glu, __ldg(&F->vbegin[1]), rpc, total, piece, v0, v1);
@@ -1001,9 +1289,9 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
       if (kind == kPhMatvec) matvec_pre(s_ph, region);
       if (pi > 0 && !grid_wait(P)) break;
       if (kind == kPhMatvec) {
-        if (!matvec_phase(s_ph, P, rp, smem32, region, s_f, s_i)) {
-          ms_abort = 1;  // seen at the next grid barrier
-        }
+        const bool ok = s_ph.tc ? tc_matvec_phase(s_ph, P, rp, smem32, region, s_f, s_i)
+                                : matvec_phase(s_ph, P, rp, smem32, region, s_f, s_i);
+        if (!ok) ms_abort = 1;  // seen at the next grid barrier
       } else if (kind == kPhAttn) {
         const int L = ms_L;
         attn_phase<D, KT>(P, s_ph, L, L >= 1 && L <= P.cap, region);
@@ -1058,6 +1346,35 @@ int launch_typed(const MParams& P, int grid, cudaStream_t st) {
 
 }  // namespace
 
+int megastep_plan_tc(MPhase& F, int grid) {
+  F.bpr = F.n / kQBlock;
+  F.row_bytes = (long long)F.bpr * kQBlockBytes;
+  F.tc = 0;
+  if (F.n % 256 || F.bpr < 64 || F.bpr * 8 > kTcItems * kCT) return 0;
+  // A 272-byte pair column is 68 words, so row gq's words sit 4 * (m * gq
+  // mod 8) banks (m = bpr / 8) after row 0's: rows whose m * gq agree mod 8
+  // would share banks.  A set is therefore c = gcd(m, 8) groups of 8 / c
+  // consecutive rows (one copy each), every group 16 bytes (4 banks) after
+  // the previous group's end, which makes the 8 rows' word reads
+  // conflict-free.
+  const int m = F.bpr / 8;
+  const int c = (m & 1) ? 1 : (m & 3) ? 2 : (m & 7) ? 4 : 8;
+  F.gsh = c == 1 ? 3 : c == 2 ? 2 : c == 4 ? 1 : 0;
+  F.SR = (int)(8 * F.row_bytes + 16 * c);
+  // two sets a tile when three such stages fit the ring, else one
+  F.T = 3LL * ((2LL * F.SR + 127) / 128 * 128) <= megastep_ring_bytes() ? 2 : 1;
+  const long long tile = ((long long)F.T * F.SR + 127) / 128 * 128;
+  if (tile > megastep_ring_bytes() / 3) return 0;
+  const long long frag = (long long)F.bpr * (tc::kXfBlock + 4) + 128;
+  const long long per_tile = 2LL * F.T * tc::kSetRows * kW * 4;  // double-buffered partials
+  if (frag + per_tile > kMsRegion) return 0;
+  F.tc = 1;
+  F.win = (int)std::min<long long>(8, (kMsRegion - frag) / per_tile);
+  F.total_rows = F.vbegin[F.nseg];
+  F.rows_per_cta = F.glu ? (F.vbegin[1] + grid - 1) / grid : (F.total_rows + grid - 1) / grid;
+  return (int)tile;
+}
+
 bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
   F.bpr = F.n / kQBlock;
   F.row_bytes = (long long)F.bpr * kQBlockBytes;
@@ -1085,7 +1402,7 @@ bool megastep_plan_matvec(MPhase& F, int grid, int stage_target) {
 }
 
 // dynamic shared memory per CTA (one CTA per SM; the rest is static)
-constexpr int kMsDynamicBudget = 220 * 1024;
+constexpr int kMsDynamicBudget = 224 * 1024;
 
 int megastep_ring_bytes() { return kMsDynamicBudget - kMsRegion; }
 

@@ -22,7 +22,7 @@ enum MXMode { kXPlain = 0, kXRmsNorm = 1 };
 
 constexpr int kMsWarps = 20;                  // consumer warps per CTA
 constexpr int kMsThreads = (kMsWarps + 1) * 32;  // + the producer warp
-constexpr int kMsRegion = 48 * 1024;           // shared region: window partials / attention
+constexpr int kMsRegion = 44 * 1024;           // shared region: window partials / attention
 
 // One phase.  Matvec phases hold up to three matrices that share their
 // activations (rows concatenated: q|k|v, gate|up).
@@ -34,6 +34,11 @@ struct MPhase {
   int n, bpr, NS, RG, R, win, paired, xmode, accumulate, argmax;
   int glu;  // gate|up: each CTA owns the same rows of both matrices and
             // writes silu(gate) * up over the gate rows
+  int tc;   // block dot products on the tensor cores: tiles of T sets of 8
+            // whole rows, SR bytes apart; a set is 8 >> gsh groups of
+            // 1 << gsh consecutive rows, each group 16 bytes after the
+            // previous one's end; win = tiles per window
+  int SR, gsh, T;
   int total_rows, rows_per_cta;
   int vbegin[4];  // first virtual row of each matrix; vbegin[nseg] = total_rows
   long long row_bytes;
@@ -69,6 +74,12 @@ struct MParams {
   const unsigned* wait_limit; // polls a grid barrier wait makes before the step gives up
   int stage_bytes, nstages;
 };
+
+// Tensor-core plan of one matvec phase (host): sets F.tc, F.SR, F.win and
+// the row split when the phase suits the tensor-core path (n % 256 == 0,
+// at least 64 blocks a row, fragments within the shared region); returns
+// its tile bytes, or 0 (F.tc = 0) when it does not.
+int megastep_plan_tc(MPhase& F, int grid);
 
 // Rows per tile, window tiles and stage size of one matvec phase (host).
 // Returns false when the rows are too long for the kernel (more than 20

@@ -127,13 +127,16 @@ static int build_phases(q8d_step* S, std::vector<MPhase>& ph, int& stage_bytes) 
   MPhase AM{};
   AM.kind = kPhArgmax;
   ph.push_back(AM);
-  // Stages of ~40 KB: every matvec phase takes the largest tile that fits.
-  // (three stages fit the ring: tiles of up to a third of it)
-  const int kStageTarget = (megastep_ring_bytes() / 3) & ~127;
+  // Stage size: the largest tensor-core tile (8 row slots) when any phase
+  // takes the tensor cores, else about a third of the ring; every CUDA-core
+  // phase takes the largest tile of whole rows that fits it.
   stage_bytes = 0;
+  for (auto& F : ph)
+    if (F.kind == kPhMatvec) stage_bytes = std::max(stage_bytes, megastep_plan_tc(F, S->grid));
+  const int target = stage_bytes ? stage_bytes : (megastep_ring_bytes() / 3) & ~127;
   for (auto& F : ph) {
-    if (F.kind != kPhMatvec) continue;
-    if (!megastep_plan_matvec(F, S->grid, kStageTarget)) return Q8D_EUNSUPPORTED;
+    if (F.kind != kPhMatvec || F.tc) continue;
+    if (!megastep_plan_matvec(F, S->grid, target)) return Q8D_EUNSUPPORTED;
     const long long sb = ((F.R * F.row_bytes + 32 + 127) / 128) * 128;
     stage_bytes = (int)std::max<long long>(stage_bytes, sb);
   }

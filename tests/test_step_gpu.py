@@ -225,6 +225,16 @@ def test_step_odd_block_counts(orc, q8d):
     run_case(orc, shape, pos=300, cap=512)
 
 
+def test_step_tensor_core_phases_ragged_sets(orc, q8d):
+    # every matvec phase on the tensor-core path (n % 256 == 0, >= 64
+    # blocks a row: hidden 2048, ffn 2560): CTA row ranges of 17 (q|k|v,
+    # gate|up), 14 (o), 20 (lm_head of 3001 rows) rows, so tiles of 8 rows
+    # end in partial ones, and some straddle the q / k / v boundaries
+    shape = synth.ModelShape("tc-ragged", 2048, 2, 16, 2, 128, 2560, 3001,
+                             qk_norm=False, qkv_bias=True, kv_dtype=synth.KV_F16)
+    run_case(orc, shape, pos=700, cap=1024)
+
+
 def test_step_position_past_cache_flags_error(orc, q8d):
     shape = synth.tiny_shape(1)
     w = synth.step_weights(shape, seed=1)
