@@ -10,13 +10,14 @@
 // (half of them on the half-rate ALU pipe), which holds the matvec near 50 %
 // issue and 0.5 of HBM.  Here a quant pair costs one PRMT and one sub.f16x2,
 // and the products go to the tensor pipe (the operand layout is in
-// q8d_mma_frag.cuh).  This kernel scales the whole vector by one power of
-// two (max|x| into [2^14, 2^15)) before the f16 hi/lo split, and builds the
-// x fragments once per launch in shared memory.
+// q8d_mma_frag.cuh).  The x fragments (each block with its own power-of-two
+// scale) are built once per launch in shared memory, in one pass over x.
 //  * Weights stream in through a ring of shared-memory stages filled with
-//    1-D bulk copies (TMA) by one producer warp: a tile is 8 rows x up to
-//    ~150 blocks (long rows are cut into slices), one copy per row into a
-//    row slot padded so that the lanes' word reads hit distinct banks.
+//    1-D bulk copies (TMA) by one producer warp: a tile is 8 or 16 rows of
+//    up to 136 blocks.  Whole rows come as bank-spread groups of
+//    consecutive rows (one copy per group); rows longer than that are cut
+//    into slices, one copy per row into a row slot padded so that the
+//    lanes' word reads hit distinct banks.
 //  * 4 lanes share a row; the warps' row partials are summed in a fixed
 //    order (deterministic).
 #include <algorithm>
@@ -44,7 +45,10 @@ struct MvParams {
   int row_bytes;     // bpr * 34, a multiple of 272
   int rows_per_cta;  // a multiple of 8
   int S, nslices;    // blocks per slice (a multiple of 8), slices per row
-  int SR;            // shared-memory row slot (bytes, multiple of 16)
+  int SR;            // shared-memory row stride (bytes, multiple of 16)
+  int gsh;           // a set is groups of 1 << gsh rows, 16 bytes apart (whole
+                     // rows: one copy per group; sliced rows: gsh = 3, a copy a row)
+  int set_bytes;     // an 8-row set: 8 * SR + 16 * (8 >> gsh)
   int stage_bytes, nstages;
   int W;             // consumer warps
   int T;             // 8-row sets per tile (1 or 2)
@@ -66,9 +70,11 @@ __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint
       const uint32_t bytes = (uint32_t)nb * kQBlockBytes;
       uint8_t* dst = smem + (size_t)P.stage_bytes * s;
       mbar_arrive_expect_tx(&full[s], bytes * nrows);
-      for (int r = 0; r < nrows; ++r)
-        bulk_g2s(dst + r * P.SR, P.w + (long long)(r0 + r) * P.row_bytes + (long long)c0 * kQBlockBytes,
-                 bytes, &full[s], pol);
+      const int gsz = P.nslices == 1 ? 1 << P.gsh : 1;  // rows a copy
+      for (int r = 0; r < nrows; r += gsz)
+        bulk_g2s(dst + (r >> 3) * P.set_bytes + (r & 7) * P.SR + ((r & 7) >> P.gsh) * 16,
+                 P.w + (long long)(r0 + r) * P.row_bytes + (long long)c0 * kQBlockBytes,
+                 bytes * (uint32_t)min(gsz, nrows - r), &full[s], pol);
       ++issued;
       if (++s == P.nstages) {
         s = 0;
@@ -82,15 +88,14 @@ __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint
 __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
-  __shared__ float s_red[kMvMaxWarps];
-  __shared__ int s_exp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = P.W;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
   uint64_t* empty = full + P.nstages;
   uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);
   uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // 128 zero bytes
-  float* part = reinterpret_cast<float*>(zpad + 128);            // [2][kWinSets*8][W]
+  float* xinv = reinterpret_cast<float*>(zpad + 128);            // [bpr] inverse block scales
+  float* part = xinv + P.bpr;                                    // [2][kWinSets*8][W]
   const int v0 = blockIdx.x * P.rows_per_cta;
   const int v1 = min(P.p, v0 + P.rows_per_cta);
   if (threadIdx.x == 0) {
@@ -109,35 +114,26 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
     if (lane == 0) issued = mv_produce(P, smem, full, empty, &s_abort, v0, v1);
   } else {
     const int nct = W * 32;
-    // ---- the vector's power-of-two scale: max|x| * 2^e in [2^14, 2^15) ----
-    float mx = 0.f;
-    const float4* x4 = reinterpret_cast<const float4*>(P.x);
-    for (int i = threadIdx.x; i < P.n / 4; i += nct) {
-      const float4 v = __ldg(x4 + i);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
+    // ---- x fragments, one pass: four (block, word) items a thread per
+    // round, all loads issued before the first use ----
+    const int nit = P.bpr * 8;
+    for (int it0 = 0; it0 < nit; it0 += 4 * nct) {
+      float v[4][4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_red[warp] = mx;
-    consumer_sync(nct);
-    if (threadIdx.x == 0) {
-      float m = 0.f;
-      for (int w = 0; w < W; ++w) m = fmaxf(m, s_red[w]);
-      int ex = 0;
-      if (m > 0.f) frexpf(m, &ex);
-      s_exp = m > 0.f ? 15 - ex : 0;
-    }
-    consumer_sync(nct);
-    const int e = s_exp;
-    // ---- x fragments: block bb, word w, hi / lo: the 4 values of the
-    // word's bytes, hi = f16(x 2^e), lo = f16(x 2^e - hi) ----
-    for (int it = threadIdx.x; it < P.bpr * 8; it += nct) {
-      const int bb = it >> 3, w = it & 7;
-      const bool even = (bb & 1) == 0;
-      float v[4];
+      for (int k = 0; k < 4; ++k) {
+        const int it = it0 + k * nct + threadIdx.x;
+        if (it < nit) {
+          load_word<1>(P.x, it >> 3, it & 7, v[k]);
+        } else {
+          v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.f;
+        }
+      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = ldexpf(__ldg(P.x + bb * kQBlock + word_quant(even, w, k)), e);
-      store_x_word(xf + (size_t)bb * kXfBlock + w * 16, v);
+      for (int k = 0; k < 4; ++k) {
+        const int it = it0 + k * nct + threadIdx.x;
+        if (it0 + k * nct >= nit) break;  // (uniform over the warps)
+        build_x_word(it, it < nit, v[k], xf, xinv);
+      }
     }
     if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
     consumer_sync(nct);
@@ -151,14 +147,15 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
     const bool bmatch = bjb == (cq & 1);
     const uint32_t xlane = bmatch ? (uint32_t)((2 * bh + 4 * bjb) * kXfBlock + bhl * 8 + (cq >> 1) * 16) : 0u;
     const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
+    const uint32_t xi32 = smem_u32(xinv) + 4u * (uint32_t)lane_block(cq);
     const uint32_t xstep = bmatch ? (uint32_t)kXfBlock : 0u;
     const uint32_t smem32 = smem_u32(smem);
     const bool lo_half = cq < 2;
-    const float inv = ldexpf(1.f, -e);
     const int S = P.S, bpr = P.bpr, nslices = P.nslices, nst = P.nstages;
-    const uint32_t stage_b = (uint32_t)P.stage_bytes, rowoff = (uint32_t)(gq * P.SR);
+    const uint32_t stage_b = (uint32_t)P.stage_bytes;
+    const uint32_t rowoff = (uint32_t)(gq * P.SR + ((gq >> P.gsh) << 4));
     const int T = P.T;
-    const uint32_t set_b = (uint32_t)(kSetRows * P.SR);  // bytes between the row sets of a tile
+    const uint32_t set_b = (uint32_t)P.set_bytes;  // bytes between the row sets of a tile
     int s = 0;
     uint32_t ph = 0;
     int set = 0, buf = 0;
@@ -171,9 +168,10 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
         const int pairs = min(S, bpr - c0) / 8;
         for (int k = warp; k < pairs; k += W) {
           const uint32_t xb = bmatch ? xf32 + (uint32_t)(c0 + 8 * k) * kXfBlock + xlane : z32;
+          const uint32_t xi = xi32 + 4u * (uint32_t)(c0 + 8 * k);
           const uint32_t rb = row32 + 272u * (uint32_t)k;
-          yacc[0] += pair_dot(rb, xb, xstep, LO, lo_half);
-          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, xstep, LO, lo_half);
+          yacc[0] += pair_dot(rb, xb, xstep, LO, lo_half, xi);
+          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, xstep, LO, lo_half, xi);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -202,7 +200,7 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
               const float* pr = part + ((size_t)buf * kWinSets * kSetRows + i) * W;
               float sum = 0.f;
               for (int w = 0; w < W; ++w) sum += pr[w];
-              P.y[row] = sum * inv;
+              P.y[row] = sum;
             }
           }
           buf ^= 1;
@@ -245,11 +243,19 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   P.nslices = (P.bpr + max_blocks - 1) / max_blocks;
   P.S = ((P.bpr + P.nslices - 1) / P.nslices + 7) / 8 * 8;
   P.nslices = (P.bpr + P.S - 1) / P.S;
-  // row slot: >= the slice, 16-byte multiple, 4 banks apart row to row
-  int SR = (P.S * kQBlockBytes + 15) / 16 * 16;
-  while ((SR / 4) % 32 != 4) SR += 16;
-  P.SR = SR;
-  P.stage_bytes = kSetRows * SR;
+  if (P.nslices == 1) {
+    // whole rows: bank-spread groups of consecutive rows, one copy each
+    P.SR = P.row_bytes;
+    P.gsh = row_group_shift(P.bpr / 8);
+  } else {
+    // row slot: >= the slice, 16-byte multiple, 4 banks apart row to row
+    int SR = (P.S * kQBlockBytes + 15) / 16 * 16;
+    while ((SR / 4) % 32 != 4) SR += 16;
+    P.SR = SR;
+    P.gsh = 3;  // (one group: no offsets; the slots spread the banks)
+  }
+  P.set_bytes = kSetRows * P.SR + 16 * (8 >> P.gsh);
+  P.stage_bytes = P.set_bytes;
   // consumer warps: the count in [8, 16] that splits a slice's unit pairs
   // (8 blocks of 8 rows) most evenly
   const int U = P.S / 8;
@@ -263,7 +269,8 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
     }
   }
   P.W = bestW;
-  const long long fixed = (long long)P.bpr * kXfBlock + 128 + 2LL * kWinSets * kSetRows * P.W * 4;
+  const long long fixed =
+      (long long)P.bpr * (kXfBlock + 4) + 128 + 2LL * kWinSets * kSetRows * P.W * 4;
   const long long budget = 220 * 1024;
   // two row sets per tile (each warp's per-tile work twice as long) when
   // three such stages fit

@@ -64,7 +64,7 @@ __shared__ int ms_L;                       // attended length of this step
 // gate|up phase (kept for the up rows): no global round trip in the window
 // reductions.
 constexpr int kRowsMax = 512;
-__shared__ float ms_rows[kRowsMax];
+__shared__ __align__(16) float ms_rows[kRowsMax];
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
@@ -72,6 +72,15 @@ __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 template <typename T>
 __device__ __forceinline__ T* ldg_ptr(T* const* p) {
   return reinterpret_cast<T*>(__ldg(reinterpret_cast<const unsigned long long*>(p)));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -128,6 +137,7 @@ __device__ bool grid_wait(const MParams& P) {
     if (!ok) *s_abort = 1;
     *s_flag = ok;
   }
+  cp_async_wait_all();  // this thread's staging copies of the next phase
   consumer_sync(kCT);
   return *s_flag != 0;
 }
@@ -141,19 +151,26 @@ __device__ __forceinline__ bool tc_weights_staged(const MPhase& F) {
 // halves of the grid barrier before it: the residual rows this CTA adds to
 // (written by this CTA, or before an earlier barrier) and the RMSNorm
 // weights staged where the activation pass reads them.
+// The copies are asynchronous (cp.async through L2, completed by grid_wait),
+// so their latency overlaps the barrier.  Thread 0 polls the barrier and
+// issues none.  The residual rows are copied in 16-byte units from the
+// 16-byte boundary at or below the CTA's first row (ms_rows_off floats
+// before it; the extra values are never used).
 __device__ void matvec_pre(const MPhase& F, uint8_t* region) {
-  if (F.accumulate && F.rows_per_cta <= kRowsMax) {
+  const int t = threadIdx.x - 32;  // (warps 1 .. kW-1)
+  if (F.accumulate && F.rows_per_cta + 3 <= kRowsMax) {
     const int r0 = blockIdx.x * F.rows_per_cta;
     const int r1 = min(F.total_rows, r0 + F.rows_per_cta);
-    for (int i = threadIdx.x; i < r1 - r0; i += kCT) ms_rows[i] = __ldcg(F.y[0] + r0 + i);
+    const int a0 = r0 & ~3, n4 = (r1 - a0 + 3) / 4;  // (the rows end 16-byte aligned)
+    for (int i = t; i >= 0 && i < n4; i += kCT - 32) cp_async16(ms_rows + 4 * i, F.y[0] + a0 + 4 * i);
   }
   if (F.tc) {
     // tensor-core phase: the RMSNorm weights at the end of the region
     // (clear of the fragments the activation pass writes)
     if (F.xmode == kXRmsNorm && tc_weights_staged(F)) {
       float4* ws = reinterpret_cast<float4*>(region + kMsRegion) - F.n / 4;
-      for (int i = threadIdx.x; i < F.n / 4; i += kCT)
-        ws[i] = __ldg(reinterpret_cast<const float4*>(F.xw) + i);
+      for (int i = t; i >= 0 && i < F.n / 4; i += kCT - 32)
+        cp_async16(ws + i, reinterpret_cast<const float4*>(F.xw) + i);
     }
     return;
   }
@@ -162,13 +179,22 @@ __device__ void matvec_pre(const MPhase& F, uint8_t* region) {
     float4* ws = reinterpret_cast<float4*>(region) + pass4;
     const int n4 = F.n / 4;
     const int rot = (int)((blockIdx.x * 97u) % (unsigned)n4);
-    for (int i = threadIdx.x; i < n4; i += kCT) {
+    for (int i = t; i >= 0 && i < n4; i += kCT - 32) {
       int j = i + rot;
       if (j >= n4) j -= n4;
       const int ph = (j & ~7) | (((j & 7) + (j >> 4)) & 7);
-      ws[ph] = __ldg(reinterpret_cast<const float4*>(F.xw) + j);
+      cp_async16(ws + ph, reinterpret_cast<const float4*>(F.xw) + j);
     }
   }
+}
+
+// The matrix row held in ms_rows[0] for phase F (the 16-byte boundary at or
+// below the CTA's first row), or -1 when ms_rows is not used (no residual
+// or gate rows, or too many rows: values then go through L2).
+__device__ __forceinline__ int ms_rbase(const MPhase& F) {
+  return (F.accumulate || F.glu) && F.rows_per_cta + 3 <= kRowsMax
+             ? (int)(blockIdx.x * F.rows_per_cta) & ~3
+             : -1;
 }
 
 // ---------------------------------------------------------------- matvec
@@ -220,8 +246,7 @@ __device__ __forceinline__ void piece_range(int glu, int nrows0, int rpc, int to
 
 // Writes the dot product `sum` of virtual row vr of phase F: adds the
 // residual, forms SiLU(gate) * up, tracks the argmax.
-// rbase: the matrix row held in ms_rows[0] (the CTA's first row), or -1
-// when the CTA's rows do not fit ms_rows (then values go through L2).
+// rbase: ms_rbase(F).
 __device__ __forceinline__ void ms_store_row(const MPhase& F, int vr, float sum, int rbase,
                                              float& bv, int& bi) {
   int sg = 0;
@@ -480,9 +505,7 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
       part32 + ((uint32_t)(ci * kPW + (lane & (kPW - 1))) + (uint32_t)rg * nP) * 4u;
   const uint32_t buf_bytes = (uint32_t)F.win * (uint32_t)F.R * nP * 4u;
   uint32_t buf = 0;
-  const int rbase = (F.accumulate || F.glu) && F.rows_per_cta <= kRowsMax
-                        ? (int)blockIdx.x * F.rows_per_cta
-                        : -1;
+  const int rbase = ms_rbase(F);
   const int npieces = F.glu ? 2 : 1;
   for (int piece = 0; piece < npieces; ++piece) {
     int v0, v1;
@@ -530,27 +553,6 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
 // Region layout: x fragments [bpr][144], a 128-byte zero pad, the blocks'
 // inverse scales [bpr] (f32), then the double-buffered window partials
 // [2][win * 8][kW].
-
-// The 4 values of word w of block bb (in word_quant order) from v + 32 bb.
-// kMode 0: L2 loads (activations other CTAs wrote), 1: read-only global
-// loads, 2: shared memory.
-template <int kMode>
-__device__ __forceinline__ void load_word(const float* v, int bb, int w, float (&o)[4]) {
-  const float* b = v + (size_t)bb * kQBlock;
-  auto ld2 = [](const float* p) {
-    const float2* q = reinterpret_cast<const float2*>(p);
-    return kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
-  };
-  if (bb & 1) {
-    const float4* q = reinterpret_cast<const float4*>(b + 4 * w);
-    const float4 a = kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
-    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
-  } else {
-    const float2 a = ld2(b + (w < 7 ? 4 * w + 2 : 0));
-    const float2 c = ld2(b + (w < 7 ? 4 * w + 4 : 30));
-    o[0] = a.x; o[1] = a.y; o[2] = c.x; o[3] = c.y;
-  }
-}
 
 constexpr int kTcItems = 4;  // (block, word) items per consumer thread: bpr <= 320
 
@@ -609,24 +611,7 @@ __device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, 
   for (int k = 0; k < kTcItems; ++k) {
     const int it = threadIdx.x + k * kCT;
     if (k * kCT >= nit) break;  // (uniform over the CTA)
-    // the block's max |x| over its 8 words (8 consecutive lanes)
-    float m = fmaxf(fmaxf(fabsf(v[k][0]), fabsf(v[k][1])), fmaxf(fabsf(v[k][2]), fabsf(v[k][3])));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-    int ex = 0;
-    if (m > 0.f) frexpf(m, &ex);
-    // m * 2^e in [2^14, 2^15) (e >= -113 for any finite m; e <= 125 keeps
-    // 2^e and 2^-e normal floats, blocks below 2^-110 scale to less)
-    const int e = m > 0.f ? min(125, 15 - ex) : 0;
-    if (it < nit) {
-      const float sc = __int_as_float((127 + e) << 23);
-      float t[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) t[j] = v[k][j] * sc;
-      store_x_word(xf + (size_t)(it >> 3) * kXfBlock + (it & 7) * 16, t);
-      if ((it & 7) == 0) xinv[it >> 3] = __int_as_float((127 - e) << 23);
-    }
+    build_x_word(it, it < nit, v[k], xf, xinv);
   }
   if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
   consumer_sync(kCT);
@@ -651,9 +636,7 @@ __device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, 
   const uint32_t part32 = smem_u32(part);
   const int tile_rows = kSetRows * T;
   const uint32_t buf_bytes = (uint32_t)(F.win * tile_rows * kW) * 4u;
-  const int rbase = (F.accumulate || F.glu) && F.rows_per_cta <= kRowsMax
-                        ? (int)blockIdx.x * F.rows_per_cta
-                        : -1;
+  const int rbase = ms_rbase(F);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   bool ok = true;
@@ -779,10 +762,6 @@ __device__ __forceinline__ void ld_row_part(const KT* p, float (&f)[DPL]) {
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
 
 // Context chunks per KV head for attended length L: P.nc (every CTA takes a
 // chunk) unless that leaves chunks of fewer than 16 rows; producer, attention
@@ -1010,66 +989,60 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
 // warp order (deterministic).
 template <int D>
 __device__ void combine_phase(const MParams& P, int L, bool len_ok, uint8_t* region) {
-  constexpr int DPL = D / 32;
+  // Every CTA merges a contiguous slice of the H * D outputs: a group of LW
+  // lanes per output element (two elements a warp for up to 80 chunks),
+  // lanes over the context chunks (loaded together, then max / sums by
+  // shuffles in a fixed order), so the merge is one round of L2 loads
+  // wherever it runs.
+  (void)region;
   const int H = P.n_heads, Hk = P.n_kv_heads, G = H / Hk;
   const int nc = attn_chunks_for(P, L);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* red = reinterpret_cast<float*>(region);  // [kW][D + 4]
-  for (int hq = blockIdx.x; hq < H; hq += gridDim.x) {
-    float* outp = P.attn + (size_t)hq * D;
+  const int LW = nc > 80 ? 32 : 16, per_warp = 32 / LW;
+  const int grp = lane / LW, gl = lane % LW;
+  const int total = H * D, per = (total + gridDim.x - 1) / gridDim.x;
+  const int e0 = blockIdx.x * per, e1 = min(total, e0 + per);
+  for (int eb = e0 + warp * per_warp; eb < e1; eb += kW * per_warp) {
+    const int e = eb + grp;  // (warp-uniform loop: every lane reaches the shuffles)
+    const bool live = e < e1;
     if (!len_ok) {
-      for (int e = threadIdx.x; e < D; e += kCT) outp[e] = __int_as_float(0x7fc00000);
+      if (live && gl == 0) P.attn[e] = __int_as_float(0x7fc00000);
       continue;
     }
+    const int hq = live ? e / D : 0, d = live ? e % D : 0;
     const int g = hq / G, h = hq % G;
-    float m = -INFINITY, l = 0.f, o[DPL];
+    // chunks c = gl + LW j of KV head g: (m, l, O[d]) of query head h
+    constexpr int kJ = 5;  // nc <= 5 * LW (at most 160: one chunk per CTA)
+    float m[kJ], l[kJ], o[kJ];
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-    // at most two chunks per warp for nc <= 40: load both, then merge
-    for (int c0 = warp; c0 < nc; c0 += 2 * kW) {
-      const int c1 = c0 + kW;
-      const size_t i0 = ((size_t)g * nc + c0) * G + h;
-      const size_t i1 = ((size_t)g * nc + min(c1, nc - 1)) * G + h;
-      const float m0 = ldcg(P.ws_m + i0), l0 = ldcg(P.ws_l + i0);
-      const float m1 = c1 < nc ? ldcg(P.ws_m + i1) : -INFINITY;
-      const float l1 = ldcg(P.ws_l + i1);
-      float a0[DPL], a1[DPL];  // through L2: the partials are rewritten every layer
-#pragma unroll
-      for (int j = 0; j < DPL; ++j) {
-        a0[j] = ldcg(P.ws_o + i0 * D + lane * DPL + j);
-        a1[j] = ldcg(P.ws_o + i1 * D + lane * DPL + j);
+    for (int j = 0; j < kJ; ++j) {
+      const int c = gl + LW * j;
+      m[j] = -INFINITY;
+      l[j] = o[j] = 0.f;
+      if (live && c < nc) {
+        const size_t i = ((size_t)g * nc + c) * G + h;
+        m[j] = ldcg(P.ws_m + i);
+        l[j] = ldcg(P.ws_l + i);
+        o[j] = ldcg(P.ws_o + i * D + d);
       }
-      const float mn = fmaxf(m, fmaxf(m0, m1));
-      const float s = exp2f(m - mn), w0 = exp2f(m0 - mn), w1 = c1 < nc ? exp2f(m1 - mn) : 0.f;
-      l = l * s + l0 * w0 + l1 * w1;
+    }
+    float M = m[0];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) o[j] = o[j] * s + a0[j] * w0 + (c1 < nc ? a1[j] * w1 : 0.f);
-      m = mn;
-    }
-    float* rw = red + warp * (D + 4);
-    if (lane == 0) {
-      rw[0] = m;
-      rw[1] = l;
-    }
+    for (int j = 1; j < kJ; ++j) M = fmaxf(M, m[j]);
+    for (int off = LW / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float ls = 0.f, acc = 0.f;
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) rw[4 + lane * DPL + j] = o[j];
-    consumer_sync(kCT);
-    for (int d = threadIdx.x; d < D; d += kCT) {
-      float M = -INFINITY;
-#pragma unroll 1
-      for (int w = 0; w < kW; ++w) M = fmaxf(M, red[w * (D + 4)]);
-      float lsum = 0.f, acc = 0.f;
-#pragma unroll 1
-      for (int w = 0; w < kW; ++w) {
-        const float mw = red[w * (D + 4)];
-        if (mw == -INFINITY) continue;
-        const float wt = exp2f(mw - M);
-        lsum = fmaf(red[w * (D + 4) + 1], wt, lsum);
-        acc = fmaf(red[w * (D + 4) + 4 + d], wt, acc);
-      }
-      outp[d] = acc / lsum;
+    for (int j = 0; j < kJ; ++j) {
+      // (empty chunks: m = -inf, l = 0, O = 0 weigh nothing)
+      const float w = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
+      ls = fmaf(l[j], w, ls);
+      acc = fmaf(o[j], w, acc);
     }
-    consumer_sync(kCT);
+    for (int off = LW / 2; off > 0; off >>= 1) {
+      ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    }
+    if (live && gl == 0) P.attn[e] = acc / ls;
   }
 }
 
@@ -1250,7 +1223,7 @@ __device__ __noinline__ int produce_all(const MParams& P, uint8_t* smem) {
 template <int D, typename KT>
 __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(16) MPhase s_ph;
+  __shared__ __align__(16) MPhase s_ph2[2];  // this phase's record and the next one's
   __shared__ float s_f[kW];
   __shared__ int s_i[kW];
   uint8_t* region = smem + (size_t)P.stage_bytes * P.nstages;  // 128-byte aligned
@@ -1279,12 +1252,20 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
     consumer_sync(kCT);
     RingPos rp{0, 0u, smem_u32(smem)};
     const uint32_t smem32 = smem_u32(smem);
+    // phase records come in by cp.async a phase ahead (16 bytes a thread)
+    constexpr int kRecChunks = (int)(sizeof(MPhase) / 16);
+    static_assert(sizeof(MPhase) % 16 == 0, "phase records are whole 16-byte chunks");
+    if (threadIdx.x < kRecChunks)
+      cp_async16(reinterpret_cast<uint8_t*>(&s_ph2[0]) + 16 * threadIdx.x,
+                 reinterpret_cast<const uint8_t*>(P.phases) + 16 * threadIdx.x);
     for (int pi = 0; pi < P.nphases; ++pi) {
       if (pi > 0) grid_arrive(P);
-      if (threadIdx.x < (int)(sizeof(MPhase) / 4))
-        reinterpret_cast<int*>(&s_ph)[threadIdx.x] =
-            __ldg(reinterpret_cast<const int*>(P.phases + pi) + threadIdx.x);
+      if (threadIdx.x < kRecChunks) cp_async_wait_all();
       consumer_sync(kCT);
+      MPhase& s_ph = s_ph2[pi & 1];
+      if (pi + 1 < P.nphases && threadIdx.x < kRecChunks)
+        cp_async16(reinterpret_cast<uint8_t*>(&s_ph2[(pi + 1) & 1]) + 16 * threadIdx.x,
+                   reinterpret_cast<const uint8_t*>(P.phases + pi + 1) + 16 * threadIdx.x);
       const int kind = s_ph.kind;
       if (kind == kPhMatvec) matvec_pre(s_ph, region);
       if (pi > 0 && !grid_wait(P)) break;
@@ -1351,16 +1332,9 @@ int megastep_plan_tc(MPhase& F, int grid) {
   F.row_bytes = (long long)F.bpr * kQBlockBytes;
   F.tc = 0;
   if (F.n % 256 || F.bpr < 64 || F.bpr * 8 > kTcItems * kCT) return 0;
-  // A 272-byte pair column is 68 words, so row gq's words sit 4 * (m * gq
-  // mod 8) banks (m = bpr / 8) after row 0's: rows whose m * gq agree mod 8
-  // would share banks.  A set is therefore c = gcd(m, 8) groups of 8 / c
-  // consecutive rows (one copy each), every group 16 bytes (4 banks) after
-  // the previous group's end, which makes the 8 rows' word reads
-  // conflict-free.
-  const int m = F.bpr / 8;
-  const int c = (m & 1) ? 1 : (m & 3) ? 2 : (m & 7) ? 4 : 8;
-  F.gsh = c == 1 ? 3 : c == 2 ? 2 : c == 4 ? 1 : 0;
-  F.SR = (int)(8 * F.row_bytes + 16 * c);
+  // sets of bank-spread row groups (tc::row_group_shift)
+  F.gsh = tc::row_group_shift(F.bpr / 8);
+  F.SR = (int)(8 * F.row_bytes + 16 * (8 >> F.gsh));
   // two sets a tile when three such stages fit the ring, else one
   F.T = 3LL * ((2LL * F.SR + 127) / 128 * 128) <= megastep_ring_bytes() ? 2 : 1;
   const long long tile = ((long long)F.T * F.SR + 127) / 128 * 128;

@@ -26,7 +26,7 @@ constexpr int kMsRegion = 44 * 1024;           // shared region: window partials
 
 // One phase.  Matvec phases hold up to three matrices that share their
 // activations (rows concatenated: q|k|v, gate|up).
-struct MPhase {
+struct alignas(16) MPhase {  // (whole 16-byte chunks: copied by cp.async)
   int kind;
   int layer;
   // matvec

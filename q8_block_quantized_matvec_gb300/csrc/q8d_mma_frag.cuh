@@ -15,9 +15,10 @@
 //    blocks.  Each thread feeds one 32-bit word of quants per MMA (its
 //    contraction indices are permuted to match: 4 consecutive bytes).
 //  * B (16 x 8): the 8 columns are 4 blocks x (x_hi, x_lo), x = hi + lo in
-//    f16 after a power-of-two scale (max |x| of the scaled range in
-//    [2^14, 2^15)), so every product is exact in f32; columns that pair a
-//    row half with the other half's blocks are zero.  A block's fragment is
+//    f16 after the block's own power-of-two scale (its max |x| into
+//    [2^14, 2^15); the inverse scale is applied with the weight scale), so
+//    every product is exact in f32; columns that pair a row half with the
+//    other half's blocks are zero.  A block's fragment is
 //    144 bytes: 8 words x 16 bytes {hi(k0,k1), hi(k2,k3), lo(k0,k1),
 //    lo(k2,k3)} in the permuted byte order (word_quant), + 16 pad bytes.
 //  * D: every thread ends a unit with the (hi, lo) partials of one (row,
@@ -99,6 +100,59 @@ __device__ __forceinline__ void store_x_word(uint8_t* dst, const float (&v)[4]) 
   *reinterpret_cast<uint4*>(dst) = q;
 }
 
+// The 4 values of word w of block bb (in word_quant order) from v + 32 bb.
+// kMode 0: L2 loads (values other CTAs wrote in this kernel), 1: read-only
+// global loads, 2: shared memory.
+template <int kMode>
+__device__ __forceinline__ void load_word(const float* v, int bb, int w, float (&o)[4]) {
+  const float* b = v + (size_t)bb * kQBlock;
+  auto ld2 = [](const float* p) {
+    const float2* q = reinterpret_cast<const float2*>(p);
+    return kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
+  };
+  if (bb & 1) {
+    const float4* q = reinterpret_cast<const float4*>(b + 4 * w);
+    const float4 a = kMode == 0 ? __ldcg(q) : kMode == 1 ? __ldg(q) : *q;
+    o[0] = a.x;
+    o[1] = a.y;
+    o[2] = a.z;
+    o[3] = a.w;
+  } else {
+    const float2 a = ld2(b + (w < 7 ? 4 * w + 2 : 0));
+    const float2 c = ld2(b + (w < 7 ? 4 * w + 4 : 30));
+    o[0] = a.x;
+    o[1] = a.y;
+    o[2] = c.x;
+    o[3] = c.y;
+  }
+}
+
+// Fragment of (block, word) item `it` (block it >> 3, word it & 7) of the
+// values v, with the block's own power-of-two scale: the 8 lanes it & ~7 ..
+// it | 7 (consecutive lanes of one warp, all calling) share the block's
+// max |x| m, and m * 2^e lies in [2^14, 2^15) (e >= -113 for any finite
+// m; e <= 125 keeps 2^e and 2^-e normal floats, so blocks below 2^-110
+// scale to less).  The word goes to xf + block * 144 + word * 16; the
+// block's inverse scale 2^-e to xinv[block].  live: the item exists.
+__device__ __forceinline__ void build_x_word(int it, bool live, const float (&v)[4], uint8_t* xf,
+                                             float* xinv) {
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+  int ex = 0;
+  if (m > 0.f) frexpf(m, &ex);
+  const int e = m > 0.f ? min(125, 15 - ex) : 0;
+  if (live) {
+    const float sc = __int_as_float((127 + e) << 23);
+    float t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) t[j] = v[j] * sc;
+    store_x_word(xf + (size_t)(it >> 3) * kXfBlock + (it & 7) * 16, t);
+    if ((it & 7) == 0) xinv[it >> 3] = __int_as_float((127 - e) << 23);
+  }
+}
+
 // Per-lane constants of the unit loop (byte offsets within a pair of units:
 // 8 consecutive blocks 8k .. 8k+7 of a tile row; the even unit is blocks
 // 8k + {0, 2, 4, 6}, the odd unit 8k + {1, 3, 5, 7}; half 0 of a unit is
@@ -172,13 +226,26 @@ __device__ __forceinline__ float unit_scale(uint32_t rb, const LaneOffs& L, bool
   return __half2float(__ushort_as_half((unsigned short)lds16a(rb + L.s_even + (odd ? 34u : 0u))));
 }
 
-// pair_units scaled by the blocks' f16 scales and summed (one power-of-two
-// scale for the whole vector, undone by the caller).
+// pair_units scaled by the blocks' f16 weight scales and the x blocks'
+// inverse scales (xi: this lane's even-unit block's entry of xinv; the odd
+// unit's is the next) and summed.
 __device__ __forceinline__ float pair_dot(uint32_t rb, uint32_t xb, uint32_t xstep, const LaneOffs& L,
-                                          bool lo_half) {
+                                          bool lo_half, uint32_t xi) {
   float pe, po;
   pair_units(rb, xb, xstep, L, lo_half, pe, po);
-  return fmaf(unit_scale(rb, L, false), pe, unit_scale(rb, L, true) * po);
+  const float se = unit_scale(rb, L, false) * lds32f(xi);
+  const float so = unit_scale(rb, L, true) * lds32f(xi + 4u);
+  return fmaf(se, pe, so * po);
+}
+
+// Bank-spread row groups of an 8-row set (rows of a whole number of 8-block
+// pairs, m = pairs a row): a 272-byte pair column is 68 words, so row gq's
+// words sit 4 * (m * gq mod 8) banks after row 0's, and rows whose m * gq
+// agree mod 8 would share banks.  A set is therefore gcd(m, 8) groups of
+// 8 / gcd(m, 8) consecutive rows (one copy each), every group 16 bytes
+// (4 banks) after the previous group's end; returns log2 of the group size.
+__host__ __device__ __forceinline__ int row_group_shift(int m) {
+  return (m & 1) ? 3 : (m & 3) ? 2 : (m & 7) ? 1 : 0;
 }
 
 }  // namespace tc

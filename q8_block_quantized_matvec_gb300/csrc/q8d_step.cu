@@ -162,6 +162,10 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   const int G = d.n_heads / d.n_kv_heads;
   S->grid = sm_count();
   const int nc = std::max(1, S->grid / d.n_kv_heads);  // attention chunks per KV head
+  if (nc > 160) {  // (the combine's lanes hold at most 5 chunks each)
+    delete S;
+    return Q8D_EUNSUPPORTED;
+  }
 
   // carve one allocation (256-byte aligned pieces)
   size_t off = 0;
