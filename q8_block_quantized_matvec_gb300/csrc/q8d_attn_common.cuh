@@ -5,6 +5,33 @@
 
 namespace q8d {
 
+// v = hi + lo with hi = f16(v), lo = f16(v - hi), for a pair of floats.
+__device__ __forceinline__ void attn_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// d += a * b on the tensor cores: m16n8k16, f16 operands, f32 accumulators.
+__device__ __forceinline__ void attn_mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four transposed 8x8 b16 tiles from shared memory (the B operand of P.V).
+__device__ __forceinline__ void attn_ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                   uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // Decode-step prologue of one head row held by a warp (lane holds elements
 // lane + 32t): bias add, per-head RMSNorm, rotary embedding of the pairs
 // (i, i + D/2), in that order ("IV.4: One command buffer per token", the

@@ -66,30 +66,8 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// v = hi + lo with hi = f16(v), lo = f16(v - hi), for a pair of floats.
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                              uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) {
@@ -213,10 +191,10 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
     const int d0 = 16 * kk + 2 * cq;
-    split2(qs[gq * D + d0], qs[gq * D + d0 + 1], qh[kk][0], ql[kk][0]);
-    split2(qs[(gq + 8) * D + d0], qs[(gq + 8) * D + d0 + 1], qh[kk][1], ql[kk][1]);
-    split2(qs[gq * D + d0 + 8], qs[gq * D + d0 + 9], qh[kk][2], ql[kk][2]);
-    split2(qs[(gq + 8) * D + d0 + 8], qs[(gq + 8) * D + d0 + 9], qh[kk][3], ql[kk][3]);
+    attn_split2(qs[gq * D + d0], qs[gq * D + d0 + 1], qh[kk][0], ql[kk][0]);
+    attn_split2(qs[(gq + 8) * D + d0], qs[(gq + 8) * D + d0 + 1], qh[kk][1], ql[kk][1]);
+    attn_split2(qs[gq * D + d0 + 8], qs[gq * D + d0 + 9], qh[kk][2], ql[kk][2]);
+    attn_split2(qs[(gq + 8) * D + d0 + 8], qs[(gq + 8) * D + d0 + 9], qh[kk][3], ql[kk][3]);
   }
   const float f0 = fh[gq], f1 = fh[gq + 8];
 
@@ -250,8 +228,8 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
         const uint8_t* krow = st + tok * C::kStride + 4 * cq + 32 * kk;
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow);
         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16);
-        mma16816(s[j], qh[kk], b0, b1);
-        mma16816(sl[j], ql[kk], b0, b1);
+        attn_mma16816(s[j], qh[kk], b0, b1);
+        attn_mma16816(sl[j], ql[kk], b0, b1);
       }
     }
 #pragma unroll
@@ -310,10 +288,10 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
     }
     // ---- P (16 heads x 16 tokens) as the A operand, hi/lo ----
     uint32_t ph[4], pl[4];
-    split2(s[0][0] * kPScale, s[0][1] * kPScale, ph[0], pl[0]);
-    split2(s[0][2] * kPScale, s[0][3] * kPScale, ph[1], pl[1]);
-    split2(s[1][0] * kPScale, s[1][1] * kPScale, ph[2], pl[2]);
-    split2(s[1][2] * kPScale, s[1][3] * kPScale, ph[3], pl[3]);
+    attn_split2(s[0][0] * kPScale, s[0][1] * kPScale, ph[0], pl[0]);
+    attn_split2(s[0][2] * kPScale, s[0][3] * kPScale, ph[1], pl[1]);
+    attn_split2(s[1][0] * kPScale, s[1][1] * kPScale, ph[2], pl[2]);
+    attn_split2(s[1][2] * kPScale, s[1][3] * kPScale, ph[3], pl[3]);
     // ---- O += P.V ----
     {
       const int mi = lane >> 3, r = lane & 7;
@@ -322,11 +300,11 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
 #pragma unroll
       for (int dn = 0; dn < D / 16; ++dn) {
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vrow + dn * 32, v0, v1, v2, v3);
-        mma16816(o[2 * dn], ph, v0, v1);
-        mma16816(o[2 * dn], pl, v0, v1);
-        mma16816(o[2 * dn + 1], ph, v2, v3);
-        mma16816(o[2 * dn + 1], pl, v2, v3);
+        attn_ldsm_x4_trans(vrow + dn * 32, v0, v1, v2, v3);
+        attn_mma16816(o[2 * dn], ph, v0, v1);
+        attn_mma16816(o[2 * dn], pl, v0, v1);
+        attn_mma16816(o[2 * dn + 1], ph, v2, v3);
+        attn_mma16816(o[2 * dn + 1], pl, v2, v3);
       }
     }
     __syncwarp();  // the stage is refilled by the next iteration's load

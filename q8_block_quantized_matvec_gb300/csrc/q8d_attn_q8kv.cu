@@ -77,29 +77,8 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void split2q(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 
-__device__ __forceinline__ void mma16816q(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
-__device__ __forceinline__ void ldsm_x4_trans_q(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                                uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
 
 // Four signed quants (one word) -> two exact f16 pairs: bytes (0, 1) and
 // (2, 3).  A sign-flipped byte b placed under the exponent byte 0x64 is the
@@ -253,10 +232,10 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
     const int d0 = 16 * kk + 4 * cq;
-    split2q(qs[gq * D + d0], qs[gq * D + d0 + 1], qh[kk][0], ql[kk][0]);
-    split2q(qs[(gq + 8) * D + d0], qs[(gq + 8) * D + d0 + 1], qh[kk][1], ql[kk][1]);
-    split2q(qs[gq * D + d0 + 2], qs[gq * D + d0 + 3], qh[kk][2], ql[kk][2]);
-    split2q(qs[(gq + 8) * D + d0 + 2], qs[(gq + 8) * D + d0 + 3], qh[kk][3], ql[kk][3]);
+    attn_split2(qs[gq * D + d0], qs[gq * D + d0 + 1], qh[kk][0], ql[kk][0]);
+    attn_split2(qs[(gq + 8) * D + d0], qs[(gq + 8) * D + d0 + 1], qh[kk][1], ql[kk][1]);
+    attn_split2(qs[gq * D + d0 + 2], qs[gq * D + d0 + 3], qh[kk][2], ql[kk][2]);
+    attn_split2(qs[(gq + 8) * D + d0 + 2], qs[(gq + 8) * D + d0 + 3], qh[kk][3], ql[kk][3]);
   }
   const float f0 = fh[gq], f1 = fh[gq + 8];
 
@@ -311,8 +290,8 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
                                       : quant_word<true>(blk, 16 * h + 4 * cq);
           uint32_t b0, b1;
           quants_to_h2(w, b0, b1);
-          mma16816q(acc[j], qh[kk], b0, b1);
-          mma16816q(acc[j], ql[kk], b0, b1);
+          attn_mma16816(acc[j], qh[kk], b0, b1);
+          attn_mma16816(acc[j], ql[kk], b0, b1);
         }
       }
 #pragma unroll
@@ -412,19 +391,19 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
     for (int bb = 0; bb < NB; ++bb) {
       const float a0 = sv[bb][0] * F, a1 = sv[bb][1] * F, a2 = sv[bb][2] * F, a3 = sv[bb][3] * F;
       uint32_t ph[4], pl[4];
-      split2q(s[0][0] * a0, s[0][1] * a1, ph[0], pl[0]);
-      split2q(s[0][2] * a0, s[0][3] * a1, ph[1], pl[1]);
-      split2q(s[1][0] * a2, s[1][1] * a3, ph[2], pl[2]);
-      split2q(s[1][2] * a2, s[1][3] * a3, ph[3], pl[3]);
+      attn_split2(s[0][0] * a0, s[0][1] * a1, ph[0], pl[0]);
+      attn_split2(s[0][2] * a0, s[0][3] * a1, ph[1], pl[1]);
+      attn_split2(s[1][0] * a2, s[1][1] * a3, ph[2], pl[2]);
+      attn_split2(s[1][2] * a2, s[1][3] * a3, ph[3], pl[3]);
 #pragma unroll
       for (int dd = 0; dd < 2; ++dd) {
         const int dn = 2 * bb + dd;  // 16 dims
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans_q(vrow + dn * 32, v0, v1, v2, v3);
-        mma16816q(o[2 * dn], ph, v0, v1);
-        mma16816q(o[2 * dn], pl, v0, v1);
-        mma16816q(o[2 * dn + 1], ph, v2, v3);
-        mma16816q(o[2 * dn + 1], pl, v2, v3);
+        attn_ldsm_x4_trans(vrow + dn * 32, v0, v1, v2, v3);
+        attn_mma16816(o[2 * dn], ph, v0, v1);
+        attn_mma16816(o[2 * dn], pl, v0, v1);
+        attn_mma16816(o[2 * dn + 1], ph, v2, v3);
+        attn_mma16816(o[2 * dn + 1], pl, v2, v3);
       }
     }
     __syncwarp();  // the stage and the V tile are rewritten next

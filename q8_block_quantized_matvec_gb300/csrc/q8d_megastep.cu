@@ -29,6 +29,7 @@
 //    prefetches each CTA's K/V chunk into L2 a phase ahead.
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "q8d_attn_common.cuh"
 #include "q8d_gemv.cuh"
@@ -987,6 +988,364 @@ __device__ void attn_phase(const MParams& P, const MPhase& F, int L, bool len_ok
 // query head hq (one CTA per query head).  Warp w takes chunks w, w + 20,
 // ... with all loads issued before use; the warps' partials are merged in
 // warp order (deterministic).
+// Attention phase over an f16 cache on the tensor cores (the layout of the
+// standalone attention kernel): the G <= 16 query heads of KV head g are
+// the 16 rows of m16n8k16 products.  The chunk's 16-token groups go to 4
+// warp pairs (warps 0..7) in turn (groups p, p + 4, ...); both warps of a
+// pair compute the group's scores and online softmax (kept in registers)
+// and each owns half of head_dim in P.V, so a warp holds 32 (D = 128)
+// accumulators.  q is split into f16 hi + lo after a power-of-two scale
+// per head, and so are the probabilities (after a 2^12 scale), so every
+// product is exact in the f32 accumulators.  Warps 8.. prepare q: each
+// head row is written to shared memory already as the hi / lo A fragments
+// of the MMA (conflict-free 32-bit reads, no splitting in the token loop).
+// Each pair's first group is copied (cp.async) before the q prologue and the
+// append; the owner CTA writes the new row into that group's tile itself
+// when it is there, and later groups read it back from the cache.  Pair 0
+// merges the pairs' {m, l, O} from shared memory and writes the partial.
+template <int D>
+struct MsMmaCfg {
+  static constexpr int kPairs = 4;                   // warp pairs (token-group slots)
+  static constexpr int kRow = D * 2;                 // f16 row bytes
+  static constexpr int kStride = kRow + 16;          // padded tile row
+  static constexpr int kStage = 2 * 16 * kStride;    // 16 K rows, then 16 V rows
+  static constexpr int kOffQ = kPairs * kStage;      // q fragments [2 hi/lo][D/16][4][32] (u32)
+  static constexpr int kOffF = kOffQ + 64 * D;       // per-head score factors [16]
+  static constexpr int kBytes = kOffF + 16 * 4;
+  static_assert(kBytes <= kMsRegion, "attention tiles fit the shared region");
+  // merge buffer of pairs 1..3 in the tiles: m, l [3][16], O [3][16][D]
+  static_assert((kPairs - 1) * 16 * (D + 2) * 4 <= kOffQ, "the merge buffer fits the tiles");
+};
+
+// Barrier of warp pair p (64 threads; ids 2.. are free: 0 is the CTA's, 1
+// the consumer warps'), and of the 8 warps of the pairs (id 6).
+__device__ __forceinline__ void pair_sync(int p) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + p) : "memory");
+}
+__device__ __forceinline__ void pairs_sync() { asm volatile("bar.sync 6, 256;" ::: "memory"); }
+
+template <int D>
+__device__ void attn_phase_mma(const MParams& P, const MPhase& F, int L, bool len_ok,
+                               uint8_t* region) {
+  using C = MsMmaCfg<D>;
+  constexpr int KS = D / 16, NH = D / 16;  // k-steps of Q.K^T; n-tiles of a dim half in P.V
+  constexpr int kPairs = C::kPairs;
+  constexpr float kPS = 4096.f;  // probabilities scaled by 2^12 before the f16 split
+  const int Hk = P.n_kv_heads, G = P.n_heads / Hk;
+  const int item = blockIdx.x;
+  if (!len_ok) return;  // the combine writes NaN outputs
+  const int nc = attn_chunks_for(P, L);
+  if (item >= Hk * nc) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, cq = lane & 3;
+  const int g = item / nc, c = item % nc;
+  const MLayer* Ly = P.layers + F.layer;
+  const int T = (L + nc - 1) / nc;
+  const int t0 = c * T, t1 = min(L, t0 + T);
+  const int nrows = max(0, t1 - t0);
+  const int ngroups = (nrows + 15) / 16;
+  // (chunks of T = ceil(L / nc) rows: for some L the last chunk is empty;
+  // it writes m = -inf, l = 0, which the combine skips, and it also takes
+  // the owner branch, appending the same rounded row as the chunk holding
+  // row L-1)
+  const bool owner = t1 == L;
+  const int pos = L - 1;
+  const int new_gi = owner && nrows > 0 ? (pos - t0) / 16 : -1;  // the new row's group
+  const float* cosr = P.rope_cos + (size_t)pos * (D / 2);
+  const float* sinr = P.rope_sin + (size_t)pos * (D / 2);
+  const long long kvw = (long long)Hk * D;
+  __half* kc = reinterpret_cast<__half*>(ldg_ptr(&Ly->kcache));
+  __half* vc = reinterpret_cast<__half*>(ldg_ptr(&Ly->vcache));
+  const uint8_t* kb = reinterpret_cast<const uint8_t*>(kc + (long long)g * D);
+  const uint8_t* vb = reinterpret_cast<const uint8_t*>(vc + (long long)g * D);
+  uint32_t* qf = reinterpret_cast<uint32_t*>(region + C::kOffQ);  // [hi/lo][kk][reg][lane]
+  float* fh = reinterpret_cast<float*>(region + C::kOffF);
+  const int pr = warp & (kPairs - 1), dh = warp / kPairs;  // (pair warps: warp < 2 * kPairs)
+  uint8_t* st = region + pr * C::kStage;
+
+  // this warp's half (rows 8 dh .. 8 dh + 7) of group gi into its pair's
+  // tile; skip_new leaves the new row to the appender
+  constexpr int kChunks = C::kRow / 16;
+  auto load_half = [&](int gi, bool skip_new) {
+    const int r0 = t0 + 16 * gi, nr = min(16, t1 - r0);
+    const uint8_t* ks = kb + (long long)r0 * kvw * 2;
+    const uint8_t* vs = vb + (long long)r0 * kvw * 2;
+#pragma unroll
+    for (int k = 0; k < 8 * kChunks / 32; ++k) {
+      const int e = lane + 32 * k;
+      const int r = 8 * dh + e / kChunks, pc = e % kChunks;
+      if (r < nr && !(skip_new && r0 + r == pos)) {
+        const long long off = (long long)r * kvw * 2 + pc * 16;
+        cp_async16(st + r * C::kStride + pc * 16, ks + off);
+        cp_async16(st + (16 + r) * C::kStride + pc * 16, vs + off);
+      }
+    }
+  };
+  if (warp < 2 * kPairs) {
+    if (pr < ngroups) load_half(pr, true);
+  } else if (warp < 2 * kPairs + 16) {
+    // q row hh = warp - 8 (rows past G are zero): bias / QK-norm / RoPE,
+    // scaled by 2^sh so that max|q| < 2^11 (the score factor 2^-sh * scale
+    // * log2(e) undoes it), split into hi / lo A fragments: the pair of
+    // columns (d, d + 1) of row hh is register (hh >= 8) + 2 (d % 16 >= 8)
+    // of lane (hh % 8) * 4 + (d % 8) / 2 at k-step d / 16
+    const int hh = warp - 2 * kPairs;
+    float v[D / 32];
+    if (hh < G) {
+      const int hq = g * G + hh;
+      const float* bq = ldg_ptr(&Ly->bq);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) v[t] = ldcg(P.q + (size_t)hq * D + lane + 32 * t);
+      head_prologue<D>(v, lane, bq ? bq + (size_t)hq * D : nullptr, ldg_ptr(&Ly->q_norm), P.eps,
+                       cosr, sinr);
+    } else {
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) v[t] = 0.f;
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) mx = fmaxf(mx, fabsf(v[t]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    // (sh >= -117 for any finite q; at most 125 keeps 2^sh a normal float:
+    // rows below 2^-114 then scale to less)
+    const int sh = mx > 0.f ? min(125, 11 - e) : 0;
+    const float sc = __int_as_float((127 + sh) << 23);
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) {
+      const float a = v[t] * sc;
+      const float b = __shfl_down_sync(0xffffffffu, a, 1);  // column d + 1
+      if ((lane & 1) == 0) {
+        const int d = lane + 32 * t;
+        uint32_t hi, lo;
+        attn_split2(a, b, hi, lo);
+        const int reg = (hh >= 8 ? 1 : 0) + ((d & 15) >= 8 ? 2 : 0);
+        const int ln = (hh & 7) * 4 + ((d & 7) >> 1);
+        qf[((d >> 4) * 4 + reg) * 32 + ln] = hi;
+        qf[((KS + (d >> 4)) * 4 + reg) * 32 + ln] = lo;
+      }
+    }
+    if (lane == 0) fh[hh] = hh < G ? ldexpf(P.scale * kLog2e, -sh) : 0.f;
+  }
+  // the owner appends the new k (bias, norm, RoPE) and v (bias) to the cache
+  // (warps 6 and 7, after their copies are issued) and, when its group is a
+  // pair's first, into that tile
+  if (owner && (warp == 6 || warp == 7)) {
+    const bool isk = warp == 6;
+    float nv[D / 32];
+    const float* src = (isk ? P.k : P.v) + (size_t)g * D;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) nv[t] = ldcg(src + lane + 32 * t);
+    if (isk) {
+      const float* bk = ldg_ptr(&Ly->bk);
+      head_prologue<D>(nv, lane, bk ? bk + (size_t)g * D : nullptr, ldg_ptr(&Ly->k_norm), P.eps,
+                       cosr, sinr);
+    } else {
+      const float* bv = ldg_ptr(&Ly->bv);
+      head_prologue<D>(nv, lane, bv ? bv + (size_t)g * D : nullptr, nullptr, 0.f, nullptr,
+                       nullptr);
+    }
+    __half* dst = (isk ? kc : vc) + (long long)pos * kvw + (long long)g * D;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) dst[lane + 32 * t] = __float2half_rn(nv[t]);
+    if (new_gi >= 0 && new_gi < kPairs) {
+      __half* row = reinterpret_cast<__half*>(region + new_gi * C::kStage +
+                                              ((isk ? 0 : 16) + (pos - t0) % 16) * C::kStride);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) row[lane + 32 * t] = __float2half_rn(nv[t]);
+    }
+  }
+  cp_async_wait_all();
+  consumer_sync(kCT);  // q fragments, first tiles and the new row in place; the cache row written
+  if (warp >= 2 * kPairs) return;  // (the pair warps finish the phase)
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[NH][4];  // this warp's dim half: columns 8 n + 2 cq (+1) of the half
+#pragma unroll
+  for (int n = 0; n < NH; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  const float f0 = fh[gq], f1 = fh[gq + 8];
+  for (int gi = pr; gi < ngroups; gi += kPairs) {
+    if (gi != pr) {  // later groups: one tile, refilled once the pair is done with it
+      pair_sync(pr);
+      load_half(gi, false);
+      cp_async_wait_all();
+      pair_sync(pr);
+    }
+    const int nr = min(16, t1 - (t0 + 16 * gi));
+    // ---- S = Q.K^T for the group's 16 tokens (two n-tiles of 8): hi and
+    // lo products in separate accumulators (four independent chains) ----
+    float sh_[2][4], sl_[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      sh_[j][0] = sh_[j][1] = sh_[j][2] = sh_[j][3] = 0.f;
+      sl_[j][0] = sl_[j][1] = sl_[j][2] = sl_[j][3] = 0.f;
+    }
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t qh[4], ql[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        qh[r] = qf[(kk * 4 + r) * 32 + lane];
+        ql[r] = qf[((KS + kk) * 4 + r) * 32 + lane];
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = min(8 * j + gq, nr - 1);
+        const uint8_t* krow = st + tok * C::kStride + 4 * cq + 32 * kk;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16);
+        attn_mma16816(sh_[j], qh, b0, b1);
+        attn_mma16816(sl_[j], ql, b0, b1);
+      }
+    }
+    // ---- log2-domain scores, mask, online softmax per row ----
+    float sc[2][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 8 * j + 2 * cq + (e & 1);
+        const float v = (sh_[j][e] + sl_[j][e]) * (e < 2 ? f0 : f1);
+        sc[j][e] = tok < nr ? v : -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[j][2], sc[j][3]));
+    }
+#pragma unroll
+    for (int o_ = 1; o_ < 4; o_ <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float c0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+    const float c1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float mrow = e < 2 ? mn0 : mn1;
+        const float pv = sc[j][e] == -INFINITY ? 0.f : exp2f(sc[j][e] - mrow);
+        sc[j][e] = pv;
+        if (e < 2) rs0 += pv;
+        else rs1 += pv;
+      }
+    }
+#pragma unroll
+    for (int o_ = 1; o_ < 4; o_ <<= 1) {
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, o_);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, o_);
+    }
+    l0 = l0 * c0 + rs0;
+    l1 = l1 * c1 + rs1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      o[n][0] *= c0;
+      o[n][1] *= c0;
+      o[n][2] *= c1;
+      o[n][3] *= c1;
+    }
+    // ---- P (16 heads x 16 tokens) as the A operand, hi / lo ----
+    uint32_t ph[4], pl[4];
+    attn_split2(sc[0][0] * kPS, sc[0][1] * kPS, ph[0], pl[0]);
+    attn_split2(sc[0][2] * kPS, sc[0][3] * kPS, ph[1], pl[1]);
+    attn_split2(sc[1][0] * kPS, sc[1][1] * kPS, ph[2], pl[2]);
+    attn_split2(sc[1][2] * kPS, sc[1][3] * kPS, ph[3], pl[3]);
+    // ---- O += P.V over this warp's dims [D/2 dh, D/2 (dh + 1)) ----
+    const int mi = lane >> 3, r = lane & 7;
+    const int tok = min((mi & 1) * 8 + r, nr - 1);
+    const uint32_t vrow =
+        smem_u32(st + (16 + tok) * C::kStride + (mi >> 1) * 16) + (uint32_t)(dh * D);  // D/2 f16
+#pragma unroll
+    for (int dn = 0; dn < NH / 2; ++dn) {
+      uint32_t v0, v1, v2, v3;
+      attn_ldsm_x4_trans(vrow + dn * 32, v0, v1, v2, v3);
+      attn_mma16816(o[2 * dn], ph, v0, v1);
+      attn_mma16816(o[2 * dn], pl, v0, v1);
+      attn_mma16816(o[2 * dn + 1], ph, v2, v3);
+      attn_mma16816(o[2 * dn + 1], pl, v2, v3);
+    }
+  }
+  // ---- pair 0 merges the pairs' {m, l, O} and writes the chunk's partial ----
+  pairs_sync();  // every pair is done with its tile: pairs 1..3 park their state there
+  float* mm = reinterpret_cast<float*>(region);  // [3][16]
+  float* ll = mm + (kPairs - 1) * 16;            // [3][16]
+  float* oo = ll + (kPairs - 1) * 16;            // [3][16][D]
+  if (pr > 0) {
+    if (cq == 0 && dh == 0) {
+      mm[(pr - 1) * 16 + gq] = m0;
+      mm[(pr - 1) * 16 + gq + 8] = m1;
+      ll[(pr - 1) * 16 + gq] = l0;
+      ll[(pr - 1) * 16 + gq + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      const int col = dh * (D / 2) + 8 * n + 2 * cq;
+      *reinterpret_cast<float2*>(oo + ((pr - 1) * 16 + gq) * D + col) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(oo + ((pr - 1) * 16 + gq + 8) * D + col) = make_float2(o[n][2], o[n][3]);
+    }
+  }
+  pairs_sync();
+  if (pr > 0) return;
+  // rows gq (m0, l0, o[.][0..1]) and gq + 8 (m1, l1, o[.][2..3])
+  float w0[kPairs], w1[kPairs];
+  float M0 = m0, M1 = m1;
+#pragma unroll
+  for (int q = 1; q < kPairs; ++q) {
+    M0 = fmaxf(M0, mm[(q - 1) * 16 + gq]);
+    M1 = fmaxf(M1, mm[(q - 1) * 16 + gq + 8]);
+  }
+  float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < kPairs; ++q) {
+    const float a = q ? mm[(q - 1) * 16 + gq] : m0, b = q ? mm[(q - 1) * 16 + gq + 8] : m1;
+    w0[q] = a == -INFINITY ? 0.f : exp2f(a - M0);
+    w1[q] = b == -INFINITY ? 0.f : exp2f(b - M1);
+    L0 = fmaf(q ? ll[(q - 1) * 16 + gq] : l0, w0[q], L0);
+    L1 = fmaf(q ? ll[(q - 1) * 16 + gq + 8] : l1, w1[q], L1);
+  }
+  float* po = P.ws_o + (size_t)item * G * D;
+#pragma unroll
+  for (int n = 0; n < NH; ++n) {
+    const int col = dh * (D / 2) + 8 * n + 2 * cq;
+    float a0 = o[n][0] * w0[0], a1 = o[n][1] * w0[0], b0 = o[n][2] * w1[0], b1 = o[n][3] * w1[0];
+#pragma unroll
+    for (int q = 1; q < kPairs; ++q) {
+      if (w0[q] != 0.f) {
+        const float2 u = *reinterpret_cast<const float2*>(oo + ((q - 1) * 16 + gq) * D + col);
+        a0 = fmaf(u.x, w0[q], a0);
+        a1 = fmaf(u.y, w0[q], a1);
+      }
+      if (w1[q] != 0.f) {
+        const float2 u = *reinterpret_cast<const float2*>(oo + ((q - 1) * 16 + gq + 8) * D + col);
+        b0 = fmaf(u.x, w1[q], b0);
+        b1 = fmaf(u.y, w1[q], b1);
+      }
+    }
+    if (gq < G)
+      *reinterpret_cast<float2*>(po + (size_t)gq * D + col) = make_float2(a0 / kPS, a1 / kPS);
+    if (gq + 8 < G)
+      *reinterpret_cast<float2*>(po + (size_t)(gq + 8) * D + col) = make_float2(b0 / kPS, b1 / kPS);
+  }
+  if (cq == 0 && dh == 0) {
+    float* pm = P.ws_m + (size_t)item * G;
+    float* pl_ = P.ws_l + (size_t)item * G;
+    if (gq < G) {
+      pm[gq] = M0;
+      pl_[gq] = L0;
+    }
+    if (gq + 8 < G) {
+      pm[gq + 8] = M1;
+      pl_[gq + 8] = L1;
+    }
+  }
+}
+
 template <int D>
 __device__ void combine_phase(const MParams& P, int L, bool len_ok, uint8_t* region) {
   // Every CTA merges a contiguous slice of the H * D outputs: a group of LW
@@ -1275,7 +1634,10 @@ __global__ void __launch_bounds__(kMsThreads, 1) q8_step_kernel(const MParams P)
         if (!ok) ms_abort = 1;  // seen at the next grid barrier
       } else if (kind == kPhAttn) {
         const int L = ms_L;
-        attn_phase<D, KT>(P, s_ph, L, L >= 1 && L <= P.cap, region);
+        if constexpr (std::is_same<KT, __half>::value)
+          attn_phase_mma<D>(P, s_ph, L, L >= 1 && L <= P.cap, region);
+        else
+          attn_phase<D, KT>(P, s_ph, L, L >= 1 && L <= P.cap, region);
       } else if (kind == kPhCombine) {
         const int L = ms_L;
         combine_phase<D>(P, L, L >= 1 && L <= P.cap, region);
