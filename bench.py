@@ -157,8 +157,8 @@ def attn_bytes(L, Hk, D, H, esize, append=True):
     return L * Hk * D * 2 * esize + 4 * 2 * H * D + (2 * Hk * D * esize if append else 0)
 
 
-STEP_KERNEL_SOURCES = ("q8d_megastep.cu", "q8d_megastep.cuh", "q8d_gemv.cuh", "q8d_internal.cuh",
-                       "q8d_attn.cuh", "q8d_attn_common.cuh", "q8d_step.cu")
+STEP_KERNEL_SOURCES = ("q8d_megastep.cu", "q8d_megastep.cuh", "q8d_gemv.cuh", "q8d_mma_frag.cuh",
+                       "q8d_internal.cuh", "q8d_attn.cuh", "q8d_attn_common.cuh", "q8d_step.cu")
 
 
 def kernel_source_sha():
