@@ -133,7 +133,11 @@ __device__ bool grid_wait(const MParams& P) {
           break;
         }
       }
-      __threadfence();
+      // (no fence here: the acquire load that saw the count synchronizes
+      // with every CTA's release add, the CTA barrier below orders this
+      // CTA's other threads after it, and their reads of other CTAs' data
+      // go through L2 (ld.global.cg, cp.async.cg); a gpu-scope fence here
+      // measured ~0.5 us per phase boundary)
     }
     if (!ok) *s_abort = 1;
     *s_flag = ok;
