@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
   uint64_t* empty = full + P.nstages;
   uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);
-  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // 128 zero bytes
-  float* xinv = reinterpret_cast<float*>(zpad + 128);            // [bpr] inverse block scales
+  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // kZeroPad zero bytes
+  float* xinv = reinterpret_cast<float*>(zpad + kZeroPad);       // [bpr] inverse block scales
   float* part = xinv + P.bpr;                                    // [2][kWinSets*8][W]
   const int v0 = blockIdx.x * P.rows_per_cta;
   const int v1 = min(P.p, v0 + P.rows_per_cta);
@@ -135,20 +135,15 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
         build_x_word(it, it < nit, v[k], xf, xinv);
       }
     }
-    if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
+    for (int i = threadIdx.x; i < kZeroPad / 4; i += nct) reinterpret_cast<uint32_t*>(zpad)[i] = 0u;
     consumer_sync(nct);
 
     // ---- main loop ----
     const int gq = lane >> 2, cq = lane & 3;
     const LaneOffs LO = lane_offsets(cq);
-    // this thread's B column: n = gq = 4h + 2jb + hl; nonzero when its block
-    // (jb) is the one this thread's contraction words belong to (cq & 1)
-    const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
-    const bool bmatch = bjb == (cq & 1);
-    const uint32_t xlane = bmatch ? (uint32_t)((2 * bh + 4 * bjb) * kXfBlock + bhl * 8 + (cq >> 1) * 16) : 0u;
+    const XLane XL = x_lane(lane);
     const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
     const uint32_t xi32 = smem_u32(xinv) + 4u * (uint32_t)lane_block(cq);
-    const uint32_t xstep = bmatch ? (uint32_t)kXfBlock : 0u;
     const uint32_t smem32 = smem_u32(smem);
     const bool lo_half = cq < 2;
     const int S = P.S, bpr = P.bpr, nslices = P.nslices, nst = P.nstages;
@@ -167,11 +162,11 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
         const int c0 = sl * S;
         const int pairs = min(S, bpr - c0) / 8;
         for (int k = warp; k < pairs; k += W) {
-          const uint32_t xb = bmatch ? xf32 + (uint32_t)(c0 + 8 * k) * kXfBlock + xlane : z32;
+          const uint32_t xb = XL.match ? xf32 + (uint32_t)((c0 / 8 + k) * kXfPair) + XL.off : z32;
           const uint32_t xi = xi32 + 4u * (uint32_t)(c0 + 8 * k);
           const uint32_t rb = row32 + 272u * (uint32_t)k;
-          yacc[0] += pair_dot(rb, xb, xstep, LO, lo_half, xi);
-          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, xstep, LO, lo_half, xi);
+          yacc[0] += pair_dot(rb, xb, XL.step, LO, lo_half, xi);
+          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, XL.step, LO, lo_half, xi);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -270,7 +265,7 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   }
   P.W = bestW;
   const long long fixed =
-      (long long)P.bpr * (kXfBlock + 4) + 128 + 2LL * kWinSets * kSetRows * P.W * 4;
+      (long long)P.bpr * (kXfBlock + 4) + kZeroPad + 2LL * kWinSets * kSetRows * P.W * 4;
   const long long budget = 220 * 1024;
   // two row sets per tile (each warp's per-tile work twice as long) when
   // three such stages fit

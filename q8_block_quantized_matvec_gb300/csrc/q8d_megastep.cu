@@ -149,7 +149,7 @@ __device__ bool grid_wait(const MParams& P) {
 
 // Whether a tensor-core phase's RMSNorm weights fit behind its fragments.
 __device__ __forceinline__ bool tc_weights_staged(const MPhase& F) {
-  return F.bpr * 276 + 128 <= kMsRegion;  // bpr * (144 + 4) + 128 + n * 4
+  return F.bpr * 260 + tc::kZeroPad <= kMsRegion;  // bpr * (128 + 4) + pad + n * 4
 }
 
 // Work of matvec phase F that depends on no other CTA, done between the
@@ -555,9 +555,9 @@ __device__ bool matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, uin
 // and the block's inverse scale multiplies its partial with the weight
 // scale: no CTA-wide reduction is needed for it.
 //
-// Region layout: x fragments [bpr][144], a 128-byte zero pad, the blocks'
-// inverse scales [bpr] (f32), then the double-buffered window partials
-// [2][win * 8][kW].
+// Region layout: x fragments (128 bytes a block, tc::x_word_offset), a
+// 512-byte zero pad, the blocks' inverse scales [bpr] (f32), then the
+// double-buffered window partials [2][win * 8][kW].
 
 constexpr int kTcItems = 4;  // (block, word) items per consumer thread: bpr <= 320
 
@@ -568,7 +568,7 @@ __device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, 
   const int bpr = F.bpr;
   uint8_t* xf = region;
   uint8_t* zpad = xf + (size_t)bpr * kXfBlock;
-  float* xinv = reinterpret_cast<float*>(zpad + 128);
+  float* xinv = reinterpret_cast<float*>(zpad + kZeroPad);
   float* part = xinv + bpr;
   // ---- x fragments (RMSNorm applied first where the phase has it) ----
   const bool rms = F.xmode == kXRmsNorm;
@@ -618,19 +618,13 @@ __device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, 
     if (k * kCT >= nit) break;  // (uniform over the CTA)
     build_x_word(it, it < nit, v[k], xf, xinv);
   }
-  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
+  if (threadIdx.x < kZeroPad / 4) reinterpret_cast<uint32_t*>(zpad)[threadIdx.x] = 0u;
   consumer_sync(kCT);
 
   // ---- units ----
   const int gq = lane >> 2, cq = lane & 3;
   const LaneOffs LO = lane_offsets(cq);
-  // this thread's B column: n = gq = 4h + 2jb + hl; nonzero when its block
-  // (jb) is the one this thread's contraction words belong to (cq & 1)
-  const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
-  const bool bmatch = bjb == (cq & 1);
-  const uint32_t xlane =
-      bmatch ? (uint32_t)((2 * bh + 4 * bjb) * kXfBlock + bhl * 8 + (cq >> 1) * 16) : 0u;
-  const uint32_t xstep = bmatch ? (uint32_t)kXfBlock : 0u;
+  const XLane XL = x_lane(lane);
   const uint32_t xf32 = smem_u32(xf), z32 = smem_u32(zpad);
   const uint32_t xi32 = smem_u32(xinv) + 4u * (uint32_t)lane_block(cq);
   const bool lo_half = cq < 2;
@@ -662,9 +656,9 @@ __device__ bool tc_matvec_phase(const MPhase& F, const MParams& P, RingPos& rp, 
         const int sl = j >= P8 ? 1 : 0;  // (T <= 2)
         const int k = j - sl * P8;
         const uint32_t rb = row32 + (uint32_t)(sl * F.SR) + 272u * (uint32_t)k;
-        const uint32_t xb = bmatch ? xf32 + (uint32_t)(8 * k) * kXfBlock + xlane : z32;
+        const uint32_t xb = XL.match ? xf32 + (uint32_t)(k * kXfPair) + XL.off : z32;
         float pe, po;
-        pair_units(rb, xb, xstep, LO, lo_half, pe, po);
+        pair_units(rb, xb, XL.step, LO, lo_half, pe, po);
         const float se = unit_scale(rb, LO, false) * lds32f(xi32 + 32u * (uint32_t)k);
         const float so = unit_scale(rb, LO, true) * lds32f(xi32 + 32u * (uint32_t)k + 4u);
         const float d = fmaf(se, pe, so * po);
@@ -1705,7 +1699,7 @@ int megastep_plan_tc(MPhase& F, int grid) {
   F.T = 3LL * ((2LL * F.SR + 127) / 128 * 128) <= megastep_ring_bytes() ? 2 : 1;
   const long long tile = ((long long)F.T * F.SR + 127) / 128 * 128;
   if (tile > megastep_ring_bytes() / 3) return 0;
-  const long long frag = (long long)F.bpr * (tc::kXfBlock + 4) + 128;
+  const long long frag = (long long)F.bpr * (tc::kXfBlock + 4) + tc::kZeroPad;
   const long long per_tile = 2LL * F.T * tc::kSetRows * kW * 4;  // double-buffered partials
   if (frag + per_tile > kMsRegion) return 0;
   F.tc = 1;

@@ -18,9 +18,12 @@
 //    f16 after the block's own power-of-two scale (its max |x| into
 //    [2^14, 2^15); the inverse scale is applied with the weight scale), so
 //    every product is exact in f32; columns that pair a row half with the
-//    other half's blocks are zero.  A block's fragment is
-//    144 bytes: 8 words x 16 bytes {hi(k0,k1), hi(k2,k3), lo(k0,k1),
-//    lo(k2,k3)} in the permuted byte order (word_quant), + 16 pad bytes.
+//    other half's blocks are zero.  A word's fragment is 16 bytes {hi(k0,k1),
+//    hi(k2,k3), lo(k0,k1), lo(k2,k3)} in the permuted byte order
+//    (word_quant); the fragments of a pair of 8 blocks (1 KB) are stored in
+//    the order the lanes read them (x_word_offset), so the 16 lanes with a
+//    nonzero B column read 128 contiguous bytes per load: no bank conflicts
+//    and no padding.  The zero columns read a 512-byte zero pad.
 //  * D: every thread ends a unit with the (hi, lo) partials of one (row,
 //    block) pair, which it scales by that block's f16 scale.
 // Blocks of odd index start two bytes after a word boundary, so their quants
@@ -35,8 +38,38 @@
 namespace q8d {
 namespace tc {
 
-constexpr int kXfBlock = 144;  // x fragment bytes per block (128 + pad)
+constexpr int kXfBlock = 128;  // x fragment bytes per block
+constexpr int kXfPair = 1024;  // ... per pair of 8 blocks
+constexpr int kZeroPad = 512;  // zero bytes the zero B columns read
 constexpr int kSetRows = 8;    // weight rows per unit
+
+// Byte offset of word w of block bb in the fragments: pair k = bb / 8; in
+// the pair, unit u = bb % 2 (even / odd blocks), step i = w / 2 of the unit
+// loop, block q = (bb % 8) / 2 of the unit, word w % 2 of the step.
+__host__ __device__ __forceinline__ uint32_t x_word_offset(int bb, int w) {
+  const int j = bb & 7;
+  return (uint32_t)((bb >> 3) * kXfPair + (j & 1) * 512 + (w >> 1) * 128 + (j >> 1) * 32 +
+                    (w & 1) * 16);
+}
+
+// This lane's B operand in a pair: its column n = gq = 4 h + 2 jb + hl is
+// block 2 h + 4 jb of a unit (q = h + 2 jb), hi or lo (hl); it is nonzero
+// when that block is the one the lane's contraction words belong to
+// (jb == cq & 1).  off: the lane's offset in a pair's fragments (even unit;
+// the odd unit's is step bytes on); zero columns read the pad.
+struct XLane {
+  uint32_t off, step;
+  bool match;
+};
+__device__ __forceinline__ XLane x_lane(int lane) {
+  const int gq = lane >> 2, cq = lane & 3;
+  const int bh = gq >> 2, bjb = (gq >> 1) & 1, bhl = gq & 1;
+  XLane X;
+  X.match = bjb == (cq & 1);
+  X.off = X.match ? (uint32_t)((bh + 2 * bjb) * 32 + (cq >> 1) * 16 + bhl * 8) : 0u;
+  X.step = X.match ? 512u : 0u;
+  return X;
+}
 
 __device__ __forceinline__ uint32_t lds32a(uint32_t addr) {
   uint32_t v;
@@ -132,7 +165,7 @@ __device__ __forceinline__ void load_word(const float* v, int bb, int w, float (
 // it | 7 (consecutive lanes of one warp, all calling) share the block's
 // max |x| m, and m * 2^e lies in [2^14, 2^15) (e >= -113 for any finite
 // m; e <= 125 keeps 2^e and 2^-e normal floats, so blocks below 2^-110
-// scale to less).  The word goes to xf + block * 144 + word * 16; the
+// scale to less).  The word goes to xf + x_word_offset(block, word); the
 // block's inverse scale 2^-e to xinv[block].  live: the item exists.
 __device__ __forceinline__ void build_x_word(int it, bool live, const float (&v)[4], uint8_t* xf,
                                              float* xinv) {
@@ -148,7 +181,7 @@ __device__ __forceinline__ void build_x_word(int it, bool live, const float (&v)
     float t[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) t[j] = v[j] * sc;
-    store_x_word(xf + (size_t)(it >> 3) * kXfBlock + (it & 7) * 16, t);
+    store_x_word(xf + x_word_offset(it >> 3, it & 7), t);
     if ((it & 7) == 0) xinv[it >> 3] = __int_as_float((127 - e) << 23);
   }
 }
@@ -187,10 +220,9 @@ __device__ __forceinline__ LaneOffs lane_offsets(int cq) {
 }
 
 // The unit partials of a pair (8 rows x blocks 8k .. 8k+7) at row32 + base;
-// xb: this lane's x fragments of the pair (its B block of the even unit,
-// word wsel; the odd unit's are xstep bytes on; the zero pad for lanes whose
-// B column is zero).  pe / po: the (row gq, block) sums of the even / odd
-// unit for this lane's block (not yet scaled).
+// xb: this lane's x fragments of the pair (pair base + XLane::off, or the
+// zero pad), xstep: XLane::step.  pe / po: the (row gq, block) sums of the
+// even / odd unit for this lane's block (not yet scaled).
 __device__ __forceinline__ void pair_units(uint32_t rb, uint32_t xb, uint32_t xstep,
                                            const LaneOffs& L, bool lo_half, float& pe, float& po) {
   float ae[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
@@ -205,8 +237,8 @@ __device__ __forceinline__ void pair_units(uint32_t rb, uint32_t xb, uint32_t xs
       we1 = __byte_perm(lds32a(rb + L.e3a + 68), lds32a(rb + L.e3b + 68), L.sel3);
     }
     const uint32_t wo0 = lds32a(rb + L.o0 + 8 * i), wo1 = lds32a(rb + L.o1 + 8 * i);
-    const uint2 be = lds64a(xb + 32 * i);
-    const uint2 bo = lds64a(xb + xstep + 32 * i);
+    const uint2 be = lds64a(xb + 128 * i);
+    const uint2 bo = lds64a(xb + xstep + 128 * i);
     uint32_t a0, a1, a2, a3;
     quant_pairs(we0, a0, a2);
     quant_pairs(we1, a1, a3);
