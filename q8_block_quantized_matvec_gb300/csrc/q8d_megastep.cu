@@ -1462,6 +1462,32 @@ __device__ __noinline__ int produce_all(const MParams& P, uint8_t* smem) {
     }
     if (kind == kPhMatvec && __ldg(&F->xmode) == kXRmsNorm)
       prefetch_l2_spread(ldg_ptr(&F->xw), (size_t)__ldg(&F->n) * 4);  // the RMSNorm weights
+    if (kind == kPhAttn && P.pf_permille > 0) {
+      // Through the short phases that follow (attention, combine, o: their
+      // weight tiles are in the ring by now) the ring is full and HBM idles:
+      // pull the first share of this CTA's rows of the next gate|up phase
+      // (both matrices) into L2 meanwhile, so that phase starts partly from
+      // L2.
+      for (int k = 1; k <= 4 && pi + k < P.nphases; ++k) {
+        const MPhase* G = F + k;
+        if (__ldg(&G->kind) != kPhMatvec || !__ldg(&G->glu)) continue;
+        const int rpc_g = __ldg(&G->rows_per_cta), nr0 = __ldg(&G->vbegin[1]);
+        const long long rb = __ldg(&G->row_bytes);
+        const int v0 = blockIdx.x * rpc_g, v1 = min(nr0, v0 + rpc_g);
+        if (v0 < v1) {
+          const long long bytes = ((long long)(v1 - v0) * rb * P.pf_permille / 1000) & ~15LL;
+          for (int sg = 0; sg < 2; ++sg) {
+            const uint8_t* base = ldg_ptr(&G->w[sg]) + (long long)v0 * rb;
+            for (long long o = 0; o < bytes; o += 32768) {
+              const uint32_t n = (uint32_t)min(32768LL, bytes - o);
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n)
+                           : "memory");
+            }
+          }
+        }
+        break;
+      }
+    }
     if (kind == kPhAttn && len_ok && (int)blockIdx.x < P.n_kv_heads * attn_chunks_for(P, L)) {
       // pull this CTA's K/V chunk (the rows before the new one) into L2 now,
       // a phase or more before the attention phase reads it

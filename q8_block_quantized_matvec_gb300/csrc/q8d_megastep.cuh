@@ -73,6 +73,7 @@ struct MParams {
   int* abort;                 // set when a CTA gives up a wait, zero at launch
   const unsigned* wait_limit; // polls a grid barrier wait makes before the step gives up
   int stage_bytes, nstages;
+  int pf_permille;  // share (1/1000) of a CTA's rows of a gate|up phase pulled into L2 ahead
 };
 
 // Tensor-core plan of one matvec phase (host): sets F.tc, F.SR, F.win and

@@ -58,6 +58,10 @@ struct q8d_step {
 namespace q8d {
 int step_validate(const q8d_step_desc* d);
 
+// Share (1/1000) of each CTA's rows of a gate|up phase that the producer
+// pulls into L2 while the short phases before it run.
+constexpr int kGluPrefetchPermille = 250;
+
 // Default number of polls a grid-barrier wait of the step kernel makes
 // before the step gives up (each poll is an L2 round trip: about a second).
 constexpr unsigned kStepWaitPolls = 1u << 21;
@@ -254,6 +258,7 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   P.wait_limit = S->bar + 2;
   P.stage_bytes = stage_bytes;
   P.nstages = std::min(8, megastep_max_stages(stage_bytes));
+  P.pf_permille = kGluPrefetchPermille;
   if (P.nstages < 2) return fail(Q8D_EUNSUPPORTED);
 
   if ((e = cudaMallocHost(&S->h_err, sizeof(int))) != cudaSuccess) return fail(record_cuda(e));
