@@ -55,23 +55,33 @@ struct MvParams {
   int* d_err;
 };
 
+// Run by the whole producer warp: every lane walks the same tiles; lane 0
+// waits for a free stage (bounded) and posts the transaction count, the
+// warp follows its result, and the tile's row (or row-group) copies are
+// dealt over the lanes.
 __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty,
                           int* abort_flag, int v0, int v1) {
+  const int lane = threadIdx.x & 31;
   const uint64_t pol = policy_evict_first();
   int s = 0, issued = 0;
   uint32_t ph = 0;
   const int tile_rows = kSetRows * P.T;
+  const int gsz = P.nslices == 1 ? 1 << P.gsh : 1;  // rows a copy
   for (int r0 = v0; r0 < v1; r0 += tile_rows) {
     const int nrows = min(tile_rows, v1 - r0);
     for (int sl = 0; sl < P.nslices; ++sl) {
-      if (issued >= P.nstages && !wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) return issued;
+      if (issued >= P.nstages) {
+        int ok = 1;
+        if (lane == 0) ok = wait_or_abort(&empty[s], ph ^ 1u, abort_flag) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return issued;
+      }
       const int c0 = sl * P.S;
       const int nb = min(P.S, P.bpr - c0);
       const uint32_t bytes = (uint32_t)nb * kQBlockBytes;
       uint8_t* dst = smem + (size_t)P.stage_bytes * s;
-      mbar_arrive_expect_tx(&full[s], bytes * nrows);
-      const int gsz = P.nslices == 1 ? 1 << P.gsh : 1;  // rows a copy
-      for (int r = 0; r < nrows; r += gsz)
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes * nrows);
+      __syncwarp();
+      for (int r = lane * gsz; r < nrows; r += 32 * gsz)
         bulk_g2s(dst + (r >> 3) * P.set_bytes + (r & 7) * P.SR + ((r & 7) >> P.gsh) * 16,
                  P.w + (long long)(r0 + r) * P.row_bytes + (long long)c0 * kQBlockBytes,
                  bytes * (uint32_t)min(gsz, nrows - r), &full[s], pol);
@@ -111,16 +121,18 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
   int issued = 0;
   bool ok = true;
   if (warp == W) {
-    if (lane == 0) issued = mv_produce(P, smem, full, empty, &s_abort, v0, v1);
+    issued = mv_produce(P, smem, full, empty, &s_abort, v0, v1);
   } else {
     const int nct = W * 32;
-    // ---- x fragments, one pass: four (block, word) items a thread per
-    // round, all loads issued before the first use ----
+    // ---- x fragments, one pass: up to kXItems (block, word) items a
+    // thread per round, all loads issued before the first use (one round
+    // for rows of up to kXItems * 480 / 8 blocks) ----
+    constexpr int kXItems = 12;
     const int nit = P.bpr * 8;
-    for (int it0 = 0; it0 < nit; it0 += 4 * nct) {
-      float v[4][4];
+    for (int it0 = 0; it0 < nit; it0 += kXItems * nct) {
+      float v[kXItems][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kXItems; ++k) {
         const int it = it0 + k * nct + threadIdx.x;
         if (it < nit) {
           load_word<1>(P.x, it >> 3, it & 7, v[k]);
@@ -129,7 +141,7 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kXItems; ++k) {
         const int it = it0 + k * nct + threadIdx.x;
         if (it0 + k * nct >= nit) break;  // (uniform over the warps)
         build_x_word(it, it < nit, v[k], xf, xinv);
