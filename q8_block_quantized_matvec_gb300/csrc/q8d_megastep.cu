@@ -1471,41 +1471,50 @@ __device__ __noinline__ int produce_all(const MParams& P, uint8_t* smem) {
       for (int k = 1; k <= 4 && pi + k < P.nphases; ++k) {
         const MPhase* G = F + k;
         if (__ldg(&G->kind) != kPhMatvec || !__ldg(&G->glu)) continue;
+        if (!__ldg(&G->tc)) break;  // (tensor-core phases only: measured there)
         const int rpc_g = __ldg(&G->rows_per_cta), nr0 = __ldg(&G->vbegin[1]);
         const long long rb = __ldg(&G->row_bytes);
         const int v0 = blockIdx.x * rpc_g, v1 = min(nr0, v0 + rpc_g);
         if (v0 < v1) {
-          const long long bytes = ((long long)(v1 - v0) * rb * P.pf_permille / 1000) & ~15LL;
+          const long long want = (long long)(v1 - v0) * rb * P.pf_permille / 1000;
           for (int sg = 0; sg < 2; ++sg) {
-            const uint8_t* base = ldg_ptr(&G->w[sg]) + (long long)v0 * rb;
-            for (long long o = 0; o < bytes; o += 32768) {
-              const uint32_t n = (uint32_t)min(32768LL, bytes - o);
-              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n)
-                           : "memory");
+            // bulk prefetches take 16-byte aligned ranges: the start rounded
+            // down and the end rounded down stay inside the matrix (its base
+            // is 16-byte aligned)
+            const uintptr_t b0 = reinterpret_cast<uintptr_t>(ldg_ptr(&G->w[sg])) + (uintptr_t)(v0 * rb);
+            const uintptr_t s0 = b0 & ~(uintptr_t)15, e0 = (b0 + (uintptr_t)want) & ~(uintptr_t)15;
+            for (uintptr_t a = s0; a < e0; a += 32768) {
+              const uint32_t n = (uint32_t)min((uintptr_t)32768, e0 - a);
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
             }
           }
         }
         break;
       }
     }
-    if (kind == kPhAttn && len_ok && (int)blockIdx.x < P.n_kv_heads * attn_chunks_for(P, L)) {
-      // pull this CTA's K/V chunk (the rows before the new one) into L2 now,
-      // a phase or more before the attention phase reads it
+    if (kind == kPhAttn && len_ok && (int)blockIdx.x < attn_chunks_for(P, L)) {
+      // pull context chunk c's K/V rows (all KV heads: whole cache rows,
+      // contiguous; the rows before the new one) into L2 now, a phase or
+      // more before the attention phase reads them: the CTA of chunk c and
+      // KV head 0 does it for the chunk's CTAs of every head, in a few large
+      // requests
       const int nc = attn_chunks_for(P, L);
-      const int g = blockIdx.x / nc, c = blockIdx.x % nc;
+      const int c = blockIdx.x;
       const int T = (L + nc - 1) / nc;
       const int t0 = c * T, t1 = min(L - 1, t0 + T);
-      const MLayer* Ly = P.layers + __ldg(&F->layer);
-      const uint8_t* kc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->kcache));
-      const uint8_t* vc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->vcache));
-      const long long rowb = (long long)P.head_dim * P.kv_esize;
-      const long long stride = rowb * P.n_kv_heads;
-      for (int t = t0; t < t1; ++t) {
-        const long long off = (long long)t * stride + (long long)g * rowb;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kc + off), "r"((uint32_t)rowb)
-                     : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vc + off), "r"((uint32_t)rowb)
-                     : "memory");
+      if (t1 > t0) {
+        const MLayer* Ly = P.layers + __ldg(&F->layer);
+        const uint8_t* kc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->kcache));
+        const uint8_t* vc = reinterpret_cast<const uint8_t*>(ldg_ptr(&Ly->vcache));
+        const long long stride = (long long)P.head_dim * P.kv_esize * P.n_kv_heads;  // a cache row
+        const long long a = (long long)t0 * stride, bytes = (long long)(t1 - t0) * stride;
+        for (long long o = 0; o < bytes; o += 32768) {
+          const uint32_t n = (uint32_t)min(32768LL, bytes - o);  // (rows are 16-byte multiples)
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kc + a + o), "r"(n)
+                       : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vc + a + o), "r"(n)
+                       : "memory");
+        }
       }
       continue;
     }
