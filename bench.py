@@ -375,10 +375,12 @@ def run_profile(args):
     elif args.profile in ("mma16", "mma64"):
         m = 16 if args.profile == "mma16" else 64
         w, x, y, n, p = small_m_inputs(m)
-        q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p)
+        need = q8d.q8d_matmul_small_m_workspace_bytes(m, n)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        q8d.q8d_matmul_small_m_ws(x, n, w, y, p, m, n, p, ws, need)
         torch.cuda.synchronize()
         cudart.cudaProfilerStart()
-        q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p)
+        q8d.q8d_matmul_small_m_ws(x, n, w, y, p, m, n, p, ws, need)
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
     elif args.profile in ("attn_stress_q8", "attn_window"):
@@ -585,12 +587,14 @@ def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
     ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for m in SMALL_M:
         w, x, y, n, p = small_m_inputs(m, rank)
+        need = q8d.q8d_matmul_small_m_workspace_bytes(m, n)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
         times = []
         with torch.cuda.stream(stream):
             for rep in range(max(reps, 3) + 1):
                 flush.fill_(rep & 0xFF)
                 ev[0].record(stream)
-                q8d.q8d_matmul_small_m(x, n, w, y, p, m, n, p, stream)
+                q8d.q8d_matmul_small_m_ws(x, n, w, y, p, m, n, p, ws, need, stream)
                 ev[1].record(stream)
                 ev[1].synchronize()
                 if rep:
@@ -599,10 +603,12 @@ def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
         nbytes = p * n // 32 * 34 + 4 * m * n + 4 * m * p
         out[f"m{m}"] = {"us": t * 1e6, "GB_s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / hbm,
                         "TFLOP_s": 2.0 * m * n * p / t / 1e12,
-                        "kernel": "q8_mma_kernel (tcgen05)" if m >= 16 else "q8_gemv_kernel / q8_rows_kernel",
+                        "kernel": ("q8_ximage_kernel + q8_mma_kernel (tcgen05)" if m >= 16
+                                   else "q8_gemv_kernel / q8_rows_kernel"),
                         "bf16_tensor_frac_of_measured": 2.0 * m * n * p / t / 1e12 / bf16_peak()}
-        del w, x, y
-    out["shape"] = "3584 -> 18944 (7B gate/up), L2 flushed before each launch"
+        del w, x, y, ws
+    out["shape"] = ("3584 -> 18944 (7B gate/up), L2 flushed before each call; m >= 9 through "
+                    "q8d_matmul_small_m_ws with a preallocated workspace")
     return out
 
 

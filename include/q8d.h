@@ -103,13 +103,36 @@ int q8d_matvec(const float* x, const void* w_q8, float* out, int n, int p, void*
  * X: device f32, row i at X + i*ldx (ldx >= n); Y: device f32, row i at
  * Y + i*ldy (ldy >= p), only the first p entries of each row are written.
  * m <= 8: f32 CUDA-core path, weights read once for all m rows, f32 accuracy.
- * m >= 9: tensor-core path (tcgen05.mma, bf16 operands from the dequantised
- * weights and the rounded activations, f32 accumulation): relative accuracy
- * ~2^-8 per product, i.e. within 1e-2 of sum|terms| per output.
- * 1 <= m <= 256; n % 32 == 0.
+ * m >= 9 and n % 256 == 0: tensor-core path (tcgen05.mma, bf16 operands
+ * from the dequantised weights and the rounded activations, f32
+ * accumulation): relative accuracy ~2^-8 per product, i.e. within 1e-2 of
+ * sum|terms| per output.  It first writes the activations, rounded to bf16,
+ * into a workspace laid out as the MMA's B operand
+ * (q8d_matmul_small_m_workspace_bytes(m, n) bytes); this entry point takes
+ * that workspace from the stream's memory pool (cudaMallocAsync) and frees
+ * it stream-ordered behind the kernels; q8d_matmul_small_m_ws uses the
+ * caller's.  Other m >= 9 shapes run the f32 CUDA-core path.
+ * 1 <= m <= 256; n % 32 == 0; X and w_q8 16-byte aligned, ldx % 4 == 0,
+ * Y 4-byte aligned (Q8D_EALIGN otherwise); Y must not overlap X or w_q8
+ * (Q8D_EINVAL).  m == 0 or p == 0: Q8D_OK, nothing written.
  * ---------------------------------------------------------------------- */
 int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m,
                        int n, int p, void* stream);
+
+/* Bytes of the workspace q8d_matmul_small_m_ws needs for m activation rows of
+ * n elements: 2 * n * (m rounded up to 16 per block of 128 rows) when the
+ * tensor-core path takes the shape (9 <= m <= 256, n % 256 == 0), else 0. */
+size_t q8d_matmul_small_m_workspace_bytes(int m, int n);
+
+/* q8d_matmul_small_m with a caller-owned workspace: device memory of at
+ * least q8d_matmul_small_m_workspace_bytes(m, n) bytes, 16-byte aligned,
+ * overlapping none of X, w_q8 and Y, not in use by other work until the
+ * call's kernels on `stream` have completed (the call writes it, then
+ * reads it).  Q8D_EINVAL if it is needed and null or too small, or
+ * overlaps an operand; Q8D_EALIGN if misaligned.  Unused (may be null)
+ * when the size is 0. */
+int q8d_matmul_small_m_ws(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m,
+                          int n, int p, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * q8d_kv_append — write one token's K and V rows into the caches

@@ -79,6 +79,10 @@ def lib():
         L.q8d_matvec.restype = i32
         L.q8d_matmul_small_m.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, vp]
         L.q8d_matmul_small_m.restype = i32
+        L.q8d_matmul_small_m_workspace_bytes.argtypes = [i32, i32]
+        L.q8d_matmul_small_m_workspace_bytes.restype = sz
+        L.q8d_matmul_small_m_ws.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, vp, sz, vp]
+        L.q8d_matmul_small_m_ws.restype = i32
         L.q8d_kv_append.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.q8d_kv_append.restype = i32
         L.q8d_gqa_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
@@ -153,6 +157,18 @@ def q8d_matvec(x, w_q8, out, n: int, p: int, stream=None) -> int:
 def q8d_matmul_small_m(X, ldx: int, w_q8, Y, ldy: int, m: int, n: int, p: int, stream=None) -> int:
     return _check(lib().q8d_matmul_small_m(_ptr(X), int(ldx), _ptr(w_q8), _ptr(Y), int(ldy), int(m),
                                            int(n), int(p), _stream(stream)), "q8d_matmul_small_m")
+
+
+def q8d_matmul_small_m_workspace_bytes(m: int, n: int) -> int:
+    return int(lib().q8d_matmul_small_m_workspace_bytes(int(m), int(n)))
+
+
+def q8d_matmul_small_m_ws(X, ldx: int, w_q8, Y, ldy: int, m: int, n: int, p: int, workspace,
+                          ws_bytes: int, stream=None) -> int:
+    return _check(lib().q8d_matmul_small_m_ws(_ptr(X), int(ldx), _ptr(w_q8), _ptr(Y), int(ldy),
+                                              int(m), int(n), int(p), _ptr(workspace),
+                                              int(ws_bytes), _stream(stream)),
+                  "q8d_matmul_small_m_ws")
 
 
 def q8d_kv_append(k, v, kcache, vcache, kv_dtype: int, kv_width: int, cap: int, d_pos, d_err,

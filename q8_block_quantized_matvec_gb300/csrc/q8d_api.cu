@@ -61,8 +61,9 @@ int sm_count() {
   return cached[dev];
 }
 
+size_t mma_small_m_workspace(int m, int n);
 int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int ldy, int m, int n,
-                       int p, cudaStream_t stream);
+                       int p, void* ws, cudaStream_t stream);
 
 // Polls an event with a wall-clock limit; on completion copies *src to *dst.
 int wait_event_bounded(cudaEvent_t ev, int timeout_ms, const int* src, int* dst) {
@@ -170,11 +171,13 @@ int q8d_matvec(const float* x, const void* w_q8, float* out, int n, int p, void*
   return rows_plan_and_launch(P, static_cast<cudaStream_t>(stream));
 }
 
-int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m, int n,
-                       int p, void* stream) {
+namespace {
+// Argument checks shared by both small-M entry points (Q8D_OK: go on).
+int small_m_check(const float* X, int ldx, const void* w_q8, const float* Y, int ldy, int m, int n,
+                  int p) {
   if (m < 0 || n < 0 || p < 0) return Q8D_EINVAL;
-  if (m == 0 || p == 0) return Q8D_OK;
   if (m > 256) return Q8D_EUNSUPPORTED;
+  if (m == 0 || p == 0) return Q8D_OK;
   if (!Y || ldy < p) return Q8D_EINVAL;
   if (n % 32) return Q8D_EUNSUPPORTED;
   if (n > 0 && (!X || !w_q8 || ldx < n)) return Q8D_EINVAL;
@@ -186,11 +189,11 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
         overlap(Y, ybytes, w_q8, q8_bytes(p, n)))
       return Q8D_EINVAL;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (m >= 9 && n > 0) {
-    const int rc = mma_small_m_launch(X, ldx, static_cast<const uint8_t*>(w_q8), Y, ldy, m, n, p, st);
-    if (rc != Q8D_EUNSUPPORTED) return rc;
-  }
+  return Q8D_OK;
+}
+
+int small_m_cuda_cores(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m, int n,
+                       int p, cudaStream_t st) {
   RowsParams P{};
   P.seg[0] = {static_cast<const uint8_t*>(w_q8), Y, p, 0};
   P.nseg = 1;
@@ -200,6 +203,50 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
   P.ldy = ldy;
   P.m = m;
   return rows_plan_and_launch(P, st);
+}
+}  // namespace
+
+size_t q8d_matmul_small_m_workspace_bytes(int m, int n) {
+  if (m < 9 || m > 256 || n <= 0 || n % 32) return 0;
+  return mma_small_m_workspace(m, n);
+}
+
+int q8d_matmul_small_m_ws(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m,
+                          int n, int p, void* workspace, size_t workspace_bytes, void* stream) {
+  const int crc = small_m_check(X, ldx, w_q8, Y, ldy, m, n, p);
+  if (crc || m == 0 || p == 0) return crc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = q8d_matmul_small_m_workspace_bytes(m, n);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return Q8D_EINVAL;
+    if (!aligned(workspace, 16)) return Q8D_EALIGN;
+    const size_t ybytes = 4ull * ((size_t)(m - 1) * ldy + p);
+    if (overlap(workspace, need, Y, ybytes) ||
+        overlap(workspace, need, X, 4ull * ((size_t)(m - 1) * ldx + n)) ||
+        overlap(workspace, need, w_q8, q8_bytes(p, n)))
+      return Q8D_EINVAL;
+    const int rc =
+        mma_small_m_launch(X, ldx, static_cast<const uint8_t*>(w_q8), Y, ldy, m, n, p, workspace, st);
+    if (rc != Q8D_EUNSUPPORTED) return rc;
+  }
+  return small_m_cuda_cores(X, ldx, w_q8, Y, ldy, m, n, p, st);
+}
+
+int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int ldy, int m, int n,
+                       int p, void* stream) {
+  const int crc = small_m_check(X, ldx, w_q8, Y, ldy, m, n, p);
+  if (crc || m == 0 || p == 0) return crc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = q8d_matmul_small_m_workspace_bytes(m, n);
+  if (need == 0) return small_m_cuda_cores(X, ldx, w_q8, Y, ldy, m, n, p, st);
+  // the activation image in stream-ordered memory, freed behind the kernels
+  void* ws = nullptr;
+  const cudaError_t e = cudaMallocAsync(&ws, need, st);
+  if (e != cudaSuccess) return record_cuda(e);
+  const int rc = q8d_matmul_small_m_ws(X, ldx, w_q8, Y, ldy, m, n, p, ws, need, stream);
+  const cudaError_t f = cudaFreeAsync(ws, st);
+  if (rc) return rc;
+  return f == cudaSuccess ? Q8D_OK : record_cuda(f);
 }
 
 int q8d_kv_append(const float* k, const float* v, void* kcache, void* vcache, int kv_dtype,

@@ -7,25 +7,38 @@
 // more than one token is in flight stages dequantised weights in on-chip
 // memory; here the tile feeds tcgen05.mma instead of SIMD-group matrices).
 //
+//  * The activations are rounded to bf16 once per call by a small kernel
+//    (q8_ximage_kernel) into a workspace that holds, for every 128-row block
+//    of X and every 128-element K half, the B operand exactly as the MMA
+//    reads it from shared memory (canonical K-major 128-byte-swizzled
+//    layout); the main kernel starts as its programmatic dependent and
+//    copies one half's B tile with a single 1-D bulk copy.
 //  * CTA = 128 weight rows (the MMA's M) x a K range; a thread-block cluster
 //    of `ksplit` CTAs along K shares one output tile and reduces the fp32
 //    partials through distributed shared memory in rank order
 //    (deterministic, no global scratch, no atomics).
-//  * Warp roles, so that dequantisation, weight streaming and MMAs overlap:
-//    one producer warp streams raw Q8_0 bytes (8 blocks = 272 bytes per row
-//    per 256-element chunk, the 128 rows a weight-row stride apart) by one
-//    2-D tensor copy per chunk (TMA: 68 32-bit elements x 128 rows; every x
+//  * Warp roles, so that dequantisation, copies and MMAs overlap: a weight
+//    producer warp streams raw Q8_0 bytes (8 blocks = 272 bytes per row per
+//    256-element chunk, the 128 rows a weight-row stride apart) by one 2-D
+//    tensor copy per chunk (TMA: 68 32-bit elements x 128 rows; every x
 //    coordinate a multiple of 16 bytes; rows past the matrix zero-filled)
-//    into a ring of stages; 16 dequantising warps turn each half chunk (128
-//    K elements) into bf16 A and B tiles in the canonical K-major
-//    128-byte-swizzled layout (a thread: one (row, block) of scale * q,
-//    computed exactly in f32 and rounded once, and its share of the X rows
-//    rounded to bf16), double-buffered; one MMA warp issues
-//    tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> f32, M = 128,
-//    N = m rounded up to 16, K = 16 per instruction) on a buffer as soon as
-//    it is written and commits to that buffer's mbarrier, which frees it
-//    for the half chunk after next.  The epilogue reads TMEM with
-//    tcgen05.ld.
+//    into a ring of stages; an activation producer warp copies the B tiles;
+//    16 dequantising warps turn each half chunk
+//    (128 K elements) into the bf16 A operand in tensor memory (TMEM): warp
+//    w owns TMEM lanes 32 (w % 4) + [0, 32) = weight rows and block w / 4 of
+//    the half; a thread reads its block with three conflict-free 16-byte
+//    shared loads, computes scale * q exactly in f32, rounds once to bf16
+//    and writes the block's 16 columns with one tcgen05.st.  A ring of
+//    kStages slots, each an A tile (64 TMEM columns) and a B tile (shared
+//    memory) with one "full" mbarrier (16 warp arrivals + the B copy's
+//    bytes) and one "empty" mbarrier; one MMA warp issues
+//    tcgen05.mma.cta_group::1.kind::f16 with A from TMEM and B from shared
+//    memory (bf16 x bf16 -> f32, M = 128, N = m rounded up to 16, K = 16 per
+//    instruction: ~93 cycles each on this part whatever N <= 128, so the 8
+//    of a half chunk bound the loop) and commits to the slot's "empty"
+//    barrier.  The accumulator (TMEM columns [0, N)) is read with
+//    tcgen05.ld and stored to Y directly, or, for a K split, reduced across
+//    the cluster through distributed shared memory.
 // Accuracy: one bf16 rounding of each weight and activation, f32
 // accumulation: |error| <= ~2^-8 * sum|terms| per output.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
@@ -41,30 +54,38 @@ namespace {
 
 using mv::wait_or_abort;
 
+// One plain poll first (the phase is usually complete), then the bounded
+// sleeping wait.
+__device__ __forceinline__ bool wait_ready(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, abort_flag);
+}
+
 constexpr int kDeqWarps = 16;                   // dequantising warps
 constexpr int kDeqThreads = kDeqWarps * 32;
-constexpr int kThreads = kDeqThreads + 64;      // + the TMA producer warp + the MMA warp
+constexpr int kWProducer = kDeqWarps;           // weight producer warp
+constexpr int kXProducer = kDeqWarps + 1;       // activation producer warp
+constexpr int kMmaWarp = kDeqWarps + 2;         // MMA issuer warp
+constexpr int kThreads = kDeqThreads + 96;
 constexpr int kM = 128;                         // weight rows per CTA (MMA M)
 constexpr int kKC = 256;                        // K elements per raw chunk (one tensor copy)
 constexpr int kHalfK = 128;                     // K elements per A/B tile (half a chunk)
 constexpr int kRawRow = (kKC / kQBlock) * kQBlockBytes;  // 272 bytes
 constexpr int kRawStage = kM * kRawRow;         // 34816 bytes
-constexpr int kAtomBytes = kM * 128;            // one 64-element K atom of A
-constexpr int kAHalf = 2 * kAtomBytes;          // an A tile of 128 K elements: 32 KB
+constexpr int kACols = kHalfK / 2;              // TMEM columns of an A tile (two bf16 a column)
+constexpr int kAColBase = 128;                  // first TMEM column of the A tiles
 constexpr int kMaxN = 128;
-constexpr int kMaxPieces = kMaxN * (kHalfK / 8) / kDeqThreads;  // B pieces per thread (<= 4)
+constexpr int kStages = 4;                      // A|B slots: TMEM columns kAColBase + 4 * 64 <= 512
+constexpr int kSmemLimit = 224 * 1024;
+constexpr int kSmemFixed = 1024 + 256;                // alignment slack, barriers
+constexpr int kMaxRawStages = 4;
 
 struct MmaParams {
-  CUtensorMap wmap;  // the weights as [p][row_bytes / 4] 32-bit elements, box [128][68]
-  const float* X;
-  int ldx;
-  const uint8_t* w;
+  CUtensorMap wmap;      // the weights as [p][row_bytes / 4] 32-bit elements, box [128][68]
+  const uint8_t* ximg;   // B operand image of this launch's activation rows
   float* Y;
   int ldy;
-  int m, n, p, npad;
+  int m, p, npad;
   int nchunks, ksplit, raw_stages;
-  long long row_bytes;
-  int* d_err;
 };
 
 // ---- tcgen05 / cluster PTX wrappers ----------------------------------------
@@ -78,12 +99,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
+// D (TMEM) += A * B^T, A read from tensor memory (lanes 0..127, columns
+// from a_tmem), B from shared memory (descriptor b).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -114,6 +137,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Warp-collective store of 16 consecutive 32-bit columns of the warp's 32
+// TMEM lanes (lane i of the warp writes TMEM lane (taddr >> 16) + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -138,11 +184,35 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Byte offset of the 16-byte chunk holding K elements [8c, 8c+8) of row r
-// inside a K-major SW128 tile whose 64-element atoms are atom_bytes apart.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c, int atom_bytes) {
-  const int atom = c >> 3, cc = c & 7;
-  return (uint32_t)(atom * atom_bytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
+// Block BLK (0..7) of a 272-byte raw row chunk as 32 bf16 of scale * q (two
+// a word, lower K first), each computed exactly in f32 and rounded once.
+// v = the 48 bytes from byte 32 * BLK of the row (16-byte aligned), so the
+// block's f16 scale is at byte 2 * BLK of v and its quants follow.
+template <int BLK>
+__device__ __forceinline__ void decode_block(const uint32_t (&v)[12], uint32_t (&pk)[16]) {
+  constexpr int kScaleWord = BLK >> 1, kScaleShift = (BLK & 1) * 16;
+  constexpr int kQWord = (BLK + 1) >> 1;  // odd BLK: quants word-aligned; even: from byte 2
+  const float sc = f16_bits_to_f32(v[kScaleWord] >> kScaleShift);
+  const uint64_t sc2 = pack2(sc, sc);
+  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t w;
+    if constexpr ((BLK & 1) != 0)
+      w = v[kQWord + k];
+    else
+      w = __funnelshift_r(v[kQWord + k], v[kQWord + k + 1], 16);
+    w ^= 0x80808080u;
+    const uint64_t q01 =
+        mul2(add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2), sc2);
+    const uint64_t q23 =
+        mul2(add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2), sc2);
+    float f0, f1, f2, f3;
+    unpack2(q01, f0, f1);
+    unpack2(q23, f2, f3);
+    pk[2 * k] = bf16x2(f0, f1);
+    pk[2 * k + 1] = bf16x2(f2, f3);
+  }
 }
 
 // 2-D tensor copy of the box at element (x, y) of the map into shared memory.
@@ -155,20 +225,52 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The B operand image of the activations: for every 128-row block rb of X
+// (npad = its rows rounded up to 16) and every 128-element K half kh, the
+// bytes [2 atoms][npad rows][128 B] at rb * 256 * n + kh * npad * 256, row r
+// of an atom holding K elements 64 * atom + [0, 64) of X row 128 * rb + r as
+// bf16 (rows past m zero), its 16-byte chunk c at position c ^ (r & 7).
+// One thread per 16-byte chunk.
+__global__ void __launch_bounds__(256) q8_ximage_kernel(const float* __restrict__ X, int ldx, int m,
+                                                         int n, long long total,
+                                                         uint8_t* __restrict__ img) {
+  griddep_wait();               // X (and the workspace's last readers) are done
+  griddep_launch_dependents();  // the matmul kernel may start its prologue
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (e >= total) return;
+  const long long per_block = 16LL * n;  // chunks of a full 128-row block
+  const int rb = (int)(e / per_block);
+  const long long rem = e - rb * per_block;
+  const int npad = min(kMaxN, (m - rb * kMaxN + 15) / 16 * 16);
+  const int kh = (int)(rem / (npad * 16));
+  const int r = (int)((rem / 16) % npad), c = (int)(rem % 16);
+  const int row = rb * kMaxN + r;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row < m) {
+    const float4* xp =
+        reinterpret_cast<const float4*>(X + (long long)row * ldx + (long long)kh * kHalfK + c * 8);
+    const float4 a = __ldg(xp), b = __ldg(xp + 1);
+    v = make_uint4(bf16x2(a.x, a.y), bf16x2(a.z, a.w), bf16x2(b.x, b.y), bf16x2(b.z, b.w));
+  }
+  uint8_t* dst = img + (long long)rb * 256 * n + (long long)kh * npad * 256 + (c >> 3) * npad * 128 +
+                 (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(dst) = v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_constant__ MmaParams P) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the swizzled atoms
+  // 1024-byte alignment for the swizzled B atoms
   const uint32_t base_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (base_s & 1023)) & 1023);
   const int b_atom = P.npad * 128;             // one 64-element K atom of B
-  uint8_t* A = smem;                           // [2][2 atoms][128 rows][128 B]
-  uint8_t* B = A + 2 * kAHalf;                 // [2][2 atoms][npad rows][128 B]
-  uint8_t* raw = B + 2 * 2 * b_atom;           // [raw_stages][128 rows][272 B]
+  const int b_tile = 2 * b_atom;               // a B tile of 128 K elements
+  uint8_t* B = smem;                           // [kStages][2 atoms][npad rows][128 B]
+  uint8_t* raw = B + (size_t)kStages * b_tile; // [raw_stages][128 rows][272 B]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(raw + (size_t)P.raw_stages * kRawStage);
   uint64_t* raw_empty = raw_full + P.raw_stages;
-  uint64_t* ab_full = raw_empty + P.raw_stages;  // [2]: half-chunk tiles written
-  uint64_t* ab_empty = ab_full + 2;              // [2]: their MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_empty + 2);
+  uint64_t* full = raw_empty + P.raw_stages;  // [kStages]: A tile written, B tile arrived
+  uint64_t* empty = full + kStages;           // [kStages]: their MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + kStages);
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -178,198 +280,246 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   const int c_end = (int)((long long)(rank + 1) * P.nchunks / P.ksplit);
   const int nloc = c_end - c_begin;
   const int nhalf = 2 * nloc;
-  const uint32_t ncols = P.npad <= 32 ? 32u : (P.npad <= 64 ? 64u : 128u);
+  // accumulator in columns [0, npad), A tiles from kAColBase
+  constexpr uint32_t kCols = 512;
+  static_assert(kAColBase + kStages * kACols <= (int)kCols, "TMEM columns");
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(ncols)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 0) {
+  bool ok = true;
+  int issued = 0;  // copies issued by this thread (producers)
+  if (warp == kWProducer && lane == 0) {
+    // every barrier, then the first weight copies at once (they need
+    // neither TMEM nor the other warps)
     for (int s = 0; s < P.raw_stages; ++s) {
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kDeqWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&ab_full[b], kDeqWarps);
-      mbar_init(&ab_empty[b], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], kDeqWarps + 1);  // + the B copy's arrive (with its bytes)
+      mbar_init(&empty[s], 1);
     }
     s_abort = 0;
     fence_barrier_init();
+    const uint64_t pol = policy_evict_first();
+    for (; issued < min(nloc, P.raw_stages); ++issued) {
+      mbar_arrive_expect_tx(&raw_full[issued], (uint32_t)kRawStage);  // the whole box (zero-filled past p)
+      tma_load_2d(raw + (size_t)issued * kRawStage, &P.wmap, (c_begin + issued) * (kRawRow / 4), r0,
+                  &raw_full[issued], pol);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int valid_rows = min(kM, P.p - r0);
-  bool ok = true;
-  int issued = 0;
 
-  if (warp == kDeqWarps) {
-    // ---- producer: one 2-D tensor copy per 8-block chunk of the 128 rows ----
+  if (warp == kWProducer) {
+    // ---- one 2-D tensor copy per 8-block chunk of the 128 rows ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      for (int i = 0; i < nloc; ++i) {
+      for (int i = issued; i < nloc; ++i) {
         const int st = i % P.raw_stages;
-        if (i >= P.raw_stages &&
-            !wait_or_abort(&raw_empty[st], (uint32_t)((i / P.raw_stages) - 1) & 1u, &s_abort))
+        if (!wait_or_abort(&raw_empty[st], (uint32_t)((i / P.raw_stages) - 1) & 1u, &s_abort))
           break;
-        mbar_arrive_expect_tx(&raw_full[st], (uint32_t)kRawStage);  // the whole box (zero-filled past p)
+        mbar_arrive_expect_tx(&raw_full[st], (uint32_t)kRawStage);
         tma_load_2d(raw + (size_t)st * kRawStage, &P.wmap, (c_begin + i) * (kRawRow / 4), r0,
                     &raw_full[st], pol);
         ++issued;
       }
     }
-  } else if (warp == kDeqWarps + 1) {
-    // ---- MMA issuer: 8 UMMAs (K = 16 each) per half-chunk, then commit ----
+  } else if (warp == kXProducer) {
+    // ---- one bulk copy per half chunk of the B operand image ----
+    if (lane == 0) {
+      griddep_wait();  // the image is written by the kernel before this one
+      fence_proxy_async_global();
+      const uint64_t pol = policy_evict_last();  // every row tile reads it
+      const uint8_t* src = P.ximg + (size_t)(2 * c_begin) * b_tile;
+      for (int j = 0; j < nhalf; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages &&
+            !wait_or_abort(&empty[st], (uint32_t)((j / kStages) - 1) & 1u, &s_abort))
+          break;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)b_tile);
+        bulk_g2s(B + (size_t)st * b_tile, src + (size_t)j * b_tile, (uint32_t)b_tile, &full[st], pol);
+        ++issued;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---- 8 UMMAs (K = 16 each) per half-chunk, then commit ----
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
                              ((uint32_t)(P.npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+      // a K step adds its byte offset / 16 to the B descriptor's start
+      // address (every address stays below 256 KB) and 8 columns to A's
+      const uint64_t b_desc0 = sw128_desc(smem_u32(B));
+      int st = 0;
+      uint32_t ph = 0;
       for (int j = 0; j < nhalf; ++j) {
-        const int b = j & 1;
-        if (!wait_or_abort(&ab_full[b], (uint32_t)(j >> 1) & 1u, &s_abort)) {
+        if (!wait_ready(&full[st], ph, &s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(A + b * kAHalf), b0 = smem_u32(B + b * 2 * b_atom);
+        const uint32_t at = tmem + (uint32_t)(kAColBase + st * kACols);
+        const uint64_t bd = b_desc0 + (uint64_t)((st * b_tile) >> 4);
 #pragma unroll
-        for (int s = 0; s < kHalfK / 16; ++s) {
-          const uint32_t koff = (uint32_t)((s & 3) * 32);
-          umma_bf16(tmem, sw128_desc(a0 + (s >> 2) * kAtomBytes + koff),
-                    sw128_desc(b0 + (s >> 2) * b_atom + koff), idesc, (j > 0 || s > 0) ? 1u : 0u);
+        for (int s = 0; s < kHalfK / 16; ++s)
+          umma_bf16_ts(tmem, at + (uint32_t)(8 * s), bd + (((s >> 2) * b_atom + (s & 3) * 32) >> 4),
+                       idesc, (j > 0 || s > 0) ? 1u : 0u);
+        umma_commit(&empty[st]);
+        if (++st == kStages) {
+          st = 0;
+          ph ^= 1u;
         }
-        umma_commit(&ab_empty[b]);
       }
     }
   } else {
-    // ---- dequantisation warps: one (row, block) item and up to npad/32 B
-    // pieces per thread and half-chunk ----
-    const int rr = (tid & 7) | ((tid >> 5) << 3);
-    const int blk = (tid >> 3) & 3;
-    const int nb = P.npad * (kHalfK / 8) / kDeqThreads;  // B pieces per thread (may be 0 or fractional)
-    const int npieces = P.npad * (kHalfK / 8);
+    // ---- dequantisation warps: weight row 32 (warp % 4) + lane (the
+    // thread's TMEM lane), block 4h + warp / 4 of half h of each chunk ----
+    const int q = warp & 3, bsel = warp >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t raw_row = smem_u32(raw) + (uint32_t)(row * kRawRow);
+    // TMEM address of this warp's lanes, slot 0, the block's 16 columns
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kAColBase + 16 * bsel);
+    int rs = 0, st = 0;
+    uint32_t rph = 0, ph = 0;  // raw stage of the current chunk, A|B slot, their parities
     for (int j = 0; j < nhalf; ++j) {
-      const int i = j >> 1, h = j & 1, b = j & 1, c = c_begin + i;
-      const int st = i % P.raw_stages;
-      // B pieces of this half: X rows, K elements c*256 + h*128 + [8 cch, 8 cch + 8)
-      float4 xa[kMaxPieces], xb[kMaxPieces];
-#pragma unroll
-      for (int u = 0; u < kMaxPieces; ++u) {
-        const int e = tid + u * kDeqThreads;
-        const int row = (e & 7) | ((e >> 7) << 3), cch = (e >> 3) & 15;
-        xa[u] = xb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (u <= nb && e < npieces && row < P.m) {
-          const float4* xp = reinterpret_cast<const float4*>(
-              P.X + (long long)row * P.ldx + (long long)c * kKC + h * kHalfK + cch * 8);
-          xa[u] = __ldg(xp);
-          xb[u] = __ldg(xp + 1);
-        }
+      const int h = j & 1;
+      if (h == 0) ok = wait_ready(&raw_full[rs], rph, &s_abort) && ok;
+      const int blk = 4 * h + bsel;  // the same for the warp's 32 lanes
+      // 48 bytes from byte 32 * blk of the row: 16-byte aligned, and the 34
+      // bytes of the block start 2 * blk bytes in (rows of 272 bytes: the
+      // loads of 8 consecutive rows cover the 32 banks once)
+      const uint32_t src = raw_row + (uint32_t)(rs * kRawStage + 32 * blk);
+      uint32_t v[12];
+      {
+        const uint4 v0 = lds128(src), v1 = lds128(src + 16), v2 = lds128(src + 32);
+        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+        v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+        v[8] = v2.x; v[9] = v2.y; v[10] = v2.z; v[11] = v2.w;
       }
-      if (h == 0) ok = wait_or_abort(&raw_full[st], (uint32_t)(i / P.raw_stages) & 1u, &s_abort) && ok;
-      // the item's block (raw row rr, block 4h + blk) as bf16 of scale * q
-      const uint8_t* rs = raw + (size_t)st * kRawStage;
       uint32_t pk[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) pk[k] = 0u;
-      if (rr < valid_rows) {
-        const uint32_t off = (uint32_t)(rr * kRawRow + (4 * h + blk) * kQBlockBytes);
-        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(rs);
-        const uint32_t wi = off >> 2;
-        const bool odd = (off & 2u) != 0;
-        uint32_t a[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) a[k] = s32[wi + k];
-        const float sc = f16_bits_to_f32(odd ? (a[0] >> 16) : (a[0] & 0xFFFFu));
-        const uint32_t sh = odd ? 32u : 16u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t wq = __funnelshift_rc(a[k], a[k + 1], sh) ^ 0x80808080u;
-          const float q0 = magic_byte(wq, magic_sel(0)) - kMagicBias;
-          const float q1 = magic_byte(wq, magic_sel(1)) - kMagicBias;
-          const float q2 = magic_byte(wq, magic_sel(2)) - kMagicBias;
-          const float q3 = magic_byte(wq, magic_sel(3)) - kMagicBias;
-          pk[2 * k] = bf16x2(q0 * sc, q1 * sc);
-          pk[2 * k + 1] = bf16x2(q2 * sc, q3 * sc);
-        }
+      switch (blk) {
+        case 0: decode_block<0>(v, pk); break;
+        case 1: decode_block<1>(v, pk); break;
+        case 2: decode_block<2>(v, pk); break;
+        case 3: decode_block<3>(v, pk); break;
+        case 4: decode_block<4>(v, pk); break;
+        case 5: decode_block<5>(v, pk); break;
+        case 6: decode_block<6>(v, pk); break;
+        default: decode_block<7>(v, pk); break;
       }
       // (the raw stage is read: release it after the chunk's second half)
       if (h == 1) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[st]);
-      }
-      // tiles of buffer b are free once the MMAs of half j - 2 completed
-      if (j >= 2) ok = wait_or_abort(&ab_empty[b], (uint32_t)((j >> 1) - 1) & 1u, &s_abort) && ok;
-      uint8_t* Ab = A + b * kAHalf;
-      const int c0 = blk * 4;  // 16-byte chunk index of the block's first 8 elements (in the half)
-      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 0, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 1, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 2, kAtomBytes)) = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-      *reinterpret_cast<uint4*>(Ab + sw128_offset(rr, c0 + 3, kAtomBytes)) = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-      uint8_t* Bb = B + b * 2 * b_atom;
-#pragma unroll
-      for (int u = 0; u < kMaxPieces; ++u) {
-        const int e = tid + u * kDeqThreads;
-        if (u <= nb && e < npieces) {
-          const int row = (e & 7) | ((e >> 7) << 3), cch = (e >> 3) & 15;
-          *reinterpret_cast<uint4*>(Bb + sw128_offset(row, cch, b_atom)) =
-              make_uint4(bf16x2(xa[u].x, xa[u].y), bf16x2(xa[u].z, xa[u].w),
-                         bf16x2(xb[u].x, xb[u].y), bf16x2(xb[u].z, xb[u].w));
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        if (++rs == P.raw_stages) {
+          rs = 0;
+          rph ^= 1u;
         }
       }
-      // generic-proxy shared writes -> visible to the tensor core (async proxy)
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // slot st is free once the MMAs of half j - kStages completed
+      if (j >= kStages) {
+        ok = wait_ready(&empty[st], ph ^ 1u, &s_abort) && ok;
+        tc_fence_after();
+      }
+      tmem_st16(a_lane + (uint32_t)(st * kACols), pk);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ab_full[b]);
+      if (lane == 0) mbar_arrive(&full[st]);
+      if (++st == kStages) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
   }
 
   // every MMA of the CTA has completed once the last half's commit arrives
   if (nhalf > 0)
-    ok = wait_or_abort(&ab_empty[(nhalf - 1) & 1], (uint32_t)((nhalf - 1) >> 1) & 1u, &s_abort) && ok;
+    ok = wait_or_abort(&empty[(nhalf - 1) % kStages], (uint32_t)((nhalf - 1) / kStages) & 1u,
+                       &s_abort) && ok;
   ok = __syncthreads_and(ok && !*(volatile int*)&s_abort);
-  if (!ok && warp == kDeqWarps && lane == 0) {
+  if (!ok && lane == 0) {
     // copies issued but never consumed may still be in flight
-    for (int k = max(0, issued - P.raw_stages); k < issued; ++k)
-      mbar_wait(&raw_full[k % P.raw_stages], (uint32_t)(k / P.raw_stages) & 1u);
+    if (warp == kWProducer)
+      for (int k = max(0, issued - P.raw_stages); k < issued; ++k)
+        mbar_wait(&raw_full[k % P.raw_stages], (uint32_t)(k / P.raw_stages) & 1u);
+    if (warp == kXProducer)
+      for (int k = max(0, issued - kStages); k < issued; ++k)
+        mbar_wait(&full[k % kStages], (uint32_t)(k / kStages) & 1u);
   }
-  // ---- epilogue: TMEM -> shared partial tile [npad][128] (reusing A) ----
+  __syncthreads();
   tc_fence_after();
-  float* part = reinterpret_cast<float*>(A);
-  if (warp < 4) {
-    const int row = warp * 32 + lane;
-    for (int c0 = 0; c0 < P.npad; c0 += 16) {
-      float v[16];
-      if (nloc > 0) {
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-      } else {
+  // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) + [0, 32) (rows),
+  // columns 16 g + [0, 16) (activation rows) for g = w / 4, w / 4 + 4, ...
+  const float nan = __int_as_float(0x7fc00000);
+  if (P.ksplit == 1) {
+    if (warp < kDeqWarps) {
+      const int r = 32 * (warp & 3) + lane;
+      for (int g = warp >> 2; 16 * g < P.npad; g += kDeqWarps / 4) {
+        float v[16];
+        if (nloc > 0) {
+          tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * g), v);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int k = 0; k < 16; ++k) v[k] = 0.f;
+        }
+        if (r < valid_rows) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (16 * g + k < P.m) P.Y[(long long)(16 * g + k) * P.ldy + r0 + r] = ok ? v[k] : nan;
+        }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) part[(c0 + j) * kM + row] = v[j];
     }
+  } else {
+    // partial tile [npad][128] in the raw ring, then rank r sums and stores
+    // every ksplit-th element of the tile, the partials of all ranks added
+    // in rank order
+    float* part = reinterpret_cast<float*>(raw);
+    if (warp < kDeqWarps) {
+      const int r = 32 * (warp & 3) + lane;
+      for (int g = warp >> 2; 16 * g < P.npad; g += kDeqWarps / 4) {
+        float v[16];
+        if (nloc > 0) {
+          tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * g), v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) part[(16 * g + k) * kM + r] = v[k];
+      }
+    }
+    __syncthreads();
+    cluster_sync();  // every CTA's partial tile is complete
+    const uint32_t part_s = smem_u32(part);
+    for (int e = tid * P.ksplit + (int)rank; e < P.m * kM; e += kThreads * P.ksplit) {
+      const int col = e / kM, r = e % kM;
+      if (r >= valid_rows) continue;
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < P.ksplit) v[k] = ld_peer(part_s + (uint32_t)(col * kM + r) * 4u, (uint32_t)k);
+      float sum = v[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k)
+        if (k < P.ksplit) sum += v[k];
+      P.Y[(long long)col * P.ldy + r0 + r] = ok ? sum : nan;
+    }
+    cluster_sync();  // every CTA keeps its shared memory until its peers have read it
   }
   tc_fence_before();
   __syncthreads();
-  if (!ok && tid == 0 && P.d_err) atomicOr(P.d_err, Q8D_DERR_WAIT);
-  cluster_sync();  // every CTA's partial tile is complete
-  if (rank == 0) {
-    const uint32_t part_s = smem_u32(part);
-    for (int e = tid; e < P.m * kM; e += kThreads) {
-      const int col = e / kM, row = e % kM;
-      if (row >= valid_rows) continue;
-      float s = part[col * kM + row];
-      for (int q = 1; q < P.ksplit; ++q) s += ld_peer(part_s + (uint32_t)(col * kM + row) * 4u, q);
-      P.Y[(long long)col * P.ldy + r0 + row] = ok ? s : __int_as_float(0x7fc00000);
-    }
-  }
-  cluster_sync();  // peers keep their shared memory until rank 0 has read it
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
                  : "memory");
   }
 }
@@ -395,14 +545,26 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Runs the tensor-core path; Q8D_EUNSUPPORTED for shapes it does not take
-// (n not a multiple of 256, or no tensor-map encoder), which the caller
+// Bytes of the B operand image of m activation rows of n elements (two
+// bytes per element, rows rounded up to 16 per 128-row block); 0 when the
+// tensor-core path does not take the shape (m < 9 or n not a multiple of
+// 256).  Host arithmetic only.
+size_t mma_small_m_workspace(int m, int n) {
+  if (m < 9 || n <= 0 || n % kKC != 0) return 0;
+  size_t rows = 0;
+  for (int i0 = 0; i0 < m; i0 += kMaxN) rows += (size_t)((std::min(kMaxN, m - i0) + 15) / 16 * 16);
+  return rows * (size_t)n * 2;
+}
+
+// Runs the tensor-core path with `ws` (mma_small_m_workspace(m, n) bytes,
+// 16-byte aligned) holding the activation image; Q8D_EUNSUPPORTED for
+// shapes it does not take or without a tensor-map encoder, which the caller
 // routes to the CUDA-core path.
 int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int ldy, int m, int n,
-                       int p, cudaStream_t stream) {
-  if (n % kKC != 0) return Q8D_EUNSUPPORTED;
+                       int p, void* ws, cudaStream_t stream) {
+  const size_t img_bytes = mma_small_m_workspace(m, n);
   const EncodeTiledFn encode = encode_tiled();
-  if (!encode) return Q8D_EUNSUPPORTED;
+  if (img_bytes == 0 || !encode) return Q8D_EUNSUPPORTED;
   // the weights as p rows of row_bytes / 4 32-bit elements (row_bytes is a
   // multiple of 272, so of 16), box = one chunk of 128 rows
   const long long row_bytes = (long long)(n / kQBlock) * kQBlockBytes;
@@ -417,8 +579,15 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return Q8D_EUNSUPPORTED;
   }
-  const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), 224 * 1024, false);
+  const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), kSmemLimit, false);
   if (crc) return crc;
+  uint8_t* img = static_cast<uint8_t*>(ws);
+  {
+    const long long total = (long long)(img_bytes / 16);
+    const int rc = launch_ex(q8_ximage_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0,
+                             stream, true, X, ldx, m, n, total, img);
+    if (rc) return rc;
+  }
   const int row_tiles = (p + kM - 1) / kM;
   const int nchunks = n / kKC;
   const int sms = sm_count();
@@ -427,31 +596,33 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
     P.wmap = wmap;
     P.m = std::min(kMaxN, m - i0);
     P.npad = (P.m + 15) / 16 * 16;
-    P.X = X + (long long)i0 * ldx;
-    P.ldx = ldx;
-    P.w = w;
+    P.ximg = img + (size_t)i0 * 2 * n;
     P.Y = Y + (long long)i0 * ldy;
     P.ldy = ldy;
-    P.n = n;
     P.p = p;
     P.nchunks = nchunks;
-    P.row_bytes = row_bytes;
     P.ksplit = std::max(1, std::min({8, sms / row_tiles, nchunks}));
-    const int fixed = 2 * kAHalf + 2 * 2 * P.npad * 128 + 1024 + 128;
-    P.raw_stages = (fixed + 3 * kRawStage <= 224 * 1024) ? 3 : 2;
-    const int smem = fixed + P.raw_stages * kRawStage;
+    // kStages A|B slots; as many weight stages as fit (2..kMaxRawStages)
+    const int b_tile = P.npad * 256;
+    P.raw_stages = std::min(kMaxRawStages, (kSmemLimit - kSmemFixed - kStages * b_tile) / kRawStage);
+    if (P.raw_stages < 2) return Q8D_EUNSUPPORTED;
+    const int smem = kSmemFixed + kStages * b_tile + P.raw_stages * kRawStage;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(row_tiles, P.ksplit, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = P.ksplit;
     attr[0].val.clusterDim.z = 1;
+    // a programmatic dependent: the prologue and the weight stream start
+    // while the image is written; the activation producer waits for it
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, q8_mma_kernel, P);
     if (e != cudaSuccess) return record_cuda(e);
   }

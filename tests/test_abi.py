@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("q8d_matvec", "q8d_matmul_small_m", "q8d_kv_append", "q8d_gqa_decode_attn",
+    for want in ("q8d_matvec", "q8d_matmul_small_m", "q8d_matmul_small_m_ws",
+                 "q8d_matmul_small_m_workspace_bytes", "q8d_kv_append", "q8d_gqa_decode_attn",
                  "q8d_gqa_workspace_bytes", "q8d_step_create", "q8d_step_launch",
                  "q8d_step_status", "q8d_step_destroy"):
         assert want in names
@@ -73,6 +74,35 @@ def test_small_m_refusals(q8d):
     assert L.q8d_matmul_small_m(A16, 66, B16, C16, 4, 2, 64, 4, None) == q8d.Q8D_EALIGN
     assert L.q8d_matmul_small_m(A16, 64, B16, C16, 4, 2, 48, 4, None) == q8d.Q8D_EUNSUPPORTED
     assert L.q8d_matmul_small_m(A16, 64, B16, C16, 4, 0, 64, 4, None) == q8d.Q8D_OK
+
+
+def test_small_m_workspace_bytes(q8d):
+    """2 bytes per element of m rows rounded up to 16 per 128-row block, for
+    the shapes the tensor-core path takes (9 <= m <= 256, n % 256 == 0)."""
+    W = q8d.q8d_matmul_small_m_workspace_bytes
+    assert W(8, 3584) == 0 and W(0, 3584) == 0 and W(257, 512) == 0
+    assert W(16, 3600) == 0 and W(16, 96) == 0          # n % 256 != 0: CUDA cores
+    assert W(9, 3584) == 2 * 3584 * 16
+    assert W(16, 3584) == 2 * 3584 * 16
+    assert W(64, 18944) == 2 * 18944 * 64
+    assert W(130, 256) == 2 * 256 * (128 + 16)
+    assert W(256, 512) == 2 * 512 * 256
+
+
+def test_small_m_ws_refusals(q8d):
+    L = q8d.lib()
+    need = q8d.q8d_matmul_small_m_workspace_bytes(16, 256)
+    D16 = 0x40000
+    args = (A16, 256, B16, C16, 4, 16, 256, 4)
+    assert L.q8d_matmul_small_m_ws(*args, None, need, None) == q8d.Q8D_EINVAL        # needed
+    assert L.q8d_matmul_small_m_ws(*args, D16, need - 16, None) == q8d.Q8D_EINVAL    # too small
+    assert L.q8d_matmul_small_m_ws(*args, D16 + 8, need, None) == q8d.Q8D_EALIGN
+    assert L.q8d_matmul_small_m_ws(*args, A16 + 4096, need, None) == q8d.Q8D_EINVAL  # overlaps X
+    assert L.q8d_matmul_small_m_ws(*args, C16 - 64, need, None) == q8d.Q8D_EINVAL   # overlaps Y
+    assert L.q8d_matmul_small_m_ws(A16, 32, B16, C16, 4, 16, 256, 4, D16, need, None) == q8d.Q8D_EINVAL
+    assert L.q8d_matmul_small_m_ws(A16, 256, B16, C16, 4, 0, 256, 4, None, 0, None) == q8d.Q8D_OK
+    assert L.q8d_matmul_small_m_ws(A16, 256, B16, C16, 4, 300, 256, 4, D16, need, None) == \
+        q8d.Q8D_EUNSUPPORTED
 
 
 def test_kv_append_refusals(q8d):

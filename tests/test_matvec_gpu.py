@@ -187,6 +187,27 @@ def test_small_m_tensor_large_m(q8d, orc, m):
     assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
 
 
+@pytest.mark.parametrize("m", [16, 130])
+def test_small_m_caller_workspace(q8d, orc, m):
+    """q8d_matmul_small_m_ws: one caller workspace serves two calls with
+    different activations, and nothing is written outside it."""
+    n, p = 512, 300
+    w = synth.q8_matrix(9, "ws.w", p, n)
+    need = q8d.q8d_matmul_small_m_workspace_bytes(m, n)
+    assert need == 2 * n * (m // 128 * 128 + (m % 128 + 15) // 16 * 16)
+    pad = 4096
+    buf = torch.full((need + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws = buf[pad:pad + need]
+    for seed in (10, 11):
+        X = synth.normal_f32(seed, f"ws.X{m}", (m, n))
+        ref, ab = orc.q8_matmul(w, X, n, p)
+        Y = torch.full((m, p), float("nan"), device="cuda")
+        q8d.q8d_matmul_small_m_ws(dev(X), n, dev(w), Y, p, m, n, p, ws, need)
+        torch.cuda.synchronize()
+        assert np.all(np.abs(Y.cpu().numpy() - ref) <= TOL_BF16 * ab), seed
+    assert (buf[:pad] == 0xA5).all() and (buf[pad + need:] == 0xA5).all()
+
+
 @pytest.mark.parametrize("m", [1, 4, 16, 64])
 def test_small_m_bench_shape_sampled(q8d, orc, m):
     """The launch the bench times: 7B gate/up (3584 -> 18944) at m rows;
