@@ -23,19 +23,19 @@
 //    tensor copy per chunk (TMA: 68 32-bit elements x 128 rows; every x
 //    coordinate a multiple of 16 bytes; rows past the matrix zero-filled)
 //    into a ring of stages; an activation producer warp copies the B tiles;
-//    16 dequantising warps turn each half chunk
-//    (128 K elements) into the bf16 A operand in tensor memory (TMEM): warp
-//    w owns TMEM lanes 32 (w % 4) + [0, 32) = weight rows and block w / 4 of
-//    the half; a thread reads its block with three conflict-free 16-byte
-//    shared loads, computes scale * q exactly in f32, rounds once to bf16
-//    and writes the block's 16 columns with one tcgen05.st.  A ring of
-//    kStages slots, each an A tile (64 TMEM columns) and a B tile (shared
-//    memory) with one "full" mbarrier (16 warp arrivals + the B copy's
-//    bytes) and one "empty" mbarrier; one MMA warp issues
+//    16 dequantising warps turn each chunk (256 K elements) into the bf16 A
+//    operand in tensor memory (TMEM): warp w owns TMEM lanes 32 (w % 4) +
+//    [0, 32) = weight rows and blocks w / 4 and w / 4 + 4 of the chunk; a
+//    thread reads a block with three conflict-free 16-byte shared loads,
+//    computes scale * q exactly in f32, rounds once to bf16 and writes the
+//    block's 16 columns with one tcgen05.st.  A ring of two or three slots,
+//    each a chunk's A tile (128 TMEM columns) and B tile (shared memory)
+//    with one "full" mbarrier (16 warp arrivals + the B copy's bytes) and
+//    one "empty" mbarrier; one MMA warp issues
 //    tcgen05.mma.cta_group::1.kind::f16 with A from TMEM and B from shared
 //    memory (bf16 x bf16 -> f32, M = 128, N = m rounded up to 16, K = 16 per
-//    instruction: ~93 cycles each on this part whatever N <= 128, so the 8
-//    of a half chunk bound the loop) and commits to the slot's "empty"
+//    instruction: ~93 cycles each on this part whatever N <= 128, so the 16
+//    of a chunk bound the loop) and commits to the slot's "empty"
 //    barrier.  The accumulator (TMEM columns [0, N)) is read with
 //    tcgen05.ld and stored to Y directly, or, for a K split, reduced across
 //    the cluster through distributed shared memory.
@@ -45,6 +45,9 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "q8d_gemv.cuh"
 #include "q8d_internal.cuh"
@@ -71,10 +74,10 @@ constexpr int kKC = 256;                        // K elements per raw chunk (one
 constexpr int kHalfK = 128;                     // K elements per A/B tile (half a chunk)
 constexpr int kRawRow = (kKC / kQBlock) * kQBlockBytes;  // 272 bytes
 constexpr int kRawStage = kM * kRawRow;         // 34816 bytes
-constexpr int kACols = kHalfK / 2;              // TMEM columns of an A tile (two bf16 a column)
+constexpr int kACols = kKC / 2;                 // TMEM columns of a chunk's A tile (two bf16 a column)
 constexpr int kAColBase = 128;                  // first TMEM column of the A tiles
 constexpr int kMaxN = 128;
-constexpr int kStages = 4;                      // A|B slots: TMEM columns kAColBase + 4 * 64 <= 512
+constexpr int kMaxStages = 3;                   // A|B slots: TMEM columns kAColBase + 3 * 128 <= 512
 constexpr int kSmemLimit = 224 * 1024;
 constexpr int kSmemFixed = 1024 + 256;                // alignment slack, barriers
 constexpr int kMaxRawStages = 4;
@@ -85,7 +88,7 @@ struct MmaParams {
   float* Y;
   int ldy;
   int m, p, npad;
-  int nchunks, ksplit, raw_stages;
+  int nchunks, ksplit, raw_stages, stages;
 };
 
 // ---- tcgen05 / cluster PTX wrappers ----------------------------------------
@@ -263,14 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   const uint32_t base_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (base_s & 1023)) & 1023);
   const int b_atom = P.npad * 128;             // one 64-element K atom of B
-  const int b_tile = 2 * b_atom;               // a B tile of 128 K elements
-  uint8_t* B = smem;                           // [kStages][2 atoms][npad rows][128 B]
-  uint8_t* raw = B + (size_t)kStages * b_tile; // [raw_stages][128 rows][272 B]
+  const int b_half = 2 * b_atom;               // B of 128 K elements (one image half)
+  const int b_tile = 2 * b_half;               // B of a chunk
+  const int S = P.stages;
+  uint8_t* B = smem;                           // [S][2 halves][2 atoms][npad rows][128 B]
+  uint8_t* raw = B + (size_t)S * b_tile;       // [raw_stages][128 rows][272 B]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(raw + (size_t)P.raw_stages * kRawStage);
   uint64_t* raw_empty = raw_full + P.raw_stages;
-  uint64_t* full = raw_empty + P.raw_stages;  // [kStages]: A tile written, B tile arrived
-  uint64_t* empty = full + kStages;           // [kStages]: their MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + kStages);
+  uint64_t* full = raw_empty + P.raw_stages;  // [S]: A tile written, B tile arrived
+  uint64_t* empty = full + S;                 // [S]: their MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + S);
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -279,10 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   const int c_begin = (int)((long long)rank * P.nchunks / P.ksplit);
   const int c_end = (int)((long long)(rank + 1) * P.nchunks / P.ksplit);
   const int nloc = c_end - c_begin;
-  const int nhalf = 2 * nloc;
   // accumulator in columns [0, npad), A tiles from kAColBase
   constexpr uint32_t kCols = 512;
-  static_assert(kAColBase + kStages * kACols <= (int)kCols, "TMEM columns");
+  static_assert(kAColBase + kMaxStages * kACols <= (int)kCols, "TMEM columns");
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kDeqWarps);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], kDeqWarps + 1);  // + the B copy's arrive (with its bytes)
       mbar_init(&empty[s], 1);
     }
@@ -334,24 +338,22 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       }
     }
   } else if (warp == kXProducer) {
-    // ---- one bulk copy per half chunk of the B operand image ----
+    // ---- one bulk copy per chunk of the B operand image (its two halves) ----
     if (lane == 0) {
       griddep_wait();  // the image is written by the kernel before this one
       fence_proxy_async_global();
       const uint64_t pol = policy_evict_last();  // every row tile reads it
-      const uint8_t* src = P.ximg + (size_t)(2 * c_begin) * b_tile;
-      for (int j = 0; j < nhalf; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages &&
-            !wait_or_abort(&empty[st], (uint32_t)((j / kStages) - 1) & 1u, &s_abort))
-          break;
+      const uint8_t* src = P.ximg + (size_t)c_begin * b_tile;
+      for (int i = 0; i < nloc; ++i) {
+        const int st = i % S;
+        if (i >= S && !wait_or_abort(&empty[st], (uint32_t)((i / S) - 1) & 1u, &s_abort)) break;
         mbar_arrive_expect_tx(&full[st], (uint32_t)b_tile);
-        bulk_g2s(B + (size_t)st * b_tile, src + (size_t)j * b_tile, (uint32_t)b_tile, &full[st], pol);
+        bulk_g2s(B + (size_t)st * b_tile, src + (size_t)i * b_tile, (uint32_t)b_tile, &full[st], pol);
         ++issued;
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---- 8 UMMAs (K = 16 each) per half-chunk, then commit ----
+    // ---- 16 UMMAs (K = 16 each) per chunk, then commit ----
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
                              ((uint32_t)(P.npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       const uint64_t b_desc0 = sw128_desc(smem_u32(B));
       int st = 0;
       uint32_t ph = 0;
-      for (int j = 0; j < nhalf; ++j) {
+      for (int i = 0; i < nloc; ++i) {
         if (!wait_ready(&full[st], ph, &s_abort)) {
           ok = false;
           break;
@@ -369,11 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
         const uint32_t at = tmem + (uint32_t)(kAColBase + st * kACols);
         const uint64_t bd = b_desc0 + (uint64_t)((st * b_tile) >> 4);
 #pragma unroll
-        for (int s = 0; s < kHalfK / 16; ++s)
-          umma_bf16_ts(tmem, at + (uint32_t)(8 * s), bd + (((s >> 2) * b_atom + (s & 3) * 32) >> 4),
-                       idesc, (j > 0 || s > 0) ? 1u : 0u);
+        for (int s = 0; s < kKC / 16; ++s)
+          umma_bf16_ts(tmem, at + (uint32_t)(8 * s),
+                       bd + (((s >> 3) * b_half + ((s >> 2) & 1) * b_atom + (s & 3) * 32) >> 4), idesc,
+                       (i > 0 || s > 0) ? 1u : 0u);
         umma_commit(&empty[st]);
-        if (++st == kStages) {
+        if (++st == S) {
           st = 0;
           ph ^= 1u;
         }
@@ -381,70 +384,68 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
     }
   } else {
     // ---- dequantisation warps: weight row 32 (warp % 4) + lane (the
-    // thread's TMEM lane), block 4h + warp / 4 of half h of each chunk ----
+    // thread's TMEM lane), blocks bsel and bsel + 4 of each chunk ----
     const int q = warp & 3, bsel = warp >> 2;
     const int row = 32 * q + lane;
-    const uint32_t raw_row = smem_u32(raw) + (uint32_t)(row * kRawRow);
-    // TMEM address of this warp's lanes, slot 0, the block's 16 columns
+    // 48 bytes from byte 32 * blk of the row: 16-byte aligned, and the 34
+    // bytes of block blk start 2 * blk bytes in (rows of 272 bytes: the
+    // loads of 8 consecutive rows cover the 32 banks once)
+    const uint32_t src0 = smem_u32(raw) + (uint32_t)(row * kRawRow + 32 * bsel);
+    // TMEM address of this warp's lanes, slot 0, block bsel's 16 columns
+    // (block bsel + 4: 64 columns further)
     const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kAColBase + 16 * bsel);
     int rs = 0, st = 0;
-    uint32_t rph = 0, ph = 0;  // raw stage of the current chunk, A|B slot, their parities
-    for (int j = 0; j < nhalf; ++j) {
-      const int h = j & 1;
-      if (h == 0) ok = wait_ready(&raw_full[rs], rph, &s_abort) && ok;
-      const int blk = 4 * h + bsel;  // the same for the warp's 32 lanes
-      // 48 bytes from byte 32 * blk of the row: 16-byte aligned, and the 34
-      // bytes of the block start 2 * blk bytes in (rows of 272 bytes: the
-      // loads of 8 consecutive rows cover the 32 banks once)
-      const uint32_t src = raw_row + (uint32_t)(rs * kRawStage + 32 * blk);
-      uint32_t v[12];
+    uint32_t rph = 0, ph = 0;  // raw stage, A|B slot, their parities
+    for (int i = 0; i < nloc; ++i) {
+      ok = wait_ready(&raw_full[rs], rph, &s_abort) && ok;
+      const uint32_t src = src0 + (uint32_t)(rs * kRawStage);
+      uint32_t v[12], u[12];
       {
         const uint4 v0 = lds128(src), v1 = lds128(src + 16), v2 = lds128(src + 32);
+        const uint4 u0 = lds128(src + 128), u1 = lds128(src + 144), u2 = lds128(src + 160);
         v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
         v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
         v[8] = v2.x; v[9] = v2.y; v[10] = v2.z; v[11] = v2.w;
+        u[0] = u0.x; u[1] = u0.y; u[2] = u0.z; u[3] = u0.w;
+        u[4] = u1.x; u[5] = u1.y; u[6] = u1.z; u[7] = u1.w;
+        u[8] = u2.x; u[9] = u2.y; u[10] = u2.z; u[11] = u2.w;
       }
-      uint32_t pk[16];
-      switch (blk) {
-        case 0: decode_block<0>(v, pk); break;
-        case 1: decode_block<1>(v, pk); break;
-        case 2: decode_block<2>(v, pk); break;
-        case 3: decode_block<3>(v, pk); break;
-        case 4: decode_block<4>(v, pk); break;
-        case 5: decode_block<5>(v, pk); break;
-        case 6: decode_block<6>(v, pk); break;
-        default: decode_block<7>(v, pk); break;
+      // the raw stage is read once the values are in registers
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&raw_empty[rs]);
+      if (++rs == P.raw_stages) {
+        rs = 0;
+        rph ^= 1u;
       }
-      // (the raw stage is read: release it after the chunk's second half)
-      if (h == 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rs]);
-        if (++rs == P.raw_stages) {
-          rs = 0;
-          rph ^= 1u;
-        }
+      uint32_t pa[16], pb[16];
+      switch (bsel) {  // the same for the warp's 32 lanes
+        case 0: decode_block<0>(v, pa); decode_block<4>(u, pb); break;
+        case 1: decode_block<1>(v, pa); decode_block<5>(u, pb); break;
+        case 2: decode_block<2>(v, pa); decode_block<6>(u, pb); break;
+        default: decode_block<3>(v, pa); decode_block<7>(u, pb); break;
       }
-      // slot st is free once the MMAs of half j - kStages completed
-      if (j >= kStages) {
+      // slot st is free once the MMAs of chunk i - S completed
+      if (i >= S) {
         ok = wait_ready(&empty[st], ph ^ 1u, &s_abort) && ok;
         tc_fence_after();
       }
-      tmem_st16(a_lane + (uint32_t)(st * kACols), pk);
+      const uint32_t ta = a_lane + (uint32_t)(st * kACols);
+      tmem_st16(ta, pa);
+      tmem_st16(ta + 64u, pb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
-      if (++st == kStages) {
+      if (++st == S) {
         st = 0;
         ph ^= 1u;
       }
     }
   }
 
-  // every MMA of the CTA has completed once the last half's commit arrives
-  if (nhalf > 0)
-    ok = wait_or_abort(&empty[(nhalf - 1) % kStages], (uint32_t)((nhalf - 1) / kStages) & 1u,
-                       &s_abort) && ok;
+  // every MMA of the CTA has completed once the last chunk's commit arrives
+  if (nloc > 0)
+    ok = wait_or_abort(&empty[(nloc - 1) % S], (uint32_t)((nloc - 1) / S) & 1u, &s_abort) && ok;
   ok = __syncthreads_and(ok && !*(volatile int*)&s_abort);
   if (!ok && lane == 0) {
     // copies issued but never consumed may still be in flight
@@ -452,8 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       for (int k = max(0, issued - P.raw_stages); k < issued; ++k)
         mbar_wait(&raw_full[k % P.raw_stages], (uint32_t)(k / P.raw_stages) & 1u);
     if (warp == kXProducer)
-      for (int k = max(0, issued - kStages); k < issued; ++k)
-        mbar_wait(&full[k % kStages], (uint32_t)(k / kStages) & 1u);
+      for (int k = max(0, issued - S); k < issued; ++k) mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u);
   }
   __syncthreads();
   tc_fence_after();
@@ -545,6 +545,40 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
+// Clusters of `ksplit` CTAs (one per SM, smem bytes each) that the device
+// runs at once; cached per (device, ksplit, smem).
+int max_active_clusters(int ksplit, int smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, std::pair<int, int>>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_pair(dev, std::make_pair(ksplit, smem));
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, ksplit, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = ksplit;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, q8_mma_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
+}
+
 // Bytes of the B operand image of m activation rows of n elements (two
 // bytes per element, rows rounded up to 16 per 128-row block); 0 when the
 // tensor-core path does not take the shape (m < 9 or n not a multiple of
@@ -601,12 +635,18 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
     P.ldy = ldy;
     P.p = p;
     P.nchunks = nchunks;
-    P.ksplit = std::max(1, std::min({8, sms / row_tiles, nchunks}));
-    // kStages A|B slots; as many weight stages as fit (2..kMaxRawStages)
-    const int b_tile = P.npad * 256;
-    P.raw_stages = std::min(kMaxRawStages, (kSmemLimit - kSmemFixed - kStages * b_tile) / kRawStage);
+    // three A|B slots (two when three leave fewer than three weight
+    // stages) and as many weight stages as fit (2..kMaxRawStages)
+    const int b_tile = P.npad * 512, left = kSmemLimit - kSmemFixed;
+    P.stages = kMaxStages;
+    if (left - P.stages * b_tile < 3 * kRawStage) P.stages = 2;
+    P.raw_stages = std::min(kMaxRawStages, (left - P.stages * b_tile) / kRawStage);
     if (P.raw_stages < 2) return Q8D_EUNSUPPORTED;
-    const int smem = kSmemFixed + kStages * b_tile + P.raw_stages * kRawStage;
+    const int smem = kSmemFixed + P.stages * b_tile + P.raw_stages * kRawStage;
+    // K split: the largest (<= 8, <= the chunks) whose row_tiles clusters
+    // all run at once (clusters of 5 or 6 pack worse into the GPCs than 4)
+    P.ksplit = std::max(1, std::min({8, sms / row_tiles, nchunks}));
+    while (P.ksplit > 1 && max_active_clusters(P.ksplit, smem) < row_tiles) --P.ksplit;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(row_tiles, P.ksplit, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
