@@ -265,6 +265,10 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
 
   const int v0 = blockIdx.x * (int)P.rows_per_cta;
   const int v1 = (int)min(P.total_rows, (long long)v0 + P.rows_per_cta);
+  // Launched as a programmatic dependent: the next kernel may start its
+  // prologue now; this one waits for the previous kernel before it reads
+  // anything or writes y.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
       mbar_init(&ring.full[s], 1);
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
     s_abort = 0;
     fence_barrier_init();
   }
+  griddep_wait();
   __syncthreads();
 
   bool ok = true;
@@ -377,7 +382,7 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.rows_per_cta = rows_cta;
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   if (grid_out) *grid_out = (int)grid;
-  return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, false, P);
+  return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, true, P);
 }
 
 }  // namespace q8d

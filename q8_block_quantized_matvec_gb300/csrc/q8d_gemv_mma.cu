@@ -108,6 +108,19 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
   float* part = xinv + P.bpr;                                    // [2][kWinSets*8][W]
   const int v0 = blockIdx.x * P.rows_per_cta;
   const int v1 = min(P.p, v0 + P.rows_per_cta);
+  // Launched as a programmatic dependent: the next kernel may start its
+  // prologue now; this one waits for the previous kernel before it copies
+  // weights into shared memory, reads x or writes y.  Until then the
+  // producer pulls the first ring-full of this CTA's rows (contiguous in
+  // memory) into L2, which reads nothing it depends on.
+  griddep_launch_dependents();
+  if (warp == W && v0 < v1) {
+    const long long bytes =
+        min((long long)P.stage_bytes * P.nstages, (long long)(v1 - v0) * P.row_bytes) & ~15LL;
+    const uint8_t* base = P.w + (long long)v0 * P.row_bytes;
+    for (long long o = (long long)lane * 16384; o < bytes; o += 32LL * 16384)
+      bulk_prefetch_l2(base + o, (uint32_t)min(16384LL, bytes - o));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
       mbar_init(&full[s], 1);
@@ -116,6 +129,7 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
     s_abort = 0;
     fence_barrier_init();
   }
+  griddep_wait();
   __syncthreads();
 
   int issued = 0;
@@ -294,7 +308,7 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   const int rc = configure_kernel(reinterpret_cast<const void*>(q8_gemv_mma_kernel), 220 * 1024, true);
   if (rc) return rc;
   if (grid_out) *grid_out = grid;
-  return launch_ex(q8_gemv_mma_kernel, dim3(grid), dim3((P.W + 1) * 32), (size_t)smem, stream, false, P);
+  return launch_ex(q8_gemv_mma_kernel, dim3(grid), dim3((P.W + 1) * 32), (size_t)smem, stream, true, P);
 }
 
 }  // namespace q8d

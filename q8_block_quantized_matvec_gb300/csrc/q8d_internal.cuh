@@ -102,6 +102,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Pulls [src, src + bytes) into L2 (TMA engine, nothing to wait for).
+// src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Orders this thread's earlier generic-proxy global writes before later
 // async-proxy (bulk copy) reads of the same addresses.
 __device__ __forceinline__ void fence_proxy_async_global() {

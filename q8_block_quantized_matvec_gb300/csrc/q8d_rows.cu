@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(W * 32, MV >= 4 ? 1 : 2)
   const int rows_cta = (int)max(0LL, v1 - v0);
 
   __shared__ int s_abort;
+  // Launched as a programmatic dependent: the next kernel may start its
+  // prologue now; this one waits for the previous kernel before it reads
+  // anything or writes y.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
       mbar_init(&full[s], 1);
@@ -170,6 +174,7 @@ __global__ void __launch_bounds__(W * 32, MV >= 4 ? 1 : 2)
     s_abort = 0;
     fence_barrier_init();
   }
+  griddep_wait();
   __syncthreads();
 
   bool ok = true;
@@ -318,7 +323,7 @@ int launch_rows(RowsParams P, long long R, cudaStream_t stream, int* grid_out) {
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   smem = smem_for(rows_cta);
   if (grid_out) *grid_out = (int)grid;
-  return launch_ex(fn, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, false, P);
+  return launch_ex(fn, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, true, P);
 }
 
 }  // namespace
