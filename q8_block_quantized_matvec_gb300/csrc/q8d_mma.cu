@@ -447,6 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   if (nloc > 0)
     ok = wait_or_abort(&empty[(nloc - 1) % S], (uint32_t)((nloc - 1) / S) & 1u, &s_abort) && ok;
   ok = __syncthreads_and(ok && !*(volatile int*)&s_abort);
+  // the next call's image kernel may start during the epilogue (it waits
+  // for this grid before it touches X or the workspace)
+  griddep_launch_dependents();
   if (!ok && lane == 0) {
     // copies issued but never consumed may still be in flight
     if (warp == kWProducer)
