@@ -164,12 +164,29 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   const int ngroups = (t_end - t_begin + kGroup - 1) / kGroup;
   const int my_groups = ngroups > warp ? (ngroups - warp + kWarpsA - 1) / kWarpsA : 0;
   uint8_t* ring = smem + warp * C::kWarpRing;
+  constexpr int kChunks = C::kRow / 16;       // 16-byte pieces per row
+  constexpr int kRowsPass = 32 / kChunks;      // rows one pass of the 32 lanes copies
+  const long long row_bytes = kvw * 2;
   auto load_group = [&](int i) {  // i-th group of this warp into stage i % kWStages
     if (i < my_groups) {
       const int t0 = t_begin + (warp + kWarpsA * i) * kGroup;
       const int nr = min(kGroup, t_end - t0);
       uint8_t* st = ring + (i % kWStages) * C::kStage;
-      constexpr int kChunks = C::kRow / 16;  // 16-byte pieces per row
+      if (nr == kGroup && t0 + kGroup <= run0_len) {
+        // 16 consecutive cache rows: one base address, fixed strides
+        const int r = lane / kChunks, pc = lane % kChunks;
+        const long long off = (long long)(run0_cell + t0 + r) * row_bytes + pc * 16;
+        const uint8_t* ks = reinterpret_cast<const uint8_t*>(kbase) + off;
+        const uint8_t* vs = reinterpret_cast<const uint8_t*>(vbase) + off;
+        uint8_t* kd = st + r * C::kStride + pc * 16;
+#pragma unroll
+        for (int k = 0; k < kGroup / kRowsPass; ++k) {
+          cp_async16(kd + k * kRowsPass * C::kStride, ks + k * kRowsPass * row_bytes);
+          cp_async16(kd + (kGroup + k * kRowsPass) * C::kStride, vs + k * kRowsPass * row_bytes);
+        }
+        cp_async_commit();
+        return;
+      }
 #pragma unroll
       for (int e = lane; e < kGroup * kChunks; e += 32) {
         const int r = e / kChunks, pc = e % kChunks;
