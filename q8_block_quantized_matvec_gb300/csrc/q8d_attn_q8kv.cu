@@ -211,6 +211,23 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
       const int t0 = t_begin + (warp + kWarpsQ * i) * kGroupQ;
       const int nr = min(kGroupQ, t_end - t0);
       uint8_t* st = ring + (i % kStagesQ) * C::kRawStage;
+      if (nr == kGroupQ && t0 + kGroupQ <= run0_len) {
+        // 16 consecutive cache rows: one base address, no window lookup
+        const uint8_t* ks = kbase + (long long)(run0_cell + t0) * rowb;
+        const uint8_t* vs = vbase + (long long)(run0_cell + t0) * rowb;
+#pragma unroll
+        for (int k = 0; k < (kGroupQ * C::kPer + 31) / 32; ++k) {
+          const int e = lane + 32 * k;
+          if (e < kGroupQ * C::kPer) {
+            const int r = e / C::kPer, pc = e % C::kPer;
+            const long long off = (long long)r * rowb + pc * C::kCopy;
+            cp_async_n<C::kCopy>(st + r * C::kRS + pc * C::kCopy, ks + off);
+            cp_async_n<C::kCopy>(st + (kGroupQ + r) * C::kRS + pc * C::kCopy, vs + off);
+          }
+        }
+        cp_commit();
+        return;
+      }
       for (int e = lane; e < kGroupQ * C::kPer; e += 32) {
         const int r = e / C::kPer, pc = e % C::kPer;
         if (r < nr) {
