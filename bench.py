@@ -428,6 +428,33 @@ def run_profile(args):
 STRESS_CAP = 32768
 
 
+def graph_seconds_per_call(calls, stream, reps=3):
+    """Seconds per call of `calls` (zero-argument callables, each one library
+    call on `stream`) captured once in a CUDA graph and replayed back to
+    back; the median of `reps` replays, one timed region per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        for c in calls:
+            c()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    with torch.cuda.stream(stream):
+        for rep in range(reps + 1):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            b.synchronize()
+            if rep:
+                times.append(a.elapsed_time(b) / 1e3 / len(calls))
+    del graph
+    return statistics.median(times)
+
+
 def stress_inputs(q8d, H, Hk, D, rank=0):
     """The long-context attention workload: 8 sequences of the model's heads,
     lengths drawn uniformly from [1, 32768] (seeded), an f16 cache of 32768
@@ -469,11 +496,21 @@ def attn_stress(q8d, H, Hk, D, reps, stream, flush, rank=0):
                 times.append(ev[0].elapsed_time(ev[1]) / 1e3)
     assert err.item() == 0
     t = statistics.median(times)
+    # back to back: 8 calls in one CUDA graph alternating over two copies of
+    # the inputs (2 x 0.54 GB, far beyond L2)
+    _, args2, err2 = stress_inputs(q8d, H, Hk, D, rank)
+    calls = [(lambda a_=a_: q8d.q8d_gqa_decode_attn(*a_, stream)) for a_ in (args_, args2) * 4]
+    t_seq = graph_seconds_per_call(calls, stream, reps)
+    assert err.item() == 0 and err2.item() == 0
+    del args2
     nbytes = sum(attn_bytes(L, Hk, D, H, 2, append=False) for L in lens)
     return {"kernel": "gqa_mma_kernel + gqa_combine_kernel (q8d_gqa_decode_attn)",
             "GB_s": nbytes / t / 1e9, "us_per_launch": t * 1e6, "kv_bytes": nbytes,
             "batch": 8, "lengths": "seeded uniform in [1, 32768]", "sum_lengths": int(sum(lens)),
-            "l2": "256 MB flush before each launch"}
+            "l2": "256 MB flush before each launch",
+            "back_to_back": {"us_per_call": t_seq * 1e6, "GB_s": nbytes / t_seq / 1e9,
+                             "timing": "8 calls in one CUDA graph over two copies of the inputs, "
+                                       "replay timed with CUDA events"}}
 
 
 def attn_stress_q8(q8d, H, Hk, D, reps, stream, flush, rank=0):
@@ -506,12 +543,27 @@ def attn_stress_q8(q8d, H, Hk, D, reps, stream, flush, rank=0):
                 times.append(ev[0].elapsed_time(ev[1]) / 1e3)
     assert err.item() == 0
     t = statistics.median(times)
+    # back to back: 8 calls in one CUDA graph alternating over two copies of
+    # the caches (2 x 0.57 GB, far beyond L2)
+    kc2 = synth.q8_matrix_torch(rank, "stress.kq8", 8 * cap, kvw, scale_lo=4e-3, scale_hi=3e-2)
+    vc2 = synth.q8_matrix_torch(rank, "stress.vq8", 8 * cap, kvw, scale_lo=4e-3, scale_hi=3e-2)
+
+    def call(k_, v_):
+        return lambda: q8d.q8d_gqa_decode_attn(q, None, None, k_, v_, q8d.Q8D_KV_Q8_0, out, 8, H,
+                                               Hk, D, cap, cap * kvw, lt, 1 / math.sqrt(D), ws,
+                                               wsb, err, stream)
+    t_seq = graph_seconds_per_call([call(kc, vc), call(kc2, vc2)] * 4, stream, reps)
+    assert err.item() == 0
+    del kc2, vc2
     row_bytes = kvw // 32 * 34
     nbytes = sum(2 * L * row_bytes + 4 * 2 * H * D for L in lens)
     return {"kernel": "gqa_q8kv_kernel + gqa_combine_kernel (q8d_gqa_decode_attn, packed Q8_0 KV)",
             "GB_s": nbytes / t / 1e9, "us_per_launch": t * 1e6, "kv_bytes": nbytes,
             "batch": 8, "lengths": "seeded uniform in [1, 32768]", "sum_lengths": int(sum(lens)),
-            "l2": "256 MB flush before each launch"}
+            "l2": "256 MB flush before each launch",
+            "back_to_back": {"us_per_call": t_seq * 1e6, "GB_s": nbytes / t_seq / 1e9,
+                             "timing": "8 calls in one CUDA graph over two copies of the caches, "
+                                       "replay timed with CUDA events"}}
 
 
 def attn_window_leg(q8d, H, Hk, D, reps, stream, flush, rank=0):
@@ -583,6 +635,8 @@ def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
     on tcgen05), L2 flushed before each timed launch; GB/s of algorithmic
     bytes (weights once, X and Y)."""
     import torch
+
+    import synth
     out = {}
     ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for m in SMALL_M:
@@ -600,15 +654,26 @@ def small_m_leg(q8d, reps, stream, flush, hbm, rank=0):
                 if rep:
                     times.append(ev[0].elapsed_time(ev[1]) / 1e3)
         t = statistics.median(times)
+        # back to back: 6 calls in one CUDA graph rotating over three copies
+        # of the weights (216 MB, beyond L2)
+        ws_ = [w] + [synth.q8_matrix_torch(rank, "smallm.w", p, n) for _ in range(2)]
+
+        def call(w_):
+            return lambda: q8d.q8d_matmul_small_m_ws(x, n, w_, y, p, m, n, p, ws, need, stream)
+        t_seq = graph_seconds_per_call([call(w_) for w_ in ws_] * 2, stream, reps)
+        del ws_
         nbytes = p * n // 32 * 34 + 4 * m * n + 4 * m * p
         out[f"m{m}"] = {"us": t * 1e6, "GB_s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / hbm,
+                        "back_to_back": {"us_per_call": t_seq * 1e6, "frac_of_peak": nbytes / t_seq / 1e9 / hbm,
+                                         "TFLOP_s": 2.0 * m * n * p / t_seq / 1e12},
                         "TFLOP_s": 2.0 * m * n * p / t / 1e12,
                         "kernel": ("q8_ximage_kernel + q8_mma_kernel (tcgen05)" if m >= 16
                                    else "q8_gemv_kernel / q8_rows_kernel"),
                         "bf16_tensor_frac_of_measured": 2.0 * m * n * p / t / 1e12 / bf16_peak()}
         del w, x, y, ws
     out["shape"] = ("3584 -> 18944 (7B gate/up), L2 flushed before each call; m >= 9 through "
-                    "q8d_matmul_small_m_ws with a preallocated workspace")
+                    "q8d_matmul_small_m_ws with a preallocated workspace; back_to_back: 6 calls "
+                    "in one CUDA graph over three copies of the weights")
     return out
 
 
