@@ -300,3 +300,56 @@ def test_matvec_mma_control_perturbed_byte(q8d):
     w2[1000, 34 * 37 + 9] ^= 0x11
     b = gpu_matvec(q8d, w2, x, n, p)
     assert a[1000] != b[1000] and np.array_equal(np.delete(a, 1000), np.delete(b, 1000))
+
+
+# ---------------------------------------------------------------------------- launch chaining
+def test_matvec_chain_without_sync(q8d, orc):
+    """Calls on one stream, each reading the previous call's output, with no
+    host synchronisation in between (the kernels are programmatic dependents
+    of the one before): every call must see its input complete.  The
+    intermediates start as NaN, so an early read would show."""
+    n1, p1, p2, p3 = 3584, 3584, 896, 3584  # tensor-core, CUDA-core, CUDA-core kernels
+    w1 = synth.q8_matrix(11, "chain.w1", p1, n1)
+    w2 = synth.q8_matrix(11, "chain.w2", p2, p1)
+    w3 = synth.q8_matrix(11, "chain.w3", p3, p2)
+    x = synth.normal_f32(11, "chain.x", n1)
+    xd, w1d, w2d, w3d = dev(x), dev(w1), dev(w2), dev(w3)
+    y1 = torch.full((p1,), float("nan"), device="cuda")
+    y2 = torch.full((p2,), float("nan"), device="cuda")
+    y3 = torch.full((p3,), float("nan"), device="cuda")
+    for _ in range(3):  # repeated: later chains overwrite live buffers
+        q8d.q8d_matvec(xd, w1d, y1, n1, p1)
+        q8d.q8d_matvec(y1, w2d, y2, p1, p2)
+        q8d.q8d_matvec(y2, w3d, y3, p2, p3)
+    torch.cuda.synchronize()
+    g1, g2, g3 = y1.cpu().numpy(), y2.cpu().numpy(), y3.cpu().numpy()
+    for w, xin, got, n, p in ((w1, x, g1, n1, p1), (w2, g1, g2, p1, p2), (w3, g2, g3, p2, p3)):
+        ref, ab = orc.q8_matvec(w, xin, n, p)
+        assert np.all(np.abs(got - ref) <= TOL * ab + 1e-30)
+
+
+def test_small_m_chain_shared_workspace(q8d, orc):
+    """Two tensor-core small-M calls back to back on one stream, sharing one
+    workspace, the second reading the first's output as its activations:
+    the second call's image kernel must wait until the first call's matmul
+    no longer reads the workspace, and must see its output complete."""
+    m, n1, p1, p2 = 16, 512, 512, 300
+    w1 = synth.q8_matrix(12, "schain.w1", p1, n1)
+    w2 = synth.q8_matrix(12, "schain.w2", p2, p1)
+    X1 = synth.normal_f32(12, "schain.X", (m, n1))
+    need = max(q8d.q8d_matmul_small_m_workspace_bytes(m, n1),
+               q8d.q8d_matmul_small_m_workspace_bytes(m, p1))
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    Y1 = torch.full((m, p1), float("nan"), device="cuda")
+    Y2 = torch.full((m, p2), float("nan"), device="cuda")
+    w1d, w2d, X1d = dev(w1), dev(w2), dev(X1)
+    for _ in range(3):
+        q8d.q8d_matmul_small_m_ws(X1d, n1, w1d, Y1, p1, m, n1, p1, ws, need)
+        q8d.q8d_matmul_small_m_ws(Y1, p1, w2d, Y2, p2, m, p1, p2, ws, need)
+    torch.cuda.synchronize()
+    G1, G2 = Y1.cpu().numpy(), Y2.cpu().numpy()
+    ref1, ab1 = orc.q8_matmul(w1, X1, n1, p1)
+    assert np.all(np.abs(G1 - ref1) <= TOL_BF16 * ab1)
+    ref2, ab2 = orc.q8_matmul(w2, G1, p1, p2)
+    assert np.all(np.abs(G2 - ref2) <= TOL_BF16 * ab2)
