@@ -102,7 +102,12 @@ int q8d_matvec(const float* x, const void* w_q8, float* out, int n, int p, void*
  *   Y[i][r] = sum_k X[i][k] * W[r][k],   i < m, r < p
  * X: device f32, row i at X + i*ldx (ldx >= n); Y: device f32, row i at
  * Y + i*ldy (ldy >= p), only the first p entries of each row are written.
- * m <= 8: f32 CUDA-core path, weights read once for all m rows, f32 accuracy.
+ * m <= 8: f32-accurate paths (within 1e-5 of sum|terms| per output): the
+ * tensor-core matvec with up to four activation rows per pass sharing every
+ * decoded weight block (exact f16 quants, activations split into f16 hi +
+ * lo, f32 accumulation) where the shape suits it (n % 256 == 0, n >= 2048,
+ * p >= 16 rows per SM, the rows' activation fragments in shared memory),
+ * else CUDA cores with the weights read once for up to four rows.
  * m >= 9 and n % 256 == 0: tensor-core path (tcgen05.mma, bf16 operands
  * from the dequantised weights and the rounded activations, f32
  * accumulation): relative accuracy ~2^-8 per product, i.e. within 1e-2 of

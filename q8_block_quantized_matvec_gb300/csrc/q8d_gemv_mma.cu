@@ -35,12 +35,16 @@ using namespace tc;
 
 constexpr int kMvMaxWarps = 16;                         // consumer warps (at most)
 constexpr int kMvThreads = (kMvMaxWarps + 1) * 32;      // + the producer warp
+// three or four activation rows: at most 12 consumer warps, so that a
+// thread may hold 128 registers (the accumulators of every row)
+__host__ __device__ constexpr int mv_max_warps(int mr) { return mr <= 2 ? kMvMaxWarps : 12; }
 constexpr int kWinSets = 4;                             // row sets per reduction window
 
 struct MvParams {
   const uint8_t* w;
-  float* y;
-  const float* x;
+  float* y;          // row i of the output at y + i * ldy
+  const float* x;    // activation row i at x + i * ldx
+  int ldx, ldy;      // (m > 1)
   int n, bpr, p;
   int row_bytes;     // bpr * 34, a multiple of 272
   int rows_per_cta;  // a multiple of 8
@@ -95,17 +99,21 @@ __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint
   return issued;
 }
 
-__global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvParams P) {
+// MR activation rows (1..4) against the same weights: each decoded weight
+// fragment feeds MR MMAs (one per row's x fragments), so the weight decode
+// and the weight stream are shared by the rows.
+template <int MR>
+__global__ void __launch_bounds__((mv_max_warps(MR) + 1) * 32, 1) q8_gemv_mma_kernel(const MvParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = P.W;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P.stage_bytes * P.nstages);
   uint64_t* empty = full + P.nstages;
-  uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);
-  uint8_t* zpad = xf + (size_t)P.bpr * kXfBlock;                 // kZeroPad zero bytes
-  float* xinv = reinterpret_cast<float*>(zpad + kZeroPad);       // [bpr] inverse block scales
-  float* part = xinv + P.bpr;                                    // [2][kWinSets*8][W]
+  uint8_t* xf = reinterpret_cast<uint8_t*>(empty + P.nstages);   // [MR][bpr] x fragments
+  uint8_t* zpad = xf + (size_t)MR * P.bpr * kXfBlock;            // kZeroPad zero bytes
+  float* xinv = reinterpret_cast<float*>(zpad + kZeroPad);       // [MR][bpr] inverse block scales
+  float* part = xinv + MR * P.bpr;                               // [MR][2][kWinSets*8][W]
   const int v0 = blockIdx.x * P.rows_per_cta;
   const int v1 = min(P.p, v0 + P.rows_per_cta);
   // Launched as a programmatic dependent: the next kernel may start its
@@ -141,15 +149,19 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
     // ---- x fragments, one pass: up to kXItems (block, word) items a
     // thread per round, all loads issued before the first use (one round
     // for rows of up to kXItems * 480 / 8 blocks) ----
+    // (items of all MR rows in one pass: item it is word it % nit of row
+    // it / nit; a row's items are whole blocks, so the 8 lanes of a block
+    // stay in one row)
     constexpr int kXItems = 12;
-    const int nit = P.bpr * 8;
-    for (int it0 = 0; it0 < nit; it0 += kXItems * nct) {
+    const int nit = P.bpr * 8, nall = MR * nit;
+    for (int it0 = 0; it0 < nall; it0 += kXItems * nct) {
       float v[kXItems][4];
 #pragma unroll
       for (int k = 0; k < kXItems; ++k) {
         const int it = it0 + k * nct + threadIdx.x;
-        if (it < nit) {
-          load_word<1>(P.x, it >> 3, it & 7, v[k]);
+        if (it < nall) {
+          const int r = it / nit, ii = it - r * nit;
+          load_word<1>(P.x + (long long)r * P.ldx, ii >> 3, ii & 7, v[k]);
         } else {
           v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.f;
         }
@@ -157,8 +169,9 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
 #pragma unroll
       for (int k = 0; k < kXItems; ++k) {
         const int it = it0 + k * nct + threadIdx.x;
-        if (it0 + k * nct >= nit) break;  // (uniform over the warps)
-        build_x_word(it, it < nit, v[k], xf, xinv);
+        if (it0 + k * nct >= nall) break;  // (uniform over the warps)
+        const int r = min(it / nit, MR - 1), ii = it - r * nit;
+        build_x_word(ii, it < nall, v[k], xf + (size_t)r * P.bpr * kXfBlock, xinv + r * P.bpr);
       }
     }
     for (int i = threadIdx.x; i < kZeroPad / 4; i += nct) reinterpret_cast<uint32_t*>(zpad)[i] = 0u;
@@ -180,19 +193,28 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
     int s = 0;
     uint32_t ph = 0;
     int set = 0, buf = 0;
+    const uint32_t xf_row = (uint32_t)bpr * kXfBlock, xi_row = 4u * (uint32_t)bpr;
     for (int r0 = v0; r0 < v1; r0 += kSetRows * T) {
-      float yacc[2] = {0.f, 0.f};  // this thread's row gq of the tile's sets
+      float yacc[2][MR];  // this thread's row gq of the tile's sets, per activation row
+#pragma unroll
+      for (int r = 0; r < MR; ++r) yacc[0][r] = yacc[1][r] = 0.f;
       for (int sl = 0; sl < nslices; ++sl) {
         ok = wait_or_abort(&full[s], ph, &s_abort) && ok;
         const uint32_t row32 = after_wait(smem32 + stage_b * (uint32_t)s + rowoff);
         const int c0 = sl * S;
         const int pairs = min(S, bpr - c0) / 8;
         for (int k = warp; k < pairs; k += W) {
-          const uint32_t xb = XL.match ? xf32 + (uint32_t)((c0 / 8 + k) * kXfPair) + XL.off : z32;
-          const uint32_t xi = xi32 + 4u * (uint32_t)(c0 + 8 * k);
+          const uint32_t xb0 = XL.match ? xf32 + (uint32_t)((c0 / 8 + k) * kXfPair) + XL.off : z32;
+          const uint32_t xi0 = xi32 + 4u * (uint32_t)(c0 + 8 * k);
+          uint32_t xb[MR], xi[MR];
+#pragma unroll
+          for (int r = 0; r < MR; ++r) {
+            xb[r] = XL.match ? xb0 + (uint32_t)r * xf_row : z32;
+            xi[r] = xi0 + (uint32_t)r * xi_row;
+          }
           const uint32_t rb = row32 + 272u * (uint32_t)k;
-          yacc[0] += pair_dot(rb, xb, XL.step, LO, lo_half, xi);
-          if (T == 2) yacc[1] += pair_dot(rb + set_b, xb, XL.step, LO, lo_half, xi);
+          pair_dot_m<MR>(rb, xb, XL.step, LO, lo_half, xi, yacc[0]);
+          if (T == 2) pair_dot_m<MR>(rb + set_b, xb, XL.step, LO, lo_half, xi, yacc[1]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -206,22 +228,26 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
       for (int t = 0; t < 2; ++t) {
         if (t >= T || r0 + kSetRows * t >= v1) break;
         const int rs0 = r0 + kSetRows * t;
-        float y = yacc[t];
-        y += __shfl_xor_sync(0xffffffffu, y, 1);
-        y += __shfl_xor_sync(0xffffffffu, y, 2);
         const int slot = set % kWinSets;
-        if (cq == 0) part[((buf * kWinSets + slot) * kSetRows + gq) * W + warp] = y;
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+          float y = yacc[t][r];
+          y += __shfl_xor_sync(0xffffffffu, y, 1);
+          y += __shfl_xor_sync(0xffffffffu, y, 2);
+          if (cq == 0) part[(((r * 2 + buf) * kWinSets + slot) * kSetRows + gq) * W + warp] = y;
+        }
         if (slot == kWinSets - 1 || rs0 + kSetRows >= v1) {
           consumer_sync(nct);
           // window reduction: rows of the window's sets, warp partials in order
           const int wr0 = rs0 - slot * kSetRows;
-          for (int i = threadIdx.x; i < (slot + 1) * kSetRows; i += nct) {
-            const int row = wr0 + i;
+          for (int i = threadIdx.x; i < MR * (slot + 1) * kSetRows; i += nct) {
+            const int r = i / ((slot + 1) * kSetRows), ii = i % ((slot + 1) * kSetRows);
+            const int row = wr0 + ii;
             if (row < v1) {
-              const float* pr = part + ((size_t)buf * kWinSets * kSetRows + i) * W;
+              const float* pr = part + (((size_t)(r * 2 + buf) * kWinSets) * kSetRows + ii) * W;
               float sum = 0.f;
               for (int w = 0; w < W; ++w) sum += pr[w];
-              P.y[row] = sum;
+              P.y[(long long)r * P.ldy + row] = sum;
             }
           }
           buf ^= 1;
@@ -241,12 +267,13 @@ __global__ void __launch_bounds__(kMvThreads, 1) q8_gemv_mma_kernel(const MvPara
 
 }  // namespace
 
-// Plans and launches the tensor-core matvec.  Q8D_EUNSUPPORTED when the
-// shape does not suit it (one matrix, n % 256 == 0 and n >= 2048, enough
-// rows to give every SM two 8-row sets); the caller then runs the
-// CUDA-core kernel.
+// Plans and launches the tensor-core matvec for R.m (1..4) activation rows.
+// Q8D_EUNSUPPORTED when the shape does not suit it (one matrix, n % 256 ==
+// 0 and n >= 2048, enough rows to give every SM two 8-row sets, the rows'
+// x fragments and three stages within shared memory); the caller then runs
+// a CUDA-core kernel.
 int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid_out) {
-  if (R.m != 1 || R.nseg != 1 || R.bpr % 8 || R.bpr < 64) return Q8D_EUNSUPPORTED;
+  if (R.m < 1 || R.m > 4 || R.nseg != 1 || R.bpr % 8 || R.bpr < 64) return Q8D_EUNSUPPORTED;
   const int sms = sm_count();
   const long long p = R.seg[0].p;
   if (p < 2LL * kSetRows * sms || p > 0x7fffffffLL) return Q8D_EUNSUPPORTED;
@@ -254,6 +281,8 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   P.w = R.seg[0].w;
   P.y = R.seg[0].y;
   P.x = R.X;
+  P.ldx = R.ldx;
+  P.ldy = R.ldy;
   P.n = R.n;
   P.bpr = R.bpr;
   P.p = (int)p;
@@ -280,9 +309,10 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   // consumer warps: the count in [8, 16] that splits a slice's unit pairs
   // (8 blocks of 8 rows) most evenly
   const int U = P.S / 8;
-  int bestW = kMvMaxWarps;
+  const int maxW = mv_max_warps(R.m);
+  int bestW = maxW;
   double best = 0.0;
-  for (int w = kMvMaxWarps; w >= 8; --w) {
+  for (int w = maxW; w >= 8; --w) {
     const double eff = (double)U / (w * ((U + w - 1) / w));
     if (eff > best + 1e-9) {
       best = eff;
@@ -290,8 +320,9 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
     }
   }
   P.W = bestW;
-  const long long fixed =
-      (long long)P.bpr * (kXfBlock + 4) + kZeroPad + 2LL * kWinSets * kSetRows * P.W * 4;
+  const int MR = R.m;
+  const long long fixed = (long long)MR * P.bpr * (kXfBlock + 4) + kZeroPad +
+                          2LL * MR * kWinSets * kSetRows * P.W * 4;
   const long long budget = 220 * 1024;
   // two row sets per tile (each warp's per-tile work twice as long) when
   // three such stages fit
@@ -305,10 +336,14 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   const long long sets_cta = (sets + sms - 1) / sms;
   P.rows_per_cta = (int)(sets_cta * kSetRows);  // (a CTA's last tile may hold one set)
   const int grid = (int)((p + P.rows_per_cta - 1) / P.rows_per_cta);
-  const int rc = configure_kernel(reinterpret_cast<const void*>(q8_gemv_mma_kernel), 220 * 1024, true);
+  auto fn = MR == 1 ? q8_gemv_mma_kernel<1>
+          : MR == 2 ? q8_gemv_mma_kernel<2>
+          : MR == 3 ? q8_gemv_mma_kernel<3>
+                    : q8_gemv_mma_kernel<4>;
+  const int rc = configure_kernel(reinterpret_cast<const void*>(fn), 220 * 1024, true);
   if (rc) return rc;
   if (grid_out) *grid_out = grid;
-  return launch_ex(q8_gemv_mma_kernel, dim3(grid), dim3((P.W + 1) * 32), (size_t)smem, stream, true, P);
+  return launch_ex(fn, dim3(grid), dim3((P.W + 1) * 32), (size_t)smem, stream, true, P);
 }
 
 }  // namespace q8d

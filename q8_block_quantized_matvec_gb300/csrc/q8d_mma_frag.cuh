@@ -270,6 +270,55 @@ __device__ __forceinline__ float pair_dot(uint32_t rb, uint32_t xb, uint32_t xst
   return fmaf(se, pe, so * po);
 }
 
+// pair_dot for MR activation rows sharing every decoded A fragment: xb[r]
+// and xi[r] are row r's fragment address and inverse-scale entry (as for
+// pair_dot); the weight decode is done once, each row adds two fragment
+// loads and two MMAs per step.  y[r] += row r's scaled sum.
+template <int MR>
+__device__ __forceinline__ void pair_dot_m(uint32_t rb, const uint32_t (&xb)[MR], uint32_t xstep,
+                                           const LaneOffs& L, bool lo_half,
+                                           const uint32_t (&xi)[MR], float (&y)[MR]) {
+  float ae[MR][4], ao[MR][4];
+#pragma unroll
+  for (int r = 0; r < MR; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ae[r][k] = ao[r][k] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t we0, we1;
+    if (i < 3) {
+      we0 = lds32a(rb + L.e0 + 8 * i);
+      we1 = lds32a(rb + L.e1 + 8 * i);
+    } else {
+      we0 = __byte_perm(lds32a(rb + L.e3a), lds32a(rb + L.e3b), L.sel3);
+      we1 = __byte_perm(lds32a(rb + L.e3a + 68), lds32a(rb + L.e3b + 68), L.sel3);
+    }
+    const uint32_t wo0 = lds32a(rb + L.o0 + 8 * i), wo1 = lds32a(rb + L.o1 + 8 * i);
+    uint32_t a0, a1, a2, a3;
+    quant_pairs(we0, a0, a2);
+    quant_pairs(we1, a1, a3);
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+      const uint2 be = lds64a(xb[r] + 128 * i);
+      mma_f16(ae[r], a0, a1, a2, a3, be.x, be.y);
+    }
+    quant_pairs(wo0, a0, a2);
+    quant_pairs(wo1, a1, a3);
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+      const uint2 bo = lds64a(xb[r] + xstep + 128 * i);
+      mma_f16(ao[r], a0, a1, a2, a3, bo.x, bo.y);
+    }
+  }
+  const float we = unit_scale(rb, L, false), wo = unit_scale(rb, L, true);
+#pragma unroll
+  for (int r = 0; r < MR; ++r) {
+    const float pe = lo_half ? ae[r][0] + ae[r][1] : ae[r][2] + ae[r][3];
+    const float po = lo_half ? ao[r][0] + ao[r][1] : ao[r][2] + ao[r][3];
+    y[r] += fmaf(we * lds32f(xi[r]), pe, wo * lds32f(xi[r] + 4u) * po);
+  }
+}
+
 // Bank-spread row groups of an 8-row set (rows of a whole number of 8-block
 // pairs, m = pairs a row): a 272-byte pair column is 68 words, so row gq's
 // words sit 4 * (m * gq mod 8) banks after row 0's, and rows whose m * gq

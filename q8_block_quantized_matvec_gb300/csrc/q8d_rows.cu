@@ -354,6 +354,19 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
     if (rc != Q8D_EUNSUPPORTED) return rc;
     rc = gemv_plan_and_launch(P, stream, grid_out);
     if (rc != Q8D_EUNSUPPORTED) return rc;
+  } else if (P.m <= 8 && P.nseg == 1) {
+    // up to four activation rows per launch of the tensor-core matvec (each
+    // decoded weight block shared by the rows' MMAs), if the shape suits it
+    RowsParams Q = P;
+    Q.m = std::min(4, P.m);
+    int rc = gemv_mma_plan_and_launch(Q, stream, grid_out);
+    if (rc != Q8D_EUNSUPPORTED) {
+      if (rc || P.m <= 4) return rc;
+      Q.m = P.m - 4;
+      Q.X = P.X + 4LL * P.ldx;
+      Q.seg[0].y = P.seg[0].y + 4LL * P.ldy;
+      return gemv_mma_plan_and_launch(Q, stream, grid_out);
+    }
   }
 
   // Several activation vectors (or a row too long for the matvec kernel):

@@ -151,6 +151,19 @@ def test_small_m_f32_parity(q8d, orc, m, n, p):
     assert np.all(np.abs(got - ref) <= TOL * ab)
 
 
+@pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
+def test_small_m_matvec_rows_tensor(q8d, orc, m):
+    """2 <= m <= 8 on the tensor-core matvec (up to four activation rows per
+    launch sharing each decoded weight block; m > 4 in two launches): the
+    f32 bar, a ragged row count and padded strides."""
+    n, p = 2048, 2500
+    w = synth.q8_matrix(13, f"mr.w{n}", p, n)
+    X = synth.normal_f32(13, f"mr.X{n}.{m}", (m, n))
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    got = gpu_small_m(q8d, w, X, n, p, ldx=n + 4, ldy=p + 3)
+    assert np.all(np.abs(got - ref) <= TOL * ab)
+
+
 @pytest.mark.parametrize("m", [9, 16, 64])
 @pytest.mark.parametrize("n,p", [(3584, 512), (256, 384), (18944, 128)])
 def test_small_m_tensor_parity(q8d, orc, m, n, p):
