@@ -35,9 +35,12 @@ using namespace tc;
 
 constexpr int kMvMaxWarps = 16;                         // consumer warps (at most)
 constexpr int kMvThreads = (kMvMaxWarps + 1) * 32;      // + the producer warp
-// three or four activation rows: at most 12 consumer warps, so that a
-// thread may hold 128 registers (the accumulators of every row)
-__host__ __device__ constexpr int mv_max_warps(int mr) { return mr <= 2 ? kMvMaxWarps : 12; }
+// more activation rows, fewer consumer warps, so that a thread may hold the
+// accumulators of every row: 128 registers for three or four rows, ~168
+// for five to eight
+__host__ __device__ constexpr int mv_max_warps(int mr) {
+  return mr <= 2 ? kMvMaxWarps : mr <= 4 ? 12 : 11;
+}
 constexpr int kWinSets = 4;                             // row sets per reduction window
 
 struct MvParams {
@@ -99,7 +102,7 @@ __device__ int mv_produce(const MvParams& P, uint8_t* smem, uint64_t* full, uint
   return issued;
 }
 
-// MR activation rows (1..4) against the same weights: each decoded weight
+// MR activation rows (1..8) against the same weights: each decoded weight
 // fragment feeds MR MMAs (one per row's x fragments), so the weight decode
 // and the weight stream are shared by the rows.
 template <int MR>
@@ -267,13 +270,13 @@ __global__ void __launch_bounds__((mv_max_warps(MR) + 1) * 32, 1) q8_gemv_mma_ke
 
 }  // namespace
 
-// Plans and launches the tensor-core matvec for R.m (1..4) activation rows.
+// Plans and launches the tensor-core matvec for R.m (1..8) activation rows.
 // Q8D_EUNSUPPORTED when the shape does not suit it (one matrix, n % 256 ==
 // 0 and n >= 2048, enough rows to give every SM two 8-row sets, the rows'
 // x fragments and three stages within shared memory); the caller then runs
 // a CUDA-core kernel.
 int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid_out) {
-  if (R.m < 1 || R.m > 4 || R.nseg != 1 || R.bpr % 8 || R.bpr < 64) return Q8D_EUNSUPPORTED;
+  if (R.m < 1 || R.m > 8 || R.nseg != 1 || R.bpr % 8 || R.bpr < 64) return Q8D_EUNSUPPORTED;
   const int sms = sm_count();
   const long long p = R.seg[0].p;
   if (p < 2LL * kSetRows * sms || p > 0x7fffffffLL) return Q8D_EUNSUPPORTED;
@@ -336,10 +339,11 @@ int gemv_mma_plan_and_launch(const RowsParams& R, cudaStream_t stream, int* grid
   const long long sets_cta = (sets + sms - 1) / sms;
   P.rows_per_cta = (int)(sets_cta * kSetRows);  // (a CTA's last tile may hold one set)
   const int grid = (int)((p + P.rows_per_cta - 1) / P.rows_per_cta);
-  auto fn = MR == 1 ? q8_gemv_mma_kernel<1>
-          : MR == 2 ? q8_gemv_mma_kernel<2>
-          : MR == 3 ? q8_gemv_mma_kernel<3>
-                    : q8_gemv_mma_kernel<4>;
+  void (*const kFns[8])(MvParams) = {q8_gemv_mma_kernel<1>, q8_gemv_mma_kernel<2>,
+                                     q8_gemv_mma_kernel<3>, q8_gemv_mma_kernel<4>,
+                                     q8_gemv_mma_kernel<5>, q8_gemv_mma_kernel<6>,
+                                     q8_gemv_mma_kernel<7>, q8_gemv_mma_kernel<8>};
+  const auto fn = kFns[MR - 1];
   const int rc = configure_kernel(reinterpret_cast<const void*>(fn), 220 * 1024, true);
   if (rc) return rc;
   if (grid_out) *grid_out = grid;

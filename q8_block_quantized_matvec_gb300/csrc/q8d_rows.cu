@@ -355,17 +355,22 @@ int rows_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
     rc = gemv_plan_and_launch(P, stream, grid_out);
     if (rc != Q8D_EUNSUPPORTED) return rc;
   } else if (P.m <= 8 && P.nseg == 1) {
-    // up to four activation rows per launch of the tensor-core matvec (each
-    // decoded weight block shared by the rows' MMAs), if the shape suits it
-    RowsParams Q = P;
-    Q.m = std::min(4, P.m);
-    int rc = gemv_mma_plan_and_launch(Q, stream, grid_out);
-    if (rc != Q8D_EUNSUPPORTED) {
-      if (rc || P.m <= 4) return rc;
-      Q.m = P.m - 4;
-      Q.X = P.X + 4LL * P.ldx;
-      Q.seg[0].y = P.seg[0].y + 4LL * P.ldy;
-      return gemv_mma_plan_and_launch(Q, stream, grid_out);
+    // the activation rows in one launch of the tensor-core matvec (each
+    // decoded weight block shared by the rows' MMAs) if the shape and the
+    // rows' fragments suit it, else in two launches of up to four rows
+    int rc = gemv_mma_plan_and_launch(P, stream, grid_out);
+    if (rc != Q8D_EUNSUPPORTED) return rc;
+    if (P.m > 4) {
+      RowsParams Q = P;
+      Q.m = 4;
+      rc = gemv_mma_plan_and_launch(Q, stream, grid_out);
+      if (rc != Q8D_EUNSUPPORTED) {
+        if (rc) return rc;
+        Q.m = P.m - 4;
+        Q.X = P.X + 4LL * P.ldx;
+        Q.seg[0].y = P.seg[0].y + 4LL * P.ldy;
+        return gemv_mma_plan_and_launch(Q, stream, grid_out);
+      }
     }
   }
 
