@@ -108,11 +108,14 @@ int q8d_matvec(const float* x, const void* w_q8, float* out, int n, int p, void*
  * lo, f32 accumulation) where the shape suits it (n % 256 == 0, n >= 2048,
  * p >= 16 rows per SM, the rows' activation fragments in shared memory),
  * else CUDA cores with the weights read once for up to four rows.
- * m >= 9 and n % 256 == 0: tensor-core path (tcgen05.mma, bf16 operands
- * from the dequantised weights and the rounded activations, f32
- * accumulation): relative accuracy ~2^-8 per product, i.e. within 1e-2 of
- * sum|terms| per output.  It first writes the activations, rounded to bf16,
- * into a workspace laid out as the MMA's B operand
+ * m >= 9 and n % 256 == 0: tensor-core path (tcgen05.mma, f16 operands:
+ * the weights as f16 of scale * q, rounded once; the activations as f16
+ * under a power-of-two scale per row, rounded once; f32 accumulation):
+ * relative accuracy ~2^-11 per product, i.e. within 2e-3 of sum|terms|
+ * per output (plus 2^-25 * sum|x| where scale * q is below 2^-14).  Block
+ * scales above 511.75 (scale * q beyond f16) make the outputs of their
+ * 128-row tile NaN.  It first writes the activations, rounded to f16, into
+ * a workspace laid out as the MMA's B operand, with the rows' scales
  * (q8d_matmul_small_m_workspace_bytes(m, n) bytes); this entry point takes
  * that workspace from the stream's memory pool (cudaMallocAsync) and frees
  * it stream-ordered behind the kernels; q8d_matmul_small_m_ws uses the
@@ -125,8 +128,9 @@ int q8d_matmul_small_m(const float* X, int ldx, const void* w_q8, float* Y, int 
                        int n, int p, void* stream);
 
 /* Bytes of the workspace q8d_matmul_small_m_ws needs for m activation rows of
- * n elements: 2 * n * (m rounded up to 16 per block of 128 rows) when the
- * tensor-core path takes the shape (9 <= m <= 256, n % 256 == 0), else 0. */
+ * n elements: 2 * n * (m rounded up to 16 per block of 128 rows) + 16 *
+ * ceil(m / 4) when the tensor-core path takes the shape (9 <= m <= 256,
+ * n % 256 == 0), else 0. */
 size_t q8d_matmul_small_m_workspace_bytes(int m, int n);
 
 /* q8d_matmul_small_m with a caller-owned workspace: device memory of at

@@ -7,12 +7,14 @@
 // more than one token is in flight stages dequantised weights in on-chip
 // memory; here the tile feeds tcgen05.mma instead of SIMD-group matrices).
 //
-//  * The activations are rounded to bf16 once per call by a small kernel
-//    (q8_ximage_kernel) into a workspace that holds, for every 128-row block
-//    of X and every 128-element K half, the B operand exactly as the MMA
-//    reads it from shared memory (canonical K-major 128-byte-swizzled
-//    layout); the main kernel starts as its programmatic dependent and
-//    copies one half's B tile with a single 1-D bulk copy.
+//  * The activations are rounded to f16 once per call by a small kernel
+//    (q8_ximage_kernel, one CTA per activation row) under a power-of-two
+//    scale per row (its max |x| into [2^14, 2^15), undone on the result)
+//    into a workspace that holds, for every 128-row block of X and every
+//    128-element K half, the B operand exactly as the MMA reads it from
+//    shared memory (canonical K-major 128-byte-swizzled layout); the main
+//    kernel starts as its programmatic dependent and copies a chunk's B
+//    tile with a single 1-D bulk copy.
 //  * CTA = 128 weight rows (the MMA's M) x a K range; a thread-block cluster
 //    of `ksplit` CTAs along K shares one output tile and reduces the fp32
 //    partials through distributed shared memory in rank order
@@ -27,20 +29,25 @@
 //    operand in tensor memory (TMEM): warp w owns TMEM lanes 32 (w % 4) +
 //    [0, 32) = weight rows and blocks w / 4 and w / 4 + 4 of the chunk; a
 //    thread reads a block with three conflict-free 16-byte shared loads,
-//    computes scale * q exactly in f32, rounds once to bf16 and writes the
-//    block's 16 columns with one tcgen05.st.  A ring of two or three slots,
+//    turns the quants into exact f16 pairs (one byte permute and one
+//    sub.f16x2 a pair), multiplies them by the block's f16 scale (one
+//    mul.f16x2: the exact product rounded once) and writes the block's 16
+//    columns with one tcgen05.st.  A ring of two or three slots,
 //    each a chunk's A tile (128 TMEM columns) and B tile (shared memory)
 //    with one "full" mbarrier (16 warp arrivals + the B copy's bytes) and
 //    one "empty" mbarrier; one MMA warp issues
 //    tcgen05.mma.cta_group::1.kind::f16 with A from TMEM and B from shared
-//    memory (bf16 x bf16 -> f32, M = 128, N = m rounded up to 16, K = 16 per
+//    memory (f16 x f16 -> f32, M = 128, N = m rounded up to 16, K = 16 per
 //    instruction: ~93 cycles each on this part whatever N <= 128, so the 16
 //    of a chunk bound the loop) and commits to the slot's "empty"
 //    barrier.  The accumulator (TMEM columns [0, N)) is read with
 //    tcgen05.ld and stored to Y directly, or, for a K split, reduced across
 //    the cluster through distributed shared memory.
-// Accuracy: one bf16 rounding of each weight and activation, f32
-// accumulation: |error| <= ~2^-8 * sum|terms| per output.
+// Accuracy: one f16 rounding of each weight (scale * q) and activation
+// (x * 2^e), f32 accumulation: |error| <= ~2^-10 * sum|terms| per output
+// (plus 2^-25 * sum|x| where scale * q falls below f16's normal range).  A
+// block scale above 511.75 could make scale * q overflow f16: the kernel
+// checks every scale and then writes NaN for its row tile.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
 #include <cuda_bf16.h>
 
@@ -71,13 +78,12 @@ constexpr int kMmaWarp = kDeqWarps + 2;         // MMA issuer warp
 constexpr int kThreads = kDeqThreads + 96;
 constexpr int kM = 128;                         // weight rows per CTA (MMA M)
 constexpr int kKC = 256;                        // K elements per raw chunk (one tensor copy)
-constexpr int kHalfK = 128;                     // K elements per A/B tile (half a chunk)
 constexpr int kRawRow = (kKC / kQBlock) * kQBlockBytes;  // 272 bytes
 constexpr int kRawStage = kM * kRawRow;         // 34816 bytes
 constexpr int kACols = kKC / 2;                 // TMEM columns of a chunk's A tile (two bf16 a column)
-constexpr int kAColBase = 128;                  // first TMEM column of the A tiles
+constexpr int kAColBase = 128;                  // first TMEM column of the A slots
 constexpr int kMaxN = 128;
-constexpr int kMaxStages = 3;                   // A|B slots: TMEM columns kAColBase + 3 * 128 <= 512
+constexpr int kMaxStages = 3;                   // A|B slots: TMEM columns 128 + 3 * 128 <= 512
 constexpr int kSmemLimit = 224 * 1024;
 constexpr int kSmemFixed = 1024 + 256;                // alignment slack, barriers
 constexpr int kMaxRawStages = 4;
@@ -85,9 +91,10 @@ constexpr int kMaxRawStages = 4;
 struct MmaParams {
   CUtensorMap wmap;      // the weights as [p][row_bytes / 4] 32-bit elements, box [128][68]
   const uint8_t* ximg;   // B operand image of this launch's activation rows
+  const float* xinv;     // their inverse power-of-two scales
   float* Y;
   int ldy;
-  int m, p, npad;
+  int m, p, npad;        // npad = m rounded up to 16: B rows = accumulator columns
   int nchunks, ksplit, raw_stages, stages;
 };
 
@@ -182,22 +189,23 @@ __device__ __forceinline__ float ld_peer(uint32_t local_saddr, uint32_t rank) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
-// Block BLK (0..7) of a 272-byte raw row chunk as 32 bf16 of scale * q (two
-// a word, lower K first), each computed exactly in f32 and rounded once.
-// v = the 48 bytes from byte 32 * BLK of the row (16-byte aligned), so the
-// block's f16 scale is at byte 2 * BLK of v and its quants follow.
+// Block BLK (0..7) of a 272-byte raw row chunk as 32 f16 of scale * q (two
+// a word, lower K first): the quants as exact f16 pairs (the sign-flipped
+// byte under the exponent byte 0x64 is 1152 + q; one sub.f16x2 removes the
+// 1152), times the block's f16 scale with one mul.f16x2 (the exact product
+// rounded once).  v = the 48 bytes from byte 32 * BLK of the row, the
+// block's scale at byte 2 * BLK of v.  range_ok: |scale| <= 511.75, so
+// that |q * scale| <= 65504 (else the call's outputs become NaN).
 template <int BLK>
-__device__ __forceinline__ void decode_block(const uint32_t (&v)[12], uint32_t (&pk)[16]) {
+__device__ __forceinline__ void decode_block_f16(const uint32_t (&v)[12], uint32_t (&pk)[16],
+                                                 bool& range_ok) {
   constexpr int kScaleWord = BLK >> 1, kScaleShift = (BLK & 1) * 16;
   constexpr int kQWord = (BLK + 1) >> 1;  // odd BLK: quants word-aligned; even: from byte 2
-  const float sc = f16_bits_to_f32(v[kScaleWord] >> kScaleShift);
-  const uint64_t sc2 = pack2(sc, sc);
-  const uint64_t bias2 = pack2(-kMagicBias, -kMagicBias);
+  const uint32_t sb = (v[kScaleWord] >> kScaleShift) & 0xFFFFu;
+  range_ok = range_ok && (sb & 0x7FFFu) <= 0x5FFFu;
+  const uint32_t sc2 = sb | (sb << 16);
+  const uint32_t bias = 0x64806480u;  // (1152, 1152)
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     uint32_t w;
@@ -206,17 +214,14 @@ __device__ __forceinline__ void decode_block(const uint32_t (&v)[12], uint32_t (
     else
       w = __funnelshift_r(v[kQWord + k], v[kQWord + k + 1], 16);
     w ^= 0x80808080u;
-    const uint64_t q01 =
-        mul2(add2(pack2(magic_byte(w, magic_sel(0)), magic_byte(w, magic_sel(1))), bias2), sc2);
-    const uint64_t q23 =
-        mul2(add2(pack2(magic_byte(w, magic_sel(2)), magic_byte(w, magic_sel(3))), bias2), sc2);
-    float f0, f1, f2, f3;
-    unpack2(q01, f0, f1);
-    unpack2(q23, f2, f3);
-    pk[2 * k] = bf16x2(f0, f1);
-    pk[2 * k + 1] = bf16x2(f2, f3);
+    uint32_t a = __byte_perm(w, 0x64646464u, 0x5140), b = __byte_perm(w, 0x64646464u, 0x7362);
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(bias));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(b) : "r"(b), "r"(bias));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(pk[2 * k]) : "r"(a), "r"(sc2));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(pk[2 * k + 1]) : "r"(b), "r"(sc2));
   }
 }
+
 
 // 2-D tensor copy of the box at element (x, y) of the map into shared memory.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -228,36 +233,64 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Rows of the B operand of a 128-row block of mb activation rows: mb
+// rounded up to 16 (zero rows past mb).
+__host__ __device__ __forceinline__ int ximage_mp(int mb) { return (mb + 15) / 16 * 16; }
+
 // The B operand image of the activations: for every 128-row block rb of X
-// (npad = its rows rounded up to 16) and every 128-element K half kh, the
-// bytes [2 atoms][npad rows][128 B] at rb * 256 * n + kh * npad * 256, row r
-// of an atom holding K elements 64 * atom + [0, 64) of X row 128 * rb + r as
-// bf16 (rows past m zero), its 16-byte chunk c at position c ^ (r & 7).
-// One thread per 16-byte chunk.
+// (mb rows, mp = ximage_mp(mb)) and every 128-element K half kh, the bytes
+// [2 atoms][mp rows][128 B] at the block's base + kh * mp * 256, row r of an
+// atom holding K elements 64 * atom + [0, 64) of activation row r as f16 of
+// x * 2^e_r (rounded once; e_r puts the row's max |x| into [2^14, 2^15)),
+// its 16-byte chunk c at position c ^ (r & 7) (canonical K-major 128-byte
+// swizzle); inv[r] = 2^-e_r.  One CTA per activation row (grid = m), which
+// also writes its share of the block's zero rows.
 __global__ void __launch_bounds__(256) q8_ximage_kernel(const float* __restrict__ X, int ldx, int m,
-                                                         int n, long long total,
-                                                         uint8_t* __restrict__ img) {
+                                                         int n, uint8_t* __restrict__ img,
+                                                         float* __restrict__ inv) {
   griddep_wait();               // X (and the workspace's last readers) are done
   griddep_launch_dependents();  // the matmul kernel may start its prologue
-  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
-  if (e >= total) return;
-  const long long per_block = 16LL * n;  // chunks of a full 128-row block
-  const int rb = (int)(e / per_block);
-  const long long rem = e - rb * per_block;
-  const int npad = min(kMaxN, (m - rb * kMaxN + 15) / 16 * 16);
-  const int kh = (int)(rem / (npad * 16));
-  const int r = (int)((rem / 16) % npad), c = (int)(rem % 16);
-  const int row = rb * kMaxN + r;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (row < m) {
-    const float4* xp =
-        reinterpret_cast<const float4*>(X + (long long)row * ldx + (long long)kh * kHalfK + c * 8);
-    const float4 a = __ldg(xp), b = __ldg(xp + 1);
-    v = make_uint4(bf16x2(a.x, a.y), bf16x2(a.z, a.w), bf16x2(b.x, b.y), bf16x2(b.z, b.w));
+  __shared__ float s_max[8];
+  const int i = blockIdx.x, tid = threadIdx.x;
+  const float* xr = X + (long long)i * ldx;
+  // max |x| of the row (n % 256 == 0: whole float4s)
+  float mx = 0.f;
+  for (int k = 4 * tid; k < n; k += 1024) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
   }
-  uint8_t* dst = img + (long long)rb * 256 * n + (long long)kh * npad * 256 + (c >> 3) * npad * 128 +
-                 (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
-  *reinterpret_cast<uint4*>(dst) = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) s_max[tid >> 5] = mx;
+  __syncthreads();
+  mx = s_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
+  int ex = 0;
+  if (mx > 0.f) frexpf(mx, &ex);
+  const int e = mx > 0.f ? min(125, 15 - ex) : 0;  // (e >= -113 for any finite max)
+  const float sc = __int_as_float((127 + e) << 23);
+  if (tid == 0) inv[i] = __int_as_float((127 - e) << 23);
+  const int rb = i / kMaxN, r = i % kMaxN;
+  const int mb = min(kMaxN, m - rb * kMaxN), mp = ximage_mp(mb);
+  uint8_t* base = img + (long long)rb * 256 * n;  // (full blocks before it: 128 rows)
+  auto at = [&](int row, int kh, int c) {  // 16-byte chunk c (of 16) of image row `row`, half kh
+    return base + (long long)kh * mp * 256 + (c >> 3) * mp * 128 + (row >> 3) * 1024 +
+           (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+  };
+  for (int q = tid; q < n / 8; q += 256) {  // 8 elements a chunk
+    const float4 a = __ldg(reinterpret_cast<const float4*>(xr + 8 * q));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(xr + 8 * q + 4));
+    const __half2 h0 = __floats2half2_rn(a.x * sc, a.y * sc), h1 = __floats2half2_rn(a.z * sc, a.w * sc);
+    const __half2 h2 = __floats2half2_rn(b.x * sc, b.y * sc), h3 = __floats2half2_rn(b.z * sc, b.w * sc);
+    const uint4 v = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                               *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+    const int kh = q / 16, c = q % 16;
+    *reinterpret_cast<uint4*>(at(r, kh, c)) = v;
+    // zero rows mb .. mp - 1: this row takes every mb-th
+    for (int zr = mb + r; zr < mp; zr += mb)
+      *reinterpret_cast<uint4*>(at(zr, kh, c)) = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_constant__ MmaParams P) {
@@ -277,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   uint64_t* empty = full + S;                 // [S]: their MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + S);
   __shared__ int s_abort;
+  __shared__ float s_ok;  // 1 if this CTA's partials are good (read by its cluster peers)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -284,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   const int c_begin = (int)((long long)rank * P.nchunks / P.ksplit);
   const int c_end = (int)((long long)(rank + 1) * P.nchunks / P.ksplit);
   const int nloc = c_end - c_begin;
-  // accumulator in columns [0, npad), A tiles from kAColBase
+  // accumulator in columns [0, npad), A slots from kAColBase
+  static_assert(kAColBase + kMaxStages * kACols <= 512, "TMEM columns");
   constexpr uint32_t kCols = 512;
-  static_assert(kAColBase + kMaxStages * kACols <= (int)kCols, "TMEM columns");
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -355,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   } else if (warp == kMmaWarp) {
     // ---- 16 UMMAs (K = 16 each) per chunk, then commit ----
     if (lane == 0) {
-      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                             ((uint32_t)(P.npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+      // f32 accumulator, f16 A and B, both K-major; N = npad, M = 128
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(P.npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
       // a K step adds its byte offset / 16 to the B descriptor's start
       // address (every address stays below 256 KB) and 8 columns to A's
       const uint64_t b_desc0 = sw128_desc(smem_u32(B));
@@ -387,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
     // thread's TMEM lane), blocks bsel and bsel + 4 of each chunk ----
     const int q = warp & 3, bsel = warp >> 2;
     const int row = 32 * q + lane;
+    bool range_ok = true;  // every block scale keeps scale * q within f16
     // 48 bytes from byte 32 * blk of the row: 16-byte aligned, and the 34
     // bytes of block blk start 2 * blk bytes in (rows of 272 bytes: the
     // loads of 8 consecutive rows cover the 32 banks once)
@@ -419,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       }
       uint32_t pa[16], pb[16];
       switch (bsel) {  // the same for the warp's 32 lanes
-        case 0: decode_block<0>(v, pa); decode_block<4>(u, pb); break;
-        case 1: decode_block<1>(v, pa); decode_block<5>(u, pb); break;
-        case 2: decode_block<2>(v, pa); decode_block<6>(u, pb); break;
-        default: decode_block<3>(v, pa); decode_block<7>(u, pb); break;
+        case 0: decode_block_f16<0>(v, pa, range_ok); decode_block_f16<4>(u, pb, range_ok); break;
+        case 1: decode_block_f16<1>(v, pa, range_ok); decode_block_f16<5>(u, pb, range_ok); break;
+        case 2: decode_block_f16<2>(v, pa, range_ok); decode_block_f16<6>(u, pb, range_ok); break;
+        default: decode_block_f16<3>(v, pa, range_ok); decode_block_f16<7>(u, pb, range_ok); break;
       }
       // slot st is free once the MMAs of chunk i - S completed
       if (i >= S) {
@@ -441,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
         ph ^= 1u;
       }
     }
+    ok = ok && range_ok;
   }
 
   // every MMA of the CTA has completed once the last chunk's commit arrives
@@ -461,19 +497,25 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) + [0, 32) (rows),
-  // columns 16 g + [0, 16) (activation rows) for g = w / 4, w / 4 + 4, ...
+  // columns 16 g + [0, 16) (activation rows) for g = w / 4, w / 4 + 4, ...,
+  // and undoes the rows' power-of-two scales
   const float nan = __int_as_float(0x7fc00000);
+  auto read_cols = [&](int g, float (&v)[16]) {
+    if (nloc > 0) {
+      tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * g), v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] *= __ldg(P.xinv + min(16 * g + k, P.m - 1));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = 0.f;
+    }
+  };
   if (P.ksplit == 1) {
     if (warp < kDeqWarps) {
       const int r = 32 * (warp & 3) + lane;
       for (int g = warp >> 2; 16 * g < P.npad; g += kDeqWarps / 4) {
         float v[16];
-        if (nloc > 0) {
-          tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * g), v);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = 0.f;
-        }
+        read_cols(g, v);
         if (r < valid_rows) {
 #pragma unroll
           for (int k = 0; k < 16; ++k)
@@ -490,19 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
       const int r = 32 * (warp & 3) + lane;
       for (int g = warp >> 2; 16 * g < P.npad; g += kDeqWarps / 4) {
         float v[16];
-        if (nloc > 0) {
-          tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * g), v);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = 0.f;
-        }
+        read_cols(g, v);
 #pragma unroll
         for (int k = 0; k < 16; ++k) part[(16 * g + k) * kM + r] = v[k];
       }
     }
+    if (tid == 0) s_ok = ok ? 1.f : 0.f;
     __syncthreads();
     cluster_sync();  // every CTA's partial tile is complete
     const uint32_t part_s = smem_u32(part);
+    bool ok_all = true;  // every rank's partials are good
+    for (int k = 0; k < P.ksplit; ++k) ok_all = ok_all && ld_peer(smem_u32(&s_ok), (uint32_t)k) != 0.f;
     for (int e = tid * P.ksplit + (int)rank; e < P.m * kM; e += kThreads * P.ksplit) {
       const int col = e / kM, r = e % kM;
       if (r >= valid_rows) continue;
@@ -514,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) q8_mma_kernel(const __grid_consta
 #pragma unroll
       for (int k = 1; k < 8; ++k)
         if (k < P.ksplit) sum += v[k];
-      P.Y[(long long)col * P.ldy + r0 + r] = ok ? sum : nan;
+      P.Y[(long long)col * P.ldy + r0 + r] = ok_all ? sum : nan;
     }
     cluster_sync();  // every CTA keeps its shared memory until its peers have read it
   }
@@ -582,15 +622,20 @@ int max_active_clusters(int ksplit, int smem) {
   return n;
 }
 
-// Bytes of the B operand image of m activation rows of n elements (two
-// bytes per element, rows rounded up to 16 per 128-row block); 0 when the
-// tensor-core path does not take the shape (m < 9 or n not a multiple of
-// 256).  Host arithmetic only.
+// Bytes of the B operand image of m activation rows of n elements: two
+// bytes per element, rows rounded up to 16 per 128-row block.
+size_t mma_small_m_image_bytes(int m, int n) {
+  size_t rows = 0;
+  for (int i0 = 0; i0 < m; i0 += kMaxN) rows += (size_t)ximage_mp(std::min(kMaxN, m - i0));
+  return rows * (size_t)n * 2;
+}
+
+// Workspace bytes of the tensor-core path: the image and m inverse scales
+// (f32, 16-byte padded); 0 when it does not take the shape (m < 9 or n not a
+// multiple of 256).  Host arithmetic only.
 size_t mma_small_m_workspace(int m, int n) {
   if (m < 9 || n <= 0 || n % kKC != 0) return 0;
-  size_t rows = 0;
-  for (int i0 = 0; i0 < m; i0 += kMaxN) rows += (size_t)((std::min(kMaxN, m - i0) + 15) / 16 * 16);
-  return rows * (size_t)n * 2;
+  return mma_small_m_image_bytes(m, n) + (size_t)(m + 3) / 4 * 16;  // + the rows' inverse scales
 }
 
 // Runs the tensor-core path with `ws` (mma_small_m_workspace(m, n) bytes,
@@ -599,9 +644,8 @@ size_t mma_small_m_workspace(int m, int n) {
 // routes to the CUDA-core path.
 int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int ldy, int m, int n,
                        int p, void* ws, cudaStream_t stream) {
-  const size_t img_bytes = mma_small_m_workspace(m, n);
   const EncodeTiledFn encode = encode_tiled();
-  if (img_bytes == 0 || !encode) return Q8D_EUNSUPPORTED;
+  if (mma_small_m_workspace(m, n) == 0 || !encode) return Q8D_EUNSUPPORTED;
   // the weights as p rows of row_bytes / 4 32-bit elements (row_bytes is a
   // multiple of 272, so of 16), box = one chunk of 128 rows
   const long long row_bytes = (long long)(n / kQBlock) * kQBlockBytes;
@@ -619,10 +663,10 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
   const int crc = configure_kernel(reinterpret_cast<const void*>(q8_mma_kernel), kSmemLimit, false);
   if (crc) return crc;
   uint8_t* img = static_cast<uint8_t*>(ws);
+  float* inv = reinterpret_cast<float*>(img + mma_small_m_image_bytes(m, n));
   {
-    const long long total = (long long)(img_bytes / 16);
-    const int rc = launch_ex(q8_ximage_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0,
-                             stream, true, X, ldx, m, n, total, img);
+    const int rc = launch_ex(q8_ximage_kernel, dim3((unsigned)m), dim3(256), 0, stream, true, X, ldx,
+                             m, n, img, inv);
     if (rc) return rc;
   }
   const int row_tiles = (p + kM - 1) / kM;
@@ -632,8 +676,9 @@ int mma_small_m_launch(const float* X, int ldx, const uint8_t* w, float* Y, int 
     MmaParams P{};
     P.wmap = wmap;
     P.m = std::min(kMaxN, m - i0);
-    P.npad = (P.m + 15) / 16 * 16;
+    P.npad = ximage_mp(P.m);
     P.ximg = img + (size_t)i0 * 2 * n;
+    P.xinv = inv + i0;
     P.Y = Y + (long long)i0 * ldy;
     P.ldy = ldy;
     P.p = p;

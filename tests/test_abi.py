@@ -80,13 +80,14 @@ def test_small_m_workspace_bytes(q8d):
     """2 bytes per element of m rows rounded up to 16 per 128-row block, for
     the shapes the tensor-core path takes (9 <= m <= 256, n % 256 == 0)."""
     W = q8d.q8d_matmul_small_m_workspace_bytes
+    scales = lambda m: 16 * ((m + 3) // 4)               # the rows' inverse scales
     assert W(8, 3584) == 0 and W(0, 3584) == 0 and W(257, 512) == 0
     assert W(16, 3600) == 0 and W(16, 96) == 0          # n % 256 != 0: CUDA cores
-    assert W(9, 3584) == 2 * 3584 * 16
-    assert W(16, 3584) == 2 * 3584 * 16
-    assert W(64, 18944) == 2 * 18944 * 64
-    assert W(130, 256) == 2 * 256 * (128 + 16)
-    assert W(256, 512) == 2 * 512 * 256
+    assert W(9, 3584) == 2 * 3584 * 16 + scales(9)
+    assert W(16, 3584) == 2 * 3584 * 16 + scales(16)
+    assert W(64, 18944) == 2 * 18944 * 64 + scales(64)
+    assert W(130, 256) == 2 * 256 * (128 + 16) + scales(130)
+    assert W(256, 512) == 2 * 512 * 256 + scales(256)
 
 
 def test_small_m_ws_refusals(q8d):

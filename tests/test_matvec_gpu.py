@@ -1,6 +1,6 @@
 """q8d_matvec and q8d_matmul_small_m (CUDA, through the C ABI) against the
 oracle.  Bar: |gpu - oracle| <= 1e-5 * sum|terms| per output (f32 path),
-1e-2 * sum|terms| for the bf16 tensor-core path (m >= 9); exact where the
+2e-3 * sum|terms| for the f16 tensor-core path (m >= 9); exact where the
 result is an exact integer or a single product."""
 import numpy as np
 import pytest
@@ -12,7 +12,9 @@ from conftest import dev
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
-TOL_BF16 = 1e-2
+# the tensor-core path (m >= 9): weights and activations each rounded once
+# to f16 (<= 2^-11 relative each), f32 accumulation: ~2^-10 per product
+TOL_TC = 2e-3
 
 
 def gpu_matvec(q8d, w, x, n, p, canary=True):
@@ -171,9 +173,9 @@ def test_small_m_tensor_parity(q8d, orc, m, n, p):
     X = synth.normal_f32(4, f"tc.X{n}.{m}", (m, n))
     ref, ab = orc.q8_matmul(w, X, n, p)
     got = gpu_small_m(q8d, w, X, n, p)
-    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+    assert np.all(np.abs(got - ref) <= TOL_TC * ab)
     # the norm-wise error is reported, and is far inside the bar
-    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) < 1e-2
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) < 2e-3
 
 
 @pytest.mark.parametrize("m", [16, 64])
@@ -185,7 +187,23 @@ def test_small_m_tensor_ragged_row_tile(q8d, orc, m, n, p):
     X = synth.normal_f32(6, f"tr.X{n}.{m}", (m, n))
     ref, ab = orc.q8_matmul(w, X, n, p)
     got = gpu_small_m(q8d, w, X, n, p, ldy=p + 5)
-    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+    assert np.all(np.abs(got - ref) <= TOL_TC * ab)
+
+
+@pytest.mark.parametrize("p", [300, 10000])  # 3 row tiles: K split in clusters; 79: none
+def test_small_m_tensor_scale_range(q8d, orc, p):
+    """A block scale above 511.75 (scale * q beyond f16): the outputs of its
+    128-row tile are NaN, every other tile is within the bar."""
+    m, n = 16, 512
+    w = synth.q8_matrix(14, f"rg.w{p}", p, n).copy()
+    row, blk = 130, 3  # second row tile
+    w[row, blk * 34:blk * 34 + 2] = np.frombuffer(np.float16(1000.0).tobytes(), np.uint8)
+    X = synth.normal_f32(14, f"rg.X{n}", (m, n))
+    got = gpu_small_m(q8d, w, X, n, p)
+    assert np.isnan(got[:, 128:256]).all()
+    ref, ab = orc.q8_matmul(w, X, n, p)
+    keep = np.r_[0:128, 256:p]
+    assert np.all(np.abs(got[:, keep] - ref[:, keep]) <= TOL_TC * ab[:, keep])
 
 
 @pytest.mark.parametrize("m", [65, 80, 128, 129, 200, 256])
@@ -197,7 +215,7 @@ def test_small_m_tensor_large_m(q8d, orc, m):
     X = synth.normal_f32(7, f"lm.X{m}", (m, n))
     ref, ab = orc.q8_matmul(w, X, n, p)
     got = gpu_small_m(q8d, w, X, n, p)
-    assert np.all(np.abs(got - ref) <= TOL_BF16 * ab)
+    assert np.all(np.abs(got - ref) <= TOL_TC * ab)
 
 
 @pytest.mark.parametrize("m", [16, 130])
@@ -207,7 +225,7 @@ def test_small_m_caller_workspace(q8d, orc, m):
     n, p = 512, 300
     w = synth.q8_matrix(9, "ws.w", p, n)
     need = q8d.q8d_matmul_small_m_workspace_bytes(m, n)
-    assert need == 2 * n * (m // 128 * 128 + (m % 128 + 15) // 16 * 16)
+    assert need == 2 * n * (m // 128 * 128 + (m % 128 + 15) // 16 * 16) + 16 * ((m + 3) // 4)
     pad = 4096
     buf = torch.full((need + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
     ws = buf[pad:pad + need]
@@ -217,7 +235,7 @@ def test_small_m_caller_workspace(q8d, orc, m):
         Y = torch.full((m, p), float("nan"), device="cuda")
         q8d.q8d_matmul_small_m_ws(dev(X), n, dev(w), Y, p, m, n, p, ws, need)
         torch.cuda.synchronize()
-        assert np.all(np.abs(Y.cpu().numpy() - ref) <= TOL_BF16 * ab), seed
+        assert np.all(np.abs(Y.cpu().numpy() - ref) <= TOL_TC * ab), seed
     assert (buf[:pad] == 0xA5).all() and (buf[pad + need:] == 0xA5).all()
 
 
@@ -231,7 +249,7 @@ def test_small_m_bench_shape_sampled(q8d, orc, m):
     got = gpu_small_m(q8d, w, X, n, p)
     rng = np.random.default_rng(3)
     rows = np.unique(np.concatenate([[0, p - 1], rng.integers(0, p, 255)])).astype(np.int64)
-    tol = TOL if m <= 8 else TOL_BF16
+    tol = TOL if m <= 8 else TOL_TC
     for i in range(m):
         ref, ab = orc.q8_matvec_rows(w, X[i], n, rows)
         assert np.all(np.abs(got[i, rows] - ref) <= tol * ab), i
@@ -363,6 +381,6 @@ def test_small_m_chain_shared_workspace(q8d, orc):
     torch.cuda.synchronize()
     G1, G2 = Y1.cpu().numpy(), Y2.cpu().numpy()
     ref1, ab1 = orc.q8_matmul(w1, X1, n1, p1)
-    assert np.all(np.abs(G1 - ref1) <= TOL_BF16 * ab1)
+    assert np.all(np.abs(G1 - ref1) <= TOL_TC * ab1)
     ref2, ab2 = orc.q8_matmul(w2, G1, p1, p2)
-    assert np.all(np.abs(G2 - ref2) <= TOL_BF16 * ab2)
+    assert np.all(np.abs(G2 - ref2) <= TOL_TC * ab2)
