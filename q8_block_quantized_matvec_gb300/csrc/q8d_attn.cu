@@ -101,8 +101,11 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const AttnParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.n_heads / P.n_kv_heads;
   // the combine kernel, launched as a programmatic dependent, may be
-  // scheduled now (it waits for this grid's results before reading them)
+  // scheduled now (it waits for this grid's results before reading them);
+  // this grid is itself a programmatic dependent of the previous work in the
+  // stream: nothing is read before that work is complete
   griddep_launch_dependents();
+  griddep_wait();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = attn_window_len(P, b);
@@ -343,6 +346,10 @@ __global__ void __launch_bounds__(kCombGroups * D) gqa_combine_kernel(const Attn
   const int b = hq / P.n_heads;
   const int j = threadIdx.x % D, grp = threadIdx.x / D;
   griddep_wait();  // the partials of the attention grid are complete and visible
+  // the next kernel may be scheduled now (it waits for this grid before it
+  // reads anything); not earlier, so that launches do not run ahead of the
+  // work in flight and take its SMs
+  griddep_launch_dependents();
   const int L = attn_window_len(P, b);
   float* o = P.out + (long long)hq * D;
   if (L < 1) {
@@ -445,7 +452,7 @@ int launch_attn_t(const AttnParams& P, cudaStream_t stream) {
   int rc = configure_kernel(reinterpret_cast<const void*>(fn), C::kSmem, false);
   if (rc) return rc;
   dim3 grid(P.nct, P.n_kv_heads);
-  rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, false, P);
+  rc = launch_ex(fn, grid, dim3(kAttnThreads), (size_t)C::kSmem, stream, true, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

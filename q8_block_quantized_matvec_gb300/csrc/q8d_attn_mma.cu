@@ -84,8 +84,11 @@ __global__ void __launch_bounds__(kThreadsA) gqa_mma_kernel(const AttnParams P) 
   const int gq = lane >> 2, cq = lane & 3;
   const int G = P.n_heads / P.n_kv_heads;
   // the combine kernel, launched as a programmatic dependent, may be
-  // scheduled now (it waits for this grid's results before reading them)
+  // scheduled now (it waits for this grid's results before reading them);
+  // this grid is itself a programmatic dependent of the previous work in the
+  // stream: nothing is read before that work is complete
   griddep_launch_dependents();
+  griddep_wait();
   int b, c, n;  // this CTA's sequence and chunk (of n): the balanced split
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = attn_window_len(P, b);
@@ -377,8 +380,7 @@ int launch_mma(const AttnParams& P, cudaStream_t stream) {
   int rc = configure_kernel(reinterpret_cast<const void*>(gqa_mma_kernel<D>), C::kSmem, false);
   if (rc) return rc;
   dim3 grid(P.nct, P.n_kv_heads);
-  rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream,
-                           false, P);
+  rc = launch_ex(gqa_mma_kernel<D>, grid, dim3(kThreadsA), (size_t)C::kSmem, stream, true, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

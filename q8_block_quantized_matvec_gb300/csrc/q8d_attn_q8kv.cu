@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreadsQ) gqa_q8kv_kernel(const AttnParams P)
   const int gq = lane >> 2, cq = lane & 3;
   const int G = P.n_heads / P.n_kv_heads;
   griddep_launch_dependents();  // the combine may be scheduled now
+  griddep_wait();  // (a programmatic dependent: the previous work is complete)
   int b, c, n;
   if (!attn_chunk_of(P, blockIdx.x, b, c, n)) return;
   const int L = attn_window_len(P, b);
@@ -477,7 +478,7 @@ int launch_q8kv(const AttnParams& P, cudaStream_t stream) {
   int rc = configure_kernel(reinterpret_cast<const void*>(gqa_q8kv_kernel<D>), C::kSmem, false);
   if (rc) return rc;
   dim3 grid(P.nct, P.n_kv_heads);
-  rc = launch_ex(gqa_q8kv_kernel<D>, grid, dim3(kThreadsQ), (size_t)C::kSmem, stream, false, P);
+  rc = launch_ex(gqa_q8kv_kernel<D>, grid, dim3(kThreadsQ), (size_t)C::kSmem, stream, true, P);
   if (rc) return rc;
   return attn_combine_launch(P, stream);
 }

@@ -266,9 +266,20 @@ __global__ void __launch_bounds__(NT) q8_gemv_kernel(const RowsParams P) {
   const int v0 = blockIdx.x * (int)P.rows_per_cta;
   const int v1 = (int)min(P.total_rows, (long long)v0 + P.rows_per_cta);
   // Launched as a programmatic dependent: the next kernel may start its
-  // prologue now; this one waits for the previous kernel before it reads
-  // anything or writes y.
+  // prologue now; this one waits for the previous kernel before it copies
+  // weights into shared memory, reads x or writes y.  Until then the
+  // producer warp pulls the first ring-full of this CTA's rows (one byte
+  // range of one matrix, widened to 16-byte boundaries inside it) into L2,
+  // which reads nothing it depends on.
   griddep_launch_dependents();
+  if (warp == W && P.nseg == 1 && v0 < v1) {
+    const long long want = min((long long)P.stage_bytes * P.nstages, (long long)(v1 - v0) * P.row_bytes);
+    const long long cap16 = ((long long)P.seg[0].p * P.row_bytes) & ~15LL;
+    const long long a0 = ((long long)v0 * P.row_bytes) & ~15LL;
+    const long long a1 = min(cap16, ((long long)v0 * P.row_bytes + want + 15) & ~15LL);
+    for (long long o = a0 + (long long)lane * 16384; o < a1; o += 32LL * 16384)
+      bulk_prefetch_l2(P.seg[0].w + o, (uint32_t)min(16384LL, a1 - o));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.nstages; ++s) {
       mbar_init(&ring.full[s], 1);
@@ -382,6 +393,25 @@ int gemv_plan_and_launch(RowsParams P, cudaStream_t stream, int* grid_out) {
   P.rows_per_cta = rows_cta;
   P.rows_per_tile = (int)std::min<long long>(R, rows_cta);
   if (grid_out) *grid_out = (int)grid;
+  if (rows_cta < R) {
+    // Fewer rows a CTA than one tile (small matrices: 7B k and v, 512 rows
+    // over the SMs): one tile of exactly its rows in one stage, RG = half of
+    // them (at most the full plan's), one window.  A few KB of shared memory
+    // and a few warps a CTA, so the next call's CTAs (another small matrix)
+    // fit beside this call's and pull their weights into L2 while it runs.
+    const int rgc = std::max(1, std::min(RG, (int)(rows_cta / 2)));
+    const int npc = (int)((rows_cta + 2LL * rgc - 1) / (2LL * rgc));
+    const long long Rc = 2LL * rgc * npc;
+    P.np = npc;
+    P.rows_per_tile = (int)rows_cta;
+    P.stage_bytes = (int)(((Rc * P.row_bytes + 32 + 127) / 128) * 128);
+    P.nstages = 1;
+    P.win = 1;
+    P.win_rows = (int)Rc;
+    const int Wc = rgc * NS;
+    const long long smc = (long long)P.stage_bytes + 16 + 2LL * Rc * NS * 32 * 4;
+    return launch_ex(fn, dim3((unsigned)grid), dim3((Wc + 1) * 32), (size_t)smc, stream, true, P);
+  }
   return launch_ex(fn, dim3((unsigned)grid), dim3((W + 1) * 32), (size_t)smem, stream, true, P);
 }
 
