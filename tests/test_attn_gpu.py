@@ -247,3 +247,71 @@ def test_attention_control_shifted_length_changes_output(q8d):
     c, _ = run_attn(q8d, q, kc, vc, synth.KV_F16, H, Hk, D, [500], cap, 0.088)
     assert not np.array_equal(a, b)
     assert np.array_equal(a.view(np.uint32), c.view(np.uint32))  # deterministic
+
+
+# ---------------------------------------------------------------------------- launch chaining
+@pytest.mark.parametrize("dtype,noalloc", [(synth.KV_F16, False), (synth.KV_F32, False),
+                                           (synth.KV_Q8_0, False), (synth.KV_F16, True)])
+def test_attention_chain_without_sync(q8d, orc, dtype, noalloc):
+    """Three decode-like rounds on one stream with no host synchronisation:
+    matvecs make q, k and v from x, attention appends k and v at row L-1 and
+    attends, and its output is the next round's x.  The attention kernels
+    and their combine are programmatic dependents of the kernels before
+    them, and every round reuses one workspace: each call must see its
+    inputs (activations, the rows appended by the previous round) complete
+    and must not overwrite partials the previous combine still reads.
+    Intermediates start as NaN, so an early read would show."""
+    H, Hk, D, L0, cap = 28, 4, 128, 300, 512
+    n, kvw, rounds = H * D, Hk * D, 3
+    # block scales ~1/(E|q| sqrt(n)): q, k, v keep x's magnitude round after
+    # round (no growth into f16 overflow)
+    wq = synth.q8_matrix(21, "achain.wq", n, n, 1e-4, 3e-4)
+    wk = synth.q8_matrix(21, "achain.wk", kvw, n, 1e-4, 3e-4)
+    wv = synth.q8_matrix(21, "achain.wv", kvw, n, 1e-4, 3e-4)
+    x0 = synth.normal_f32(21, "achain.x", n)
+    if dtype == synth.KV_Q8_0:  # packed rows of 34-byte blocks
+        kc = synth.q8_kv_cache(21, "achain.kq", cap, kvw)
+        vc = synth.q8_kv_cache(21, "achain.vq", cap, kvw)
+    else:
+        npdt = np.float16 if dtype == synth.KV_F16 else np.float32
+        kc = np.zeros((cap, kvw), npdt)
+        vc = np.zeros((cap, kvw), npdt)
+        kc[:L0 - 1] = synth.normal_f16(21, "achain.k", (L0 - 1, kvw))
+        vc[:L0 - 1] = synth.normal_f16(21, "achain.v", (L0 - 1, kvw))
+    kc0, vc0 = kc.copy(), vc.copy()
+    wqd, wkd, wvd, kcd, vcd = dev(wq), dev(wk), dev(wv), dev(kc), dev(vc)
+    nan = lambda m: torch.full((m,), float("nan"), device="cuda")
+    xs = [dev(x0)] + [nan(n) for _ in range(rounds)]  # xs[r + 1]: round r's attention output
+    qs, ks, vs = [nan(n) for _ in range(rounds)], [nan(kvw) for _ in range(rounds)], \
+        [nan(kvw) for _ in range(rounds)]
+    lens = [torch.tensor([L0 + r], dtype=torch.int32, device="cuda") for r in range(rounds)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1 / math.sqrt(D)
+    ws_bytes = q8d.q8d_gqa_workspace_bytes(1, H, Hk, D, cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    for r in range(rounds):
+        q8d.q8d_matvec(xs[r], wqd, qs[r], n, n)
+        q8d.q8d_matvec(xs[r], wkd, ks[r], n, kvw)
+        q8d.q8d_matvec(xs[r], wvd, vs[r], n, kvw)
+        args = (qs[r], ks[r], vs[r], kcd, vcd, dtype, xs[r + 1], 1, H, Hk, D, cap, cap * kvw, lens[r],
+                scale)
+        if noalloc:
+            q8d.q8d_gqa_decode_attn_noalloc(*args, err)
+        else:
+            q8d.q8d_gqa_decode_attn(*args, ws, ws_bytes, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = [t.cpu().numpy() for t in xs]
+    kc_o, vc_o = kc0.copy(), vc0.copy()
+    for r in range(rounds):
+        q_g, k_g, v_g = qs[r].cpu().numpy(), ks[r].cpu().numpy(), vs[r].cpu().numpy()
+        for w, g, p in ((wq, q_g, n), (wk, k_g, kvw), (wv, v_g, kvw)):
+            ref, ab = orc.q8_matvec(w, got[r], n, p)
+            assert np.all(np.abs(g - ref) <= TOL * ab + 1e-30)
+        orc.kv_append(k_g, v_g, kc_o, vc_o, dtype, L0 - 1 + r)
+        ref, ab = orc.gqa_decode_attn(q_g, kc_o, vc_o, dtype, H, Hk, D, L0 + r, scale)
+        assert np.all(np.abs(got[r + 1] - ref) <= TOL * ab)
+    bits = {synth.KV_F16: np.uint16, synth.KV_F32: np.uint32, synth.KV_Q8_0: np.uint8}[dtype]
+    assert np.array_equal(kcd.cpu().numpy().view(bits), kc_o.view(bits))
+    assert np.array_equal(vcd.cpu().numpy().view(bits), vc_o.view(bits))
