@@ -379,8 +379,9 @@ def run_profile(args):
             q8d.q8d_matvec(xs[n], w, y, n, p)
         torch.cuda.synchronize()
         cudart.cudaProfilerStop()
-    elif args.profile in ("matvec", "matvec_down"):
-        n, p = (3584, 18944) if args.profile == "matvec" else (18944, 3584)
+    elif args.profile in ("matvec", "matvec_down", "matvec_kv"):
+        n, p = {"matvec": (3584, 18944), "matvec_down": (18944, 3584),
+                "matvec_kv": (3584, 512)}[args.profile]
         w = synth.q8_matrix_torch(0, "prof.w", p, n)
         x = synth.normal_torch(0, "prof.x", n, torch.float32)
         y = torch.empty(p, device="cuda")
@@ -882,7 +883,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations")
     ap.add_argument("--kernel-reps", type=int, default=3)
     ap.add_argument("--profile",
-                    choices=["step", "matvec", "matvec_down", "attn", "attn_stress", "mma16", "mma64",
+                    choices=["step", "matvec", "matvec_down", "matvec_kv", "attn", "attn_stress", "mma16", "mma64",
                              "matvec_sweep", "attn_stress_q8", "attn_window"],
                     default=None,
                     help="run a short fixed workload between cudaProfilerStart/Stop for ncu "
