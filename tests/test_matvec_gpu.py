@@ -30,7 +30,10 @@ def gpu_matvec(q8d, w, x, n, p, canary=True):
 
 
 SHAPES = [(32, 1), (64, 3), (96, 50), (896, 33), (896, 137), (1024, 3072), (1024, 1),
-          (2048, 101), (3072, 77), (3584, 300), (4864, 200), (18944, 67), (160, 999)]
+          (2048, 101), (3072, 77), (3584, 300), (4864, 200), (18944, 67), (160, 999),
+          # a few rows per CTA (one tile sized to them): 3, 4 and 5 rows of 20,
+          # 2 and 10 column-segment warps
+          (18944, 456), (2048, 600), (4864, 750)]
 
 
 @pytest.mark.parametrize("n,p", SHAPES)
