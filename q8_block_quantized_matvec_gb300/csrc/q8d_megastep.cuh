@@ -78,7 +78,7 @@ struct MParams {
 
 // Tensor-core plan of one matvec phase (host): sets F.tc, F.SR, F.win and
 // the row split when the phase suits the tensor-core path (n % 256 == 0,
-// at least 64 blocks a row, fragments within the shared region); returns
+// at least 32 blocks a row, fragments within the shared region); returns
 // its tile bytes, or 0 (F.tc = 0) when it does not.
 int megastep_plan_tc(MPhase& F, int grid);
 
