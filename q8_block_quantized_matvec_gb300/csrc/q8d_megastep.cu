@@ -1762,10 +1762,17 @@ int megastep_plan_tc(MPhase& F, int grid) {
   const long long frag = (long long)F.bpr * (tc::kXfBlock + 4) + tc::kZeroPad;
   const long long per_tile = 2LL * F.T * tc::kSetRows * kW * 4;  // double-buffered partials
   if (frag + per_tile > kMsRegion) return 0;
+  const int total = F.vbegin[F.nseg];
+  const int rpc = F.glu ? (F.vbegin[1] + grid - 1) / grid : (total + grid - 1) / grid;
+  // Rows of 32 blocks give a 16-row tile only 8 unit pairs for the 20
+  // warps: on the tensor cores they pay off in short phases (a few tiles a
+  // CTA, latency-bound) but not in long ones (the Qwen3-0.6B lm_head, 1000
+  // rows a CTA, streamed 2.4x slower than on the CUDA cores).
+  if (F.bpr < 64 && rpc > 128) return 0;
   F.tc = 1;
   F.win = (int)std::min<long long>(8, (kMsRegion - frag) / per_tile);
-  F.total_rows = F.vbegin[F.nseg];
-  F.rows_per_cta = F.glu ? (F.vbegin[1] + grid - 1) / grid : (F.total_rows + grid - 1) / grid;
+  F.total_rows = total;
+  F.rows_per_cta = rpc;
   return (int)tile;
 }
 
