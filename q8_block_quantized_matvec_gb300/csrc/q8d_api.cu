@@ -99,6 +99,9 @@ int step_validate(const q8d_step_desc* d) {
   if (d->head_dim != 64 && d->head_dim != 128) return Q8D_EUNSUPPORTED;
   if (d->n_heads % d->n_kv_heads) return Q8D_EUNSUPPORTED;
   if (d->n_heads / d->n_kv_heads > 16) return Q8D_EUNSUPPORTED;
+  // the step's f16-cache attention prepares the query rows of a KV head's
+  // group with the 12 warps beside its 8 pair warps
+  if (d->kv_dtype == Q8D_KV_F16 && d->n_heads / d->n_kv_heads > 12) return Q8D_EUNSUPPORTED;
   if (d->hidden % 32 || d->ffn % 32) return Q8D_EUNSUPPORTED;
   if (d->kv_dtype != Q8D_KV_F32 && d->kv_dtype != Q8D_KV_F16) return Q8D_EUNSUPPORTED;
   if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f)) return Q8D_EINVAL;

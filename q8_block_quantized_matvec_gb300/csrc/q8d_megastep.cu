@@ -1011,8 +1011,8 @@ struct MsMmaCfg {
   static constexpr int kOffF = kOffQ + 64 * D;       // per-head score factors [16]
   static constexpr int kBytes = kOffF + 16 * 4;
   static_assert(kBytes <= kMsRegion, "attention tiles fit the shared region");
-  // merge buffer of pairs 1..3 in the tiles: m, l [3][16], O [3][16][D]
-  static_assert((kPairs - 1) * 16 * (D + 2) * 4 <= kOffQ, "the merge buffer fits the tiles");
+  // merge buffer of the pairs in the tiles: m, l [4][16], O [4][16][D]
+  static_assert(kPairs * 16 * (D + 2) * 4 <= kOffQ, "the merge buffer fits the tiles");
 };
 
 // Barrier of warp pair p (64 threads; ids 2.. are free: 0 is the CTA's, 1
@@ -1082,7 +1082,8 @@ __device__ void attn_phase_mma(const MParams& P, const MPhase& F, int L, bool le
   if (warp < 2 * kPairs) {
     if (pr < ngroups) load_half(pr, true);
   } else if (warp < 2 * kPairs + 16) {
-    // q row hh = warp - 8 (rows past G are zero): bias / QK-norm / RoPE,
+    // q row hh = warp - 8 (rows past G are zero; the 12 warps cover G <= 12,
+    // which the step's set-up checks for f16 caches): bias / QK-norm / RoPE,
     // scaled by 2^sh so that max|q| < 2^11 (the score factor 2^-sh * scale
     // * log2(e) undoes it), split into hi / lo A fragments: the pair of
     // columns (d, d + 1) of row hh is register (hh >= 8) + 2 (d % 16 >= 8)
@@ -1269,77 +1270,44 @@ __device__ void attn_phase_mma(const MParams& P, const MPhase& F, int L, bool le
       attn_mma16816(o[2 * dn + 1], pl, v2, v3);
     }
   }
-  // ---- pair 0 merges the pairs' {m, l, O} and writes the chunk's partial ----
-  pairs_sync();  // every pair is done with its tile: pairs 1..3 park their state there
-  float* mm = reinterpret_cast<float*>(region);  // [3][16]
-  float* ll = mm + (kPairs - 1) * 16;            // [3][16]
-  float* oo = ll + (kPairs - 1) * 16;            // [3][16][D]
-  if (pr > 0) {
-    if (cq == 0 && dh == 0) {
-      mm[(pr - 1) * 16 + gq] = m0;
-      mm[(pr - 1) * 16 + gq + 8] = m1;
-      ll[(pr - 1) * 16 + gq] = l0;
-      ll[(pr - 1) * 16 + gq + 8] = l1;
-    }
-#pragma unroll
-    for (int n = 0; n < NH; ++n) {
-      const int col = dh * (D / 2) + 8 * n + 2 * cq;
-      *reinterpret_cast<float2*>(oo + ((pr - 1) * 16 + gq) * D + col) = make_float2(o[n][0], o[n][1]);
-      *reinterpret_cast<float2*>(oo + ((pr - 1) * 16 + gq + 8) * D + col) = make_float2(o[n][2], o[n][3]);
-    }
+  // ---- the pairs' {m, l, O} merged by all 8 pair warps, output elements
+  // dealt over their threads (in the order of the single-pair merge: the
+  // same results); the chunk's partial written ----
+  pairs_sync();  // every pair is done with its tile: each parks its state there
+  float* mm = reinterpret_cast<float*>(region);  // [4][16]
+  float* ll = mm + kPairs * 16;                  // [4][16]
+  float* oo = ll + kPairs * 16;                  // [4][16][D]
+  if (cq == 0 && dh == 0) {
+    mm[pr * 16 + gq] = m0;
+    mm[pr * 16 + gq + 8] = m1;
+    ll[pr * 16 + gq] = l0;
+    ll[pr * 16 + gq + 8] = l1;
   }
-  pairs_sync();
-  if (pr > 0) return;
-  // rows gq (m0, l0, o[.][0..1]) and gq + 8 (m1, l1, o[.][2..3])
-  float w0[kPairs], w1[kPairs];
-  float M0 = m0, M1 = m1;
-#pragma unroll
-  for (int q = 1; q < kPairs; ++q) {
-    M0 = fmaxf(M0, mm[(q - 1) * 16 + gq]);
-    M1 = fmaxf(M1, mm[(q - 1) * 16 + gq + 8]);
-  }
-  float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-  for (int q = 0; q < kPairs; ++q) {
-    const float a = q ? mm[(q - 1) * 16 + gq] : m0, b = q ? mm[(q - 1) * 16 + gq + 8] : m1;
-    w0[q] = a == -INFINITY ? 0.f : exp2f(a - M0);
-    w1[q] = b == -INFINITY ? 0.f : exp2f(b - M1);
-    L0 = fmaf(q ? ll[(q - 1) * 16 + gq] : l0, w0[q], L0);
-    L1 = fmaf(q ? ll[(q - 1) * 16 + gq + 8] : l1, w1[q], L1);
-  }
-  float* po = P.ws_o + (size_t)item * G * D;
 #pragma unroll
   for (int n = 0; n < NH; ++n) {
     const int col = dh * (D / 2) + 8 * n + 2 * cq;
-    float a0 = o[n][0] * w0[0], a1 = o[n][1] * w0[0], b0 = o[n][2] * w1[0], b1 = o[n][3] * w1[0];
-#pragma unroll
-    for (int q = 1; q < kPairs; ++q) {
-      if (w0[q] != 0.f) {
-        const float2 u = *reinterpret_cast<const float2*>(oo + ((q - 1) * 16 + gq) * D + col);
-        a0 = fmaf(u.x, w0[q], a0);
-        a1 = fmaf(u.y, w0[q], a1);
-      }
-      if (w1[q] != 0.f) {
-        const float2 u = *reinterpret_cast<const float2*>(oo + ((q - 1) * 16 + gq + 8) * D + col);
-        b0 = fmaf(u.x, w1[q], b0);
-        b1 = fmaf(u.y, w1[q], b1);
-      }
-    }
-    if (gq < G)
-      *reinterpret_cast<float2*>(po + (size_t)gq * D + col) = make_float2(a0 / kPS, a1 / kPS);
-    if (gq + 8 < G)
-      *reinterpret_cast<float2*>(po + (size_t)(gq + 8) * D + col) = make_float2(b0 / kPS, b1 / kPS);
+    *reinterpret_cast<float2*>(oo + (pr * 16 + gq) * D + col) = make_float2(o[n][0], o[n][1]);
+    *reinterpret_cast<float2*>(oo + (pr * 16 + gq + 8) * D + col) = make_float2(o[n][2], o[n][3]);
   }
-  if (cq == 0 && dh == 0) {
-    float* pm = P.ws_m + (size_t)item * G;
-    float* pl_ = P.ws_l + (size_t)item * G;
-    if (gq < G) {
-      pm[gq] = M0;
-      pl_[gq] = L0;
+  pairs_sync();
+  float* po = P.ws_o + (size_t)item * G * D;
+  for (int e = threadIdx.x; e < G * D; e += 2 * kPairs * 32) {  // (threads 0..255: the pair warps)
+    const int h = e / D, d = e % D;
+    float M = mm[h];
+#pragma unroll
+    for (int q = 1; q < kPairs; ++q) M = fmaxf(M, mm[q * 16 + h]);
+    float Ls = 0.f, acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+      const float mq = mm[q * 16 + h];
+      const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
+      Ls = fmaf(ll[q * 16 + h], w, Ls);
+      acc = fmaf(oo[(q * 16 + h) * D + d], w, acc);
     }
-    if (gq + 8 < G) {
-      pm[gq + 8] = M1;
-      pl_[gq + 8] = L1;
+    po[e] = acc / kPS;
+    if (d == 0) {
+      P.ws_m[(size_t)item * G + h] = M;
+      P.ws_l[(size_t)item * G + h] = Ls;
     }
   }
 }

@@ -175,6 +175,12 @@ def test_step_create_refusals(q8d):
     d.head_dim = 64
     d.n_heads = 3
     assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EUNSUPPORTED  # H % Hk
+    d.n_heads = 26
+    assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EUNSUPPORTED  # 13 > 12, f16
+    d.n_heads = 34
+    d.kv_dtype = 0
+    assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EUNSUPPORTED  # 17 > 16
+    d.kv_dtype = 1
     d.n_heads = 4
     d.embed = A16 + 2
     assert L.q8d_step_create(C.byref(d), None, C.byref(h)) == q8d.Q8D_EALIGN

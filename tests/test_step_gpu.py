@@ -210,6 +210,24 @@ def test_step_attention_subtiles(orc, q8d, name, D, kvd, Hk, pos, qkn, bias):
     run_case(orc, shape, pos=pos, cap=pos + 64)
 
 
+# The largest query groups per KV head the step takes: 12 with an f16 cache
+# (the tensor-core attention prepares one q row per warp beside its 8 pair
+# warps), 16 with an f32 cache (one head per warp).
+GROUP_CASES = [
+    ("g12-d64-f16", 64, synth.KV_F16, 12),
+    ("g12-d128-f16", 128, synth.KV_F16, 12),
+    ("g16-d128-f32", 128, synth.KV_F32, 16),
+    ("g16-d64-f32", 64, synth.KV_F32, 16),
+]
+
+
+@pytest.mark.parametrize("name,D,kvd,G", GROUP_CASES)
+def test_step_large_query_groups(orc, q8d, name, D, kvd, G):
+    shape = synth.ModelShape(name, 256, 2, G, 1, D, 512, 500,
+                             qk_norm=True, qkv_bias=True, kv_dtype=kvd)
+    run_case(orc, shape, pos=300, cap=512)
+
+
 def test_step_head_dim_128_f32_cache(orc, q8d):
     # the step kernel's (head_dim 128, f32 cache) instance
     shape = synth.ModelShape("d128-f32", 256, 2, 4, 2, 128, 320, 600,
