@@ -951,18 +951,17 @@ def main():
     value = replica_throughput(t_dev, args.steps, dist)
     t_dev = world * args.steps / value  # the slowest rank's time
 
-    # ---- end to end through the public API: H2D token+pos, graph, D2H token ----
+    # ---- end to end through the public API: every step copies its token id
+    # and position from pinned host memory, runs the graph and copies the
+    # next token id back (q8d_step_launch_host: one call), and the host
+    # waits for it and feeds it to the next step ----
     h_in = torch.tensor([17, ctx - 1], dtype=torch.int32).pin_memory()
     h_out = torch.empty(1, dtype=torch.int32).pin_memory()
     barrier()
     t0 = time.perf_counter()
     for s in range(args.steps):
         h_in[1] = ctx - 1 + s
-        with torch.cuda.stream(stream):
-            ds.token.copy_(h_in[0:1], non_blocking=True)   # host -> device: token id
-            ds.pos.copy_(h_in[1:2], non_blocking=True)     # host -> device: position
-            ds.launch(stream)
-            h_out.copy_(ds.token, non_blocking=True)       # device -> host: next token id
+        ds.launch_host(h_in, h_out, stream)   # H2D token + position, step, D2H next token
         stream.synchronize()
         h_in[0] = int(h_out[0])
     t_e2e = time.perf_counter() - t0

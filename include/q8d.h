@@ -309,6 +309,18 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out);
 /* Enqueues one decode step (one graph launch) on `stream`. */
 int q8d_step_launch(q8d_step* step, void* stream);
 
+/* One decode step with its inputs and output in host memory, in one call:
+ * copies h_token_pos[0] (token id) and h_token_pos[1] (position) to the
+ * step's device token and position (one 8-byte copy when they are adjacent
+ * in device memory, d_pos == d_token + 1), launches the step graph, and
+ * copies the next token id to *h_next_token, all enqueued on `stream`
+ * (asynchronous: read *h_next_token after synchronising the stream; pinned
+ * host memory keeps the copies asynchronous).  Either pointer may be NULL
+ * to skip that copy.  The same operation as the host copies around
+ * q8d_step_launch ("IV.4: One command buffer per token": token and
+ * position in, next token out), with one call per step instead of four. */
+int q8d_step_launch_host(q8d_step* step, const int* h_token_pos, int* h_next_token, void* stream);
+
 /* Copies the step's device error word into *err (synchronous; waits for
  * work already enqueued on `stream`, polling with a time limit of
  * timeout_ms milliseconds, <= 0 meaning 10 s).  Returns Q8D_ETIMEOUT if the

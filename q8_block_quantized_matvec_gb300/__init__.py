@@ -102,6 +102,8 @@ def lib():
         L.q8d_step_create.restype = i32
         L.q8d_step_launch.argtypes = [vp, vp]
         L.q8d_step_launch.restype = i32
+        L.q8d_step_launch_host.argtypes = [vp, vp, vp, vp]
+        L.q8d_step_launch_host.restype = i32
         L.q8d_step_status.argtypes = [vp, vp, i32, C.POINTER(i32)]
         L.q8d_step_status.restype = i32
         L.q8d_step_set_wait_limit.argtypes = [vp, C.c_uint, vp]
@@ -234,6 +236,13 @@ class Step:
 
     def launch(self, stream=None) -> int:
         return _check(lib().q8d_step_launch(self.handle, _stream(stream)), "q8d_step_launch")
+
+    def launch_host(self, h_token_pos, h_next_token, stream=None) -> int:
+        """q8d_step_launch_host: host int32 [token, position] in (or None),
+        the next token id out to host int32 [1] (or None); both pinned CPU
+        tensors, read the output after synchronising the stream."""
+        return _check(lib().q8d_step_launch_host(self.handle, _ptr(h_token_pos), _ptr(h_next_token),
+                                                 _stream(stream)), "q8d_step_launch_host")
 
     def status(self, stream=None, timeout_ms: int = 10000) -> int:
         err = C.c_int(0)

@@ -319,6 +319,28 @@ int q8d_step_launch(q8d_step* S, void* stream) {
   return e == cudaSuccess ? Q8D_OK : record_cuda(e);
 }
 
+int q8d_step_launch_host(q8d_step* S, const int* h_token_pos, int* h_next_token, void* stream) {
+  if (!S || !S->exec) return Q8D_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (h_token_pos) {
+    if (S->desc.d_pos == S->desc.d_token + 1) {
+      e = cudaMemcpyAsync(S->desc.d_token, h_token_pos, 2 * sizeof(int), cudaMemcpyHostToDevice, st);
+    } else {
+      e = cudaMemcpyAsync(S->desc.d_token, h_token_pos, sizeof(int), cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(S->desc.d_pos, h_token_pos + 1, sizeof(int), cudaMemcpyHostToDevice, st);
+    }
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  if ((e = cudaGraphLaunch(S->exec, st)) != cudaSuccess) return record_cuda(e);
+  if (h_next_token &&
+      (e = cudaMemcpyAsync(h_next_token, S->desc.d_token, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
+          cudaSuccess)
+    return record_cuda(e);
+  return Q8D_OK;
+}
+
 int q8d_step_status(q8d_step* S, void* stream, int timeout_ms, int* err) {
   if (!S || !err) return Q8D_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

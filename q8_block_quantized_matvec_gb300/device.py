@@ -43,8 +43,10 @@ class DeviceStep:
         self.embed = to_device(weights.embed, device)
         self.out_norm = to_device(weights.out_norm, device)
         self.lm_head = to_device(weights.lm_head, device)
-        self.token = torch.zeros(1, dtype=torch.int32, device=device)
-        self.pos = torch.zeros(1, dtype=torch.int32, device=device)
+        # token id and position side by side: one 8-byte copy sets both
+        self.token_pos = torch.zeros(2, dtype=torch.int32, device=device)
+        self.token = self.token_pos[0:1]
+        self.pos = self.token_pos[1:2]
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.logits = torch.empty(s.vocab, dtype=torch.float32, device=device) if keep_logits else None
 
@@ -72,6 +74,11 @@ class DeviceStep:
 
     def launch(self, stream=None):
         self.step.launch(stream)
+
+    def launch_host(self, h_token_pos, h_next_token, stream=None):
+        """One step with host I/O (q8d_step_launch_host): pinned int32
+        [token, position] in, pinned int32 [1] next token out."""
+        self.step.launch_host(h_token_pos, h_next_token, stream)
 
     def kernel_count(self) -> int:
         return self.step.kernel_count()

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for want in ("q8d_matvec", "q8d_matmul_small_m", "q8d_matmul_small_m_ws",
                  "q8d_matmul_small_m_workspace_bytes", "q8d_kv_append", "q8d_gqa_decode_attn",
                  "q8d_gqa_workspace_bytes", "q8d_step_create", "q8d_step_launch",
-                 "q8d_step_status", "q8d_step_destroy"):
+                 "q8d_step_status", "q8d_step_destroy", "q8d_step_launch_host"):
         assert want in names
 
 
@@ -166,6 +166,7 @@ def test_step_create_refusals(q8d):
     L = q8d.lib()
     h = C.c_void_p()
     assert L.q8d_step_create(None, None, C.byref(h)) == q8d.Q8D_EINVAL
+    assert L.q8d_step_launch_host(None, None, None, None) == q8d.Q8D_EINVAL
     layers = (q8d.LayerDesc * 1)()
     for nm, _ in q8d.LayerDesc._fields_:
         setattr(layers[0], nm, A16)

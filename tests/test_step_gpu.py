@@ -158,6 +158,46 @@ def test_step_tiny_consecutive_tokens(orc, q8d):
     assert len(rel) == 3
 
 
+def test_step_launch_host_io(orc, q8d):
+    """q8d_step_launch_host: token and position from pinned host memory, the
+    next token back to host memory, one call a step.  Three steps decode the
+    same tokens as launches with the state set on the device, the oracle's
+    tokens, and a mid-sequence restart from the host (a position fed back
+    one step) reproduces the step it repeats."""
+    shape = synth.tiny_shape(3)
+    w = weights_for(shape, 0)
+    pos0, cap = 4, 16
+    caches = [synth.kv_prefix(shape, 0, li, cap, pos0) for li in range(shape.n_layers)]
+    host = orc.HostStep(w, cap, [(k.copy(), v.copy()) for k, v in caches])
+    ds = DeviceStep(w, cap, caches)
+    h_in = torch.tensor([17, pos0], dtype=torch.int32).pin_memory()
+    h_out = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    toks = []
+    tok_ref = 17
+    for s in range(3):
+        h_in[1] = pos0 + s
+        ds.launch_host(h_in, h_out)
+        torch.cuda.synchronize()
+        logits_ref, nxt_ref = host.step(tok_ref, pos0 + s)
+        assert compare_step(ds.logits.cpu().numpy(), logits_ref, int(h_out[0]), nxt_ref) < STEP_TOL
+        assert int(h_out[0]) == int(ds.token.item())          # the copy is the device token
+        assert int(ds.pos.item()) == pos0 + s + 1
+        toks.append(int(h_out[0]))
+        h_in[0] = int(h_out[0])
+        tok_ref = nxt_ref
+    # repeat the last step from the host: same input, same position, same token
+    h_in[0], h_in[1] = toks[1], pos0 + 2
+    ds.launch_host(h_in, h_out)
+    torch.cuda.synchronize()
+    assert int(h_out[0]) == toks[2]
+    # no input copy: continues from the device state
+    ds.launch_host(None, h_out)
+    torch.cuda.synchronize()
+    assert int(ds.pos.item()) == pos0 + 4
+    assert ds.step.status() == 0
+    ds.close()
+
+
 def test_step_qwen3_0_6b_shape(orc, q8d):
     run_case(orc, synth.QWEN3_0_6B, pos=511, cap=2048)
 
