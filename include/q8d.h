@@ -268,8 +268,8 @@ int q8d_gqa_decode_attn_noalloc(const float* q, const float* k_new, const float*
  * and must stay valid until q8d_step_destroy.  Weights, caches and RMSNorm
  * weights must be 16-byte aligned, the other f32 vectors 4-byte aligned
  * (Q8D_EALIGN otherwise).  head_dim in {64, 128}; n_heads % n_kv_heads ==
- * 0; n_heads/n_kv_heads <= 16 with an f32 cache, <= 12 with an f16 cache
- * (Q8D_EUNSUPPORTED otherwise).
+ * 0; n_heads/n_kv_heads <= 16 with an f32 cache, <= 12 with an f16 cache;
+ * n_kv_heads at most the device's SM count (Q8D_EUNSUPPORTED otherwise).
  * ---------------------------------------------------------------------- */
 typedef struct q8d_layer_desc {
   const void *wq, *wk, *wv, *wo, *wg, *wu, *wd; /* Q8_0: [H*hd][hidden], [Hk*hd][hidden] x2,

@@ -167,8 +167,9 @@ int q8d_step_create(const q8d_step_desc* desc, void* stream, q8d_step** out) {
   S->grid = sm_count();
   const int nc = std::max(1, S->grid / d.n_kv_heads);  // attention chunks per KV head
   // (the combine's lanes hold at most 5 chunks each; the final argmax's
-  // warp at most 8 CTAs a lane)
-  if (nc > 160 || S->grid > 256) {
+  // warp at most 8 CTAs a lane; the attention phase gives every KV head at
+  // least one of the grid's CTAs)
+  if (nc > 160 || S->grid > 256 || d.n_kv_heads > S->grid) {
     delete S;
     return Q8D_EUNSUPPORTED;
   }

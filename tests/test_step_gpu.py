@@ -306,6 +306,18 @@ def test_step_position_past_cache_flags_error(orc, q8d):
     ds.close()
 
 
+def test_step_refuses_more_kv_heads_than_sms(q8d):
+    """The attention phase gives each KV head at least one CTA of the
+    one-per-SM grid: more KV heads than SMs are refused at creation."""
+    hk = torch.cuda.get_device_properties(0).multi_processor_count + 8
+    shape = synth.ModelShape("many-kv", 256, 1, hk, hk, 64, 256, 100,
+                             qk_norm=False, qkv_bias=False, kv_dtype=synth.KV_F16)
+    w = synth.step_weights(shape, seed=1)
+    with pytest.raises(q8d.Q8DError) as e:
+        DeviceStep(w, 4)
+    assert e.value.status == q8d.Q8D_EUNSUPPORTED
+
+
 def test_step_bad_token_flags_error(orc, q8d):
     shape = synth.tiny_shape(1)
     w = synth.step_weights(shape, seed=1)
